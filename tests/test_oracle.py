@@ -1,0 +1,461 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each test checks the oracle against something other than itself: values the
+pages print (tests/golden/*.json, each with its citation), an independent
+library routine (torch's float8 dtypes), exact rational arithmetic, brute
+force, or a closed form.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mx_oracle as O
+
+
+def load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+TORCH_FP8 = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+
+
+# ---------------------------------------------------------------- decoding
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_decode_all_codes_match_torch(fmt):
+    """All 256 codes decode like torch's OCP float8 dtype (library routine)."""
+    mine = O.decode_table(fmt)
+    ref = torch.arange(256, dtype=torch.uint8).view(TORCH_FP8[fmt]).double().numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+    assert np.array_equal(np.signbit(mine[ok]), np.signbit(ref[ok]))
+
+
+def test_format_facts_from_page(golden_dir):
+    g = load(golden_dir, "format_facts.json")
+    t4 = O.decode_table("e4m3")
+    e4 = g["e4m3"]
+    finite = t4[np.isfinite(t4)]
+    assert finite.max() == e4["max"] and t4[0x7E] == 448.0 and t4[0xFE] == -448.0
+    assert [c for c in range(256) if np.isnan(t4[c])] == e4["nan_codes"]
+    assert not np.isinf(t4).any()
+    pos = np.sort(finite[finite > 0])
+    assert pos[0] == e4["min_subnormal"]
+    assert pos[pos >= e4["min_normal"]][0] == e4["min_normal"]
+    assert pos[pos < e4["min_normal"]].max() < e4["min_normal"]
+    for lo, hi, step in e4["spacing"]:
+        grid = pos[(pos >= lo) & (pos <= hi)]
+        assert np.all(np.diff(grid) == step)
+    t5 = O.decode_table("e5m2")
+    f5 = t5[np.isfinite(t5)]
+    assert f5.max() == g["e5m2"]["max"]
+    assert np.sort(f5[f5 > 0])[0] == g["e5m2"]["min_subnormal"]
+    pos5 = np.sort(f5[f5 > 0])
+    for lo, hi, step in g["e5m2"]["spacing"]:
+        grid = pos5[(pos5 >= lo) & (pos5 < hi)]
+        assert np.all(np.diff(grid) == step)
+    assert np.isinf(t5).sum() == 2
+
+
+def test_e8m0_decode_from_page(golden_dir):
+    g = load(golden_dir, "e8m0.json")
+    for code, val in g["decode"].items():
+        assert O.decode_e8m0(int(code)) == val
+    assert O.decode_e8m0(0) > 0
+    assert math.isnan(O.decode_e8m0(g["nan_code"]))
+    with pytest.raises(ValueError):
+        O.decode_e8m0(256)
+    vals = O.e8m0_values(np.array([0x77, 0x80, 0, 255], dtype=np.uint8))
+    assert vals[0] == 2.0 ** -8 and vals[1] == 2.0 and vals[2] == 2.0 ** -127
+    assert math.isnan(vals[3])
+
+
+def test_payload_model_from_page(golden_dir):
+    """Two rows of 32 E4M3 codes: 64 code bytes + 4 (FP32 tensor scale) = 68,
+    or + 2 E8M0 block scales = 66; the scale overheads are 6.25% / 3.125%."""
+    g = load(golden_dir, "e8m0.json")
+    codes = 2 * O.BLOCK
+    assert codes + 4 == g["payload_bytes"]["two_rows_of_32_e4m3_tensor_scale"]
+    assert codes + 2 * 1 == g["payload_bytes"]["two_rows_of_32_e4m3_mx"]
+    assert 100 * 4 / codes == g["scale_overhead_percent"]["tensor"]
+    assert 100 * 2 / codes == g["scale_overhead_percent"]["mx"]
+
+
+# ---------------------------------------------------------------- encoding
+
+def test_cast_audit_from_page(golden_dir):
+    g = load(golden_dir, "cast_audit.json")
+    codes = O.encode_sat_rne(g["fmt"], np.array(g["inputs"]))
+    vals = O.decode_table(g["fmt"])[codes]
+    assert vals.tolist() == g["outputs"]
+    assert np.signbit(vals).tolist() == g["output_signbit"]
+    t = O.decode_table("e4m3")
+    for code, val in g["byte_decoding"].items():
+        assert t[int(code, 16)] == val and np.signbit(t[int(code, 16)]) == np.signbit(val)
+
+
+def test_saturation_and_rne_from_page(golden_dir):
+    g = load(golden_dir, "format_facts.json")
+    t4 = O.decode_table("e4m3")
+    for x, y in g["e4m3"]["saturate"]:
+        assert t4[O.encode_sat_rne("e4m3", np.array([x]))[0]] == y
+        assert t4[O.encode_sat_rne("e4m3", np.array([-x]))[0]] == -y
+    r = g["rounding"]
+    assert t4[O.encode_sat_rne(r["fmt"], np.array([r["x"]]))[0]] == r["rne"]
+    lo, hi = r["neighbors"]
+    grid = np.sort(t4[np.isfinite(t4)])
+    assert lo in grid and hi in grid and not np.any((grid > lo) & (grid < hi))
+    t5 = O.decode_table("e5m2")
+    for x in [57344.0, 60000.0, 61440.0, 1e9, math.inf]:
+        assert t5[O.encode_sat_rne("e5m2", np.array([x]))[0]] == 57344.0
+    assert O.encode_sat_rne("e4m3", np.array([math.inf]))[0] == 0x7E
+    assert O.encode_sat_rne("e4m3", np.array([math.nan]))[0] == O.NAN_CODE
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_encode_every_bf16_pattern_matches_torch(fmt):
+    """Exhaustive: every finite bf16 value, scale 1, against torch's RNE cast
+    of the value pre-clamped to the finite range (an independent routine)."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = O.bf16_bits_to_float64(bits)
+    ok = np.isfinite(vals)
+    vals = vals[ok]
+    mine = O.encode_sat_rne(fmt, vals)
+    mx = O.FORMATS[fmt].max_finite
+    ref = torch.from_numpy(np.clip(vals, -mx, mx)).float().to(TORCH_FP8[fmt])
+    ref = ref.view(torch.uint8).numpy()
+    assert np.array_equal(mine, ref)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_encode_decode_round_trip(fmt):
+    t = O.decode_table(fmt)
+    codes = np.array([c for c in range(256) if np.isfinite(t[c])], dtype=np.uint8)
+    assert np.array_equal(O.encode_sat_rne(fmt, t[codes]), codes)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_midpoints_tie_to_even_code(fmt):
+    """Between adjacent positive finite codes c, c+1 (consecutive integers),
+    the exact midpoint goes to the one with an even mantissa LSB, slightly
+    off the midpoint goes to the nearer one."""
+    t = O.decode_table(fmt)
+    for c in range(0, 0x7F):
+        lo, hi = t[c], t[c + 1]
+        if not (np.isfinite(lo) and np.isfinite(hi)):
+            continue
+        mid = (lo + hi) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert O.encode_sat_rne(fmt, np.array([mid]))[0] == even
+        assert O.encode_sat_rne(fmt, np.array([-mid]))[0] == even | 0x80
+        eps = (hi - lo) / 1024
+        assert O.encode_sat_rne(fmt, np.array([mid - eps]))[0] == c
+        assert O.encode_sat_rne(fmt, np.array([mid + eps]))[0] == c + 1
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_encode_is_monotone_and_keeps_sign(fmt):
+    rng = np.random.default_rng(5)
+    v = np.sort(np.concatenate([rng.standard_normal(20000) * s for s in (1e-4, 1, 100, 1e5)]))
+    vals = O.decode_table(fmt)[O.encode_sat_rne(fmt, v)]
+    assert np.all(np.diff(vals) >= 0)
+    assert np.all(np.signbit(vals) == np.signbit(v))
+
+
+# ---------------------------------------------------------------- block scales
+
+def test_floor_rule_puts_scaled_amax_in_top_binade():
+    """OCP floor rule: after scaling, amax lies in [2^emax, 2^(emax+1))."""
+    rng = np.random.default_rng(1)
+    amax = np.exp(rng.uniform(-60, 60, 5000))  # no exponent clamping here
+    for fmt in ("e4m3", "e5m2"):
+        f = O.FORMATS[fmt]
+        e = O.scale_exponent_floor(fmt, amax)
+        s = amax * 2.0 ** (-e.astype(np.float64))
+        assert np.all((s >= 2.0 ** f.emax_elem) & (s < 2.0 ** (f.emax_elem + 1)))
+
+
+def test_ceil_rule_brute_force():
+    """Page's conservative rule: the smallest e in [-127, 200] with
+    amax <= max * 2^e, found by linear search with exact comparisons."""
+    rng = np.random.default_rng(2)
+    amax = np.concatenate([np.exp(rng.uniform(-60, 60, 300)),
+                           [448.0, 449.0, 447.0, 896.0, 2.0 ** -140, 57344.0]])
+    for fmt in ("e4m3", "e5m2"):
+        mx = O.FORMATS[fmt].max_finite
+        got = O.scale_exponent_ceil(fmt, amax)
+        for a, e in zip(amax, got):
+            want = next(k for k in range(-127, 200) if a <= mx * 2.0 ** k)
+            assert e == want
+
+
+def test_ceil_equals_floor_plus_one_iff_significand_above_1_75():
+    rng = np.random.default_rng(3)
+    amax = np.exp(rng.uniform(-40, 40, 20000))
+    sig = amax / 2.0 ** O.floor_log2_exact(amax)
+    for fmt in ("e4m3", "e5m2"):
+        diff = O.scale_exponent_ceil(fmt, amax) - O.scale_exponent_floor(fmt, amax)
+        assert np.array_equal(diff, (sig > 1.75).astype(np.int64))
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_quantize_codes_match_torch_cast_given_scale(fmt):
+    """Given each block's scale, the codes equal torch's RNE cast of the
+    exactly scaled, pre-clamped values."""
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((64, 256)) * np.exp(rng.uniform(-10, 10, (64, 1)))
+    x[rng.random(x.shape) < 0.01] *= 300
+    x = O.bf16_bits_to_float64((x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16))
+    q = O.quantize(x, fmt, "row")
+    s = O.e8m0_values(q.scales)
+    scaled = x.reshape(64, 8, 32) / s[:, :, None]
+    mx = O.FORMATS[fmt].max_finite
+    ref = torch.from_numpy(np.clip(scaled, -mx, mx).reshape(64, 256)).float()
+    ref = ref.to(TORCH_FP8[fmt]).view(torch.uint8).numpy()
+    assert np.array_equal(q.codes, ref)
+
+
+def test_zero_nan_inf_and_subnormal_blocks():
+    x = np.zeros((4, 64))
+    x[0, 5] = -0.0
+    x[1, :32] = np.nan
+    x[1, 40] = 1.0
+    x[2, 3] = np.inf
+    x[3, :32] = 2.0 ** -133          # smallest bf16 subnormal
+    x[3, 32:] = 3 * 2.0 ** -130
+    q = O.quantize(x, "e4m3", "row")
+    assert q.scales[0].tolist() == [127, 127]          # zero block: S = 1
+    assert q.codes[0, 5] == 0x80 and q.codes[0, 4] == 0
+    assert q.scales[1].tolist() == [255, 127 - 8]
+    assert np.all(q.codes[1, :32] == O.NAN_CODE)
+    assert q.scales[2, 0] == 255 and np.all(q.codes[2, :32] == O.NAN_CODE)
+    assert q.scales[3].tolist() == [0, 0]               # clamped at 2^-127
+    t = O.decode_table("e4m3")
+    assert t[q.codes[3, 0]] == 2.0 ** -6 and t[q.codes[3, 32]] == 3 * 2.0 ** -3
+    assert np.isnan(O.dequantize(q)[1, :32]).all()
+
+
+def test_column_blocks_run_along_rows():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((64, 48))
+    x[3, 7] = 1000.0
+    qc = O.quantize(x, "e4m3", "col")
+    assert qc.codes.shape == (48, 64) and qc.scales.shape == (48, 2)
+    qr = O.quantize(x.T.copy(), "e4m3", "row")
+    assert np.array_equal(qc.codes, qr.codes) and np.array_equal(qc.scales, qr.scales)
+    big = qc.scales[7, 0]
+    assert big > qc.scales[7, 1] and big > qc.scales[6, 0] and big > qc.scales[8, 0]
+
+
+# ---------------------------------------------------------------- two-row experiment
+
+def two_row_fixture(g):
+    x = np.array([g["pattern_small"] * g["repeat"], g["pattern_large"] * g["repeat"]],
+                 dtype=np.float32).astype(np.float64)
+    w = np.array(g["weight_pattern"] * g["repeat"], dtype=np.float32).astype(np.float64)
+    return x, w.reshape(32, 1)
+
+
+def test_two_row_experiment_ceil_rule_from_page(golden_dir):
+    g = load(golden_dir, "two_row_fixture.json")
+    c = g["ceil_rule"]
+    x, w = two_row_fixture(g)
+    qx = O.quantize(x, "e4m3", "row", rule="ceil")
+    qw = O.quantize(w, "e4m3", "col", rule="ceil")
+    assert [O.decode_e8m0(int(s)) for s in qx.scales[:, 0]] == c["x_scales"]
+    xh = O.dequantize(qx)
+    assert round(xh[0, 0], 8) == c["x_hat_0_0"]
+    assert xh[1, 3] == c["x_hat_1_3"]
+    y, _ = O.gemm(qx, qw)
+    d = c["print_decimals"]
+    assert [round(v, d) for v in y.ravel()] == c["mx_y"]
+    ref = (x @ w).ravel()
+    ref32 = (x.astype(np.float32) @ w.astype(np.float32)).ravel()  # the page's FP32 matmul
+    assert [round(float(v), d) for v in ref32] == c["reference_y"]
+    err = np.abs(y.ravel() - ref)
+    assert abs(err[0] - c["mx_abs_error"][0]) < 1e-7 and err[1] == c["mx_abs_error"][1]
+    sel = np.zeros((32, 1))
+    sel[3, 0] = 1.0
+    ys, _ = O.gemm(qx, O.quantize(sel, "e4m3", "col", rule="ceil"))
+    assert ys.ravel().tolist() == c["selector_mx"]
+    assert (x @ sel).ravel().tolist() == c["selector_reference"]
+
+
+def test_two_row_experiment_tensor_scale_from_page(golden_dir):
+    """The tensor-wide column: one FP32 scale amax/448 for all of X."""
+    g = load(golden_dir, "two_row_fixture.json")
+    ts = g["tensor_scale"]
+    x, w = two_row_fixture(g)
+    sx = np.float32(np.abs(x).max()) / np.float32(448.0)
+    sw = np.float32(np.abs(w).max()) / np.float32(448.0)
+    assert round(float(sx), 6) == ts["tensor_scale_x"]
+    xq = O.decode_table("e4m3")[O.encode_sat_rne("e4m3", x / float(sx))] * float(sx)
+    wq = O.decode_table("e4m3")[O.encode_sat_rne("e4m3", w / float(sw))] * float(sw)
+    assert xq[0, 0] == ts["x_hat_0_0"]
+    y = (xq.astype(np.float32) @ wq.astype(np.float32)).ravel()  # the page's FP32 matmul
+    assert [round(float(v), 6) for v in y] == ts["tensor_y"]
+
+
+def test_two_row_experiment_floor_rule_saturates_spike(golden_dir):
+    """Floor rule on the same fixture: the spike row's scale is 2^0, so 500
+    saturates to 448 (derived from the rule; not printed by the page)."""
+    g = load(golden_dir, "two_row_fixture.json")
+    x, w = two_row_fixture(g)
+    qx = O.quantize(x, "e4m3", "row")
+    assert [O.decode_e8m0(int(s)) for s in qx.scales[:, 0]] == [2.0 ** -8, 1.0]
+    assert O.dequantize(qx)[1, 3] == 448.0 and qx.codes[1, 3] == 0x7E
+    y, _ = O.gemm(qx, O.quantize(w, "e4m3", "col"))
+    assert y.ravel().tolist() == [0.6015625, 23.75]
+
+
+# ---------------------------------------------------------------- GEMM
+
+def int_operands(rng, rows, k, fmt, lim):
+    """Codes of small integers (exact in the format) with scale 2^0."""
+    vals = rng.integers(-lim, lim + 1, size=(rows, k)).astype(np.float64)
+    codes = O.encode_sat_rne(fmt, vals)
+    return vals, O.MxBlocks(codes, np.full((rows, k // 32), 127, np.uint8), O.FORMATS[fmt])
+
+
+@pytest.mark.parametrize("fa,fb", [("e4m3", "e4m3"), ("e5m2", "e4m3"), ("e4m3", "e5m2")])
+def test_gemm_integer_closed_form(fa, fb):
+    """All scales 1 and integer codes: Y is the integer matmul (exact)."""
+    rng = np.random.default_rng(7)
+    av, a = int_operands(rng, 5, 96, fa, 8)
+    bv, b = int_operands(rng, 3, 96, fb, 8)
+    y, t = O.gemm(a, b)
+    want = av.astype(np.int64) @ bv.astype(np.int64).T
+    assert np.array_equal(y, want.astype(np.float64))
+    assert np.array_equal(t, (np.abs(av).astype(np.int64) @ np.abs(bv).astype(np.int64).T))
+
+
+def random_mx(rng, rows, k, fmt, scale_lo=110, scale_hi=140):
+    t = O.decode_table(fmt)
+    finite = np.array([c for c in range(256) if np.isfinite(t[c])], dtype=np.uint8)
+    codes = rng.choice(finite, size=(rows, k))
+    scales = rng.integers(scale_lo, scale_hi, size=(rows, k // 32)).astype(np.uint8)
+    return O.MxBlocks(codes, scales, O.FORMATS[fmt])
+
+
+def test_gemm_matches_exact_rational_sum():
+    """Random codes and non-uniform scales: float64 oracle vs exact Fractions."""
+    rng = np.random.default_rng(8)
+    a = random_mx(rng, 3, 96, "e4m3")
+    b = random_mx(rng, 2, 96, "e5m2")
+    y, t = O.gemm(a, b)
+    exact = O.exact_gemm_fraction(a, b)
+    for i in range(3):
+        for j in range(2):
+            assert abs(Fraction(y[i, j]) - exact[i][j]) <= Fraction(t[i, j]) * Fraction(1, 2 ** 45)
+    # T is the sum of |products| (brute force)
+    ta, tb = O.decode_table("e4m3"), O.decode_table("e5m2")
+    sa, sb = O.e8m0_values(a.scales), O.e8m0_values(b.scales)
+    for i in range(3):
+        for j in range(2):
+            want = sum(abs(ta[a.codes[i, k]] * sa[i, k // 32] * tb[b.codes[j, k]] * sb[j, k // 32])
+                       for k in range(96))
+            assert abs(t[i, j] - want) <= 1e-12 * want
+
+
+def test_gemm_keeps_block_scales_inside_the_sum(golden_dir):
+    """Two K-blocks with partial sums 2 and 3 and scale products 4 and 8: the
+    definition gives 2*4 + 3*8, not 4*(2+3) (the page's 34-vs-25 point)."""
+    g = load(golden_dir, "block_sum.json")
+    assert sum(p * s for p, s in zip(g["partials"], g["scale_products"])) == g["block_scaled_sum"]
+    v = g["e8m0_variant"]
+    a_codes = np.zeros((1, 64), np.uint8)
+    b_codes = np.zeros((1, 64), np.uint8)
+    one = O.encode_sat_rne("e4m3", np.array([1.0]))[0]
+    a_codes[0, 0:2] = one          # block 0: partial 1 + 1 = 2
+    a_codes[0, 32:35] = one        # block 1: partial 3
+    b_codes[0, :] = one
+    sa = np.array([[127 + 2, 127 + 3]], np.uint8)      # 4, 8
+    sb = np.array([[127, 127]], np.uint8)
+    y, _ = O.gemm(O.MxBlocks(a_codes, sa, O.E4M3), O.MxBlocks(b_codes, sb, O.E4M3))
+    assert y[0, 0] == v["block_scaled_sum"] != v["pulled_out_sum"]
+
+
+def test_gemm_block_form_equals_dequantized_matmul():
+    rng = np.random.default_rng(9)
+    a = random_mx(rng, 17, 160, "e4m3")
+    b = random_mx(rng, 9, 160, "e4m3")
+    y, t = O.gemm(a, b)
+    ref = O.dequantize(a) @ O.dequantize(b).T
+    assert np.all(np.abs(y - ref) <= 1e-13 * t)
+
+
+def test_gemm_operand_orientation():
+    """A [M,K] and B [N,K]: a transposed or swapped operand fails here."""
+    rng = np.random.default_rng(10)
+    av, a = int_operands(rng, 4, 64, "e4m3", 5)
+    bv, b = int_operands(rng, 7, 64, "e4m3", 5)
+    y, _ = O.gemm(a, b)
+    assert y.shape == (4, 7)
+    assert y[2, 5] == float(np.dot(av[2], bv[5]))
+
+
+def test_grouped_gemm_is_per_group_dense():
+    rng = np.random.default_rng(11)
+    offsets = np.array([0, 0, 5, 37, 37, 40])
+    a = random_mx(rng, 40, 64, "e4m3")
+    bs = [random_mx(rng, 6, 64, "e4m3") for _ in range(5)]
+    y, _ = O.grouped_gemm(a, offsets, bs)
+    for g in range(5):
+        lo, hi = offsets[g], offsets[g + 1]
+        for i in range(lo, hi):
+            row = O.MxBlocks(a.codes[i:i + 1], a.scales[i:i + 1], a.fmt)
+            assert np.array_equal(y[i], O.gemm(row, bs[g])[0][0])
+
+
+# ---------------------------------------------------------------- swizzle
+
+@pytest.mark.parametrize("rows,kb", [(1, 1), (128, 4), (130, 5), (300, 17), (256, 224)])
+def test_swizzle_is_a_bijection_and_round_trips(rows, kb):
+    size = O.scale_bytes(rows, kb)
+    r, c = np.meshgrid(np.arange(-(-rows // 128) * 128), np.arange(-(-kb // 4) * 4), indexing="ij")
+    off = O.swizzle_offset(r, c, kb).ravel()
+    assert np.array_equal(np.sort(off), np.arange(size))
+    rng = np.random.default_rng(rows * 1000 + kb)
+    s = rng.integers(0, 255, size=(rows, kb)).astype(np.uint8)
+    buf = O.swizzle_scales(s)
+    assert buf.size == size
+    assert np.array_equal(O.unswizzle_scales(buf, rows, kb), s)
+    mask = np.ones(size, bool)
+    mask[O.swizzle_offset(*np.meshgrid(np.arange(rows), np.arange(kb), indexing="ij"), kb).ravel()] = False
+    assert np.all(buf[mask] == 0)
+
+
+def test_swizzle_tile_structure():
+    """Each 128x4 tile is one contiguous 512-byte unit; 32-row groups of a
+    tile interleave at 4-byte slots of 16-byte lines."""
+    kb = 8
+    assert O.swizzle_offset(0, 0, kb) == 0
+    assert O.swizzle_offset(0, 4, kb) == 512
+    assert O.swizzle_offset(128, 0, kb) == 1024
+    assert O.swizzle_offset(1, 0, kb) == 16
+    assert O.swizzle_offset(32, 0, kb) == 4
+    assert O.swizzle_offset(0, 3, kb) == 3
+
+
+def test_grouped_swizzle_places_each_group_at_a_tile_boundary():
+    rng = np.random.default_rng(12)
+    offsets = np.array([0, 3, 3, 200, 201, 460])
+    s = rng.integers(0, 255, size=(460, 8)).astype(np.uint8)
+    buf = O.swizzle_scales_grouped(s, offsets)
+    starts = O.grouped_scale_rows(offsets)
+    assert starts.tolist() == [0, 128, 128, 384, 512, 896]
+    assert buf.size >= O.scale_bytes(starts[-1], 8)
+    for g in range(5):
+        lo, hi = offsets[g], offsets[g + 1]
+        if lo == hi:
+            continue
+        base = starts[g] // 128 * 2 * 512
+        part = buf[base:base + O.scale_bytes(hi - lo, 8)]
+        assert np.array_equal(O.unswizzle_scales(part, hi - lo, 8), s[lo:hi])
