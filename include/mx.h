@@ -1,0 +1,199 @@
+/*
+ * mx.h -- C ABI of libmx, the MXFP8 training-matmul library for GB300 (sm_103a).
+ *
+ * The library has two parts, after "Low-Precision GPU Programming"
+ * (leetllm.com):
+ *
+ *   1. MX quantization (sections "Format taxonomy: range, spacing, and
+ *      bitfields", "Numerical hazards: subnormals, saturation, and rounding"
+ *      and "Microscaling: the two-row experiment"): every block of 32
+ *      consecutive elements along the contraction axis K shares one E8M0
+ *      power-of-two scale S, and each element becomes the OCP E4M3 or E5M2
+ *      code of x / S, rounded to nearest even with saturation to the finite
+ *      range.
+ *   2. The block-scaled GEMM (section "Scale ownership and the GEMM
+ *      dataflow"): Y[i,j] = sum_b S_A[i,b] * S_B[j,b] * sum_{k in b}
+ *      A~[i,k] * B~[j,k], accumulated in FP32 on the tensor cores, with an
+ *      epilogue that writes FP32 or BF16 (round to nearest even).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers marked "device" must point to device memory of the current
+ *    CUDA device; the caller allocates and owns every buffer.  The library
+ *    allocates no device memory.
+ *  - Work is enqueued on `stream` (0 = legacy default stream).  No entry
+ *    point synchronizes the stream or the device.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    non-MX_OK status means nothing was enqueued.
+ *  - Faults detected on the device (a pipeline wait that timed out, invalid
+ *    group offsets) are recorded in a per-process device status word and
+ *    reported by mx_device_status(), which synchronizes `stream`.
+ *  - Every device pointer must be 16-byte aligned, and every leading
+ *    dimension must span a multiple of 16 bytes (MX_ERR_MISALIGNED).
+ *
+ * Scale layout ("swizzled", the operand layout of the tensor-core
+ * block-scaled MMA; the pages require the layout to be recorded with the
+ * kernel but do not define it -- section "Hardware support and kernel ABI
+ * contracts"):
+ *  - Scales of a [rows, K] operand (K/32 blocks per row) are stored in tiles
+ *    of 128 rows x 4 blocks = 512 bytes.  Tile (rt, kt) starts at byte
+ *    (rt * ceil(K/128) + kt) * 512.  Inside a tile, the scale of local row r
+ *    (0..127) and local block c (0..3) is at byte
+ *    (r % 32) * 16 + (r / 32) * 4 + c.
+ *  - Padding entries (rows >= rows, blocks >= K/32) are written as 0x00 by
+ *    the quantizer and never influence a valid GEMM output.
+ *  - A scale byte c encodes 2^(c - 127); 0xFF is NaN.
+ */
+#ifndef MX_H_
+#define MX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MX_OK = 0,
+  MX_ERR_INVALID_ARG = 1,   /* shape, enum or null-pointer error              */
+  MX_ERR_MISALIGNED = 2,    /* pointer or leading dimension not 16-byte aligned */
+  MX_ERR_UNSUPPORTED = 3,   /* valid but not implemented combination          */
+  MX_ERR_CUDA = 4,          /* a CUDA runtime / driver call failed            */
+  MX_ERR_TIMEOUT = 5,       /* a device pipeline wait gave up (device status) */
+  MX_ERR_DEVICE_ARG = 6     /* the device found invalid data (group offsets)  */
+} mx_status;
+
+/* Element formats (OCP OFP8).  E4M3: max 448, no Inf, NaN 0x7F/0xFF.
+ * E5M2: max 57344, IEEE-like Inf and NaN. */
+typedef enum { MX_E4M3 = 0, MX_E5M2 = 1 } mx_fmt;
+
+/* Wide element types: quantizer input and GEMM output. */
+typedef enum { MX_BF16 = 0, MX_FP32 = 1 } mx_dtype;
+
+/* Which quantizations to produce from one read of the wide tensor.
+ * ROWWISE: 1x32 blocks along the columns of x.  COLWISE: 32x1 blocks along
+ * the rows of x, written transposed so that the blocked axis is contiguous.
+ * (section "Microscaling: the two-row experiment": both orientations are
+ * derived from the original wide data, never by moving codes.) */
+typedef enum { MX_ROWWISE = 1, MX_COLWISE = 2, MX_BOTH = 3 } mx_axis;
+
+/* Block scale rule.
+ * MX_SCALE_FLOOR: S = 2^(floor(log2 amax) - emax_elem), emax_elem = 8 for
+ *   E4M3 and 15 for E5M2 (the OCP MX rule); values above the format maximum
+ *   after scaling saturate.
+ * MX_SCALE_CEIL: S = 2^ceil(log2(amax / max)), the conservative rule the
+ *   two-row experiment uses; no element saturates.
+ * Both: exponent clamped to [-127, 127]; an all-zero block takes S = 1; a
+ * block holding NaN or Inf takes scale 0xFF and the NaN code 0x7F for every
+ * element. */
+typedef enum { MX_SCALE_FLOOR = 0, MX_SCALE_CEIL = 1 } mx_scale_rule;
+
+/* Bytes of the swizzled scale buffer of a [rows, k] operand:
+ * ceil(rows/128)*128 * ceil(k/32/4)*4.  k must be a multiple of 32
+ * (returns 0 otherwise or for negative sizes). */
+size_t mx_scale_bytes(int64_t rows, int64_t k);
+
+/* Upper bound of the per-group padded scale buffer used by
+ * mx_quantize_grouped / mx_grouped_gemm for any split of total_rows into
+ * `groups` groups: (ceil(total_rows/128) + groups) * 128 * ceil(k/128) * 4. */
+size_t mx_grouped_scale_bytes(int64_t total_rows, int32_t groups, int64_t k);
+
+/* MX quantization of a bf16 matrix x[rows, cols] (row-major, leading
+ * dimension ldx elements), section "Microscaling: the two-row experiment".
+ *
+ *  ROWWISE (needs cols % 32 == 0): q_row[rows, cols] codes (row-major,
+ *    leading dimension cols) and s_row = swizzled scales of the
+ *    [rows, cols] operand (mx_scale_bytes(rows, cols) bytes).
+ *  COLWISE (needs rows % 32 == 0): q_col[cols, rows] codes -- the transpose,
+ *    leading dimension rows -- and s_col = swizzled scales of the
+ *    [cols, rows] operand (mx_scale_bytes(cols, rows) bytes).
+ *  BOTH: both of the above from one read of x.
+ *
+ * x, q_*, s_* are device pointers; unused outputs may be NULL.
+ * cols % 8 == 0, ldx % 8 == 0, ldx >= cols.  x_dtype must be MX_BF16.
+ * Codes and scales are bit-exact functions of x (no rounding-order freedom). */
+mx_status mx_quantize(const void* x, mx_dtype x_dtype, int64_t rows, int64_t cols,
+                      int64_t ldx, mx_fmt fmt, mx_axis axis, mx_scale_rule rule,
+                      uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                      cudaStream_t stream);
+
+/* Rowwise MX quantization of routed tokens x[total_rows, cols] grouped by
+ * expert: rows [d_offsets[g], d_offsets[g+1]) belong to group g.  Codes are
+ * written as by mx_quantize ROWWISE; scales use the per-group padded layout
+ * that mx_grouped_gemm reads: group g's scales form their own swizzled
+ * matrix starting at row P_g = sum_{h<g} ceil(m_h/128)*128, i.e. at byte
+ * (P_g/128) * ceil(cols/128) * 512.  s must hold
+ * mx_grouped_scale_bytes(total_rows, groups, cols) bytes; bytes past the
+ * last group are left untouched.  d_offsets: device int32[groups + 1],
+ * d_offsets[0] = 0, non-decreasing, d_offsets[groups] = total_rows; invalid
+ * offsets are reported through mx_device_status (MX_ERR_DEVICE_ARG) and
+ * nothing is written.  1 <= groups <= 4096. */
+mx_status mx_quantize_grouped(const void* x, mx_dtype x_dtype, int64_t total_rows,
+                              int64_t cols, int64_t ldx, mx_fmt fmt, mx_scale_rule rule,
+                              int32_t groups, const int32_t* d_offsets,
+                              uint8_t* q, uint8_t* s, cudaStream_t stream);
+
+/* Block-scaled GEMM, section "Scale ownership and the GEMM dataflow":
+ *   y[i, j] = sum_b S_A[i,b] S_B[j,b] sum_{k in b} A~[i,k] B~[j,k]
+ * A: a[m, k] codes (row-major, K contiguous, leading dimension k) with
+ *    swizzled scales sa of the [m, k] operand -- e.g. X quantized ROWWISE.
+ * B: b[n, k] codes (K contiguous, leading dimension k) with swizzled scales
+ *    sb of the [n, k] operand -- e.g. W[k, n] quantized COLWISE (= W^T).
+ * fa, fb: E4M3 or E5M2, any combination.
+ * y: device, [m, n] row-major with leading dimension ldy (elements),
+ *    FP32 or BF16 (RNE from the FP32 accumulator).
+ * Constraints: k % 32 == 0, k >= 32, n % 8 == 0, ldy >= n.
+ * Accumulation is FP32 on the tensor cores; its internal order is
+ * implementation-defined (section "Accumulator type isn't the whole
+ * arithmetic contract"). */
+mx_status mx_gemm(int64_t m, int64_t n, int64_t k,
+                  const uint8_t* a, const uint8_t* sa, mx_fmt fa,
+                  const uint8_t* b, const uint8_t* sb, mx_fmt fb,
+                  void* y, mx_dtype y_dtype, int64_t ldy, cudaStream_t stream);
+
+/* Grouped (mixture-of-experts) block-scaled GEMM: for every group g,
+ *   y[o_g : o_{g+1}, :] = A[o_g : o_{g+1}, :] * B_g^T
+ * with the per-row block scales of the dense GEMM.
+ * a: [total_m, k] codes of the concatenated tokens; sa: per-group padded
+ *    swizzled scales (as written by mx_quantize_grouped).
+ * b: [groups, n, k] codes (each B_g K-contiguous); sb: groups consecutive
+ *    swizzled scale matrices of [n, k], group g at byte g * mx_scale_bytes(n, k).
+ * y: [total_m, n] row-major (leading dimension n).  Rows of empty groups do
+ *    not exist; rows outside [0, total_m) are never written.
+ * d_offsets: device int32[groups + 1] as for mx_quantize_grouped; read on
+ *    the device (no host synchronization).  n % 128 == 0, k % 32 == 0. */
+mx_status mx_grouped_gemm(int32_t groups, const int32_t* d_offsets, int64_t total_m,
+                          int64_t n, int64_t k,
+                          const uint8_t* a, const uint8_t* sa, mx_fmt fa,
+                          const uint8_t* b, const uint8_t* sb, mx_fmt fb,
+                          void* y, mx_dtype y_dtype, cudaStream_t stream);
+
+/* Synchronizes `stream`, then returns and clears the device status word of
+ * the current device: MX_OK, MX_ERR_TIMEOUT (a kernel's bounded pipeline wait
+ * gave up; its outputs are undefined) or MX_ERR_DEVICE_ARG (invalid group
+ * offsets).  MX_ERR_CUDA if the synchronization itself failed. */
+mx_status mx_device_status(cudaStream_t stream);
+
+/* Static string naming a status code. */
+const char* mx_status_str(mx_status status);
+
+/* Bounded pipeline waits: every mbarrier wait inside the kernels gives up
+ * after `ns` nanoseconds (default 2e9 when ns == 0), records MX_ERR_TIMEOUT
+ * in the device status word and lets the kernel drain and exit.  Applies to
+ * launches enqueued after the call, on every device. */
+mx_status mx_set_wait_timeout_ns(uint64_t ns);
+
+/* Self-test of the bounded wait: enqueues one tiny kernel that waits on an
+ * mbarrier that nothing ever completes, with a limit of `ns` nanoseconds.
+ * mx_device_status() afterwards must return MX_ERR_TIMEOUT.  No TMA, MMA or
+ * tensor memory is involved. */
+mx_status mx_selftest_wait_timeout(uint64_t ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MX_H_ */

@@ -1,0 +1,257 @@
+"""MXFP8 training matmul for GB300: a thin Python binding over libmx.so.
+
+The binding only marshals arguments: every step of quantization and of the
+block-scaled GEMM runs in the CUDA kernels behind the C ABI declared in
+include/mx.h.  PyTorch supplies device memory and the current stream.
+There is no CPU fallback: calling any entry point without the built
+library raises.
+
+Low-level functions carry the C names (mx_quantize, mx_quantize_grouped,
+mx_gemm, mx_grouped_gemm, mx_device_status, ...) and take raw pointers;
+`quantize`, `quantize_grouped`, `gemm` and `grouped_gemm` wrap them for
+torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmx.so")
+
+MX_OK = 0
+STATUS_NAMES = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_MISALIGNED",
+                3: "MX_ERR_UNSUPPORTED", 4: "MX_ERR_CUDA", 5: "MX_ERR_TIMEOUT",
+                6: "MX_ERR_DEVICE_ARG"}
+FMT = {"e4m3": 0, "e5m2": 1}
+DTYPE = {"bf16": 0, "fp32": 1}
+AXIS = {"row": 1, "col": 2, "both": 3}
+RULE = {"floor": 0, "ceil": 1}
+
+EXPORTS = ("mx_scale_bytes", "mx_grouped_scale_bytes", "mx_quantize", "mx_quantize_grouped",
+           "mx_gemm", "mx_grouped_gemm", "mx_device_status", "mx_status_str",
+           "mx_set_wait_timeout_ns", "mx_selftest_wait_timeout")
+
+
+class MxError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+
+
+def _declare(lib):
+    c = ctypes
+    i64, i32, u64, vp = c.c_int64, c.c_int32, c.c_uint64, c.c_void_p
+    lib.mx_scale_bytes.argtypes = [i64, i64]
+    lib.mx_scale_bytes.restype = c.c_size_t
+    lib.mx_grouped_scale_bytes.argtypes = [i64, i32, i64]
+    lib.mx_grouped_scale_bytes.restype = c.c_size_t
+    lib.mx_quantize.argtypes = [vp, c.c_int, i64, i64, i64, c.c_int, c.c_int, c.c_int,
+                                vp, vp, vp, vp, vp]
+    lib.mx_quantize.restype = c.c_int
+    lib.mx_quantize_grouped.argtypes = [vp, c.c_int, i64, i64, i64, c.c_int, c.c_int, i32, vp,
+                                        vp, vp, vp]
+    lib.mx_quantize_grouped.restype = c.c_int
+    lib.mx_gemm.argtypes = [i64, i64, i64, vp, vp, c.c_int, vp, vp, c.c_int, vp, c.c_int, i64, vp]
+    lib.mx_gemm.restype = c.c_int
+    lib.mx_grouped_gemm.argtypes = [i32, vp, i64, i64, i64, vp, vp, c.c_int, vp, vp, c.c_int, vp,
+                                    c.c_int, vp]
+    lib.mx_grouped_gemm.restype = c.c_int
+    lib.mx_device_status.argtypes = [vp]
+    lib.mx_device_status.restype = c.c_int
+    lib.mx_status_str.argtypes = [c.c_int]
+    lib.mx_status_str.restype = c.c_char_p
+    lib.mx_set_wait_timeout_ns.argtypes = [u64]
+    lib.mx_set_wait_timeout_ns.restype = c.c_int
+    lib.mx_selftest_wait_timeout.argtypes = [u64, vp]
+    lib.mx_selftest_wait_timeout.restype = c.c_int
+
+
+def lib():
+    """The loaded libmx.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built; run `python -m mxfp8_block_scaled_mx_gb300.build`")
+        handle = ctypes.CDLL(LIB_PATH)
+        _declare(handle)
+        _lib = handle
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != MX_OK:
+        raise MxError(fn, status)
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+# ---------------------------------------------------------------- C-named calls
+
+def mx_scale_bytes(rows: int, k: int) -> int:
+    return int(lib().mx_scale_bytes(rows, k))
+
+
+def mx_grouped_scale_bytes(total_rows: int, groups: int, k: int) -> int:
+    return int(lib().mx_grouped_scale_bytes(total_rows, groups, k))
+
+
+def mx_quantize(x, x_dtype, rows, cols, ldx, fmt, axis, rule, q_row, s_row, q_col, s_col,
+                stream) -> int:
+    return lib().mx_quantize(x, x_dtype, rows, cols, ldx, fmt, axis, rule, q_row, s_row, q_col,
+                             s_col, stream)
+
+
+def mx_quantize_grouped(x, x_dtype, total_rows, cols, ldx, fmt, rule, groups, d_offsets, q, s,
+                        stream) -> int:
+    return lib().mx_quantize_grouped(x, x_dtype, total_rows, cols, ldx, fmt, rule, groups,
+                                     d_offsets, q, s, stream)
+
+
+def mx_gemm(m, n, k, a, sa, fa, b, sb, fb, y, y_dtype, ldy, stream) -> int:
+    return lib().mx_gemm(m, n, k, a, sa, fa, b, sb, fb, y, y_dtype, ldy, stream)
+
+
+def mx_grouped_gemm(groups, d_offsets, total_m, n, k, a, sa, fa, b, sb, fb, y, y_dtype,
+                    stream) -> int:
+    return lib().mx_grouped_gemm(groups, d_offsets, total_m, n, k, a, sa, fa, b, sb, fb, y,
+                                 y_dtype, stream)
+
+
+def mx_device_status(stream=None) -> int:
+    return lib().mx_device_status(_stream(stream))
+
+
+def mx_status_str(status: int) -> str:
+    return lib().mx_status_str(status).decode()
+
+
+def mx_set_wait_timeout_ns(ns: int) -> int:
+    return lib().mx_set_wait_timeout_ns(ns)
+
+
+def mx_selftest_wait_timeout(ns: int, stream=None) -> int:
+    return lib().mx_selftest_wait_timeout(ns, _stream(stream))
+
+
+# ---------------------------------------------------------------- tensor API
+
+@dataclass
+class MxTensor:
+    """MX operand: codes [rows, k] (K contiguous) and swizzled E8M0 scales."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    fmt: str
+
+    @property
+    def rows(self) -> int:
+        return self.codes.shape[-2]
+
+    @property
+    def k(self) -> int:
+        return self.codes.shape[-1]
+
+
+def quantize(x: torch.Tensor, fmt: str = "e4m3", axis: str = "row", rule: str = "floor",
+             stream=None):
+    """bf16 [rows, cols] -> MxTensor (axis 'row' or 'col') or a (row, col)
+    pair (axis 'both').  Column-wise codes come back as [cols, rows]."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda:
+        raise ValueError("x must be a 2-D bf16 CUDA tensor")
+    if x.stride(1) != 1:
+        raise ValueError("x must be row-major with unit column stride")
+    rows, cols = x.shape
+    dev = x.device
+    q_row = s_row = q_col = s_col = None
+    if axis in ("row", "both"):
+        q_row = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+        s_row = torch.empty(max(mx_scale_bytes(rows, cols), 1), dtype=torch.uint8, device=dev)
+    if axis in ("col", "both"):
+        q_col = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+        s_col = torch.empty(max(mx_scale_bytes(cols, rows), 1), dtype=torch.uint8, device=dev)
+    st = mx_quantize(_ptr(x), DTYPE["bf16"], rows, cols, x.stride(0), FMT[fmt], AXIS[axis],
+                     RULE[rule], _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col),
+                     _stream(stream))
+    _check("mx_quantize", st)
+    row = MxTensor(q_row, s_row, fmt) if q_row is not None else None
+    col = MxTensor(q_col, s_col, fmt) if q_col is not None else None
+    if axis == "row":
+        return row
+    if axis == "col":
+        return col
+    return row, col
+
+
+def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt: str = "e4m3",
+                     rule: str = "floor", stream=None) -> MxTensor:
+    """Rowwise quantization of expert-grouped tokens; offsets is a device
+    int32 tensor of groups+1 entries.  Scales use the per-group padded
+    layout that grouped_gemm reads."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
+        raise ValueError("x must be a row-major 2-D bf16 CUDA tensor")
+    if offsets.dtype != torch.int32 or not offsets.is_cuda:
+        raise ValueError("offsets must be a CUDA int32 tensor")
+    rows, cols = x.shape
+    groups = offsets.numel() - 1
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    s = torch.zeros(max(mx_grouped_scale_bytes(rows, groups, cols), 1), dtype=torch.uint8,
+                    device=x.device)
+    st = mx_quantize_grouped(_ptr(x), DTYPE["bf16"], rows, cols, x.stride(0), FMT[fmt],
+                             RULE[rule], groups, _ptr(offsets), _ptr(q), _ptr(s), _stream(stream))
+    _check("mx_quantize_grouped", st)
+    return MxTensor(q, s, fmt)
+
+
+def gemm(a: MxTensor, b: MxTensor, out_dtype: str = "bf16", out: torch.Tensor | None = None,
+         stream=None) -> torch.Tensor:
+    """y[m, n] = block-scaled A[m, k] * B[n, k]^T."""
+    m, k = a.codes.shape
+    n, k2 = b.codes.shape
+    if k != k2:
+        raise ValueError("K mismatch")
+    tdtype = torch.float32 if out_dtype == "fp32" else torch.bfloat16
+    if out is None:
+        out = torch.empty((m, n), dtype=tdtype, device=a.codes.device)
+    st = mx_gemm(m, n, k, _ptr(a.codes), _ptr(a.scales), FMT[a.fmt], _ptr(b.codes),
+                 _ptr(b.scales), FMT[b.fmt], _ptr(out), DTYPE[out_dtype], out.stride(0),
+                 _stream(stream))
+    _check("mx_gemm", st)
+    return out
+
+
+def grouped_gemm(a: MxTensor, offsets: torch.Tensor, b: MxTensor, out_dtype: str = "bf16",
+                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Per group g: y[o_g:o_{g+1}] = A[o_g:o_{g+1}] * B_g^T.  b.codes is
+    [groups, n, k]; b.scales holds groups consecutive swizzled matrices."""
+    total_m, k = a.codes.shape
+    groups, n, k2 = b.codes.shape
+    if k != k2 or offsets.numel() != groups + 1:
+        raise ValueError("shape mismatch")
+    tdtype = torch.float32 if out_dtype == "fp32" else torch.bfloat16
+    if out is None:
+        out = torch.empty((total_m, n), dtype=tdtype, device=a.codes.device)
+    st = mx_grouped_gemm(groups, _ptr(offsets), total_m, n, k, _ptr(a.codes), _ptr(a.scales),
+                         FMT[a.fmt], _ptr(b.codes), _ptr(b.scales), FMT[b.fmt], _ptr(out),
+                         DTYPE[out_dtype], _stream(stream))
+    _check("mx_grouped_gemm", st)
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronize and return (and clear) the device status word."""
+    return mx_device_status(stream)

@@ -1,0 +1,443 @@
+// gemm.cu -- block-scaled MXFP8 GEMM on the fifth-generation tensor cores.
+//
+// "Low-Precision GPU Programming" (leetllm.com), section "Scale ownership
+// and the GEMM dataflow": with 32-element blocks along K the scale product
+// of each block stays inside the outer sum,
+//     Y[i,j] = sum_b S_A[i,b] S_B[j,b] sum_{k in b} A~[i,k] B~[j,k],
+// and block-scaled matrix instructions consume the scale operands directly.
+// Here that instruction is tcgen05.mma.kind::mxf8f6f4.block_scale: one MMA
+// covers K = 32 (one scale block), takes E4M3/E5M2 operands from shared
+// memory and E8M0 scales from tensor memory, and accumulates in FP32 in
+// tensor memory.
+//
+// Structure (one persistent block of 6 warps per SM):
+//   warp 0      TMA producer: A and B code tiles (128-byte swizzle) with
+//               cp.async.bulk.tensor, the 512-byte scale units with
+//               cp.async.bulk, into a ring of kStages shared-memory slots
+//               guarded by full/empty mbarriers.
+//   warp 1      allocates tensor memory; one lane issues tcgen05.cp
+//               (scales -> tensor memory) and tcgen05.mma, and releases each
+//               slot with tcgen05.commit.
+//   warps 2..5  epilogue: tcgen05.ld of the FP32 accumulator, conversion to
+//               FP32/BF16 (RNE), staging through shared memory and 128-byte
+//               coalesced stores, masked at the matrix (or group) edge.
+// With 128-wide tiles the accumulator is double-buffered in tensor memory
+// so the epilogue of one tile overlaps the main loop of the next.
+//
+// Grouped (mixture-of-experts) mode walks (group, m-tile, n-tile) triples;
+// group offsets are read on the device and turned into a tile prefix by
+// every block, so the host never synchronizes.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "groups.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+#include "status.cuh"
+
+namespace mx {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;            // K elements (bytes) per pipeline stage = 4 scale blocks
+constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kBandM = 16;         // m-tiles per raster band (L2 reuse of B)
+constexpr uint32_t kTmemCols = 512;
+
+struct GroupSmem {
+  int32_t off[kMaxGroups + 1];
+  int32_t tiles[kMaxGroups + 1];
+  int32_t valid;
+};
+
+template <int BN, bool GROUPED>
+struct Cfg {
+  static constexpr int kStages = BN == 128 ? 6 : 4;
+  static constexpr int kAccStages = BN == 128 ? 2 : 1;
+  static constexpr int kABytes = BM * BK;
+  static constexpr int kBBytes = BN * BK;
+  static constexpr int kSfbUnits = BN / 128;
+  static constexpr int kSfaCols = 4;
+  static constexpr int kSfSlotCols = 4 + 4 * kSfbUnits;
+  static constexpr int kSfBaseCol = kAccStages * BN;
+  static_assert(kSfBaseCol + kStages * kSfSlotCols <= int(kTmemCols), "tensor memory budget");
+  // shared memory layout (offsets from a 1024-aligned base)
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffSfa = kOffB + kStages * kBBytes;
+  static constexpr int kOffSfb = kOffSfa + kStages * 512;
+  static constexpr int kOffEpi = kOffSfb + kStages * kSfbUnits * 512;
+  static constexpr int kOffBar = kOffEpi + kEpiWarps * 4096;
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccStages + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kOffGroup = kOffMisc + 64;
+  static constexpr int kSmemBytes =
+      kOffGroup + (GROUPED ? int(sizeof(GroupSmem)) : 0) + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+struct TileInfo {
+  int64_t m0;       // first row of A / Y
+  int64_t m_end;    // rows >= m_end are not stored
+  int64_t n0;       // first column of Y
+  int64_t b_row0;   // first row of the B tile in the [rows, k] B tensor
+  int64_t sfa_rt;   // 128-row scale tile of A
+  int64_t sfb_rt0;  // first 128-row scale tile of B
+  int64_t n_lim;    // columns >= n_lim are not stored (= n)
+};
+
+template <int BN, bool GROUPED>
+__device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t t, int64_t n_tiles,
+                                              const GroupSmem* gs) {
+  TileInfo ti;
+  int64_t m_blk, n_blk;
+  if constexpr (GROUPED) {
+    const int64_t mt = t / n_tiles;
+    n_blk = t - mt * n_tiles;
+    const int g = find_group(gs->tiles, p.groups, static_cast<int32_t>(mt));
+    m_blk = mt - gs->tiles[g];
+    ti.m0 = static_cast<int64_t>(gs->off[g]) + m_blk * BM;
+    ti.m_end = gs->off[g + 1];
+    ti.n0 = n_blk * BN;
+    ti.b_row0 = static_cast<int64_t>(g) * p.n + ti.n0;
+    ti.sfa_rt = mt;
+    ti.sfb_rt0 = ti.b_row0 / 128;
+  } else {
+    const int64_t m_tiles = (p.m + BM - 1) / BM;
+    const int64_t band_tiles = kBandM * n_tiles;
+    const int64_t band = t / band_tiles;
+    const int64_t within = t - band * band_tiles;
+    const int64_t m_in_band = ::min(static_cast<int64_t>(kBandM), m_tiles - band * kBandM);
+    n_blk = within / m_in_band;
+    m_blk = band * kBandM + (within - n_blk * m_in_band);
+    ti.m0 = m_blk * BM;
+    ti.m_end = p.m;
+    ti.n0 = n_blk * BN;
+    ti.b_row0 = ti.n0;
+    ti.sfa_rt = m_blk;
+    ti.sfb_rt0 = ti.n0 / 128;
+  }
+  ti.n_lim = p.n;
+  return ti;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int BN, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+  using C = Cfg<BN, GROUPED>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem + C::kOffA;
+  uint8_t* sB = smem + C::kOffB;
+  uint8_t* sSfa = smem + C::kOffSfa;
+  uint8_t* sSfb = smem + C::kOffSfb;
+  uint8_t* sEpi = smem + C::kOffEpi;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::kStages;
+  uint64_t* acc_full = bars + 2 * C::kStages;
+  uint64_t* acc_empty = acc_full + C::kAccStages;
+  uint64_t* mma_done = acc_empty + C::kAccStages;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
+
+  GroupSmem* gs = reinterpret_cast<GroupSmem*>(smem + C::kOffGroup);
+
+  const uint32_t warp = warp_id();
+  const uint32_t lane = lane_id();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int s = 0; s < C::kStages; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], 1);
+      }
+      for (int s = 0; s < C::kAccStages; ++s) {
+        mbar_init(&acc_full[s], 1);
+        mbar_init(&acc_empty[s], kEpiWarps * 32);
+      }
+      mbar_init(mma_done, 1);
+      *s_abort = 0u;
+      fence_mbarrier_init();
+      tma_prefetch_desc(&tmap_a);
+      tma_prefetch_desc(&tmap_b);
+    }
+    __syncwarp();
+    if constexpr (GROUPED) {
+      group_tile_prefix(p.offsets, p.groups, p.m, gs->off, gs->tiles, &gs->valid);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *s_tmem;
+
+  const int64_t n_tiles = (p.n + BN - 1) / BN;
+  int64_t num_tiles;
+  if constexpr (GROUPED) {
+    if (!gs->valid) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) record_device_status(p.status, MX_DEV_BAD_OFFSETS);
+      num_tiles = 0;
+    } else {
+      num_tiles = static_cast<int64_t>(gs->tiles[p.groups]) * n_tiles;
+    }
+  } else {
+    num_tiles = ((p.m + BM - 1) / BM) * n_tiles;
+  }
+  const int64_t k_tiles = (p.k + BK - 1) / BK;
+  const int32_t k_blocks = static_cast<int32_t>(p.k / 32);
+  const int64_t scale_tiles_k = k_tiles;  // 512-byte scale units per 128-row tile
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t stage = 0, phase = 0;
+    uint32_t fills[C::kStages];
+#pragma unroll
+    for (int s = 0; s < C::kStages; ++s) fills[s] = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      const TileInfo ti = tile_info<BN, GROUPED>(p, t, n_tiles, gs);
+      int sfb_units = 0;
+#pragma unroll
+      for (int j = 0; j < C::kSfbUnits; ++j)
+        if (ti.n0 + 128 * j < p.n) ++sfb_units;
+      const uint32_t tx = C::kABytes + C::kBBytes + 512u + 512u * sfb_units;
+      for (int64_t kt = 0; kt < k_tiles; ++kt) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[stage], tx);
+        fills[stage]++;
+        tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full[stage], static_cast<int32_t>(kt * BK),
+                    static_cast<int32_t>(ti.m0));
+        tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full[stage], static_cast<int32_t>(kt * BK),
+                    static_cast<int32_t>(ti.b_row0));
+        bulk_load(sSfa + stage * 512, p.sa + (ti.sfa_rt * scale_tiles_k + kt) * 512, 512,
+                  &full[stage]);
+        for (int j = 0; j < sfb_units; ++j)
+          bulk_load(sSfb + (stage * C::kSfbUnits + j) * 512,
+                    p.sb + ((ti.sfb_rt0 + j) * scale_tiles_k + kt) * 512, 512, &full[stage]);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // Drain: every issued copy must land before the block exits.
+    for (int s = 0; s < C::kStages; ++s)
+      if (fills[s])
+        mbar_wait(&full[s], (fills[s] - 1) & 1u, s_abort, p.status, p.wait_limit_ns, true);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    uint32_t stage = 0, phase = 0;
+    uint32_t acc = 0, acc_phase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) break;
+      tc_fence_after_sync();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int64_t kt = 0; kt < k_tiles; ++kt) {
+        if (!mbar_wait(&full[stage], phase, s_abort, p.status, p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t sf_tmem = tmem_base + C::kSfBaseCol + stage * C::kSfSlotCols;
+        tc_cp_32x128b_warpx4(sf_tmem, smem_desc(smem_u32(sSfa + stage * 512), 0, 128, 0));
+#pragma unroll
+        for (int j = 0; j < C::kSfbUnits; ++j)
+          tc_cp_32x128b_warpx4(sf_tmem + C::kSfaCols + 4 * j,
+                               smem_desc(smem_u32(sSfb + (stage * C::kSfbUnits + j) * 512), 0,
+                                         128, 0));
+        const uint64_t adesc = smem_desc(smem_u32(sA + stage * C::kABytes), 16, 1024, 2);
+        const uint64_t bdesc = smem_desc(smem_u32(sB + stage * C::kBBytes), 16, 1024, 2);
+        const int32_t kb_here = ::min(4, k_blocks - static_cast<int32_t>(kt) * 4);
+        for (int32_t kb = 0; kb < kb_here; ++kb) {
+          const uint32_t idesc = mxf8_idesc(p.fa, p.fb, BM, BN, kb, kb);
+          // +32 bytes along K inside the 128-byte swizzled row = +2 in the
+          // 16-byte address field.
+          tc_mma_mxf8(d_tmem, adesc + 2u * kb, bdesc + 2u * kb, idesc, sf_tmem,
+                      sf_tmem + C::kSfaCols, (kt > 0 || kb > 0) ? 1u : 0u);
+        }
+        tc_commit(&empty[stage]);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      tc_commit(&acc_full[acc]);
+      if (++acc == C::kAccStages) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    // Every issued tensor-core operation must finish before tensor memory
+    // is released.
+    tc_commit(mma_done);
+    mbar_wait(mma_done, 0, s_abort, p.status, p.wait_limit_ns, true);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t q = warp & 3u;  // tensor-memory lane quarter of this warp
+    uint8_t* stage_buf = sEpi + (warp - 2) * 4096;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      const TileInfo ti = tile_info<BN, GROUPED>(p, t, n_tiles, gs);
+      const bool got = mbar_wait(&acc_full[acc], acc_phase, s_abort, p.status, p.wait_limit_ns);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after_sync();
+      const uint32_t t_row = tmem_base + ((q * 32u) << 16) + acc * BN;
+      const int64_t row_base = ti.m0 + q * 32;
+      uint8_t* my_row = stage_buf + lane * 128;
+      if (p.y_fp32) {
+        float* y = static_cast<float*>(p.y);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(my_row + ((j ^ (lane & 7)) * 16)) =
+                make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int rr = it * 4 + (lane >> 3);
+            const int j = lane & 7;
+            const int64_t grow = row_base + rr;
+            const int64_t gcol = ti.n0 + c * 32 + j * 4;
+            if (grow < ti.m_end && gcol < ti.n_lim) {
+              const uint4 v =
+                  *reinterpret_cast<const uint4*>(stage_buf + rr * 128 + ((j ^ (rr & 7)) * 16));
+              *reinterpret_cast<uint4*>(y + grow * p.ldy + gcol) = v;
+            }
+          }
+          __syncwarp();
+        }
+      } else {
+        uint16_t* y = static_cast<uint16_t*>(p.y);
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(t_row + c * 64, r0);
+          tmem_ld_32x32b_x32(t_row + c * 64 + 32, r1);
+          tmem_ld_wait();
+          uint32_t w[32];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+            w[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(my_row + ((j ^ (lane & 7)) * 16)) =
+                make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int rr = it * 4 + (lane >> 3);
+            const int j = lane & 7;
+            const int64_t grow = row_base + rr;
+            const int64_t gcol = ti.n0 + c * 64 + j * 8;
+            if (grow < ti.m_end && gcol < ti.n_lim) {
+              const uint4 v =
+                  *reinterpret_cast<const uint4*>(stage_buf + rr * 128 + ((j ^ (rr & 7)) * 16));
+              *reinterpret_cast<uint4*>(y + grow * p.ldy + gcol) = v;
+            }
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&acc_empty[acc]);
+      if (++acc == C::kAccStages) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+__global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+    // Nothing ever arrives on `bar`: the wait must give up by itself.
+    mbar_wait(&bar, 0, &abort_flag, status, limit_ns);
+  }
+}
+
+template <int BN, bool GROUPED>
+cudaError_t launch_impl(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                        int num_sms, cudaStream_t stream) {
+  using C = Cfg<BN, GROUPED>;
+  auto kern = mx_gemm_kernel<BN, GROUPED>;
+  // Per device, the attribute is idempotent and cheap; set it every time.
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  int64_t tiles;
+  const int64_t n_tiles = (p.n + BN - 1) / BN;
+  if (GROUPED) {
+    tiles = ((p.m + BM - 1) / BM + p.groups) * n_tiles;
+  } else {
+    tiles = ((p.m + BM - 1) / BM) * n_tiles;
+  }
+  if (tiles == 0) return cudaSuccess;
+  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_default_block_n(const GemmParams& p) {
+  (void)p;
+  return 128;
+}
+
+cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                        int block_n, int num_sms, cudaStream_t stream) {
+  const bool grouped = p.groups > 0;
+  if (block_n == 256) {
+    return grouped ? launch_impl<256, true>(p, ta, tb, num_sms, stream)
+                   : launch_impl<256, false>(p, ta, tb, num_sms, stream);
+  }
+  return grouped ? launch_impl<128, true>(p, ta, tb, num_sms, stream)
+                 : launch_impl<128, false>(p, ta, tb, num_sms, stream);
+}
+
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace mx

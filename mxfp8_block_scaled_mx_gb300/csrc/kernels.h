@@ -1,0 +1,57 @@
+// kernels.h -- launch interface between the C-ABI layer (mx_api.cu) and the
+// CUDA kernels (quantize.cu, gemm.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace mx {
+
+struct QuantizeParams {
+  const uint16_t* x;   // bf16 bit patterns, [rows, cols], leading dimension ldx
+  int64_t rows;
+  int64_t cols;
+  int64_t ldx;
+  uint8_t* q_row;      // [rows, cols] codes or nullptr
+  uint8_t* s_row;      // swizzled scales of the [rows, cols] operand
+  uint8_t* q_col;      // [cols, rows] codes or nullptr
+  uint8_t* s_col;      // swizzled scales of the [cols, rows] operand
+  int32_t fmt;         // 0 = E4M3, 1 = E5M2
+  int32_t rule;        // 0 = floor, 1 = ceil
+  const int32_t* offsets;  // grouped rowwise only: device int32[groups + 1]
+  int32_t groups;
+  uint32_t* status;    // device status word
+};
+
+cudaError_t launch_quantize(const QuantizeParams& p, cudaStream_t stream);
+cudaError_t launch_quantize_grouped(const QuantizeParams& p, cudaStream_t stream);
+
+struct GemmParams {
+  int64_t m;           // rows of A and Y (grouped: total rows)
+  int64_t n;           // rows of each B (columns of Y)
+  int64_t k;           // contraction length, multiple of 32
+  const uint8_t* sa;   // swizzled scales of A (grouped: per-group padded)
+  const uint8_t* sb;   // swizzled scales of B (grouped: one matrix per group)
+  void* y;
+  int64_t ldy;         // elements
+  int32_t y_fp32;      // 1: FP32 output, 0: BF16 output
+  int32_t fa;          // 0 = E4M3, 1 = E5M2
+  int32_t fb;
+  const int32_t* offsets;  // grouped only: device int32[groups + 1]
+  int32_t groups;          // 0 for the dense GEMM
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+};
+
+// Tile width along N of the GEMM kernel: 128 (double-buffered accumulator)
+// or 256 (single accumulator).  Returns 0 if unsupported.
+int gemm_default_block_n(const GemmParams& p);
+
+cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                        int block_n, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace mx

@@ -1,0 +1,274 @@
+// mx_api.cu -- the C ABI (include/mx.h): argument validation, TMA tensor
+// map encoding through the driver entry point, device status word, and
+// kernel launches on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "mx.h"
+
+namespace {
+
+// The device status word (one per device, in this module's device memory).
+__device__ uint32_t g_status_word;
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  uint32_t* status = nullptr;  // device address of g_status_word on this device
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+uint64_t g_wait_ns = kDefaultWaitNs;
+
+mx_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MX_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MX_ERR_CUDA;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return MX_ERR_CUDA;
+    st.status = static_cast<uint32_t*>(addr);
+    if (cudaMemset(st.status, 0, sizeof(uint32_t)) != cudaSuccess) return MX_ERR_CUDA;
+    st.ready = true;
+  }
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return MX_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = &st;
+  return MX_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_fmt(mx_fmt f) { return f == MX_E4M3 || f == MX_E5M2; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// 2-D uint8 tensor map over a [rows, inner] row-major matrix with row stride
+// `stride` bytes, tile box {128 bytes, box_rows}, 128-byte swizzle, zero
+// fill outside the matrix.
+mx_status encode_codes_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows,
+                           int64_t stride, uint32_t box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride)};
+  cuuint32_t box[2] = {128u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
+int block_n_choice(const mx::GemmParams& p) {
+  const char* env = std::getenv("MX_GEMM_BLOCK_N");
+  if (env) {
+    const int v = std::atoi(env);
+    if (v == 128 || v == 256) return v;
+  }
+  return mx::gemm_default_block_n(p);
+}
+
+mx_status gemm_common(int64_t m, int64_t n, int64_t k, const uint8_t* a, const uint8_t* sa,
+                      mx_fmt fa, const uint8_t* b, const uint8_t* sb, mx_fmt fb, void* y,
+                      mx_dtype y_dtype, int64_t ldy, int32_t groups, const int32_t* d_offsets,
+                      int64_t b_rows, cudaStream_t stream) {
+  if (!a || !sa || !b || !sb || !y) return MX_ERR_INVALID_ARG;
+  if (m < 0 || n <= 0 || k < 32 || k % 32 != 0 || n % 8 != 0 || ldy < n) return MX_ERR_INVALID_ARG;
+  if (!valid_fmt(fa) || !valid_fmt(fb)) return MX_ERR_INVALID_ARG;
+  if (y_dtype != MX_BF16 && y_dtype != MX_FP32) return MX_ERR_INVALID_ARG;
+  if (m > INT32_MAX || b_rows > INT32_MAX || k > INT32_MAX) return MX_ERR_UNSUPPORTED;
+  const int64_t elt = y_dtype == MX_FP32 ? 4 : 2;
+  if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(y) ||
+      (ldy * elt) % 16 != 0)
+    return MX_ERR_MISALIGNED;
+  DeviceState* st = nullptr;
+  mx_status s = device_state(&st);
+  if (s != MX_OK) return s;
+  if (m == 0) return MX_OK;
+
+  mx::GemmParams p{};
+  p.m = m;
+  p.n = n;
+  p.k = k;
+  p.sa = sa;
+  p.sb = sb;
+  p.y = y;
+  p.ldy = ldy;
+  p.y_fp32 = y_dtype == MX_FP32 ? 1 : 0;
+  p.fa = fa;
+  p.fb = fb;
+  p.offsets = d_offsets;
+  p.groups = groups;
+  p.status = st->status;
+  p.wait_limit_ns = g_wait_ns;
+  const int block_n = block_n_choice(p);
+
+  CUtensorMap ta, tb;
+  if ((s = encode_codes_map(&ta, a, k, m, k, 128)) != MX_OK) return s;
+  if ((s = encode_codes_map(&tb, b, k, b_rows, k, static_cast<uint32_t>(block_n))) != MX_OK)
+    return s;
+  if (mx::launch_gemm(p, ta, tb, block_n, st->num_sms, stream) != cudaSuccess) return MX_ERR_CUDA;
+  return MX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mx_scale_bytes(int64_t rows, int64_t k) {
+  if (rows < 0 || k < 0 || k % 32 != 0) return 0;
+  return static_cast<size_t>(ceil_div(rows, 128) * 128 * ceil_div(k / 32, 4) * 4);
+}
+
+size_t mx_grouped_scale_bytes(int64_t total_rows, int32_t groups, int64_t k) {
+  if (total_rows < 0 || groups < 0 || k < 0 || k % 32 != 0) return 0;
+  return static_cast<size_t>((ceil_div(total_rows, 128) + groups) * 128 * ceil_div(k, 128) * 4);
+}
+
+mx_status mx_quantize(const void* x, mx_dtype x_dtype, int64_t rows, int64_t cols, int64_t ldx,
+                      mx_fmt fmt, mx_axis axis, mx_scale_rule rule, uint8_t* q_row,
+                      uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, cudaStream_t stream) {
+  if (x_dtype != MX_BF16) return x_dtype == MX_FP32 ? MX_ERR_UNSUPPORTED : MX_ERR_INVALID_ARG;
+  if (!valid_fmt(fmt) || (rule != MX_SCALE_FLOOR && rule != MX_SCALE_CEIL))
+    return MX_ERR_INVALID_ARG;
+  if (axis != MX_ROWWISE && axis != MX_COLWISE && axis != MX_BOTH) return MX_ERR_INVALID_ARG;
+  const bool row = axis & MX_ROWWISE;
+  const bool col = axis & MX_COLWISE;
+  if (!x || (row && (!q_row || !s_row)) || (col && (!q_col || !s_col))) return MX_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || ldx < cols || cols % 8 != 0) return MX_ERR_INVALID_ARG;
+  if (row && cols % 32 != 0) return MX_ERR_INVALID_ARG;
+  if (col && rows % 32 != 0) return MX_ERR_INVALID_ARG;
+  if (ceil_div(cols, 128) > 65535) return MX_ERR_UNSUPPORTED;
+  if (!aligned16(x) || ldx % 8 != 0) return MX_ERR_MISALIGNED;
+  if ((row && (!aligned16(q_row) || !aligned16(s_row))) ||
+      (col && (!aligned16(q_col) || !aligned16(s_col))))
+    return MX_ERR_MISALIGNED;
+  DeviceState* st = nullptr;
+  mx_status s = device_state(&st);
+  if (s != MX_OK) return s;
+  mx::QuantizeParams p{};
+  p.x = static_cast<const uint16_t*>(x);
+  p.rows = rows;
+  p.cols = cols;
+  p.ldx = ldx;
+  p.q_row = row ? q_row : nullptr;
+  p.s_row = row ? s_row : nullptr;
+  p.q_col = col ? q_col : nullptr;
+  p.s_col = col ? s_col : nullptr;
+  p.fmt = fmt;
+  p.rule = rule;
+  p.status = st->status;
+  return mx::launch_quantize(p, stream) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+mx_status mx_quantize_grouped(const void* x, mx_dtype x_dtype, int64_t total_rows, int64_t cols,
+                              int64_t ldx, mx_fmt fmt, mx_scale_rule rule, int32_t groups,
+                              const int32_t* d_offsets, uint8_t* q, uint8_t* s,
+                              cudaStream_t stream) {
+  if (x_dtype != MX_BF16) return x_dtype == MX_FP32 ? MX_ERR_UNSUPPORTED : MX_ERR_INVALID_ARG;
+  if (!valid_fmt(fmt) || (rule != MX_SCALE_FLOOR && rule != MX_SCALE_CEIL))
+    return MX_ERR_INVALID_ARG;
+  if (!x || !q || !s || !d_offsets) return MX_ERR_INVALID_ARG;
+  if (groups < 1 || groups > 1024) return MX_ERR_INVALID_ARG;
+  if (total_rows < 0 || total_rows > INT32_MAX || cols < 0 || cols % 32 != 0 || ldx < cols)
+    return MX_ERR_INVALID_ARG;
+  if (ceil_div(cols, 128) > 65535) return MX_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(s) || ldx % 8 != 0) return MX_ERR_MISALIGNED;
+  DeviceState* st = nullptr;
+  mx_status status = device_state(&st);
+  if (status != MX_OK) return status;
+  mx::QuantizeParams p{};
+  p.x = static_cast<const uint16_t*>(x);
+  p.rows = total_rows;
+  p.cols = cols;
+  p.ldx = ldx;
+  p.q_row = q;
+  p.s_row = s;
+  p.fmt = fmt;
+  p.rule = rule;
+  p.offsets = d_offsets;
+  p.groups = groups;
+  p.status = st->status;
+  return mx::launch_quantize_grouped(p, stream) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+mx_status mx_gemm(int64_t m, int64_t n, int64_t k, const uint8_t* a, const uint8_t* sa, mx_fmt fa,
+                  const uint8_t* b, const uint8_t* sb, mx_fmt fb, void* y, mx_dtype y_dtype,
+                  int64_t ldy, cudaStream_t stream) {
+  return gemm_common(m, n, k, a, sa, fa, b, sb, fb, y, y_dtype, ldy, 0, nullptr, n, stream);
+}
+
+mx_status mx_grouped_gemm(int32_t groups, const int32_t* d_offsets, int64_t total_m, int64_t n,
+                          int64_t k, const uint8_t* a, const uint8_t* sa, mx_fmt fa,
+                          const uint8_t* b, const uint8_t* sb, mx_fmt fb, void* y,
+                          mx_dtype y_dtype, cudaStream_t stream) {
+  if (groups < 1 || groups > 1024 || !d_offsets) return MX_ERR_INVALID_ARG;
+  if (n % 128 != 0) return MX_ERR_INVALID_ARG;
+  return gemm_common(total_m, n, k, a, sa, fa, b, sb, fb, y, y_dtype, n, groups, d_offsets,
+                     static_cast<int64_t>(groups) * n, stream);
+}
+
+mx_status mx_device_status(cudaStream_t stream) {
+  DeviceState* st = nullptr;
+  mx_status s = device_state(&st);
+  if (s != MX_OK) return s;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MX_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, st->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MX_ERR_CUDA;
+  if (word != 0 && cudaMemset(st->status, 0, sizeof(word)) != cudaSuccess) return MX_ERR_CUDA;
+  if (word & 1u) return MX_ERR_TIMEOUT;
+  if (word & 2u) return MX_ERR_DEVICE_ARG;
+  return MX_OK;
+}
+
+mx_status mx_set_wait_timeout_ns(uint64_t ns) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_wait_ns = ns == 0 ? kDefaultWaitNs : ns;
+  return MX_OK;
+}
+
+mx_status mx_selftest_wait_timeout(uint64_t ns, cudaStream_t stream) {
+  if (ns == 0 || ns > 10000000000ull) return MX_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  mx_status s = device_state(&st);
+  if (s != MX_OK) return s;
+  return mx::launch_wait_selftest(st->status, ns, stream) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+const char* mx_status_str(mx_status status) {
+  switch (status) {
+    case MX_OK: return "MX_OK";
+    case MX_ERR_INVALID_ARG: return "MX_ERR_INVALID_ARG";
+    case MX_ERR_MISALIGNED: return "MX_ERR_MISALIGNED";
+    case MX_ERR_UNSUPPORTED: return "MX_ERR_UNSUPPORTED";
+    case MX_ERR_CUDA: return "MX_ERR_CUDA";
+    case MX_ERR_TIMEOUT: return "MX_ERR_TIMEOUT";
+    case MX_ERR_DEVICE_ARG: return "MX_ERR_DEVICE_ARG";
+  }
+  return "MX_ERR_UNKNOWN";
+}
+
+}  // extern "C"

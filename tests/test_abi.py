@@ -1,0 +1,104 @@
+"""Host-only checks of the C ABI (no GPU): the library loads, exports every
+symbol include/mx.h declares, computes buffer sizes, and rejects invalid
+arguments on the host before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mxcheck import ROOT, ensure_built
+
+HEADER = os.path.join(ROOT, "include", "mx.h")
+
+
+@pytest.fixture(scope="module")
+def mx():
+    ensure_built()
+    import mxfp8_block_scaled_mx_gb300 as mx
+    return mx
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mx_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(mx):
+    names = declared_functions()
+    assert len(names) >= 10
+    handle = ctypes.CDLL(mx.LIB_PATH)
+    for name in names:
+        assert hasattr(handle, name), name
+    assert set(names) == set(mx.EXPORTS)
+
+
+def test_scale_bytes(mx):
+    assert mx.mx_scale_bytes(256, 512) == 256 * 16
+    assert mx.mx_scale_bytes(1, 32) == 128 * 4
+    assert mx.mx_scale_bytes(130, 160) == 256 * 8
+    assert mx.mx_scale_bytes(16384, 7168) == 16384 * 224
+    assert mx.mx_scale_bytes(10, 33) == 0
+    assert mx.mx_grouped_scale_bytes(65536, 64, 7168) == (512 + 64) * 128 * 224
+    assert mx.mx_status_str(0) == "MX_OK"
+    assert mx.mx_status_str(5) == "MX_ERR_TIMEOUT"
+
+
+FAKE = 0x10000  # an aligned non-null address; validation rejects before any use
+
+
+def test_quantize_rejects_bad_arguments_on_the_host(mx):
+    q = mx.mx_quantize
+    s = 0
+    # K (cols) not a multiple of 32 for rowwise
+    assert q(FAKE, 0, 64, 40, 40, 0, 1, 0, FAKE, FAKE, None, None, s) == 1
+    # rows not a multiple of 32 for colwise
+    assert q(FAKE, 0, 40, 64, 64, 0, 2, 0, None, None, FAKE, FAKE, s) == 1
+    # bad enums
+    assert q(FAKE, 0, 64, 64, 64, 7, 1, 0, FAKE, FAKE, None, None, s) == 1
+    assert q(FAKE, 0, 64, 64, 64, 0, 4, 0, FAKE, FAKE, None, None, s) == 1
+    assert q(FAKE, 0, 64, 64, 64, 0, 1, 9, FAKE, FAKE, None, None, s) == 1
+    # fp32 input is a valid type but not implemented
+    assert q(FAKE, 1, 64, 64, 64, 0, 1, 0, FAKE, FAKE, None, None, s) == 3
+    # null outputs
+    assert q(FAKE, 0, 64, 64, 64, 0, 1, 0, None, FAKE, None, None, s) == 1
+    assert q(None, 0, 64, 64, 64, 0, 1, 0, FAKE, FAKE, None, None, s) == 1
+    # ldx < cols
+    assert q(FAKE, 0, 64, 64, 32, 0, 1, 0, FAKE, FAKE, None, None, s) == 1
+    # misaligned input pointer / leading dimension
+    assert q(FAKE + 2, 0, 64, 64, 64, 0, 1, 0, FAKE, FAKE, None, None, s) == 2
+    assert q(FAKE, 0, 64, 64, 68, 0, 1, 0, FAKE, FAKE, None, None, s) == 2
+    assert q(FAKE, 0, 64, 64, 64, 0, 1, 0, FAKE + 8, FAKE, None, None, s) == 2
+
+
+def test_gemm_rejects_bad_arguments_on_the_host(mx):
+    g = mx.mx_gemm
+    s = 0
+    ok = dict(m=64, n=64, k=64)
+    assert g(64, 64, 48, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # k % 32
+    assert g(64, 64, 0, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1       # k == 0
+    assert g(64, 60, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # n % 8
+    assert g(64, 64, 64, FAKE, FAKE, 2, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # fmt
+    assert g(64, 64, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 5, 64, s) == 1      # out dtype
+    assert g(64, 64, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 32, s) == 1      # ldy < n
+    assert g(64, 64, 64, None, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # null
+    assert g(64, 64, 64, FAKE + 4, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 2  # misaligned
+    assert g(64, 64, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 68, s) == 2      # ldy*2 % 16
+    assert ok
+
+
+def test_grouped_calls_reject_bad_arguments_on_the_host(mx):
+    gg = mx.mx_grouped_gemm
+    assert gg(0, FAKE, 64, 128, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 0) == 1      # groups
+    assert gg(2000, FAKE, 64, 128, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 0) == 1   # > 1024
+    assert gg(4, None, 64, 128, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 0) == 1      # offsets
+    assert gg(4, FAKE, 64, 136, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 0) == 1      # n % 128
+    qg = mx.mx_quantize_grouped
+    assert qg(FAKE, 0, 64, 64, 64, 0, 0, 0, FAKE, FAKE, FAKE, 0) == 1                  # groups
+    assert qg(FAKE, 0, 64, 48, 48, 0, 0, 4, FAKE, FAKE, FAKE, 0) == 1                  # cols % 32
+    assert qg(FAKE, 0, 64, 64, 64, 0, 0, 4, None, FAKE, FAKE, 0) == 1                  # offsets
+
+
+def test_selftest_rejects_zero_limit(mx):
+    assert mx.mx_selftest_wait_timeout(0, 0) == 1
