@@ -1,0 +1,541 @@
+"""Benchmark of the MXFP8 training matmul on GB300.
+
+Default workload (one "step"): the dense forward layer M=16384 tokens,
+K=7168, N=18432 -- MX-quantize X rowwise (E4M3), MX-quantize W columnwise
+(E4M3), block-scaled GEMM with BF16 output, all through the C ABI.  The
+line's value is the step's GEMM work (2MNK) over the step time in TFLOP/s.
+Inputs are larger than L2 (X 235 MB, W 264 MB, Y 604 MB), so every step
+streams from HBM.
+
+The same JSON line carries per-kernel measurements of every hot-path row
+(quantize bandwidth sweep, dense forward / dgrad / wgrad GEMMs, the MoE
+grouped GEMM), each against its roofline, the end-to-end number with host
+buffers, SM clocks sampled during the timed region, and the CPU oracle
+timed on a bounded sample as a reported baseline.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun each rank runs its own batch (weak scaling, no collective
+on the data path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("MXFP8 GEMM TFLOP/s and % dense MXFP8 peak; quantize GB/s and % HBM peak (1 GB300)")
+UNIT = "TFLOP/s"
+FWD = dict(m=16384, n=18432, k=7168)
+WORKLOAD = "dense forward layer: quantize X[16384x7168] rowwise + W[7168x18432] colwise " \
+           "(MXFP8 E4M3, 32-blocks, E8M0) + block-scaled GEMM, BF16 out"
+NOMINAL_FP8_OVER_BF16 = 2.0            # 4.5 / 2.25 PFLOP/s dense, nominal ratio
+REF_ROWS, REF_COLS = 32, 256   # per-step sample of the reference (oracle) arm
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 100 ms while the timed region runs."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx_, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx_.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() in ("active", "0x1", "1", "yes"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        busy = [s for s in sm if s >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx_) if mx_ else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- device helpers
+
+def setup_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """Largest value over all ranks (the slowest rank sets the step time)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+class ForwardLayer:
+    """Preallocated buffers and the three C-ABI calls of one forward step."""
+
+    def __init__(self, mx, x, w, stream):
+        import torch
+        self.mx = mx
+        m, k = x.shape
+        k2, n = w.shape
+        assert k == k2
+        self.m, self.n, self.k = m, n, k
+        dev = x.device
+        self.x, self.w = x, w
+        self.qx = torch.empty((m, k), dtype=torch.uint8, device=dev)
+        self.sx = torch.empty(mx.mx_scale_bytes(m, k), dtype=torch.uint8, device=dev)
+        self.qw = torch.empty((n, k), dtype=torch.uint8, device=dev)
+        self.sw = torch.empty(mx.mx_scale_bytes(n, k), dtype=torch.uint8, device=dev)
+        self.y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        self.stream = stream
+        self.h = int(stream.cuda_stream)
+
+    def quantize_x(self):
+        mx = self.mx
+        st = mx.mx_quantize(self.x.data_ptr(), 0, self.m, self.k, self.k, 0, 1, 0,
+                            self.qx.data_ptr(), self.sx.data_ptr(), None, None, self.h)
+        assert st == 0, st
+
+    def quantize_w(self):
+        mx = self.mx
+        st = mx.mx_quantize(self.w.data_ptr(), 0, self.k, self.n, self.n, 0, 2, 0, None, None,
+                            self.qw.data_ptr(), self.sw.data_ptr(), self.h)
+        assert st == 0, st
+
+    def gemm(self):
+        mx = self.mx
+        st = mx.mx_gemm(self.m, self.n, self.k, self.qx.data_ptr(), self.sx.data_ptr(), 0,
+                        self.qw.data_ptr(), self.sw.data_ptr(), 0, self.y.data_ptr(), 0, self.n,
+                        self.h)
+        assert st == 0, st
+
+    def step(self):
+        self.quantize_x()
+        self.quantize_w()
+        self.gemm()
+
+    launches_per_step = 3
+
+
+def time_kernel(fn, stream, reps: int, warmup: int = 3) -> float:
+    """Mean duration (ms) of fn() over reps launches, CUDA events on `stream`."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in times)
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+# ---------------------------------------------------------------- per-row measurements
+
+def measure_rows(mx, peaks, dev, stream):
+    """Per-kernel measurements of the other hot-path rows (rank 0, N=1)."""
+    import torch
+    from mxfp8_block_scaled_mx_gb300 import workloads as W
+    h = int(stream.cuda_stream)
+    out = {}
+    hbm = peaks["hbm_gbs"]
+    fp8_peak = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
+    scrub = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    # quantize bandwidth sweep: 4096x4096 (fits in L2: flush between runs) and 16384x8192
+    for (r, c), seed in (((4096, 4096), 0), ((16384, 8192), 1)):
+        x = W.quantize_sweep((r, c), seed=seed, device=dev)
+        qr = torch.empty((r, c), dtype=torch.uint8, device=dev)
+        sr = torch.empty(mx.mx_scale_bytes(r, c), dtype=torch.uint8, device=dev)
+        qc = torch.empty((c, r), dtype=torch.uint8, device=dev)
+        sc = torch.empty(mx.mx_scale_bytes(c, r), dtype=torch.uint8, device=dev)
+        for mode, axis, bpe in (("row", 1, 3.03125), ("col", 2, 3.03125), ("both", 3, 4.0625)):
+            def q():
+                st = mx.mx_quantize(x.data_ptr(), 0, r, c, c, 0, axis, 0,
+                                    qr.data_ptr() if axis & 1 else None,
+                                    sr.data_ptr() if axis & 1 else None,
+                                    qc.data_ptr() if axis & 2 else None,
+                                    sc.data_ptr() if axis & 2 else None, h)
+                assert st == 0
+            ms = []
+            for _ in range(20):
+                flush_l2(scrub)
+                ms.append(time_kernel(q, stream, 1, warmup=0 if ms else 3))
+            t = statistics.median(ms)
+            gbs = r * c * bpe / (t * 1e-3) / 1e9
+            out[f"quantize_{r}x{c}_{mode}"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
+                                               "frac_hbm": round(gbs / hbm, 3),
+                                               "bytes_per_elem": bpe}
+        del x, qr, sr, qc, sc
+
+    # backward GEMMs (FP32 out) and the MoE grouped GEMM
+    x, w = W.dense_forward(device=dev)
+    dy = W.dense_grad_output(device=dev)
+    rq = mx.quantize(dy, "e5m2", "row", stream=stream)
+    wq = mx.quantize(w, "e4m3", "row", stream=stream)
+    dx = torch.empty((dy.shape[0], w.shape[0]), dtype=torch.float32, device=dev)
+    t = time_kernel(lambda: mx.gemm(rq, wq, "fp32", out=dx, stream=stream), stream, 10)
+    fl = 2 * dy.shape[0] * w.shape[0] * dy.shape[1]
+    out["dgrad_16384x7168x18432_e5m2xe4m3_fp32"] = {
+        "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
+        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
+    del rq, wq, dx
+    xq = mx.quantize(x, "e4m3", "col", stream=stream)
+    dq = mx.quantize(dy, "e5m2", "col", stream=stream)
+    dw = torch.empty((x.shape[1], dy.shape[1]), dtype=torch.float32, device=dev)
+    t = time_kernel(lambda: mx.gemm(xq, dq, "fp32", out=dw, stream=stream), stream, 10)
+    fl = 2 * x.shape[1] * dy.shape[1] * x.shape[0]
+    out["wgrad_7168x18432x16384_e4m3xe5m2_fp32"] = {
+        "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
+        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
+    del xq, dq, dw, x, w, dy
+
+    xm, wm, offsets = W.moe_inputs(device=dev)
+    e, n, k = wm.shape
+    d_off = torch.from_numpy(offsets).to(dev)
+    qa = mx.quantize_grouped(xm, d_off, "e4m3", stream=stream)
+    qw = mx.quantize(wm.view(e * n, k), "e4m3", "row", stream=stream)
+    qb = mx.MxTensor(qw.codes.view(e, n, k), qw.scales, "e4m3")
+    ym = torch.empty((xm.shape[0], n), dtype=torch.bfloat16, device=dev)
+    t = time_kernel(lambda: mx.grouped_gemm(qa, d_off, qb, "bf16", out=ym, stream=stream),
+                    stream, 10)
+    fl = 2 * xm.shape[0] * n * k
+    sizes = [int(v) for v in (offsets[1:] - offsets[:-1])]
+    out["moe_grouped_64x(2048x7168)_65536tok_bf16"] = {
+        "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
+        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3),
+        "group_sizes_min_max": [min(sizes), max(sizes)], "empty_groups": sizes.count(0)}
+    t = time_kernel(lambda: mx.quantize_grouped(xm, d_off, "e4m3", stream=stream), stream, 10)
+    gbs = xm.numel() * 3.03125 / (t * 1e-3) / 1e9
+    out["moe_quantize_grouped_65536x7168"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
+                                              "frac_hbm": round(gbs / hbm, 3)}
+    return out
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+
+def oracle_sample(rows: int = 512, cols: int = 2048):
+    """The CPU oracle, as it stands, on a bounded sample of the forward
+    workload: `rows` token rows of X and `cols` columns of W with the full
+    K = 7168, drawn from the workload's distributions; oracle quantize of
+    both slices plus the oracle block-scaled GEMM.
+    Returns (TFLOP/s, seconds, description)."""
+    from mxfp8_block_scaled_mx_gb300 import workloads as W
+    from oracle import mx_oracle as O
+    k = FWD["k"]
+    xs = W.synth_matrix((rows, k), 1.0, 0.005, 50.0, 500.0, seed=404)
+    ws = W.synth_matrix((k, cols), 0.02, seed=405)
+    t0 = time.perf_counter()
+    a = O.quantize(xs.float().double().numpy(), "e4m3", "row")
+    b = O.quantize(ws.float().double().numpy(), "e4m3", "col")
+    O.gemm(a, b)
+    dt = time.perf_counter() - t0
+    flops = 2 * rows * cols * k
+    return flops / dt / 1e12, dt, (f"oracle quantize of X[{rows}x{k}] rowwise and W[{k}x{cols}] "
+                                   f"colwise, then oracle GEMM {rows}x{cols}x{k} "
+                                   "(float64 numpy), same distributions as the forward layer")
+
+
+def cpu_threads():
+    return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- main arms
+
+def run_reference(args):
+    world, rank, _ = setup_dist()
+    if rank != 0:
+        return 0
+    # each step: a small bounded sample so K steps end within minutes
+    for _ in range(args.warmup):
+        oracle_sample(REF_ROWS, REF_COLS)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        v, dt, desc = oracle_sample(REF_ROWS, REF_COLS)
+        vals.append(v)
+        secs.append(dt)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.median(secs) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": desc},
+        "cpu_baseline": {"kind": "oracle", "value": value, "unit": UNIT, "cores": cpu_threads(),
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def gemm_traffic_record():
+    """DRAM bytes per launch of the forward GEMM from the committed ncu
+    summary, valid only while gemm.cu is unchanged (its sha256 recorded
+    beside the figure)."""
+    path = os.path.join(ROOT, "profiles", "gemm_forward_traffic.md")
+    src = os.path.join(ROOT, "mxfp8_block_scaled_mx_gb300", "csrc", "gemm.cu")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    rec = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            key, val = line.strip()[2:].split(":", 1)
+            rec[key.strip()] = val.strip().strip("`")
+    if rec.get("gemm.cu sha256") != sha:
+        return None
+    try:
+        return float(rec["dram bytes per full-size launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_gpu(args):
+    import torch
+    import mxfp8_block_scaled_mx_gb300 as mx
+    from mxfp8_block_scaled_mx_gb300 import workloads as W
+
+    world, rank, local = setup_dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    mx.lib()
+    peaks, peak_src = read_peaks()
+    stream = torch.cuda.Stream(device=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        x, w = W.dense_forward(seed=rank, device=dev)
+        layer = ForwardLayer(mx, x, w, stream)
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            layer.step()
+        torch.cuda.synchronize()
+
+        # ---------------- device-resident timed region
+        ev = []
+        barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clocks:
+            start = torch.cuda.Event(enable_timing=True)
+            stop = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            for _ in range(args.steps):
+                layer.quantize_x()
+                layer.quantize_w()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                layer.gemm()
+                b.record(stream)
+                ev.append((a, b))
+            stop.record(stream)
+            torch.cuda.synchronize()
+        barrier()
+        elapsed_ms = start.elapsed_time(stop)
+        gemm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+        assert mx.mx_device_status(stream) == 0
+
+        flops_step = 2 * layer.m * layer.n * layer.k
+        ms_per_step = elapsed_ms / args.steps
+        value = world * flops_step / (ms_per_step * 1e-3) / 1e12
+
+        # quantize kernels timed alone (same buffers) for their GB/s
+        tq_x = time_kernel(layer.quantize_x, stream, 20)
+        tq_w = time_kernel(layer.quantize_w, stream, 20)
+
+        # ---------------- end to end: host buffers through the C ABI
+        hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        hw = torch.empty(w.shape, dtype=w.dtype, pin_memory=True)
+        hx.copy_(x)
+        hw.copy_(w)
+        hy = torch.empty(layer.y.shape, dtype=layer.y.dtype, pin_memory=True)
+        e2e_steps = max(3, min(args.steps, 20))
+        for _ in range(2):
+            x.copy_(hx, non_blocking=True)
+            w.copy_(hw, non_blocking=True)
+            layer.step()
+            hy.copy_(layer.y, non_blocking=True)
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            x.copy_(hx, non_blocking=True)
+            w.copy_(hw, non_blocking=True)
+            layer.step()
+            hy.copy_(layer.y, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+        e2e_value = world * flops_step / (e2e_ms * 1e-3) / 1e12
+        h2d = hx.numel() * hx.element_size() + hw.numel() * hw.element_size()
+        d2h = hy.numel() * hy.element_size()
+
+        rows = None
+        if rank == 0 and world == 1 and not args.no_rows:
+            del hx, hw, hy
+            rows = measure_rows(mx, peaks, dev, stream)
+
+    if rank != 0:
+        return 0
+
+    fp8_peak = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
+    gemm_tflops = flops_step / (gemm_ms * 1e-3) / 1e12
+    traffic = gemm_traffic_record()
+    hbm = peaks["hbm_gbs"]
+    qx_bytes = layer.m * layer.k * 3.03125
+    qw_bytes = layer.k * layer.n * 3.03125
+    clk = clocks.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "m": layer.m, "n": layer.n, "k": layer.k,
+                   "l2": "inputs larger than L2 (X 235 MB, W 264 MB, Y 604 MB per step)",
+                   "per_rank_batch": "one 16384-token batch per GPU",
+                   "value_def": "2*M*N*K of the step / step time (quantize X + quantize W + GEMM)"},
+        "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1),
+                     "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / fp8_peak, 4), "traffic": traffic,
+                     "kernel": "mx_gemm_kernel (forward, BF16 out)",
+                     "peak_source": f"{peak_src} bf16 burst {peaks['bf16_tflops']} TFLOP/s x "
+                                    f"{NOMINAL_FP8_OVER_BF16} (nominal dense fp8/bf16 ratio)",
+                     "frac_of_sustained": round(
+                         gemm_tflops / (peaks["bf16_tflops_sustained"] * NOMINAL_FP8_OVER_BF16), 4)},
+        "step_parts_ms": {"gemm": round(gemm_ms, 4), "quantize_x_alone": round(tq_x, 4),
+                          "quantize_w_alone": round(tq_w, 4)},
+        "quantize": {"x_rowwise_GB/s": round(qx_bytes / (tq_x * 1e-3) / 1e9, 1),
+                     "w_colwise_GB/s": round(qw_bytes / (tq_w * 1e-3) / 1e9, 1),
+                     "hbm_peak_GB/s": hbm,
+                     "x_frac_hbm": round(qx_bytes / (tq_x * 1e-3) / 1e9 / hbm, 3),
+                     "w_frac_hbm": round(qw_bytes / (tq_w * 1e-3) / 1e9 / hbm, 3)},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": layer.launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rows is not None:
+        line["rows"] = rows
+    if world == 1 and not args.no_cpu_baseline:
+        v, dt, desc = oracle_sample()
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                                "sample": desc, "seconds": round(dt, 2)}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="mx", choices=["mx", "reference"])
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-row extra kernels")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,78 @@
+"""Run one hot-path kernel on one shape a few times (for profilers).
+
+    python -m mxfp8_block_scaled_mx_gb300.cases gemm --m 4096 --n 18432 --k 7168 [--reps 3]
+    python -m mxfp8_block_scaled_mx_gb300.cases quantize --rows 16384 --cols 8192 --axis row
+    python -m mxfp8_block_scaled_mx_gb300.cases grouped --tokens 16384 --experts 16
+
+Inputs are the seeded synthetic workloads; each case launches the kernel
+`--reps` times after building its inputs and prints the mean event time.
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+import torch
+
+import mxfp8_block_scaled_mx_gb300 as mx
+from mxfp8_block_scaled_mx_gb300 import workloads as W
+
+
+def _time(fn, reps):
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=["gemm", "quantize", "grouped"])
+    ap.add_argument("--m", type=int, default=4096)
+    ap.add_argument("--n", type=int, default=18432)
+    ap.add_argument("--k", type=int, default=7168)
+    ap.add_argument("--rows", type=int, default=16384)
+    ap.add_argument("--cols", type=int, default=8192)
+    ap.add_argument("--axis", default="row", choices=["row", "col", "both"])
+    ap.add_argument("--tokens", type=int, default=16384)
+    ap.add_argument("--experts", type=int, default=16)
+    ap.add_argument("--out", default="bf16", choices=["bf16", "fp32"])
+    ap.add_argument("--reps", type=int, default=3)
+    a = ap.parse_args(argv)
+    dev = torch.device("cuda", 0)
+    if a.case == "gemm":
+        x, w = W.dense_forward(a.m, a.n, a.k, device=dev)
+        qa = mx.quantize(x, "e4m3", "row")
+        qb = mx.quantize(w, "e4m3", "col")
+        del x, w
+        y = torch.empty((a.m, a.n), dtype=torch.bfloat16 if a.out == "bf16" else torch.float32,
+                        device=dev)
+        ms = _time(lambda: mx.gemm(qa, qb, a.out, out=y), a.reps)
+        print(f"gemm {a.m}x{a.n}x{a.k}: {ms:.4f} ms, {2 * a.m * a.n * a.k / ms / 1e9:.1f} TFLOP/s")
+    elif a.case == "quantize":
+        x = W.quantize_sweep((a.rows, a.cols), seed=1, device=dev)
+        ms = _time(lambda: mx.quantize(x, "e4m3", a.axis), a.reps)
+        bpe = 4.0625 if a.axis == "both" else 3.03125
+        print(f"quantize {a.rows}x{a.cols} {a.axis}: {ms:.4f} ms, "
+              f"{a.rows * a.cols * bpe / ms / 1e6:.1f} GB/s")
+    else:
+        x, w, offsets = W.moe_inputs(a.tokens, a.experts, a.k, 2048, device=dev)
+        e, n, k = w.shape
+        d_off = torch.from_numpy(offsets).to(dev)
+        qa = mx.quantize_grouped(x, d_off, "e4m3")
+        qw = mx.quantize(w.view(e * n, k), "e4m3", "row")
+        qb = mx.MxTensor(qw.codes.view(e, n, k), qw.scales, "e4m3")
+        ms = _time(lambda: mx.grouped_gemm(qa, d_off, qb, "bf16"), a.reps)
+        print(f"grouped {a.tokens} tokens x {a.experts} experts ({n}x{k}): {ms:.4f} ms, "
+              f"{2 * a.tokens * n * k / ms / 1e9:.1f} TFLOP/s")
+    assert mx.device_status() == 0
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
