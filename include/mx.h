@@ -130,7 +130,7 @@ mx_status mx_quantize(const void* x, mx_dtype x_dtype, int64_t rows, int64_t col
  * last group are left untouched.  d_offsets: device int32[groups + 1],
  * d_offsets[0] = 0, non-decreasing, d_offsets[groups] = total_rows; invalid
  * offsets are reported through mx_device_status (MX_ERR_DEVICE_ARG) and
- * nothing is written.  1 <= groups <= 4096. */
+ * nothing is written.  1 <= groups <= 1000. */
 mx_status mx_quantize_grouped(const void* x, mx_dtype x_dtype, int64_t total_rows,
                               int64_t cols, int64_t ldx, mx_fmt fmt, mx_scale_rule rule,
                               int32_t groups, const int32_t* d_offsets,

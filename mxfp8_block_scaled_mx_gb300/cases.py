@@ -19,6 +19,7 @@ from mxfp8_block_scaled_mx_gb300 import workloads as W
 
 
 def _time(fn, reps):
+    fn()  # warm-up launch (module load, attributes)
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)

@@ -24,6 +24,12 @@
 // With 128-wide tiles the accumulator is double-buffered in tensor memory
 // so the epilogue of one tile overlaps the main loop of the next.
 //
+// Clusters of CM = 2 blocks take two m-tiles of the same n-tile: each block
+// loads its own A tile and half of the shared B tile, multicasting that half
+// to both blocks, so B crosses from L2 once per pair.  A stage is released
+// only when both blocks' MMAs are done with it (the MMA commit arrives on
+// the empty barrier of both blocks).
+//
 // Grouped (mixture-of-experts) mode walks (group, m-tile, n-tile) triples;
 // group offsets are read on the device and turned into a tile prefix by
 // every block, so the host never synchronizes.
@@ -49,13 +55,14 @@ constexpr uint32_t kTmemCols = 512;
 
 struct GroupSmem {
   int32_t off[kMaxGroups + 1];
-  int32_t tiles[kMaxGroups + 1];
+  int32_t tiles[kMaxGroups + 1];   // 128-row tiles before each group
+  int32_t units[kMaxGroups + 1];   // cluster units (CM tiles) before each group
   int32_t valid;
 };
 
 template <int BN, bool GROUPED>
 struct Cfg {
-  static constexpr int kStages = BN == 128 ? 6 : 4;
+  static constexpr int kStages = BN == 128 ? (GROUPED ? 5 : 6) : 4;
   static constexpr int kAccStages = BN == 128 ? 2 : 1;
   static constexpr int kABytes = BM * BK;
   static constexpr int kBBytes = BN * BK;
@@ -84,43 +91,48 @@ struct TileInfo {
   int64_t m_end;    // rows >= m_end are not stored
   int64_t n0;       // first column of Y
   int64_t b_row0;   // first row of the B tile in the [rows, k] B tensor
-  int64_t sfa_rt;   // 128-row scale tile of A
+  int64_t sfa_rt;   // 128-row scale tile of A (-1: this block's tile is padding)
   int64_t sfb_rt0;  // first 128-row scale tile of B
-  int64_t n_lim;    // columns >= n_lim are not stored (= n)
 };
 
-template <int BN, bool GROUPED>
-__device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t t, int64_t n_tiles,
-                                              const GroupSmem* gs) {
+// Work unit u of a cluster = CM m-tiles x one n-tile; block `rank` of the
+// cluster takes m-tile CM*mu + rank.  Dense units follow a banded raster
+// (kBandM m-tiles per band, n outer inside a band) so a band of A stays in
+// L2 while B streams; grouped units walk groups, then m-units, then n.
+template <int BN, bool GROUPED, int CM>
+__device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t u, int64_t n_tiles,
+                                              uint32_t rank, const GroupSmem* gs) {
   TileInfo ti;
-  int64_t m_blk, n_blk;
   if constexpr (GROUPED) {
-    const int64_t mt = t / n_tiles;
-    n_blk = t - mt * n_tiles;
-    const int g = find_group(gs->tiles, p.groups, static_cast<int32_t>(mt));
-    m_blk = mt - gs->tiles[g];
-    ti.m0 = static_cast<int64_t>(gs->off[g]) + m_blk * BM;
-    ti.m_end = gs->off[g + 1];
+    const int64_t mu = u / n_tiles;
+    const int64_t n_blk = u - mu * n_tiles;
+    const int g = find_group(gs->units, p.groups, static_cast<int32_t>(mu));
+    const int64_t lm = (mu - gs->units[g]) * CM + rank;  // m-tile inside the group
+    const int64_t g_tiles = gs->tiles[g + 1] - gs->tiles[g];
+    ti.m0 = static_cast<int64_t>(gs->off[g]) + lm * BM;
+    ti.m_end = lm < g_tiles ? static_cast<int64_t>(gs->off[g + 1]) : ti.m0;
+    ti.sfa_rt = lm < g_tiles ? gs->tiles[g] + lm : -1;
     ti.n0 = n_blk * BN;
     ti.b_row0 = static_cast<int64_t>(g) * p.n + ti.n0;
-    ti.sfa_rt = mt;
     ti.sfb_rt0 = ti.b_row0 / 128;
   } else {
     const int64_t m_tiles = (p.m + BM - 1) / BM;
-    const int64_t band_tiles = kBandM * n_tiles;
-    const int64_t band = t / band_tiles;
-    const int64_t within = t - band * band_tiles;
-    const int64_t m_in_band = ::min(static_cast<int64_t>(kBandM), m_tiles - band * kBandM);
-    n_blk = within / m_in_band;
-    m_blk = band * kBandM + (within - n_blk * m_in_band);
+    const int64_t m_units = (m_tiles + CM - 1) / CM;
+    constexpr int64_t band_units = kBandM / CM;
+    const int64_t band_size = band_units * n_tiles;
+    const int64_t band = u / band_size;
+    const int64_t within = u - band * band_size;
+    const int64_t in_band = ::min(band_units, m_units - band * band_units);
+    const int64_t n_blk = within / in_band;
+    const int64_t mu = band * band_units + (within - n_blk * in_band);
+    const int64_t m_blk = mu * CM + rank;
     ti.m0 = m_blk * BM;
     ti.m_end = p.m;
+    ti.sfa_rt = m_blk < m_tiles ? m_blk : -1;
     ti.n0 = n_blk * BN;
     ti.b_row0 = ti.n0;
-    ti.sfa_rt = m_blk;
     ti.sfb_rt0 = ti.n0 / 128;
   }
-  ti.n_lim = p.n;
   return ti;
 }
 
@@ -130,11 +142,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
-template <int BN, bool GROUPED>
+template <int BN, bool GROUPED, int CM>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
   using C = Cfg<BN, GROUPED>;
+  static_assert(CM == 1 || CM == 2, "cluster size");
+  constexpr uint16_t kPairMask = 0x3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -151,17 +165,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* mma_done = acc_empty + C::kAccStages;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
-
   GroupSmem* gs = reinterpret_cast<GroupSmem*>(smem + C::kOffGroup);
 
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
+  const uint32_t rank = CM > 1 ? cluster_ctarank() : 0u;
+  const int64_t cluster_id = blockIdx.x / CM;
+  const int64_t num_clusters = gridDim.x / CM;
 
   if (warp == 0) {
     if (lane == 0) {
       for (int s = 0; s < C::kStages; ++s) {
         mbar_init(&full[s], 1);
-        mbar_init(&empty[s], 1);
+        mbar_init(&empty[s], CM);  // one MMA commit from every block of the cluster
       }
       for (int s = 0; s < C::kAccStages; ++s) {
         mbar_init(&acc_full[s], 1);
@@ -175,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     if constexpr (GROUPED) {
-      group_tile_prefix(p.offsets, p.groups, p.m, gs->off, gs->tiles, &gs->valid);
+      group_tile_prefix(p.offsets, p.groups, p.m, gs->off, gs->tiles, &gs->valid, CM, gs->units);
     }
   }
   if (warp == 1) {
@@ -183,21 +199,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before_sync();
-  __syncthreads();
+  // Barriers of every block of the cluster must be initialized before any
+  // block multicasts into them.
+  if constexpr (CM > 1) {
+    cluster_sync();
+  } else {
+    __syncthreads();
+  }
   tc_fence_after_sync();
   const uint32_t tmem_base = *s_tmem;
 
   const int64_t n_tiles = (p.n + BN - 1) / BN;
-  int64_t num_tiles;
+  int64_t num_units;
   if constexpr (GROUPED) {
     if (!gs->valid) {
       if (blockIdx.x == 0 && threadIdx.x == 0) record_device_status(p.status, MX_DEV_BAD_OFFSETS);
-      num_tiles = 0;
+      num_units = 0;
     } else {
-      num_tiles = static_cast<int64_t>(gs->tiles[p.groups]) * n_tiles;
+      num_units = static_cast<int64_t>(gs->units[p.groups]) * n_tiles;
     }
   } else {
-    num_tiles = ((p.m + BM - 1) / BM) * n_tiles;
+    num_units = ((p.m + BM * CM - 1) / (BM * CM)) * n_tiles;
   }
   const int64_t k_tiles = (p.k + BK - 1) / BK;
   const int32_t k_blocks = static_cast<int32_t>(p.k / 32);
@@ -206,76 +228,115 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     uint32_t stage = 0, phase = 0;
-    uint32_t fills[C::kStages];
-#pragma unroll
-    for (int s = 0; s < C::kStages; ++s) fills[s] = 0;
+    int64_t issued = 0;  // stage fills issued so far
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      const TileInfo ti = tile_info<BN, GROUPED>(p, t, n_tiles, gs);
+    for (int64_t u = cluster_id; u < num_units && ok; u += num_clusters) {
+      const TileInfo ti = tile_info<BN, GROUPED, CM>(p, u, n_tiles, rank, gs);
       int sfb_units = 0;
 #pragma unroll
       for (int j = 0; j < C::kSfbUnits; ++j)
         if (ti.n0 + 128 * j < p.n) ++sfb_units;
-      const uint32_t tx = C::kABytes + C::kBBytes + 512u + 512u * sfb_units;
-      for (int64_t kt = 0; kt < k_tiles; ++kt) {
+      const uint32_t tx =
+          C::kABytes + C::kBBytes + (ti.sfa_rt >= 0 ? 512u : 0u) + 512u * sfb_units;
+      const uint8_t* sfa_src = p.sa + (ti.sfa_rt >= 0 ? ti.sfa_rt : 0) * scale_tiles_k * 512;
+      const uint8_t* sfb_src = p.sb + ti.sfb_rt0 * scale_tiles_k * 512;
+      const int64_t sfb_stride = scale_tiles_k * 512;
+      const int32_t a_row = static_cast<int32_t>(ti.m0);
+      const int32_t b_row = static_cast<int32_t>(ti.b_row0 + rank * (BN / CM));
+      const int32_t kt_count = static_cast<int32_t>(k_tiles);
+      for (int32_t kt = 0; kt < kt_count; ++kt) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
         }
         mbar_arrive_expect_tx(&full[stage], tx);
-        fills[stage]++;
-        tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full[stage], static_cast<int32_t>(kt * BK),
-                    static_cast<int32_t>(ti.m0));
-        tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full[stage], static_cast<int32_t>(kt * BK),
-                    static_cast<int32_t>(ti.b_row0));
-        bulk_load(sSfa + stage * 512, p.sa + (ti.sfa_rt * scale_tiles_k + kt) * 512, 512,
-                  &full[stage]);
+        ++issued;
+        const int32_t kx = kt * BK;
+        tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full[stage], kx, a_row);
+        if constexpr (CM > 1) {
+          // this block's half of the shared B tile, delivered to both blocks
+          tma_load_2d_multicast(sB + stage * C::kBBytes + rank * (C::kBBytes / CM), &tmap_b,
+                                &full[stage], kx, b_row, kPairMask);
+        } else {
+          tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full[stage], kx, b_row);
+        }
+        if (ti.sfa_rt >= 0) bulk_load(sSfa + stage * 512, sfa_src, 512, &full[stage]);
         for (int j = 0; j < sfb_units; ++j)
-          bulk_load(sSfb + (stage * C::kSfbUnits + j) * 512,
-                    p.sb + ((ti.sfb_rt0 + j) * scale_tiles_k + kt) * 512, 512, &full[stage]);
+          bulk_load(sSfb + (stage * C::kSfbUnits + j) * 512, sfb_src + j * sfb_stride, 512,
+                    &full[stage]);
+        sfa_src += 512;
+        sfb_src += 512;
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-    // Drain: every issued copy must land before the block exits.
-    for (int s = 0; s < C::kStages; ++s)
-      if (fills[s])
-        mbar_wait(&full[s], (fills[s] - 1) & 1u, s_abort, p.status, p.wait_limit_ns, true);
+    // Drain: every copy into this block's shared memory must land before
+    // the block exits.
+    for (int s = 0; s < C::kStages; ++s) {
+      const int64_t fills = issued > s ? (issued - s + C::kStages - 1) / C::kStages : 0;
+      if (fills)
+        mbar_wait(&full[s], static_cast<uint32_t>((fills - 1) & 1), s_abort, p.status,
+                  p.wait_limit_ns, true);
+    }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
+    // This one thread paces the tensor core, so its loop does only 32-bit
+    // adds: descriptor halves and instruction descriptors are precomputed.
+    constexpr uint32_t kHiOperand = smem_desc_hi(1024, 2);  // 8-row groups 1 KB apart, 128B swizzle
+    constexpr uint32_t kHiScale = smem_desc_hi(128, 0);     // 32 rows x 16 B, no swizzle
+    const uint32_t a_lo0 = smem_desc_lo(smem_u32(sA), 16);
+    const uint32_t b_lo0 = smem_desc_lo(smem_u32(sB), 16);
+    const uint32_t sfa_lo0 = smem_desc_lo(smem_u32(sSfa), 0);
+    const uint32_t sfb_lo0 = smem_desc_lo(smem_u32(sSfb), 0);
+    const uint32_t idesc0 = mxf8_idesc(p.fa, p.fb, BM, BN, 0, 0);
+    const int32_t kt_count = static_cast<int32_t>(k_tiles);
+    const int32_t kt_full = k_blocks / 4;  // k-tiles with all four scale blocks
     uint32_t stage = 0, phase = 0;
     uint32_t acc = 0, acc_phase = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    for (int64_t u = cluster_id; u < num_units && ok; u += num_clusters) {
       if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) break;
       tc_fence_after_sync();
       const uint32_t d_tmem = tmem_base + acc * BN;
-      for (int64_t kt = 0; kt < k_tiles; ++kt) {
+      for (int32_t kt = 0; kt < kt_count; ++kt) {
         if (!mbar_wait(&full[stage], phase, s_abort, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t sf_tmem = tmem_base + C::kSfBaseCol + stage * C::kSfSlotCols;
-        tc_cp_32x128b_warpx4(sf_tmem, smem_desc(smem_u32(sSfa + stage * 512), 0, 128, 0));
+        tc_cp_32x128b_warpx4_lohi(sf_tmem, sfa_lo0 + stage * (512 >> 4), kHiScale);
 #pragma unroll
         for (int j = 0; j < C::kSfbUnits; ++j)
-          tc_cp_32x128b_warpx4(sf_tmem + C::kSfaCols + 4 * j,
-                               smem_desc(smem_u32(sSfb + (stage * C::kSfbUnits + j) * 512), 0,
-                                         128, 0));
-        const uint64_t adesc = smem_desc(smem_u32(sA + stage * C::kABytes), 16, 1024, 2);
-        const uint64_t bdesc = smem_desc(smem_u32(sB + stage * C::kBBytes), 16, 1024, 2);
-        const int32_t kb_here = ::min(4, k_blocks - static_cast<int32_t>(kt) * 4);
-        for (int32_t kb = 0; kb < kb_here; ++kb) {
-          const uint32_t idesc = mxf8_idesc(p.fa, p.fb, BM, BN, kb, kb);
-          // +32 bytes along K inside the 128-byte swizzled row = +2 in the
-          // 16-byte address field.
-          tc_mma_mxf8(d_tmem, adesc + 2u * kb, bdesc + 2u * kb, idesc, sf_tmem,
-                      sf_tmem + C::kSfaCols, (kt > 0 || kb > 0) ? 1u : 0u);
+          tc_cp_32x128b_warpx4_lohi(sf_tmem + C::kSfaCols + 4 * j,
+                                    sfb_lo0 + (stage * C::kSfbUnits + j) * (512 >> 4), kHiScale);
+        const uint32_t a_lo = a_lo0 + stage * (C::kABytes >> 4);
+        const uint32_t b_lo = b_lo0 + stage * (C::kBBytes >> 4);
+        const uint32_t sfb_tmem = sf_tmem + C::kSfaCols;
+        // +32 bytes along K inside the 128-byte swizzled row = +2 in the
+        // 16-byte address field; block kb's scales are byte kb of the
+        // scale columns (scale-factor ids in the instruction descriptor).
+        if (kt < kt_full) {
+          tc_mma_mxf8_lohi(d_tmem, a_lo, kHiOperand, b_lo, kHiOperand, idesc0, sf_tmem, sfb_tmem,
+                           kt > 0 ? 1u : 0u);
+#pragma unroll
+          for (uint32_t kb = 1; kb < 4; ++kb)
+            tc_mma_mxf8_lohi(d_tmem, a_lo + 2u * kb, kHiOperand, b_lo + 2u * kb, kHiOperand,
+                             idesc0 | (kb << 4) | (kb << 29), sf_tmem, sfb_tmem, 1u);
+        } else {
+          const uint32_t kb_here = static_cast<uint32_t>(k_blocks - kt * 4);
+          for (uint32_t kb = 0; kb < kb_here; ++kb)
+            tc_mma_mxf8_lohi(d_tmem, a_lo + 2u * kb, kHiOperand, b_lo + 2u * kb, kHiOperand,
+                             idesc0 | (kb << 4) | (kb << 29), sf_tmem, sfb_tmem,
+                             (kt > 0 || kb > 0) ? 1u : 0u);
         }
-        tc_commit(&empty[stage]);
+        if constexpr (CM > 1) {
+          tc_commit_multicast(&empty[stage], kPairMask);
+        } else {
+          tc_commit(&empty[stage]);
+        }
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1u;
@@ -297,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t q = warp & 3u;  // tensor-memory lane quarter of this warp
     uint8_t* stage_buf = sEpi + (warp - 2) * 4096;
     uint32_t acc = 0, acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-      const TileInfo ti = tile_info<BN, GROUPED>(p, t, n_tiles, gs);
+    for (int64_t u = cluster_id; u < num_units; u += num_clusters) {
+      const TileInfo ti = tile_info<BN, GROUPED, CM>(p, u, n_tiles, rank, gs);
       const bool got = mbar_wait(&acc_full[acc], acc_phase, s_abort, p.status, p.wait_limit_ns);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
@@ -323,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = lane & 7;
             const int64_t grow = row_base + rr;
             const int64_t gcol = ti.n0 + c * 32 + j * 4;
-            if (grow < ti.m_end && gcol < ti.n_lim) {
+            if (grow < ti.m_end && gcol < p.n) {
               const uint4 v =
                   *reinterpret_cast<const uint4*>(stage_buf + rr * 128 + ((j ^ (rr & 7)) * 16));
               *reinterpret_cast<uint4*>(y + grow * p.ldy + gcol) = v;
@@ -356,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = lane & 7;
             const int64_t grow = row_base + rr;
             const int64_t gcol = ti.n0 + c * 64 + j * 8;
-            if (grow < ti.m_end && gcol < ti.n_lim) {
+            if (grow < ti.m_end && gcol < p.n) {
               const uint4 v =
                   *reinterpret_cast<const uint4*>(stage_buf + rr * 128 + ((j ^ (rr & 7)) * 16));
               *reinterpret_cast<uint4*>(y + grow * p.ldy + gcol) = v;
@@ -381,6 +442,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  // No block of the cluster may exit while its peer can still multicast
+  // into its shared memory or arrive on its barriers.
+  if constexpr (CM > 1) cluster_sync();
 }
 
 __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
@@ -395,44 +459,66 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
   }
 }
 
-template <int BN, bool GROUPED>
+template <int BN, bool GROUPED, int CM>
 cudaError_t launch_impl(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                         int num_sms, cudaStream_t stream) {
   using C = Cfg<BN, GROUPED>;
-  auto kern = mx_gemm_kernel<BN, GROUPED>;
+  auto kern = mx_gemm_kernel<BN, GROUPED, CM>;
   // Per device, the attribute is idempotent and cheap; set it every time.
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  int64_t tiles;
   const int64_t n_tiles = (p.n + BN - 1) / BN;
-  if (GROUPED) {
-    tiles = ((p.m + BM - 1) / BM + p.groups) * n_tiles;
-  } else {
-    tiles = ((p.m + BM - 1) / BM) * n_tiles;
+  const int64_t m_tiles = (p.m + BM - 1) / BM;
+  // upper bound of the work units (grouped: every group may add a partial unit)
+  const int64_t units = GROUPED ? ((m_tiles + p.groups + CM - 1) / CM + p.groups) * n_tiles
+                                : ((m_tiles + CM - 1) / CM) * n_tiles;
+  if (units == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CM;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int max_clusters = num_sms / CM;
+  if (CM > 1) {
+    cfg.gridDim = dim3(static_cast<unsigned>(max_clusters * CM));
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) == cudaSuccess && active > 0)
+      max_clusters = ::min(max_clusters, active);
   }
-  if (tiles == 0) return cudaSuccess;
-  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb, p);
-  return cudaGetLastError();
+  const int64_t clusters = units < max_clusters ? units : max_clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CM));
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
 }
 
 }  // namespace
 
 int gemm_default_block_n(const GemmParams& p) {
   (void)p;
-  return 128;
+  return 256;
 }
 
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                        int block_n, int num_sms, cudaStream_t stream) {
+                        int block_n, int cluster_m, int num_sms, cudaStream_t stream) {
   const bool grouped = p.groups > 0;
   if (block_n == 256) {
-    return grouped ? launch_impl<256, true>(p, ta, tb, num_sms, stream)
-                   : launch_impl<256, false>(p, ta, tb, num_sms, stream);
+    if (cluster_m == 2)
+      return grouped ? launch_impl<256, true, 2>(p, ta, tb, num_sms, stream)
+                     : launch_impl<256, false, 2>(p, ta, tb, num_sms, stream);
+    return grouped ? launch_impl<256, true, 1>(p, ta, tb, num_sms, stream)
+                   : launch_impl<256, false, 1>(p, ta, tb, num_sms, stream);
   }
-  return grouped ? launch_impl<128, true>(p, ta, tb, num_sms, stream)
-                 : launch_impl<128, false>(p, ta, tb, num_sms, stream);
+  if (cluster_m == 2)
+    return grouped ? launch_impl<128, true, 2>(p, ta, tb, num_sms, stream)
+                   : launch_impl<128, false, 2>(p, ta, tb, num_sms, stream);
+  return grouped ? launch_impl<128, true, 1>(p, ta, tb, num_sms, stream)
+                 : launch_impl<128, false, 1>(p, ta, tb, num_sms, stream);
 }
 
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {

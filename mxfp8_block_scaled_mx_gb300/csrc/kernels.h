@@ -46,11 +46,12 @@ struct GemmParams {
 };
 
 // Tile width along N of the GEMM kernel: 128 (double-buffered accumulator)
-// or 256 (single accumulator).  Returns 0 if unsupported.
+// or 256 (single accumulator).
 int gemm_default_block_n(const GemmParams& p);
 
+// cluster_m: 1, or 2 for block pairs sharing (multicasting) the B tile.
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                        int block_n, int num_sms, cudaStream_t stream);
+                        int block_n, int cluster_m, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 

@@ -23,10 +23,13 @@ def mx():
     return mx
 
 
-@pytest.fixture(params=["128", "256"])
+@pytest.fixture(params=[("128", "1"), ("256", "1"), ("128", "2"), ("256", "2")],
+                ids=["bn128-c1", "bn256-c1", "bn128-c2", "bn256-c2"])
 def block_n(request, monkeypatch):
-    monkeypatch.setenv("MX_GEMM_BLOCK_N", request.param)
-    return int(request.param)
+    """Tile width along N and cluster size (1, or 2 = block pairs sharing B)."""
+    monkeypatch.setenv("MX_GEMM_BLOCK_N", request.param[0])
+    monkeypatch.setenv("MX_GEMM_CLUSTER_M", request.param[1])
+    return int(request.param[0])
 
 
 def random_mx(rng, rows, k, fmt, lo=118, hi=136):

@@ -17,10 +17,13 @@ def mx():
     return mx
 
 
-@pytest.fixture(params=["128", "256"])
+@pytest.fixture(params=[("128", "1"), ("256", "1"), ("128", "2"), ("256", "2")],
+                ids=["bn128-c1", "bn256-c1", "bn128-c2", "bn256-c2"])
 def block_n(request, monkeypatch):
-    monkeypatch.setenv("MX_GEMM_BLOCK_N", request.param)
-    return int(request.param)
+    """Tile width along N and cluster size (1, or 2 = block pairs sharing B)."""
+    monkeypatch.setenv("MX_GEMM_BLOCK_N", request.param[0])
+    monkeypatch.setenv("MX_GEMM_CLUSTER_M", request.param[1])
+    return int(request.param[0])
 
 
 def run_grouped(mx, sizes, n, k, out, seed=0, fa="e4m3", fb="e4m3"):
