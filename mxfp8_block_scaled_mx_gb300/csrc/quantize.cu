@@ -16,9 +16,10 @@
 //    exactly one 512-byte swizzled unit, assembled in shared memory and
 //    written with one coalesced store.
 //  - Columnwise: the tile is staged in shared memory; each thread reduces
-//    and encodes one column of a 32-row block, the codes are transposed in
-//    shared memory and written back as 128-byte rows of the [cols, rows]
-//    output, again with one 512-byte scale unit per tile.
+//    and encodes two adjacent columns of a 32-row block (one 32-bit shared
+//    load and one SIMD max per row), the codes are transposed in shared
+//    memory and written back as 128-byte rows of the [cols, rows] output,
+//    again with one 512-byte scale unit per tile.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -42,13 +43,19 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
+// Per-halfword unsigned max of two packed pairs (one SIMD instruction).
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // Largest magnitude bit pattern (sign cleared) among the 8 bf16 of v.  For
 // non-NaN bf16 the unsigned order of these patterns is the order of |x|;
 // NaN patterns sort above +Inf (0x7F80).
 __device__ __forceinline__ uint32_t amax_bits8(const uint4 v) {
-  uint32_t m = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
-  m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
-  m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
+  uint32_t m = max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+  m = max_u16x2(m, max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
   return max(m & 0xFFFFu, m >> 16);
 }
 
@@ -129,8 +136,8 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
   const int tid = threadIdx.x;
   uint8_t* s_unit_row = smem;              // 512 B
   uint8_t* s_unit_col = smem + 512;        // 512 B
-  uint16_t* s_x = reinterpret_cast<uint16_t*>(smem + 1024);                 // 128 x 128 bf16
-  uint8_t* s_q = smem + 1024 + kTile * kTile * 2;                           // 128 x 144 B
+  uint32_t* s_x = reinterpret_cast<uint32_t*>(smem + 1024);  // 128 rows x 64 bf16 pairs
+  uint8_t* s_q = smem + 1024 + kTile * kTile * 2;             // 128 x 144 B
 
   // Zero the scale units (padding entries stay 0).
   if (tid < 128) {
@@ -138,29 +145,35 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
     if (COL) reinterpret_cast<uint32_t*>(s_unit_col)[tid] = 0u;
   }
 
-  const int ch = tid & 15;  // 8-column chunk within the tile
+  // Thread t holds the 8-column chunk t % 16 of rows t / 16 + 16 * it.
+  const int ch = tid & 15;
+  const int lr0 = tid >> 4;
   const int64_t gc = c0 + ch * 8;
   const bool col_ok = gc < p.cols;
+  const uint16_t* xp = p.x + (tc.x_row0 + lr0) * p.ldx + gc;
+  const int64_t x_step = 16 * p.ldx;
   uint4 v[8];
 #pragma unroll
   for (int it = 0; it < 8; ++it) {
-    const int lr = it * 16 + (tid >> 4);
-    const bool ok = col_ok && lr < tc.rows_valid;
-    v[it] = ok ? ld_stream(p.x + (tc.x_row0 + lr) * p.ldx + gc) : make_uint4(0, 0, 0, 0);
+    const bool ok = col_ok && lr0 + it * 16 < tc.rows_valid;
+    v[it] = ok ? ld_stream(xp + it * x_step) : make_uint4(0, 0, 0, 0);
   }
   __syncthreads();  // scale units zeroed
 
   if constexpr (ROW) {
+    uint8_t* qp = p.q_row + (tc.x_row0 + lr0) * p.cols + gc;
+    const int64_t q_step = 16 * p.cols;
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
-      const int lr = it * 16 + (tid >> 4);
+      const int lr = lr0 + it * 16;
       const bool ok = col_ok && lr < tc.rows_valid;
+      // the four lanes holding one 32-element block share its amax
       uint32_t a = amax_bits8(v[it]);
       a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
       a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
       uint2 codes;
       uint8_t sbyte;
-      if (a > 0x7F80u || a == 0x7F80u) {  // NaN or Inf in the block
+      if (a >= 0x7F80u) {  // NaN or Inf in the block
         codes = make_uint2(kNanCode4, kNanCode4);
         sbyte = kNanScale;
       } else {
@@ -169,56 +182,69 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
         sbyte = static_cast<uint8_t>(e + 127);
       }
       if (ok) {
-        *reinterpret_cast<uint2*>(p.q_row + (tc.x_row0 + lr) * p.cols + gc) = codes;
+        *reinterpret_cast<uint2*>(qp + it * q_step) = codes;
         if ((tid & 3) == 0) s_unit_row[unit_offset(lr, ch >> 2)] = sbyte;
       }
     }
   }
 
   if constexpr (COL) {
-    // Stage the tile: row lr at s_x + lr*128 (256-byte rows).
+    // Stage the tile: row lr holds 64 bf16 pairs (256 bytes).
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int lr = it * 16 + (tid >> 4);
-      *reinterpret_cast<uint4*>(s_x + lr * kTile + ch * 8) = v[it];
-    }
+    for (int it = 0; it < 8; ++it)
+      *reinterpret_cast<uint4*>(s_x + (lr0 + it * 16) * 64 + ch * 4) = v[it];
   }
   __syncthreads();
 
   if constexpr (COL) {
-    const int c = tid & 127;
-    const bool cok = c0 + c < p.cols;
-#pragma unroll 1
-    for (int rbi = tid >> 7; rbi < 4; rbi += 2) {
-      const bool ok = cok && rbi * 32 < tc.rows_valid;
-      uint32_t h[32];
-      uint32_t a = 0;
+    // Thread t: columns 2*(t % 64) and 2*(t % 64) + 1, 32-row block t / 64.
+    // One 32-bit shared load gives both columns of a row, so the amax of
+    // the two column blocks is one SIMD max per row.
+    const int cp = tid & 63;
+    const int rb = tid >> 6;
+    const bool ok = c0 + 2 * cp < p.cols && rb * 32 < tc.rows_valid;
+    uint32_t w[32];
+    uint32_t a2 = 0;
 #pragma unroll
-      for (int r = 0; r < 32; ++r) {
-        h[r] = s_x[(rbi * 32 + r) * kTile + c];
-        a = max(a, h[r] & 0x7FFFu);
-      }
-      uint32_t w[8];
-      uint8_t sbyte;
-      if (a >= 0x7F80u) {
+    for (int r = 0; r < 32; ++r) {
+      w[r] = s_x[(rb * 32 + r) * 64 + cp];
+      a2 = max_u16x2(a2, w[r] & 0x7FFF7FFFu);
+    }
+    const uint32_t a_lo = a2 & 0xFFFFu;
+    const uint32_t a_hi = a2 >> 16;
+    const bool nan_lo = a_lo >= 0x7F80u;
+    const bool nan_hi = a_hi >= 0x7F80u;
+    const int e_lo = nan_lo ? 0 : scale_exponent(a_lo, emax, p.rule);
+    const int e_hi = nan_hi ? 0 : scale_exponent(a_hi, emax, p.rule);
+    const float m_lo = pow2_neg(e_lo);
+    const float m_hi = pow2_neg(e_hi);
+    uint32_t q_lo[8], q_hi[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) w[i] = kNanCode4;
-        sbyte = kNanScale;
-      } else {
-        const int e = scale_exponent(a, emax, p.rule);
-        const float mul = pow2_neg(e);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t p01 = h[4 * i] | (h[4 * i + 1] << 16);
-          const uint32_t p23 = h[4 * i + 2] | (h[4 * i + 3] << 16);
-          w[i] = encode_word<FMT>(p01, mul) | (encode_word<FMT>(p23, mul) << 16);
-        }
-        sbyte = static_cast<uint8_t>(e + 127);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(s_q + c * kColPitch + rbi * 32);
-      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      if (ok) s_unit_col[unit_offset(c, rbi)] = sbyte;
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t w0 = w[4 * i], w1 = w[4 * i + 1], w2 = w[4 * i + 2], w3 = w[4 * i + 3];
+      q_lo[i] = cvt_pair<FMT>(__fmul_rn(__uint_as_float(w0 << 16), m_lo),
+                              __fmul_rn(__uint_as_float(w1 << 16), m_lo)) |
+                (cvt_pair<FMT>(__fmul_rn(__uint_as_float(w2 << 16), m_lo),
+                               __fmul_rn(__uint_as_float(w3 << 16), m_lo))
+                 << 16);
+      q_hi[i] = cvt_pair<FMT>(__fmul_rn(__uint_as_float(w0 & 0xFFFF0000u), m_hi),
+                              __fmul_rn(__uint_as_float(w1 & 0xFFFF0000u), m_hi)) |
+                (cvt_pair<FMT>(__fmul_rn(__uint_as_float(w2 & 0xFFFF0000u), m_hi),
+                               __fmul_rn(__uint_as_float(w3 & 0xFFFF0000u), m_hi))
+                 << 16);
+      if (nan_lo) q_lo[i] = kNanCode4;
+      if (nan_hi) q_hi[i] = kNanCode4;
+    }
+    uint4* d0 = reinterpret_cast<uint4*>(s_q + (2 * cp) * kColPitch + rb * 32);
+    uint4* d1 = reinterpret_cast<uint4*>(s_q + (2 * cp + 1) * kColPitch + rb * 32);
+    d0[0] = make_uint4(q_lo[0], q_lo[1], q_lo[2], q_lo[3]);
+    d0[1] = make_uint4(q_lo[4], q_lo[5], q_lo[6], q_lo[7]);
+    d1[0] = make_uint4(q_hi[0], q_hi[1], q_hi[2], q_hi[3]);
+    d1[1] = make_uint4(q_hi[4], q_hi[5], q_hi[6], q_hi[7]);
+    if (ok) {
+      s_unit_col[unit_offset(2 * cp, rb)] = nan_lo ? kNanScale : static_cast<uint8_t>(e_lo + 127);
+      s_unit_col[unit_offset(2 * cp + 1, rb)] =
+          nan_hi ? kNanScale : static_cast<uint8_t>(e_hi + 127);
     }
   }
   __syncthreads();
