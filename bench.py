@@ -353,7 +353,7 @@ def gemm_traffic_record():
     """DRAM bytes per launch of the forward GEMM from the committed ncu
     summary, valid only while gemm.cu is unchanged (its sha256 recorded
     beside the figure)."""
-    path = os.path.join(ROOT, "profiles", "gemm_forward_traffic.md")
+    path = os.path.join(ROOT, "profiles", "mx_gemm_forward_16384x18432x7168_dram.md")
     src = os.path.join(ROOT, "mxfp8_block_scaled_mx_gb300", "csrc", "gemm.cu")
     try:
         text = open(path).read()
