@@ -10,7 +10,7 @@
 // memory and E8M0 scales from tensor memory, and accumulates in FP32 in
 // tensor memory.
 //
-// Structure (one persistent block of 6 warps per SM):
+// Structure (one persistent block of 10 warps per SM):
 //   warp 0      TMA producer: A and B code tiles (128-byte swizzle) with
 //               cp.async.bulk.tensor, the 512-byte scale units with
 //               cp.async.bulk, into a ring of kStages shared-memory slots
@@ -18,9 +18,11 @@
 //   warp 1      allocates tensor memory; one lane issues tcgen05.cp
 //               (scales -> tensor memory) and tcgen05.mma, and releases each
 //               slot with tcgen05.commit.
-//   warps 2..5  epilogue: tcgen05.ld of the FP32 accumulator, conversion to
-//               FP32/BF16 (RNE), staging through shared memory and 128-byte
-//               coalesced stores, masked at the matrix (or group) edge.
+//   warps 2..9  epilogue: tcgen05.ld of the FP32 accumulator into registers
+//               (two warps per 32-lane quarter, half the columns each), early
+//               release of the accumulator, then conversion to FP32/BF16
+//               (RNE), staging through shared memory and coalesced 64-byte
+//               row segments, masked at the matrix (or group) edge.
 // With 128-wide tiles the accumulator is double-buffered in tensor memory
 // so the epilogue of one tile overlaps the main loop of the next.
 //
@@ -48,9 +50,9 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 128;            // K elements (bytes) per pipeline stage = 4 scale blocks
-constexpr int kThreads = 192;
-constexpr int kEpiWarps = 4;
-constexpr int kBandM = 16;         // m-tiles per raster band (L2 reuse of B)
+constexpr int kEpiWarps = 8;       // two per tensor-memory lane quarter
+constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr int kEpiStageBytes = 2048;  // per epilogue warp: 32 rows x 64 bytes
 constexpr uint32_t kTmemCols = 512;
 
 struct GroupSmem {
@@ -77,7 +79,7 @@ struct Cfg {
   static constexpr int kOffSfa = kOffB + kStages * kBBytes;
   static constexpr int kOffSfb = kOffSfa + kStages * 512;
   static constexpr int kOffEpi = kOffSfb + kStages * kSfbUnits * 512;
-  static constexpr int kOffBar = kOffEpi + kEpiWarps * 4096;
+  static constexpr int kOffBar = kOffEpi + kEpiWarps * kEpiStageBytes;
   static constexpr int kNumBars = 2 * kStages + 2 * kAccStages + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffGroup = kOffMisc + 64;
@@ -97,8 +99,9 @@ struct TileInfo {
 
 // Work unit u of a cluster = CM m-tiles x one n-tile; block `rank` of the
 // cluster takes m-tile CM*mu + rank.  Dense units follow a banded raster
-// (kBandM m-tiles per band, n outer inside a band) so a band of A stays in
-// L2 while B streams; grouped units walk groups, then m-units, then n.
+// (p.band_m m-tiles per band, n outer inside a band) so a band of A stays in
+// L2 while B streams once per band; grouped units walk groups, then
+// m-units, then n.
 template <int BN, bool GROUPED, int CM>
 __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t u, int64_t n_tiles,
                                               uint32_t rank, const GroupSmem* gs) {
@@ -118,7 +121,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t u, in
   } else {
     const int64_t m_tiles = (p.m + BM - 1) / BM;
     const int64_t m_units = (m_tiles + CM - 1) / CM;
-    constexpr int64_t band_units = kBandM / CM;
+    const int64_t band_units = p.band_m / CM;
     const int64_t band_size = band_units * n_tiles;
     const int64_t band = u / band_size;
     const int64_t within = u - band * band_size;
@@ -355,79 +358,93 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(mma_done, 0, s_abort, p.status, p.wait_limit_ns, true);
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
-    const uint32_t q = warp & 3u;  // tensor-memory lane quarter of this warp
-    uint8_t* stage_buf = sEpi + (warp - 2) * 4096;
+    // Eight warps: warp w reads lane quarter w % 4 (rows 32*(w%4) ..) and
+    // column half (w - 2) / 4 of the accumulator.  Each warp first pulls its
+    // whole share out of tensor memory into registers (FP32, or packed BF16),
+    // releases the accumulator to the MMA warp, and only then converts and
+    // stores through a 2 KB shared staging buffer, so the stores overlap the
+    // next tile's main loop.
+    constexpr int kCols = BN / 2;                  // accumulator columns per warp
+    const uint32_t q = warp & 3u;
+    const uint32_t half = (warp - 2) >> 2;
+    uint8_t* stage_buf = sEpi + (warp - 2) * kEpiStageBytes;
     uint32_t acc = 0, acc_phase = 0;
     for (int64_t u = cluster_id; u < num_units; u += num_clusters) {
       const TileInfo ti = tile_info<BN, GROUPED, CM>(p, u, n_tiles, rank, gs);
       const bool got = mbar_wait(&acc_full[acc], acc_phase, s_abort, p.status, p.wait_limit_ns);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
-      const uint32_t t_row = tmem_base + ((q * 32u) << 16) + acc * BN;
-      const int64_t row_base = ti.m0 + q * 32;
-      uint8_t* my_row = stage_buf + lane * 128;
+      const uint32_t t_row = tmem_base + ((q * 32u) << 16) + acc * BN + half * kCols;
+      const int64_t grow0 = ti.m0 + q * 32;
+      const int64_t gcol0 = ti.n0 + half * kCols;
+      // staged rows are 64 bytes: 16-byte chunk j of row r sits at chunk
+      // j ^ ((r >> 1) & 3), which keeps both the row-wise writes and the
+      // 4-lanes-per-row reads free of bank conflicts.
+      auto chunk_at = [](int r, int j) { return r * 64 + ((j ^ ((r >> 1) & 3)) * 16); };
       if (p.y_fp32) {
-        float* y = static_cast<float*>(p.y);
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + c * 32, r);
-          tmem_ld_wait();
+        uint32_t v[kCols];
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(my_row + ((j ^ (lane & 7)) * 16)) =
-                make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        for (int c = 0; c < kCols / 32; ++c)
+          tmem_ld_32x32b_x32(t_row + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+        tmem_ld_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&acc_empty[acc]);
+        float* y = static_cast<float*>(p.y);
+#pragma unroll
+        for (int pass = 0; pass < kCols / 16; ++pass) {  // 16 FP32 columns = 64 bytes per row
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(stage_buf + chunk_at(lane, j)) =
+                make_uint4(v[pass * 16 + 4 * j], v[pass * 16 + 4 * j + 1],
+                           v[pass * 16 + 4 * j + 2], v[pass * 16 + 4 * j + 3]);
           __syncwarp();
 #pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int rr = it * 4 + (lane >> 3);
-            const int j = lane & 7;
-            const int64_t grow = row_base + rr;
-            const int64_t gcol = ti.n0 + c * 32 + j * 4;
-            if (grow < ti.m_end && gcol < p.n) {
-              const uint4 v =
-                  *reinterpret_cast<const uint4*>(stage_buf + rr * 128 + ((j ^ (rr & 7)) * 16));
-              *reinterpret_cast<uint4*>(y + grow * p.ldy + gcol) = v;
-            }
+          for (int it = 0; it < 4; ++it) {
+            const int rr = it * 8 + (lane >> 2);
+            const int j = lane & 3;
+            const int64_t grow = grow0 + rr;
+            const int64_t gcol = gcol0 + pass * 16 + j * 4;
+            if (grow < ti.m_end && gcol < p.n)
+              *reinterpret_cast<uint4*>(y + grow * p.ldy + gcol) =
+                  *reinterpret_cast<const uint4*>(stage_buf + chunk_at(rr, j));
           }
           __syncwarp();
         }
       } else {
-        uint16_t* y = static_cast<uint16_t*>(p.y);
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-          uint32_t r0[32], r1[32];
-          tmem_ld_32x32b_x32(t_row + c * 64, r0);
-          tmem_ld_32x32b_x32(t_row + c * 64 + 32, r1);
+        uint32_t w[kCols / 2];
+#pragma unroll
+        for (int c = 0; c < kCols / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + c * 32, r);
           tmem_ld_wait();
-          uint32_t w[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            w[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
-            w[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
-          }
+          for (int i = 0; i < 16; ++i)
+            w[c * 16 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+        }
+        tc_fence_before_sync();
+        mbar_arrive(&acc_empty[acc]);
+        uint16_t* y = static_cast<uint16_t*>(p.y);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(my_row + ((j ^ (lane & 7)) * 16)) =
-                make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        for (int pass = 0; pass < kCols / 32; ++pass) {  // 32 BF16 columns = 64 bytes per row
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(stage_buf + chunk_at(lane, j)) =
+                make_uint4(w[pass * 16 + 4 * j], w[pass * 16 + 4 * j + 1],
+                           w[pass * 16 + 4 * j + 2], w[pass * 16 + 4 * j + 3]);
           __syncwarp();
 #pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int rr = it * 4 + (lane >> 3);
-            const int j = lane & 7;
-            const int64_t grow = row_base + rr;
-            const int64_t gcol = ti.n0 + c * 64 + j * 8;
-            if (grow < ti.m_end && gcol < p.n) {
-              const uint4 v =
-                  *reinterpret_cast<const uint4*>(stage_buf + rr * 128 + ((j ^ (rr & 7)) * 16));
-              *reinterpret_cast<uint4*>(y + grow * p.ldy + gcol) = v;
-            }
+          for (int it = 0; it < 4; ++it) {
+            const int rr = it * 8 + (lane >> 2);
+            const int j = lane & 3;
+            const int64_t grow = grow0 + rr;
+            const int64_t gcol = gcol0 + pass * 32 + j * 8;
+            if (grow < ti.m_end && gcol < p.n)
+              *reinterpret_cast<uint4*>(y + grow * p.ldy + gcol) =
+                  *reinterpret_cast<const uint4*>(stage_buf + chunk_at(rr, j));
           }
           __syncwarp();
         }
       }
-      tc_fence_before_sync();
-      mbar_arrive(&acc_empty[acc]);
       if (++acc == C::kAccStages) {
         acc = 0;
         acc_phase ^= 1u;

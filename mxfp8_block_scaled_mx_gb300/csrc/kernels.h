@@ -43,6 +43,7 @@ struct GemmParams {
   int32_t groups;          // 0 for the dense GEMM
   uint32_t* status;
   uint64_t wait_limit_ns;
+  int32_t band_m;          // m-tiles per raster band (dense), a multiple of 2
 };
 
 // Tile width along N of the GEMM kernel: 128 (double-buffered accumulator)

@@ -123,6 +123,11 @@ mx_status gemm_common(int64_t m, int64_t n, int64_t k, const uint8_t* a, const u
   p.groups = groups;
   p.status = st->status;
   p.wait_limit_ns = g_wait_ns;
+  p.band_m = 32;
+  if (const char* env = std::getenv("MX_GEMM_BAND_M")) {
+    const int v = std::atoi(env);
+    if (v >= 2 && v % 2 == 0) p.band_m = v;
+  }
   const int block_n = block_n_choice(p);
   // Dense GEMMs pair blocks (B tile multicast); grouped GEMMs measured
   // slightly faster unpaired.  MX_GEMM_CLUSTER_M overrides (1 or 2).
