@@ -294,7 +294,7 @@ def measure_rows(mx, peaks, dev, stream):
 
 # ---------------------------------------------------------------- CPU oracle baseline
 
-def oracle_sample(rows: int = 512, cols: int = 2048):
+def oracle_sample(rows: int = 4096, cols: int = 4096):
     """The CPU oracle, as it stands, on a bounded sample of the forward
     workload: `rows` token rows of X and `cols` columns of W with the full
     K = 7168, drawn from the workload's distributions; oracle quantize of

@@ -481,10 +481,16 @@ cudaError_t launch_impl(const GemmParams& p, const CUtensorMap& ta, const CUtens
                         int num_sms, cudaStream_t stream) {
   using C = Cfg<BN, GROUPED>;
   auto kern = mx_gemm_kernel<BN, GROUPED, CM>;
-  // Per device, the attribute is idempotent and cheap; set it every time.
-  cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  // The attribute is per function and device; set it once per device.
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
   const int64_t n_tiles = (p.n + BN - 1) / BN;
   const int64_t m_tiles = (p.m + BM - 1) / BM;
   // upper bound of the work units (grouped: every group may add a partial unit)

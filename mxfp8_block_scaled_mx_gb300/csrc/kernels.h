@@ -23,10 +23,14 @@ struct QuantizeParams {
   const int32_t* offsets;  // grouped rowwise only: device int32[groups + 1]
   int32_t groups;
   uint32_t* status;    // device status word
+  uint64_t wait_limit_ns;
 };
 
-cudaError_t launch_quantize(const QuantizeParams& p, cudaStream_t stream);
-cudaError_t launch_quantize_grouped(const QuantizeParams& p, cudaStream_t stream);
+// tmap_x: 2-D bf16 tensor map over x (box 128 x 128, no swizzle).
+cudaError_t launch_quantize(const QuantizeParams& p, const CUtensorMap& tmap_x, int num_sms,
+                            cudaStream_t stream);
+cudaError_t launch_quantize_grouped(const QuantizeParams& p, const CUtensorMap& tmap_x,
+                                    int num_sms, cudaStream_t stream);
 
 struct GemmParams {
   int64_t m;           // rows of A and Y (grouped: total rows)

@@ -81,6 +81,21 @@ mx_status encode_codes_map(CUtensorMap* map, const void* base, int64_t inner, in
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
+// 2-D bf16 tensor map over x[rows, cols] (leading dimension ldx elements),
+// tile box 128 x 128, no swizzle, zero fill outside the matrix.
+mx_status encode_bf16_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
+                          int64_t ldx) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx * 2)};
+  cuuint32_t box[2] = {128u, 128u};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
 int block_n_choice(const mx::GemmParams& p) {
   const char* env = std::getenv("MX_GEMM_BLOCK_N");
   if (env) {
@@ -191,7 +206,11 @@ mx_status mx_quantize(const void* x, mx_dtype x_dtype, int64_t rows, int64_t col
   p.fmt = fmt;
   p.rule = rule;
   p.status = st->status;
-  return mx::launch_quantize(p, stream) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+  p.wait_limit_ns = g_wait_ns;
+  if (rows == 0 || cols == 0) return MX_OK;
+  CUtensorMap tmap;
+  if ((s = encode_bf16_map(&tmap, x, cols, rows, ldx)) != MX_OK) return s;
+  return mx::launch_quantize(p, tmap, st->num_sms, stream) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
 mx_status mx_quantize_grouped(const void* x, mx_dtype x_dtype, int64_t total_rows, int64_t cols,
@@ -222,7 +241,14 @@ mx_status mx_quantize_grouped(const void* x, mx_dtype x_dtype, int64_t total_row
   p.offsets = d_offsets;
   p.groups = groups;
   p.status = st->status;
-  return mx::launch_quantize_grouped(p, stream) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+  p.wait_limit_ns = g_wait_ns;
+  if (cols == 0) return MX_OK;
+  CUtensorMap tmap;
+  // an empty token set still needs a valid map (1 row) for the offsets check
+  if ((status = encode_bf16_map(&tmap, x, cols, total_rows > 0 ? total_rows : 1, ldx)) != MX_OK)
+    return status;
+  return mx::launch_quantize_grouped(p, tmap, st->num_sms, stream) == cudaSuccess ? MX_OK
+                                                                                  : MX_ERR_CUDA;
 }
 
 mx_status mx_gemm(int64_t m, int64_t n, int64_t k, const uint8_t* a, const uint8_t* sa, mx_fmt fa,

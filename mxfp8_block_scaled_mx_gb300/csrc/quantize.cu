@@ -7,41 +7,41 @@
 // "Numerical hazards: subnormals, saturation, and rounding" (round to
 // nearest even, subnormals kept, saturation after rounding).
 //
-// One block of 256 threads owns a 128-row x 128-column tile of x.  Each
-// thread issues eight coalesced 16-byte loads up front.
+// The kernel is HBM-bound, so it is built around deep prefetch: one
+// persistent block per SM, a producer thread that streams 128x128 bf16 tiles
+// (32 KB) into a ring of shared-memory slots with cp.async.bulk.tensor, and
+// two groups of eight consumer warps that quantize alternate tiles straight
+// out of shared memory while the next tiles are in flight.
 //  - Rowwise: the four lanes that hold one 32-element block reduce its amax
-//    with two xor-shuffles, derive the scale exponent from the bf16 bit
-//    pattern, scale by an exact power of two and convert pairs with the
-//    hardware cvt.rn.satfinite instruction.  The tile's 128 x 4 scales form
-//    exactly one 512-byte swizzled unit, assembled in shared memory and
-//    written with one coalesced store.
-//  - Columnwise: the tile is staged in shared memory; each thread reduces
-//    and encodes two adjacent columns of a 32-row block (one 32-bit shared
-//    load and one SIMD max per row), the codes are transposed in shared
-//    memory and written back as 128-byte rows of the [cols, rows] output,
-//    again with one 512-byte scale unit per tile.
+//    with two xor-shuffles (SIMD max.u16x2 within a lane), derive the scale
+//    exponent from the bf16 bit pattern, scale by an exact power of two and
+//    convert pairs with the hardware cvt.rn.satfinite instruction.  The
+//    tile's 128 x 4 scales form exactly one 512-byte swizzled unit,
+//    assembled in shared memory and written with one coalesced store.
+//  - Columnwise: each thread reduces and encodes two adjacent columns of a
+//    32-row block (one 32-bit shared load and one SIMD max per row), the
+//    codes are transposed in shared memory and written back as 128-byte rows
+//    of the [cols, rows] output, again with one 512-byte scale unit per tile.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 #include "groups.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 #include "status.cuh"
 
 namespace mx {
 namespace {
 
-constexpr int kTile = 128;          // rows and columns of x per block
-constexpr int kThreads = 256;
-constexpr int kColPitch = 144;      // bytes per transposed code row in smem (conflict-free)
-
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
+constexpr int kTile = 128;                    // rows and columns of x per tile
+constexpr int kGroupThreads = 256;            // one consumer group: 8 warps
+constexpr int kGroups = 2;                    // consumer groups (alternate tiles)
+constexpr int kThreads = kGroups * kGroupThreads + 32;  // + one producer warp
+constexpr int kStages = 4;                    // bf16 tile slots in flight
+constexpr int kTileBytes = kTile * kTile * 2; // 32 KB
+constexpr int kColPitch = 144;                // bytes per transposed code row in smem
 
 // Per-halfword unsigned max of two packed pairs (one SIMD instruction).
 __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
@@ -123,50 +123,89 @@ __device__ __forceinline__ int unit_offset(int r, int c) {
   return (r & 31) * 16 + (r >> 5) * 4 + c;
 }
 
-struct TileCoords {
-  int64_t x_row0;       // first row of x held by this block
+struct Tile {
+  int64_t x_row0;       // first row of x in the tile
+  int64_t c0;           // first column of x in the tile
   int64_t rows_valid;   // rows of the tile that exist (<= 128)
   int64_t scale_rt;     // row-tile index of the rowwise scale unit
 };
 
+struct GroupInfo {
+  int32_t off[kMaxGroups + 1];
+  int32_t tiles[kMaxGroups + 1];
+  int32_t valid;
+};
+
+// Tile t of the launch: dense tiles are (row tile, column tile) in
+// row-major order; grouped tiles walk the per-group padded row tiles.
+template <bool GROUPED>
+__device__ __forceinline__ Tile tile_of(const QuantizeParams& p, int64_t t, int64_t col_tiles,
+                                        const GroupInfo* gi) {
+  Tile tl;
+  const int64_t rt = t / col_tiles;
+  tl.c0 = (t - rt * col_tiles) * kTile;
+  tl.scale_rt = rt;
+  if constexpr (GROUPED) {
+    const int g = find_group(gi->tiles, p.groups, static_cast<int32_t>(rt));
+    tl.x_row0 = static_cast<int64_t>(gi->off[g]) + (rt - gi->tiles[g]) * kTile;
+    tl.rows_valid = ::min(static_cast<int64_t>(kTile), gi->off[g + 1] - tl.x_row0);
+  } else {
+    tl.x_row0 = rt * kTile;
+    tl.rows_valid = ::min(static_cast<int64_t>(kTile), p.rows - tl.x_row0);
+  }
+  return tl;
+}
+
+__device__ __forceinline__ void group_bar(int group) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kGroupThreads) : "memory");
+}
+
+// Group barrier that also returns, to every thread, whether `pred` held for
+// any thread of the group (so a bail-out decision is uniform).
+__device__ __forceinline__ bool group_bar_any(int group, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(1 + group), "r"(kGroupThreads)
+      : "memory");
+  return r != 0;
+}
+
+// One consumer group quantizes one tile held in ring slot `xs` (128 rows of
+// 256 bytes).  `lt` is the thread's index inside the group.
 template <int FMT, bool ROW, bool COL>
-__device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const TileCoords tc,
-                                              int64_t c0, uint8_t* smem) {
+__device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Tile& tl,
+                                              const uint8_t* xs, uint8_t* s_q,
+                                              uint8_t* s_unit_row, uint8_t* s_unit_col,
+                                              uint64_t* empty_bar, int group, int lt) {
   constexpr int emax = FMT == 0 ? 8 : 15;
-  const int tid = threadIdx.x;
-  uint8_t* s_unit_row = smem;              // 512 B
-  uint8_t* s_unit_col = smem + 512;        // 512 B
-  uint32_t* s_x = reinterpret_cast<uint32_t*>(smem + 1024);  // 128 rows x 64 bf16 pairs
-  uint8_t* s_q = smem + 1024 + kTile * kTile * 2;             // 128 x 144 B
+  const uint32_t lane = lt & 31;
 
-  // Zero the scale units (padding entries stay 0).
-  if (tid < 128) {
-    if (ROW) reinterpret_cast<uint32_t*>(s_unit_row)[tid] = 0u;
-    if (COL) reinterpret_cast<uint32_t*>(s_unit_col)[tid] = 0u;
-  }
-
-  // Thread t holds the 8-column chunk t % 16 of rows t / 16 + 16 * it.
-  const int ch = tid & 15;
-  const int lr0 = tid >> 4;
-  const int64_t gc = c0 + ch * 8;
+  // Thread lt holds the 8-column chunk lt % 16 of rows lt / 16 + 16 * it.
+  const int ch = lt & 15;
+  const int lr0 = lt >> 4;
+  const int64_t gc = tl.c0 + ch * 8;
   const bool col_ok = gc < p.cols;
-  const uint16_t* xp = p.x + (tc.x_row0 + lr0) * p.ldx + gc;
-  const int64_t x_step = 16 * p.ldx;
-  uint4 v[8];
-#pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const bool ok = col_ok && lr0 + it * 16 < tc.rows_valid;
-    v[it] = ok ? ld_stream(xp + it * x_step) : make_uint4(0, 0, 0, 0);
-  }
-  __syncthreads();  // scale units zeroed
 
   if constexpr (ROW) {
-    uint8_t* qp = p.q_row + (tc.x_row0 + lr0) * p.cols + gc;
+    uint4 v[8];
+#pragma unroll
+    for (int it = 0; it < 8; ++it)
+      v[it] = *reinterpret_cast<const uint4*>(xs + (lr0 + it * 16) * (kTile * 2) + ch * 16);
+    if constexpr (!COL) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);  // slot fully read by this warp
+    }
+    uint8_t* qp = p.q_row + (tl.x_row0 + lr0) * p.cols + gc;
     const int64_t q_step = 16 * p.cols;
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
       const int lr = lr0 + it * 16;
-      const bool ok = col_ok && lr < tc.rows_valid;
+      const bool ok = col_ok && lr < tl.rows_valid;
       // the four lanes holding one 32-element block share its amax
       uint32_t a = amax_bits8(v[it]);
       a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
@@ -183,33 +222,28 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
       }
       if (ok) {
         *reinterpret_cast<uint2*>(qp + it * q_step) = codes;
-        if ((tid & 3) == 0) s_unit_row[unit_offset(lr, ch >> 2)] = sbyte;
+        if ((lt & 3) == 0) s_unit_row[unit_offset(lr, ch >> 2)] = sbyte;
       }
     }
   }
 
   if constexpr (COL) {
-    // Stage the tile: row lr holds 64 bf16 pairs (256 bytes).
-#pragma unroll
-    for (int it = 0; it < 8; ++it)
-      *reinterpret_cast<uint4*>(s_x + (lr0 + it * 16) * 64 + ch * 4) = v[it];
-  }
-  __syncthreads();
-
-  if constexpr (COL) {
-    // Thread t: columns 2*(t % 64) and 2*(t % 64) + 1, 32-row block t / 64.
-    // One 32-bit shared load gives both columns of a row, so the amax of
-    // the two column blocks is one SIMD max per row.
-    const int cp = tid & 63;
-    const int rb = tid >> 6;
-    const bool ok = c0 + 2 * cp < p.cols && rb * 32 < tc.rows_valid;
+    // Thread lt: columns 2*(lt % 64) and 2*(lt % 64) + 1, 32-row block
+    // lt / 64.  One 32-bit shared load gives both columns of a row, so the
+    // amax of the two column blocks is one SIMD max per row.
+    const uint32_t* xw = reinterpret_cast<const uint32_t*>(xs);
+    const int cp = lt & 63;
+    const int rb = lt >> 6;
+    const bool ok = tl.c0 + 2 * cp < p.cols && rb * 32 < tl.rows_valid;
     uint32_t w[32];
     uint32_t a2 = 0;
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
-      w[r] = s_x[(rb * 32 + r) * 64 + cp];
+      w[r] = xw[(rb * 32 + r) * 64 + cp];
       a2 = max_u16x2(a2, w[r] & 0x7FFF7FFFu);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar);  // slot fully read by this warp
     const uint32_t a_lo = a2 & 0xFFFFu;
     const uint32_t a_hi = a2 >> 16;
     const bool nan_lo = a_lo >= 0x7F80u;
@@ -247,117 +281,180 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
           nan_hi ? kNanScale : static_cast<uint8_t>(e_hi + 127);
     }
   }
-  __syncthreads();
+  group_bar(group);  // scale units and transposed codes complete
 
   if constexpr (ROW) {
-    if (tid < 32) {
+    if (lt < 32) {
       const int64_t tiles_k = (p.cols + 127) / 128;
-      const int64_t unit = tc.scale_rt * tiles_k + c0 / 128;
-      reinterpret_cast<uint4*>(p.s_row + unit * 512)[tid] =
-          reinterpret_cast<const uint4*>(s_unit_row)[tid];
+      const int64_t unit = tl.scale_rt * tiles_k + tl.c0 / 128;
+      reinterpret_cast<uint4*>(p.s_row + unit * 512)[lt] =
+          reinterpret_cast<const uint4*>(s_unit_row)[lt];
     }
   }
   if constexpr (COL) {
     // Transposed codes: output row (c0 + c) holds x rows [x_row0, x_row0 + 128).
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int idx = i * kThreads + tid;
+      const int idx = i * kGroupThreads + lt;
       const int c = idx >> 3;
       const int j = idx & 7;
-      if (c0 + c < p.cols && j * 16 < tc.rows_valid) {
+      if (tl.c0 + c < p.cols && j * 16 < tl.rows_valid) {
         const uint4 q = *reinterpret_cast<const uint4*>(s_q + c * kColPitch + j * 16);
-        *reinterpret_cast<uint4*>(p.q_col + (c0 + c) * p.rows + tc.x_row0 + j * 16) = q;
+        *reinterpret_cast<uint4*>(p.q_col + (tl.c0 + c) * p.rows + tl.x_row0 + j * 16) = q;
       }
     }
-    if (tid < 32) {
+    if (lt < 32) {
       const int64_t tiles_k = (p.rows + 127) / 128;
-      const int64_t unit = (c0 / 128) * tiles_k + tc.x_row0 / 128;
-      reinterpret_cast<uint4*>(p.s_col + unit * 512)[tid] =
-          reinterpret_cast<const uint4*>(s_unit_col)[tid];
+      const int64_t unit = (tl.c0 / 128) * tiles_k + tl.x_row0 / 128;
+      reinterpret_cast<uint4*>(p.s_col + unit * 512)[lt] =
+          reinterpret_cast<const uint4*>(s_unit_col)[lt];
     }
   }
 }
 
-template <int FMT, bool ROW, bool COL>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(const QuantizeParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kTile;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kTile;
-  TileCoords tc;
-  tc.x_row0 = r0;
-  tc.rows_valid = ::min(static_cast<int64_t>(kTile), p.rows - r0);
-  tc.scale_rt = blockIdx.x;
-  quantize_tile<FMT, ROW, COL>(p, tc, c0, smem);
-}
+struct QSmem {
+  static constexpr int kOffRing = 0;
+  static constexpr int kOffGroupBuf = kOffRing + kStages * kTileBytes;
+  static constexpr int kGroupBufBytes = kTile * kColPitch + 1024;  // s_q + two scale units
+  static constexpr int kOffBar = kOffGroupBuf + kGroups * kGroupBufBytes;
+  static constexpr int kOffMisc = kOffBar + 2 * kStages * 8;
+  static constexpr int kOffGroupInfo = kOffMisc + 16;
+  static constexpr int kBytes = kOffGroupInfo + int(sizeof(GroupInfo)) + 1024;
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+};
 
-// Rowwise quantization of expert-grouped rows.  blockIdx.x walks the
-// padded scale row tiles; tile t belongs to group g with
-// s_tiles[g] <= t < s_tiles[g+1] and covers rows o_g + 128 (t - s_tiles[g])
-// onward, clipped to the group.
-template <int FMT>
-__global__ void __launch_bounds__(kThreads) quantize_grouped_kernel(const QuantizeParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ int32_t s_off[kMaxGroups + 1];
-  __shared__ int32_t s_tiles[kMaxGroups + 1];
-  __shared__ int32_t s_valid;
-  group_tile_prefix(p.offsets, p.groups, p.rows, s_off, s_tiles, &s_valid);
+template <int FMT, bool ROW, bool COL, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 1)
+    quantize_kernel(const __grid_constant__ CUtensorMap tmap_x, const QuantizeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + QSmem::kOffBar);
+  uint64_t* empty = full + kStages;
+  volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + QSmem::kOffMisc);
+  GroupInfo* gi = reinterpret_cast<GroupInfo*>(smem + QSmem::kOffGroupInfo);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  constexpr int kProducerWarp = kGroups * kGroupThreads / 32;
+
+  if (warp == kProducerWarp && lane == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kGroupThreads / 32);  // one arrival per consumer warp
+    }
+    *s_abort = 0u;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tmap_x);
+  }
+  if constexpr (GROUPED) group_tile_prefix(p.offsets, p.groups, p.rows, gi->off, gi->tiles, &gi->valid);
   __syncthreads();
-  if (!s_valid) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
-      record_device_status(p.status, MX_DEV_BAD_OFFSETS);
-    return;
+
+  const int64_t col_tiles = (p.cols + kTile - 1) / kTile;
+  int64_t num_tiles;
+  if constexpr (GROUPED) {
+    if (!gi->valid) {
+      if (blockIdx.x == 0 && tid == 0) record_device_status(p.status, MX_DEV_BAD_OFFSETS);
+      num_tiles = 0;
+    } else {
+      num_tiles = static_cast<int64_t>(gi->tiles[p.groups]) * col_tiles;
+    }
+  } else {
+    num_tiles = ((p.rows + kTile - 1) / kTile) * col_tiles;
   }
-  const int32_t t = blockIdx.x;
-  if (t >= s_tiles[p.groups]) return;
-  const int g = find_group(s_tiles, p.groups, t);
-  TileCoords tc;
-  tc.x_row0 = static_cast<int64_t>(s_off[g]) + static_cast<int64_t>(t - s_tiles[g]) * kTile;
-  tc.rows_valid = ::min(static_cast<int64_t>(kTile), static_cast<int64_t>(s_off[g + 1]) - tc.x_row0);
-  tc.scale_rt = t;
-  quantize_tile<FMT, true, false>(p, tc, static_cast<int64_t>(blockIdx.y) * kTile, smem);
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      int64_t issued = 0;
+      for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x, ++issued) {
+        const uint32_t s = static_cast<uint32_t>(issued % kStages);
+        const uint32_t ph = static_cast<uint32_t>((issued / kStages) & 1);
+        if (!mbar_wait(&empty[s], ph ^ 1u, s_abort, p.status, p.wait_limit_ns)) break;
+        const Tile tl = tile_of<GROUPED>(p, t, col_tiles, gi);
+        mbar_arrive_expect_tx(&full[s], kTileBytes);
+        tma_load_2d(smem + QSmem::kOffRing + s * kTileBytes, &tmap_x, &full[s],
+                    static_cast<int32_t>(tl.c0), static_cast<int32_t>(tl.x_row0));
+      }
+      // every issued copy lands before the block exits
+      for (int s = 0; s < kStages; ++s) {
+        const int64_t fills = issued > s ? (issued - s + kStages - 1) / kStages : 0;
+        if (fills)
+          mbar_wait(&full[s], static_cast<uint32_t>((fills - 1) & 1), s_abort, p.status,
+                    p.wait_limit_ns, true);
+      }
+    }
+  } else {
+    const int group = warp / (kGroupThreads / 32);
+    const int lt = tid - group * kGroupThreads;
+    uint8_t* gbuf = smem + QSmem::kOffGroupBuf + group * QSmem::kGroupBufBytes;
+    uint8_t* s_q = gbuf;
+    uint8_t* s_unit_row = gbuf + kTile * kColPitch;
+    uint8_t* s_unit_col = s_unit_row + 512;
+    int64_t i = group;  // this block's tile counter; the group takes every kGroups-th tile
+    for (int64_t t = blockIdx.x + group * static_cast<int64_t>(gridDim.x); t < num_tiles;
+         t += kGroups * static_cast<int64_t>(gridDim.x), i += kGroups) {
+      const uint32_t s = static_cast<uint32_t>(i % kStages);
+      const uint32_t ph = static_cast<uint32_t>((i / kStages) & 1);
+      const Tile tl = tile_of<GROUPED>(p, t, col_tiles, gi);
+      group_bar(group);  // the group's previous tile is fully written out
+      if (lt < 128) {
+        if (ROW) reinterpret_cast<uint32_t*>(s_unit_row)[lt] = 0u;
+        if (COL) reinterpret_cast<uint32_t*>(s_unit_col)[lt] = 0u;
+      }
+      const bool got = mbar_wait(&full[s], ph, s_abort, p.status, p.wait_limit_ns);
+      // scale units zeroed; a wait that gave up anywhere stops the whole group
+      if (group_bar_any(group, !got)) break;
+      quantize_tile<FMT, ROW, COL>(p, tl, smem + QSmem::kOffRing + s * kTileBytes, s_q,
+                                   s_unit_row, s_unit_col, &empty[s], group, lt);
+    }
+  }
 }
 
-template <int FMT, bool ROW, bool COL>
-cudaError_t launch_dense(const QuantizeParams& p, cudaStream_t stream) {
-  auto kern = quantize_kernel<FMT, ROW, COL>;
-  const int smem = COL ? 1024 + kTile * kTile * 2 + kTile * kColPitch : 1024;
-  if (smem > 48 * 1024) {
-    cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+template <int FMT, bool ROW, bool COL, bool GROUPED>
+cudaError_t launch_one(const QuantizeParams& p, const CUtensorMap& tmap, int64_t tiles,
+                       int num_sms, cudaStream_t stream) {
+  auto kern = quantize_kernel<FMT, ROW, COL, GROUPED>;
+  // The attribute is per function and device; set it once per device.
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QSmem::kBytes);
     if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  dim3 grid(static_cast<unsigned>((p.rows + kTile - 1) / kTile),
-            static_cast<unsigned>((p.cols + kTile - 1) / kTile));
-  kern<<<grid, kThreads, smem, stream>>>(p);
+  const int64_t grid = tiles < num_sms ? tiles : num_sms;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<static_cast<unsigned>(grid), kThreads, QSmem::kBytes, stream>>>(tmap, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_quantize(const QuantizeParams& p, cudaStream_t stream) {
+cudaError_t launch_quantize(const QuantizeParams& p, const CUtensorMap& tmap_x, int num_sms,
+                            cudaStream_t stream) {
   if (p.rows == 0 || p.cols == 0) return cudaSuccess;
   const bool row = p.q_row != nullptr;
   const bool col = p.q_col != nullptr;
+  const int64_t tiles = ((p.rows + kTile - 1) / kTile) * ((p.cols + kTile - 1) / kTile);
   if (p.fmt == 0) {
-    if (row && col) return launch_dense<0, true, true>(p, stream);
-    if (row) return launch_dense<0, true, false>(p, stream);
-    return launch_dense<0, false, true>(p, stream);
+    if (row && col) return launch_one<0, true, true, false>(p, tmap_x, tiles, num_sms, stream);
+    if (row) return launch_one<0, true, false, false>(p, tmap_x, tiles, num_sms, stream);
+    return launch_one<0, false, true, false>(p, tmap_x, tiles, num_sms, stream);
   }
-  if (row && col) return launch_dense<1, true, true>(p, stream);
-  if (row) return launch_dense<1, true, false>(p, stream);
-  return launch_dense<1, false, true>(p, stream);
+  if (row && col) return launch_one<1, true, true, false>(p, tmap_x, tiles, num_sms, stream);
+  if (row) return launch_one<1, true, false, false>(p, tmap_x, tiles, num_sms, stream);
+  return launch_one<1, false, true, false>(p, tmap_x, tiles, num_sms, stream);
 }
 
-cudaError_t launch_quantize_grouped(const QuantizeParams& p, cudaStream_t stream) {
+cudaError_t launch_quantize_grouped(const QuantizeParams& p, const CUtensorMap& tmap_x,
+                                    int num_sms, cudaStream_t stream) {
   if (p.cols == 0) return cudaSuccess;
-  const int64_t max_tiles = (p.rows + kTile - 1) / kTile + p.groups;
-  dim3 grid(static_cast<unsigned>(max_tiles), static_cast<unsigned>((p.cols + kTile - 1) / kTile));
-  if (p.fmt == 0) {
-    quantize_grouped_kernel<0><<<grid, kThreads, 1024, stream>>>(p);
-  } else {
-    quantize_grouped_kernel<1><<<grid, kThreads, 1024, stream>>>(p);
-  }
-  return cudaGetLastError();
+  // upper bound of the padded row tiles; the kernel computes the exact count
+  const int64_t tiles = ((p.rows + kTile - 1) / kTile + p.groups) * ((p.cols + kTile - 1) / kTile);
+  if (p.fmt == 0) return launch_one<0, true, false, true>(p, tmap_x, tiles, num_sms, stream);
+  return launch_one<1, true, false, true>(p, tmap_x, tiles, num_sms, stream);
 }
 
 }  // namespace mx
