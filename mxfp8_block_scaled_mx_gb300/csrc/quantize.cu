@@ -10,7 +10,7 @@
 // The kernel is HBM-bound, so it is built around deep prefetch: one
 // persistent block per SM, a producer thread that streams 128x128 bf16 tiles
 // (32 KB) into a ring of shared-memory slots with cp.async.bulk.tensor, and
-// two groups of eight consumer warps that quantize alternate tiles straight
+// two groups of eight consumer warps that take tiles round-robin, straight
 // out of shared memory while the next tiles are in flight.
 //  - Rowwise: the four lanes that hold one 32-element block reduce its amax
 //    with two xor-shuffles (SIMD max.u16x2 within a lane), derive the scale
@@ -37,9 +37,8 @@ namespace {
 
 constexpr int kTile = 128;                    // rows and columns of x per tile
 constexpr int kGroupThreads = 256;            // one consumer group: 8 warps
-constexpr int kGroups = 2;                    // consumer groups (alternate tiles)
+constexpr int kGroups = 2;                    // consumer groups (round-robin tiles)
 constexpr int kThreads = kGroups * kGroupThreads + 32;  // + one producer warp
-constexpr int kStages = 4;                    // bf16 tile slots in flight
 constexpr int kTileBytes = kTile * kTile * 2; // 32 KB
 constexpr int kColPitch = 144;                // bytes per transposed code row in smem
 
@@ -312,10 +311,20 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
   }
 }
 
+// Shared memory: the tile ring, then per consumer group the transposed-code
+// buffer (columnwise modes only) and two scale units.
+template <bool COL>
 struct QSmem {
+  static constexpr int kStages = COL ? 4 : 6;   // bf16 tile slots in flight
+  // Tile i lives in slot i % kStages and is consumed by group i % kGroups.
+  // Successive users of a slot (tiles i and i + kStages) must belong to the
+  // same group: a group can then never wait on a slot's next phase while
+  // the slot's current phase is still outstanding, which a parity wait
+  // cannot tell apart from a completed phase.
+  static_assert(kStages % kGroups == 0, "ring slots must map to one consumer group");
   static constexpr int kOffRing = 0;
   static constexpr int kOffGroupBuf = kOffRing + kStages * kTileBytes;
-  static constexpr int kGroupBufBytes = kTile * kColPitch + 1024;  // s_q + two scale units
+  static constexpr int kGroupBufBytes = (COL ? kTile * kColPitch : 0) + 1024;
   static constexpr int kOffBar = kOffGroupBuf + kGroups * kGroupBufBytes;
   static constexpr int kOffMisc = kOffBar + 2 * kStages * 8;
   static constexpr int kOffGroupInfo = kOffMisc + 16;
@@ -326,6 +335,8 @@ struct QSmem {
 template <int FMT, bool ROW, bool COL, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     quantize_kernel(const __grid_constant__ CUtensorMap tmap_x, const QuantizeParams p) {
+  using QSmem = mx::QSmem<COL>;
+  constexpr int kStages = QSmem::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -388,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lt = tid - group * kGroupThreads;
     uint8_t* gbuf = smem + QSmem::kOffGroupBuf + group * QSmem::kGroupBufBytes;
     uint8_t* s_q = gbuf;
-    uint8_t* s_unit_row = gbuf + kTile * kColPitch;
+    uint8_t* s_unit_row = gbuf + (COL ? kTile * kColPitch : 0);
     uint8_t* s_unit_col = s_unit_row + 512;
     int64_t i = group;  // this block's tile counter; the group takes every kGroups-th tile
     for (int64_t t = blockIdx.x + group * static_cast<int64_t>(gridDim.x); t < num_tiles;
@@ -414,6 +425,7 @@ template <int FMT, bool ROW, bool COL, bool GROUPED>
 cudaError_t launch_one(const QuantizeParams& p, const CUtensorMap& tmap, int64_t tiles,
                        int num_sms, cudaStream_t stream) {
   auto kern = quantize_kernel<FMT, ROW, COL, GROUPED>;
+  using QSmem = mx::QSmem<COL>;
   // The attribute is per function and device; set it once per device.
   static bool attr_set[64] = {};
   int dev = 0;
