@@ -248,8 +248,19 @@ def measure_rows(mx, peaks, dev, stream):
                                                "bytes_per_elem": bpe}
         del x, qr, sr, qc, sc
 
-    # backward GEMMs (FP32 out) and the MoE grouped GEMM
+    # backward GEMMs (FP32 out), the fused bias+SiLU forward, the MoE grouped GEMM
     x, w = W.dense_forward(device=dev)
+    xq = mx.quantize(x, "e4m3", "row", stream=stream)
+    wq = mx.quantize(w, "e4m3", "col", stream=stream)
+    bias = torch.randn(w.shape[1], device=dev, dtype=torch.float32)
+    yf = torch.empty((x.shape[0], w.shape[1]), dtype=torch.bfloat16, device=dev)
+    t = time_kernel(lambda: mx.gemm(xq, wq, "bf16", out=yf, stream=stream, bias=bias, act="silu"),
+                    stream, 10)
+    fl = 2 * x.shape[0] * w.shape[1] * x.shape[1]
+    out["forward_bias_silu_16384x18432x7168_bf16"] = {
+        "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
+        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
+    del xq, wq, yf, bias
     dy = W.dense_grad_output(device=dev)
     rq = mx.quantize(dy, "e5m2", "row", stream=stream)
     wq = mx.quantize(w, "e4m3", "row", stream=stream)

@@ -154,6 +154,23 @@ mx_status mx_gemm(int64_t m, int64_t n, int64_t k,
                   const uint8_t* b, const uint8_t* sb, mx_fmt fb,
                   void* y, mx_dtype y_dtype, int64_t ldy, cudaStream_t stream);
 
+/* Activation of the fused epilogue. */
+typedef enum { MX_ACT_NONE = 0, MX_ACT_SILU = 1 } mx_activation;
+
+/* mx_gemm with the fused epilogue of the kernel contract in section
+ * "Hardware support and kernel ABI contracts" (FP32 bias, SiLU, BF16 out):
+ *   y[i, j] = act(acc[i, j] + bias[j]),  act(z) = z / (1 + exp(-z)) for SiLU
+ * The bias add and the activation run in FP32 on the FP32 accumulator,
+ * followed by one rounding to y_dtype (RNE for BF16).
+ * bias: device float[n], 16-byte aligned, or NULL for no bias.
+ * act: MX_ACT_NONE or MX_ACT_SILU.  Other arguments and constraints as
+ * mx_gemm. */
+mx_status mx_gemm_bias_act(int64_t m, int64_t n, int64_t k,
+                           const uint8_t* a, const uint8_t* sa, mx_fmt fa,
+                           const uint8_t* b, const uint8_t* sb, mx_fmt fb,
+                           const float* bias, mx_activation act,
+                           void* y, mx_dtype y_dtype, int64_t ldy, cudaStream_t stream);
+
 /* Grouped (mixture-of-experts) block-scaled GEMM: for every group g,
  *   y[o_g : o_{g+1}, :] = A[o_g : o_{g+1}, :] * B_g^T
  * with the per-row block scales of the dense GEMM.

@@ -31,8 +31,10 @@ DTYPE = {"bf16": 0, "fp32": 1}
 AXIS = {"row": 1, "col": 2, "both": 3}
 RULE = {"floor": 0, "ceil": 1}
 
+ACT = {"none": 0, "silu": 1}
+
 EXPORTS = ("mx_scale_bytes", "mx_grouped_scale_bytes", "mx_quantize", "mx_quantize_grouped",
-           "mx_gemm", "mx_grouped_gemm", "mx_device_status", "mx_status_str",
+           "mx_gemm", "mx_gemm_bias_act", "mx_grouped_gemm", "mx_device_status", "mx_status_str",
            "mx_set_wait_timeout_ns", "mx_selftest_wait_timeout")
 
 
@@ -60,6 +62,9 @@ def _declare(lib):
     lib.mx_quantize_grouped.restype = c.c_int
     lib.mx_gemm.argtypes = [i64, i64, i64, vp, vp, c.c_int, vp, vp, c.c_int, vp, c.c_int, i64, vp]
     lib.mx_gemm.restype = c.c_int
+    lib.mx_gemm_bias_act.argtypes = [i64, i64, i64, vp, vp, c.c_int, vp, vp, c.c_int, vp, c.c_int,
+                                     vp, c.c_int, i64, vp]
+    lib.mx_gemm_bias_act.restype = c.c_int
     lib.mx_grouped_gemm.argtypes = [i32, vp, i64, i64, i64, vp, vp, c.c_int, vp, vp, c.c_int, vp,
                                     c.c_int, vp]
     lib.mx_grouped_gemm.restype = c.c_int
@@ -125,6 +130,11 @@ def mx_quantize_grouped(x, x_dtype, total_rows, cols, ldx, fmt, rule, groups, d_
 
 def mx_gemm(m, n, k, a, sa, fa, b, sb, fb, y, y_dtype, ldy, stream) -> int:
     return lib().mx_gemm(m, n, k, a, sa, fa, b, sb, fb, y, y_dtype, ldy, stream)
+
+
+def mx_gemm_bias_act(m, n, k, a, sa, fa, b, sb, fb, bias, act, y, y_dtype, ldy, stream) -> int:
+    return lib().mx_gemm_bias_act(m, n, k, a, sa, fa, b, sb, fb, bias, act, y, y_dtype, ldy,
+                                  stream)
 
 
 def mx_grouped_gemm(groups, d_offsets, total_m, n, k, a, sa, fa, b, sb, fb, y, y_dtype,
@@ -218,8 +228,9 @@ def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt: str = "e4m3",
 
 
 def gemm(a: MxTensor, b: MxTensor, out_dtype: str = "bf16", out: torch.Tensor | None = None,
-         stream=None) -> torch.Tensor:
-    """y[m, n] = block-scaled A[m, k] * B[n, k]^T."""
+         stream=None, bias: torch.Tensor | None = None, act: str = "none") -> torch.Tensor:
+    """y[m, n] = block-scaled A[m, k] * B[n, k]^T; with `bias` (FP32 [n]) or
+    `act` ("silu") the fused epilogue computes act(y + bias)."""
     m, k = a.codes.shape
     n, k2 = b.codes.shape
     if k != k2:
@@ -227,10 +238,18 @@ def gemm(a: MxTensor, b: MxTensor, out_dtype: str = "bf16", out: torch.Tensor | 
     tdtype = torch.float32 if out_dtype == "fp32" else torch.bfloat16
     if out is None:
         out = torch.empty((m, n), dtype=tdtype, device=a.codes.device)
-    st = mx_gemm(m, n, k, _ptr(a.codes), _ptr(a.scales), FMT[a.fmt], _ptr(b.codes),
-                 _ptr(b.scales), FMT[b.fmt], _ptr(out), DTYPE[out_dtype], out.stride(0),
-                 _stream(stream))
-    _check("mx_gemm", st)
+    if bias is None and act == "none":
+        st = mx_gemm(m, n, k, _ptr(a.codes), _ptr(a.scales), FMT[a.fmt], _ptr(b.codes),
+                     _ptr(b.scales), FMT[b.fmt], _ptr(out), DTYPE[out_dtype], out.stride(0),
+                     _stream(stream))
+        _check("mx_gemm", st)
+        return out
+    if bias is not None and (bias.dtype != torch.float32 or bias.numel() != n or not bias.is_cuda):
+        raise ValueError("bias must be a CUDA float32 tensor of n elements")
+    st = mx_gemm_bias_act(m, n, k, _ptr(a.codes), _ptr(a.scales), FMT[a.fmt], _ptr(b.codes),
+                          _ptr(b.scales), FMT[b.fmt], _ptr(bias), ACT[act], _ptr(out),
+                          DTYPE[out_dtype], out.stride(0), _stream(stream))
+    _check("mx_gemm_bias_act", st)
     return out
 
 

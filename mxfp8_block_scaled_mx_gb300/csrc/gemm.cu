@@ -20,9 +20,11 @@
 //               slot with tcgen05.commit.
 //   warps 2..9  epilogue: tcgen05.ld of the FP32 accumulator into registers
 //               (two warps per 32-lane quarter, half the columns each), early
-//               release of the accumulator, then conversion to FP32/BF16
-//               (RNE), staging through shared memory and coalesced 64-byte
-//               row segments, masked at the matrix (or group) edge.
+//               release of the accumulator, then (optionally) the FP32
+//               bias and SiLU of the kernel contract's epilogue, conversion
+//               to FP32/BF16 (RNE), staging through shared memory and
+//               coalesced 64-byte row segments, masked at the matrix (or
+//               group) edge.
 // With 128-wide tiles the accumulator is double-buffered in tensor memory
 // so the epilogue of one tile overlaps the main loop of the next.
 //
@@ -39,7 +41,9 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
+#include "epilogue.cuh"
 #include "groups.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -139,13 +143,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t u, in
   return ti;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-template <int BN, bool GROUPED, int CM>
+template <int BN, bool GROUPED, int CM, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
@@ -377,74 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_row = tmem_base + ((q * 32u) << 16) + acc * BN + half * kCols;
       const int64_t grow0 = ti.m0 + q * 32;
       const int64_t gcol0 = ti.n0 + half * kCols;
-      // staged rows are 64 bytes: 16-byte chunk j of row r sits at chunk
-      // j ^ ((r >> 1) & 3), which keeps both the row-wise writes and the
-      // 4-lanes-per-row reads free of bank conflicts.
-      auto chunk_at = [](int r, int j) { return r * 64 + ((j ^ ((r >> 1) & 3)) * 16); };
-      if (p.y_fp32) {
-        uint32_t v[kCols];
-#pragma unroll
-        for (int c = 0; c < kCols / 32; ++c)
-          tmem_ld_32x32b_x32(t_row + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
-        tmem_ld_wait();
+      epilogue_share<BN, FUSED>(p, t_row, grow0, gcol0, ti.m_end, stage_buf, lane, [&] {
         tc_fence_before_sync();
         mbar_arrive(&acc_empty[acc]);
-        float* y = static_cast<float*>(p.y);
-#pragma unroll
-        for (int pass = 0; pass < kCols / 16; ++pass) {  // 16 FP32 columns = 64 bytes per row
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(stage_buf + chunk_at(lane, j)) =
-                make_uint4(v[pass * 16 + 4 * j], v[pass * 16 + 4 * j + 1],
-                           v[pass * 16 + 4 * j + 2], v[pass * 16 + 4 * j + 3]);
-          __syncwarp();
-#pragma unroll
-          for (int it = 0; it < 4; ++it) {
-            const int rr = it * 8 + (lane >> 2);
-            const int j = lane & 3;
-            const int64_t grow = grow0 + rr;
-            const int64_t gcol = gcol0 + pass * 16 + j * 4;
-            if (grow < ti.m_end && gcol < p.n)
-              *reinterpret_cast<uint4*>(y + grow * p.ldy + gcol) =
-                  *reinterpret_cast<const uint4*>(stage_buf + chunk_at(rr, j));
-          }
-          __syncwarp();
-        }
-      } else {
-        uint32_t w[kCols / 2];
-#pragma unroll
-        for (int c = 0; c < kCols / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + c * 32, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[c * 16 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-        }
-        tc_fence_before_sync();
-        mbar_arrive(&acc_empty[acc]);
-        uint16_t* y = static_cast<uint16_t*>(p.y);
-#pragma unroll
-        for (int pass = 0; pass < kCols / 32; ++pass) {  // 32 BF16 columns = 64 bytes per row
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(stage_buf + chunk_at(lane, j)) =
-                make_uint4(w[pass * 16 + 4 * j], w[pass * 16 + 4 * j + 1],
-                           w[pass * 16 + 4 * j + 2], w[pass * 16 + 4 * j + 3]);
-          __syncwarp();
-#pragma unroll
-          for (int it = 0; it < 4; ++it) {
-            const int rr = it * 8 + (lane >> 2);
-            const int j = lane & 3;
-            const int64_t grow = grow0 + rr;
-            const int64_t gcol = gcol0 + pass * 32 + j * 8;
-            if (grow < ti.m_end && gcol < p.n)
-              *reinterpret_cast<uint4*>(y + grow * p.ldy + gcol) =
-                  *reinterpret_cast<const uint4*>(stage_buf + chunk_at(rr, j));
-          }
-          __syncwarp();
-        }
-      }
+      });
       if (++acc == C::kAccStages) {
         acc = 0;
         acc_phase ^= 1u;
@@ -476,11 +410,11 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
   }
 }
 
-template <int BN, bool GROUPED, int CM>
+template <int BN, bool GROUPED, int CM, bool FUSED = false>
 cudaError_t launch_impl(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                         int num_sms, cudaStream_t stream) {
   using C = Cfg<BN, GROUPED>;
-  auto kern = mx_gemm_kernel<BN, GROUPED, CM>;
+  auto kern = mx_gemm_kernel<BN, GROUPED, CM, FUSED>;
   // The attribute is per function and device; set it once per device.
   static bool attr_set[64] = {};
   int dev = 0;
@@ -530,6 +464,14 @@ int gemm_default_block_n(const GemmParams& p) {
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                         int block_n, int cluster_m, int num_sms, cudaStream_t stream) {
   const bool grouped = p.groups > 0;
+  if (p.bias != nullptr || p.act != 0) {  // fused epilogue: dense GEMMs only
+    if (grouped) return cudaErrorNotSupported;
+    if (block_n == 256)
+      return cluster_m == 2 ? launch_impl<256, false, 2, true>(p, ta, tb, num_sms, stream)
+                            : launch_impl<256, false, 1, true>(p, ta, tb, num_sms, stream);
+    return cluster_m == 2 ? launch_impl<128, false, 2, true>(p, ta, tb, num_sms, stream)
+                          : launch_impl<128, false, 1, true>(p, ta, tb, num_sms, stream);
+  }
   if (block_n == 256) {
     if (cluster_m == 2)
       return grouped ? launch_impl<256, true, 2>(p, ta, tb, num_sms, stream)

@@ -48,6 +48,8 @@ struct GemmParams {
   uint32_t* status;
   uint64_t wait_limit_ns;
   int32_t band_m;          // m-tiles per raster band (dense), a multiple of 2
+  const float* bias;       // fused epilogue: FP32 bias per output column, or nullptr
+  int32_t act;             // fused epilogue: 0 none, 1 SiLU
 };
 
 // Tile width along N of the GEMM kernel: 128 (double-buffered accumulator)

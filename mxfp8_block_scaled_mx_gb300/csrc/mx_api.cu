@@ -108,7 +108,8 @@ int block_n_choice(const mx::GemmParams& p) {
 mx_status gemm_common(int64_t m, int64_t n, int64_t k, const uint8_t* a, const uint8_t* sa,
                       mx_fmt fa, const uint8_t* b, const uint8_t* sb, mx_fmt fb, void* y,
                       mx_dtype y_dtype, int64_t ldy, int32_t groups, const int32_t* d_offsets,
-                      int64_t b_rows, cudaStream_t stream) {
+                      int64_t b_rows, cudaStream_t stream, const float* bias = nullptr,
+                      int32_t act = 0) {
   if (!a || !sa || !b || !sb || !y) return MX_ERR_INVALID_ARG;
   if (m < 0 || n <= 0 || k < 32 || k % 32 != 0 || n % 8 != 0 || ldy < n) return MX_ERR_INVALID_ARG;
   if (!valid_fmt(fa) || !valid_fmt(fb)) return MX_ERR_INVALID_ARG;
@@ -138,6 +139,8 @@ mx_status gemm_common(int64_t m, int64_t n, int64_t k, const uint8_t* a, const u
   p.groups = groups;
   p.status = st->status;
   p.wait_limit_ns = g_wait_ns;
+  p.bias = bias;
+  p.act = act;
   p.band_m = 32;
   if (const char* env = std::getenv("MX_GEMM_BAND_M")) {
     const int v = std::atoi(env);
@@ -255,6 +258,16 @@ mx_status mx_gemm(int64_t m, int64_t n, int64_t k, const uint8_t* a, const uint8
                   const uint8_t* b, const uint8_t* sb, mx_fmt fb, void* y, mx_dtype y_dtype,
                   int64_t ldy, cudaStream_t stream) {
   return gemm_common(m, n, k, a, sa, fa, b, sb, fb, y, y_dtype, ldy, 0, nullptr, n, stream);
+}
+
+mx_status mx_gemm_bias_act(int64_t m, int64_t n, int64_t k, const uint8_t* a, const uint8_t* sa,
+                           mx_fmt fa, const uint8_t* b, const uint8_t* sb, mx_fmt fb,
+                           const float* bias, mx_activation act, void* y, mx_dtype y_dtype,
+                           int64_t ldy, cudaStream_t stream) {
+  if (act != MX_ACT_NONE && act != MX_ACT_SILU) return MX_ERR_INVALID_ARG;
+  if (bias != nullptr && !aligned16(bias)) return MX_ERR_MISALIGNED;
+  return gemm_common(m, n, k, a, sa, fa, b, sb, fb, y, y_dtype, ldy, 0, nullptr, n, stream, bias,
+                     act);
 }
 
 mx_status mx_grouped_gemm(int32_t groups, const int32_t* d_offsets, int64_t total_m, int64_t n,

@@ -24,6 +24,9 @@ states.  Sources (page title, section):
 * same page, "Scale ownership and the GEMM dataflow" -- with 32-element
   blocks along K the block scale product stays inside the outer sum:
   Y_ij = sum_b S_X[i,b] * S_W[b,j] * sum_{k in b} Xq[i,k] * Wq[k,j].
+* same page, "Hardware support and kernel ABI contracts" -- the kernel
+  contract's epilogue: an FP32 bias per output column, then SiLU, then BF16.
+  SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z)).
 * The MX block scale rule used by the product ("floor" rule of the OCP MX
   specification, as the benchmark spec gives it):
   S = 2^(floor(log2 amax) - emax_elem), emax_elem = 8 (E4M3) or 15 (E5M2).
@@ -402,6 +405,25 @@ def gemm(a: MxBlocks, b: MxBlocks):
         y += sprod * partial
         t += sprod * (np.abs(av[:, blk, :]) @ np.abs(bv[:, blk, :]).T)
     return y, t
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """SiLU(z) = z / (1 + exp(-z)) in float64 (exp overflow gives -0 / 0)."""
+    z = np.asarray(z, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+ACTIVATIONS = {"none": lambda z: np.asarray(z, dtype=np.float64), "silu": silu}
+
+
+def gemm_bias_act(a: MxBlocks, b: MxBlocks, bias=None, act: str = "none"):
+    """Epilogue of the kernel contract: out = act(Y + bias[None, :]) with Y the
+    block-scaled GEMM; bias is one value per output column (or None).
+    Returns (out, Y + bias, T)."""
+    y, t = gemm(a, b)
+    z = y if bias is None else y + np.asarray(bias, dtype=np.float64)[None, :]
+    return ACTIVATIONS[act](z), z, t
 
 
 def grouped_gemm(a: MxBlocks, offsets, b_groups):

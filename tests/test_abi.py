@@ -100,5 +100,12 @@ def test_grouped_calls_reject_bad_arguments_on_the_host(mx):
     assert qg(FAKE, 0, 64, 64, 64, 0, 0, 4, None, FAKE, FAKE, 0) == 1                  # offsets
 
 
+def test_fused_epilogue_rejects_bad_arguments_on_the_host(mx):
+    f = mx.mx_gemm_bias_act
+    assert f(64, 64, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, None, 7, FAKE, 0, 64, 0) == 1      # act
+    assert f(64, 64, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE + 4, 1, FAKE, 0, 64, 0) == 2  # bias align
+    assert f(64, 64, 48, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 1, FAKE, 0, 64, 0) == 1      # k % 32
+
+
 def test_selftest_rejects_zero_limit(mx):
     assert mx.mx_selftest_wait_timeout(0, 0) == 1

@@ -189,6 +189,45 @@ def test_dgrad_and_wgrad_full_size_sampled(mx):
     assert mx.device_status() == 0
 
 
+def fused_error_ratio(y_gpu, out_ref, z_ref, t_ref, out_dtype):
+    """Fused-epilogue bound: the GEMM bound carried through the activation
+    (|silu'| <= 1.1), FP32 rounding of the add and the activation (2^-20
+    relative), and one BF16 ulp for BF16 outputs."""
+    from mxcheck import bf16_ulp
+    y = to_f64(y_gpu)
+    allowed = 1.1e-4 * t_ref + 2.0 ** -20 * (np.abs(z_ref) + np.abs(out_ref))
+    if out_dtype == "bf16":
+        allowed = allowed + bf16_ulp(out_ref)
+    assert np.isfinite(y).all()
+    return float((np.abs(y - out_ref) / np.maximum(allowed, 1e-300)).max())
+
+
+@pytest.mark.parametrize("m,n,k", [(128, 256, 256), (300, 264, 1056), (77, 520, 160)])
+@pytest.mark.parametrize("act", ["none", "silu"])
+@pytest.mark.parametrize("with_bias", [True, False])
+def test_fused_bias_act_epilogue(mx, block_n, m, n, k, act, with_bias):
+    """The kernel contract's epilogue: act(acc + bias[col]) in FP32, one
+    rounding to BF16 / FP32."""
+    if not with_bias and act == "none":
+        pytest.skip("plain GEMM")
+    rng = np.random.default_rng(m + n + k)
+    a = random_mx(rng, m, k, "e4m3", 118, 126)
+    b = random_mx(rng, n, k, "e4m3", 118, 126)
+    bias = rng.standard_normal(n).astype(np.float32) * 4 if with_bias else None
+    out_ref, z_ref, t_ref = O.gemm_bias_act(a, b, None if bias is None else bias.astype(np.float64), act)
+    bt = torch.from_numpy(bias).cuda() if with_bias else None
+    for out in ("bf16", "fp32"):
+        y = mx.gemm(mx_from_oracle(a), mx_from_oracle(b), out, bias=bt, act=act)
+        r = fused_error_ratio(y, out_ref, z_ref, t_ref, out)
+        assert r <= 1.0, f"fused epilogue error {r:.3g} x bound ({out})"
+    assert mx.device_status() == 0
+
+
+def test_fused_epilogue_rejects_grouped_and_bad_args(mx):
+    assert mx.mx_gemm_bias_act(128, 128, 64, 16, 16, 0, 16, 16, 0, None, 7, 16, 0, 128, 0) == 1
+    assert mx.mx_gemm_bias_act(128, 128, 64, 16, 16, 0, 16, 16, 0, 20, 1, 16, 0, 128, 0) == 2
+
+
 def test_wait_timeout_selftest(mx):
     """A wait on an mbarrier that nothing completes gives up by itself and
     reports MX_ERR_TIMEOUT; the context stays usable."""

@@ -459,3 +459,45 @@ def test_grouped_swizzle_places_each_group_at_a_tile_boundary():
         base = starts[g] // 128 * 2 * 512
         part = buf[base:base + O.scale_bytes(hi - lo, 8)]
         assert np.array_equal(O.unswizzle_scales(part, hi - lo, 8), s[lo:hi])
+
+
+# ---------------------------------------------------------------- fused epilogue
+
+def test_silu_matches_torch_and_identities():
+    """SiLU against torch's float64 silu (library routine), plus closed forms:
+    silu(0) = 0, silu(z) - silu(-z) = z, silu(z) -> z for large z, -> -0
+    for very negative z."""
+    z = np.concatenate([np.linspace(-30, 30, 2001), [-1e4, 1e4, 0.0]])
+    mine = O.silu(z)
+    ref = torch.nn.functional.silu(torch.from_numpy(z)).numpy()
+    assert np.allclose(mine, ref, rtol=1e-15, atol=1e-300)
+    assert O.silu(np.array([0.0]))[0] == 0.0
+    assert np.allclose(O.silu(z) - O.silu(-z), z, rtol=1e-14, atol=1e-14)
+    assert O.silu(np.array([1e4]))[0] == 1e4
+    assert O.silu(np.array([-1e4]))[0] == 0.0
+
+
+def test_bias_is_an_extra_k_block_of_ones():
+    """Y + bias equals the block-scaled GEMM with one more K-block in which A
+    holds 1.0 in its first column and B holds the bias there (bias values
+    chosen exactly representable)."""
+    rng = np.random.default_rng(13)
+    m, n, k = 6, 5, 64
+    av = rng.integers(-5, 6, size=(m, k)).astype(np.float64)
+    bv = rng.integers(-5, 6, size=(n, k)).astype(np.float64)
+    bias = rng.integers(-7, 8, size=n).astype(np.float64) * 0.25
+    a = O.MxBlocks(O.encode_sat_rne("e4m3", av), np.full((m, 2), 127, np.uint8), O.E4M3)
+    b = O.MxBlocks(O.encode_sat_rne("e4m3", bv), np.full((n, 2), 127, np.uint8), O.E4M3)
+    out, z, _ = O.gemm_bias_act(a, b, bias, "none")
+    a2 = np.zeros((m, k + 32))
+    a2[:, :k] = av
+    a2[:, k] = 1.0
+    b2 = np.zeros((n, k + 32))
+    b2[:, :k] = bv
+    b2[:, k] = bias
+    qa = O.MxBlocks(O.encode_sat_rne("e4m3", a2), np.full((m, 3), 127, np.uint8), O.E4M3)
+    qb = O.MxBlocks(O.encode_sat_rne("e4m3", b2), np.full((n, 3), 127, np.uint8), O.E4M3)
+    y2, _ = O.gemm(qa, qb)
+    assert np.array_equal(out, y2) and np.array_equal(z, y2)
+    act, _, _ = O.gemm_bias_act(a, b, bias, "silu")
+    assert np.array_equal(act, O.silu(y2))
