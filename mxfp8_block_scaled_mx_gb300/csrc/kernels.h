@@ -60,6 +60,14 @@ int gemm_default_block_n(const GemmParams& p);
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                         int block_n, int cluster_m, int num_sms, cudaStream_t stream);
 
+// Block-pair GEMM (cta_group::2, 256 x 256 pair tiles; dense only).
+// tmap_a / tmap_b: codes, box 128 rows; tmap_sa / tmap_sb: the swizzled
+// scale buffers viewed as uint32 [row_tiles][k_tiles][128], boxes of one
+// (A) and two (B) 512-byte units.
+cudaError_t launch_gemm_pair(const GemmParams& p, const CUtensorMap& tmap_a,
+                             const CUtensorMap& tmap_b, const CUtensorMap& tmap_sa,
+                             const CUtensorMap& tmap_sb, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace mx

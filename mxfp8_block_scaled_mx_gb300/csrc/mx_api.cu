@@ -96,6 +96,31 @@ mx_status encode_bf16_map(CUtensorMap* map, const void* base, int64_t cols, int6
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
+// The swizzled scale buffer of a [rows, k] operand viewed as uint32
+// [ceil(rows/128)][ceil(k/128)][128] (one 512-byte unit per 128-row x
+// 128-K tile); box of `units` consecutive row tiles at one K tile.
+mx_status encode_scale_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k,
+                           uint32_t units) {
+  const int64_t row_tiles = ceil_div(rows, 128);
+  const int64_t k_tiles = ceil_div(k, 128);
+  cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(k_tiles),
+                        static_cast<cuuint64_t>(row_tiles)};
+  cuuint64_t strides[2] = {512u, static_cast<cuuint64_t>(512 * k_tiles)};
+  cuuint32_t box[3] = {128u, 1u, units};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
+bool use_pair_kernel(int32_t groups) {
+  if (groups > 0) return false;
+  const char* env = std::getenv("MX_GEMM_PAIR");
+  return env != nullptr && std::atoi(env) == 1;
+}
+
 int block_n_choice(const mx::GemmParams& p) {
   const char* env = std::getenv("MX_GEMM_BLOCK_N");
   if (env) {
@@ -154,6 +179,16 @@ mx_status gemm_common(int64_t m, int64_t n, int64_t k, const uint8_t* a, const u
 
   CUtensorMap ta, tb;
   if ((s = encode_codes_map(&ta, a, k, m, k, 128)) != MX_OK) return s;
+  if (use_pair_kernel(groups)) {
+    // block pairs: each block loads 128 rows of the 256-row B tile
+    CUtensorMap tsa, tsb;
+    if ((s = encode_codes_map(&tb, b, k, b_rows, k, 128)) != MX_OK) return s;
+    if ((s = encode_scale_map(&tsa, sa, m, k, 1)) != MX_OK) return s;
+    if ((s = encode_scale_map(&tsb, sb, b_rows, k, 2)) != MX_OK) return s;
+    if (mx::launch_gemm_pair(p, ta, tb, tsa, tsb, st->num_sms, stream) != cudaSuccess)
+      return MX_ERR_CUDA;
+    return MX_OK;
+  }
   // With block pairs each block loads half of the B tile (multicast).
   const uint32_t b_box_rows = static_cast<uint32_t>(block_n / cluster_m);
   if ((s = encode_codes_map(&tb, b, k, b_rows, k, b_box_rows)) != MX_OK) return s;
