@@ -246,6 +246,25 @@ def measure_rows(mx, peaks, dev, stream):
             out[f"quantize_{r}x{c}_{mode}"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
                                                "frac_hbm": round(gbs / hbm, 3),
                                                "bytes_per_elem": bpe}
+        if (r, c) == (16384, 8192):
+            # stochastic rounding (E5M2, the gradient format): the 16-bit
+            # random draws are an input, +2 bytes per element
+            rb = W.random_bits16((r, c), seed=11, device=dev)
+
+            def qsr():
+                st = mx.mx_quantize_sr(x.data_ptr(), 0, r, c, c, rb.data_ptr(), c, 1, 1, 0,
+                                       qr.data_ptr(), sr.data_ptr(), None, None, h)
+                assert st == 0
+            ms = []
+            for _ in range(20):
+                flush_l2(scrub)
+                ms.append(time_kernel(qsr, stream, 1, warmup=0 if ms else 3))
+            t = statistics.median(ms)
+            gbs = r * c * 5.03125 / (t * 1e-3) / 1e9
+            out[f"quantize_{r}x{c}_row_sr_e5m2"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
+                                                   "frac_hbm": round(gbs / hbm, 3),
+                                                   "bytes_per_elem": 5.03125}
+            del rb
         del x, qr, sr, qc, sc
 
     # backward GEMMs (FP32 out), the fused bias+SiLU forward, the MoE grouped GEMM

@@ -120,6 +120,20 @@ mx_status mx_quantize(const void* x, mx_dtype x_dtype, int64_t rows, int64_t col
                       uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                       cudaStream_t stream);
 
+/* mx_quantize with stochastic rounding in place of round-to-nearest-even
+ * (section "Rounding: RNE versus stochastic rounding").  rbits: device
+ * uint16[rows, cols] (leading dimension ldr elements, ldr % 8 == 0), one
+ * random integer r per element of x, used by both orientations.  With l <= |v|
+ * < u the neighbouring grid values of the exactly scaled element v, |v| goes
+ * to u iff r < floor(2^16 (|v| - l) / (u - l)), else to l; the result then
+ * saturates like the RNE path.  Scales are those of mx_quantize (they depend
+ * only on the block amax).  For a given rbits the codes are bit-exact. */
+mx_status mx_quantize_sr(const void* x, mx_dtype x_dtype, int64_t rows, int64_t cols,
+                         int64_t ldx, const uint16_t* rbits, int64_t ldr, mx_fmt fmt,
+                         mx_axis axis, mx_scale_rule rule,
+                         uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                         cudaStream_t stream);
+
 /* Rowwise MX quantization of routed tokens x[total_rows, cols] grouped by
  * expert: rows [d_offsets[g], d_offsets[g+1]) belong to group g.  Codes are
  * written as by mx_quantize ROWWISE; scales use the per-group padded layout

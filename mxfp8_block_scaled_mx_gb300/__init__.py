@@ -33,7 +33,8 @@ RULE = {"floor": 0, "ceil": 1}
 
 ACT = {"none": 0, "silu": 1}
 
-EXPORTS = ("mx_scale_bytes", "mx_grouped_scale_bytes", "mx_quantize", "mx_quantize_grouped",
+EXPORTS = ("mx_scale_bytes", "mx_grouped_scale_bytes", "mx_quantize", "mx_quantize_sr",
+           "mx_quantize_grouped",
            "mx_gemm", "mx_gemm_bias_act", "mx_grouped_gemm", "mx_device_status", "mx_status_str",
            "mx_set_wait_timeout_ns", "mx_selftest_wait_timeout")
 
@@ -57,6 +58,9 @@ def _declare(lib):
     lib.mx_quantize.argtypes = [vp, c.c_int, i64, i64, i64, c.c_int, c.c_int, c.c_int,
                                 vp, vp, vp, vp, vp]
     lib.mx_quantize.restype = c.c_int
+    lib.mx_quantize_sr.argtypes = [vp, c.c_int, i64, i64, i64, vp, i64, c.c_int, c.c_int,
+                                   c.c_int, vp, vp, vp, vp, vp]
+    lib.mx_quantize_sr.restype = c.c_int
     lib.mx_quantize_grouped.argtypes = [vp, c.c_int, i64, i64, i64, c.c_int, c.c_int, i32, vp,
                                         vp, vp, vp]
     lib.mx_quantize_grouped.restype = c.c_int
@@ -122,6 +126,12 @@ def mx_quantize(x, x_dtype, rows, cols, ldx, fmt, axis, rule, q_row, s_row, q_co
                              s_col, stream)
 
 
+def mx_quantize_sr(x, x_dtype, rows, cols, ldx, rbits, ldr, fmt, axis, rule, q_row, s_row, q_col,
+                   s_col, stream) -> int:
+    return lib().mx_quantize_sr(x, x_dtype, rows, cols, ldx, rbits, ldr, fmt, axis, rule, q_row,
+                                s_row, q_col, s_col, stream)
+
+
 def mx_quantize_grouped(x, x_dtype, total_rows, cols, ldx, fmt, rule, groups, d_offsets, q, s,
                         stream) -> int:
     return lib().mx_quantize_grouped(x, x_dtype, total_rows, cols, ldx, fmt, rule, groups,
@@ -178,9 +188,11 @@ class MxTensor:
 
 
 def quantize(x: torch.Tensor, fmt: str = "e4m3", axis: str = "row", rule: str = "floor",
-             stream=None):
+             stream=None, rand: torch.Tensor | None = None):
     """bf16 [rows, cols] -> MxTensor (axis 'row' or 'col') or a (row, col)
-    pair (axis 'both').  Column-wise codes come back as [cols, rows]."""
+    pair (axis 'both').  Column-wise codes come back as [cols, rows].  With
+    `rand` (16-bit random integers, int16 [rows, cols]) the codes use
+    stochastic rounding."""
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda:
         raise ValueError("x must be a 2-D bf16 CUDA tensor")
     if x.stride(1) != 1:
@@ -194,10 +206,20 @@ def quantize(x: torch.Tensor, fmt: str = "e4m3", axis: str = "row", rule: str = 
     if axis in ("col", "both"):
         q_col = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
         s_col = torch.empty(max(mx_scale_bytes(cols, rows), 1), dtype=torch.uint8, device=dev)
-    st = mx_quantize(_ptr(x), DTYPE["bf16"], rows, cols, x.stride(0), FMT[fmt], AXIS[axis],
-                     RULE[rule], _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col),
-                     _stream(stream))
-    _check("mx_quantize", st)
+    if rand is None:
+        st = mx_quantize(_ptr(x), DTYPE["bf16"], rows, cols, x.stride(0), FMT[fmt], AXIS[axis],
+                         RULE[rule], _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col),
+                         _stream(stream))
+        _check("mx_quantize", st)
+    else:
+        if rand.dtype != torch.int16 or rand.shape != x.shape or not rand.is_cuda:
+            raise ValueError("rand must be a CUDA int16 tensor shaped like x")
+        if rand.stride(1) != 1:
+            raise ValueError("rand must have unit column stride")
+        st = mx_quantize_sr(_ptr(x), DTYPE["bf16"], rows, cols, x.stride(0), _ptr(rand),
+                            rand.stride(0), FMT[fmt], AXIS[axis], RULE[rule], _ptr(q_row),
+                            _ptr(s_row), _ptr(q_col), _ptr(s_col), _stream(stream))
+        _check("mx_quantize_sr", st)
     row = MxTensor(q_row, s_row, fmt) if q_row is not None else None
     col = MxTensor(q_col, s_col, fmt) if q_col is not None else None
     if axis == "row":

@@ -26,9 +26,11 @@ struct QuantizeParams {
   uint64_t wait_limit_ns;
 };
 
-// tmap_x: 2-D bf16 tensor map over x (box 128 x 128, no swizzle).
-cudaError_t launch_quantize(const QuantizeParams& p, const CUtensorMap& tmap_x, int num_sms,
-                            cudaStream_t stream);
+// tmap_x: 2-D bf16 tensor map over x (box 128 x 128, no swizzle); tmap_r:
+// the same over the 16-bit random integers for stochastic rounding, or
+// nullptr for round-to-nearest-even.
+cudaError_t launch_quantize(const QuantizeParams& p, const CUtensorMap& tmap_x,
+                            const CUtensorMap* tmap_r, int num_sms, cudaStream_t stream);
 cudaError_t launch_quantize_grouped(const QuantizeParams& p, const CUtensorMap& tmap_x,
                                     int num_sms, cudaStream_t stream);
 

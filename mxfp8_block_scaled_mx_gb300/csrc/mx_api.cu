@@ -211,9 +211,14 @@ size_t mx_grouped_scale_bytes(int64_t total_rows, int32_t groups, int64_t k) {
   return static_cast<size_t>((ceil_div(total_rows, 128) + groups) * 128 * ceil_div(k, 128) * 4);
 }
 
-mx_status mx_quantize(const void* x, mx_dtype x_dtype, int64_t rows, int64_t cols, int64_t ldx,
-                      mx_fmt fmt, mx_axis axis, mx_scale_rule rule, uint8_t* q_row,
-                      uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+mx_status quantize_common(const void* x, mx_dtype x_dtype, int64_t rows, int64_t cols,
+                          int64_t ldx, const uint16_t* rbits, int64_t ldr, mx_fmt fmt,
+                          mx_axis axis, mx_scale_rule rule, uint8_t* q_row, uint8_t* s_row,
+                          uint8_t* q_col, uint8_t* s_col, cudaStream_t stream) {
   if (x_dtype != MX_BF16) return x_dtype == MX_FP32 ? MX_ERR_UNSUPPORTED : MX_ERR_INVALID_ARG;
   if (!valid_fmt(fmt) || (rule != MX_SCALE_FLOOR && rule != MX_SCALE_CEIL))
     return MX_ERR_INVALID_ARG;
@@ -222,10 +227,12 @@ mx_status mx_quantize(const void* x, mx_dtype x_dtype, int64_t rows, int64_t col
   const bool col = axis & MX_COLWISE;
   if (!x || (row && (!q_row || !s_row)) || (col && (!q_col || !s_col))) return MX_ERR_INVALID_ARG;
   if (rows < 0 || cols < 0 || ldx < cols || cols % 8 != 0) return MX_ERR_INVALID_ARG;
+  if (rbits && ldr < cols) return MX_ERR_INVALID_ARG;
   if (row && cols % 32 != 0) return MX_ERR_INVALID_ARG;
   if (col && rows % 32 != 0) return MX_ERR_INVALID_ARG;
   if (ceil_div(cols, 128) > 65535) return MX_ERR_UNSUPPORTED;
   if (!aligned16(x) || ldx % 8 != 0) return MX_ERR_MISALIGNED;
+  if (rbits && (!aligned16(rbits) || ldr % 8 != 0)) return MX_ERR_MISALIGNED;
   if ((row && (!aligned16(q_row) || !aligned16(s_row))) ||
       (col && (!aligned16(q_col) || !aligned16(s_col))))
     return MX_ERR_MISALIGNED;
@@ -246,9 +253,34 @@ mx_status mx_quantize(const void* x, mx_dtype x_dtype, int64_t rows, int64_t col
   p.status = st->status;
   p.wait_limit_ns = g_wait_ns;
   if (rows == 0 || cols == 0) return MX_OK;
-  CUtensorMap tmap;
+  CUtensorMap tmap, tmap_r;
   if ((s = encode_bf16_map(&tmap, x, cols, rows, ldx)) != MX_OK) return s;
-  return mx::launch_quantize(p, tmap, st->num_sms, stream) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+  // the random integers are 16-bit like bf16: the same tile geometry
+  if (rbits && (s = encode_bf16_map(&tmap_r, rbits, cols, rows, ldr)) != MX_OK) return s;
+  return mx::launch_quantize(p, tmap, rbits ? &tmap_r : nullptr, st->num_sms, stream) ==
+                 cudaSuccess
+             ? MX_OK
+             : MX_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+mx_status mx_quantize(const void* x, mx_dtype x_dtype, int64_t rows, int64_t cols, int64_t ldx,
+                      mx_fmt fmt, mx_axis axis, mx_scale_rule rule, uint8_t* q_row,
+                      uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, cudaStream_t stream) {
+  return quantize_common(x, x_dtype, rows, cols, ldx, nullptr, 0, fmt, axis, rule, q_row, s_row,
+                         q_col, s_col, stream);
+}
+
+mx_status mx_quantize_sr(const void* x, mx_dtype x_dtype, int64_t rows, int64_t cols, int64_t ldx,
+                         const uint16_t* rbits, int64_t ldr, mx_fmt fmt, mx_axis axis,
+                         mx_scale_rule rule, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                         uint8_t* s_col, cudaStream_t stream) {
+  if (!rbits) return MX_ERR_INVALID_ARG;
+  return quantize_common(x, x_dtype, rows, cols, ldx, rbits, ldr, fmt, axis, rule, q_row, s_row,
+                         q_col, s_col, stream);
 }
 
 mx_status mx_quantize_grouped(const void* x, mx_dtype x_dtype, int64_t total_rows, int64_t cols,

