@@ -27,8 +27,8 @@ states.  Sources (page title, section):
 * same page, "Hardware support and kernel ABI contracts" -- the kernel
   contract's epilogue: an FP32 bias per output column, then SiLU, then BF16.
   SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z)).
-* The MX block scale rule used by the product ("floor" rule of the OCP MX
-  specification, as the benchmark spec gives it):
+* The MX block scale rule used by the product (the "floor" rule of the OCP
+  MX specification):
   S = 2^(floor(log2 amax) - emax_elem), emax_elem = 8 (E4M3) or 15 (E5M2).
 
 Readings where the pages are silent (each also listed in the design doc):
@@ -487,6 +487,64 @@ def grouped_gemm(a: MxBlocks, offsets, b_groups):
         sub = MxBlocks(a.codes[lo:hi], a.scales[lo:hi], a.fmt)
         y[lo:hi], t[lo:hi] = gemm(sub, b_groups[g])
     return y, t
+
+
+def quantize_grouped_cols(x: np.ndarray, offsets, fmt, rule: str = "floor"):
+    """Columnwise MX quantization inside each group of rows of a [total, C]
+    array (the token-major activations or output gradients of a mixture of
+    experts).  Group g is X_g = x[o_g:o_{g+1}]; its 32-row blocks start at
+    the group's first row, so no block spans two groups, and a final
+    partial block is completed with zero rows (the page's zero-padded final
+    block).  Zeros raise no amax and add nothing to a sum.  Returns one
+    MxBlocks per group: codes [C, roundup(m_g, 32)], K = the group's tokens.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    offsets = np.asarray(offsets, dtype=np.int64)
+    out = []
+    for g in range(len(offsets) - 1):
+        lo, hi = int(offsets[g]), int(offsets[g + 1])
+        padded = np.zeros((-(-(hi - lo) // BLOCK) * BLOCK, x.shape[1]))
+        padded[:hi - lo] = x[lo:hi]
+        out.append(quantize(padded, fmt, "col", rule))
+    return out
+
+
+def grouped_wgrad(a_groups, b_groups):
+    """Per expert g: Y[g] = gemm(A_g, B_g), where A_g [M, K_g] and B_g [N, K_g]
+    are columnwise quantizations over that expert's tokens (K_g its padded
+    token count): the weight gradient of each expert, contracted over the
+    expert's own tokens only.  An expert without tokens gets Y[g] = 0.
+    Returns (Y [G, M, N], T [G, M, N])."""
+    groups = len(a_groups)
+    m = a_groups[0].codes.shape[0]
+    n = b_groups[0].codes.shape[0]
+    y = np.zeros((groups, m, n))
+    t = np.zeros((groups, m, n))
+    for g in range(groups):
+        if a_groups[g].codes.shape[1]:
+            y[g], t[g] = gemm(a_groups[g], b_groups[g])
+    return y, t
+
+
+def pack_grouped_cols(groups_mx, offsets, ldq: int):
+    """Side-by-side layout of per-group columnwise operands along K: group
+    g's codes occupy columns [s_g, s_g + roundup(m_g, 32)) of a [C, ldq]
+    matrix, s_g = sum_{h<g} roundup(m_h, 128) (every group starts at a
+    128-column boundary, the start of a scale tile); the rest of the group's
+    128-column segment holds code 0 and scale byte 0.  Returns (codes
+    [C, ldq], canonical scales [C, ldq / 32]).  Layout only: no arithmetic."""
+    starts = grouped_scale_rows(offsets)
+    c = groups_mx[0].codes.shape[0]
+    if starts[-1] > ldq or ldq % TILE_ROWS:
+        raise ValueError("ldq too small or not a multiple of 128")
+    codes = np.zeros((c, ldq), dtype=np.uint8)
+    scales = np.zeros((c, ldq // BLOCK), dtype=np.uint8)
+    for g, q in enumerate(groups_mx):
+        s0 = int(starts[g])
+        kp = q.codes.shape[1]
+        codes[:, s0:s0 + kp] = q.codes
+        scales[:, s0 // BLOCK:(s0 + kp) // BLOCK] = q.scales
+    return codes, scales
 
 
 # --------------------------------------------------------------------------

@@ -414,6 +414,96 @@ def test_grouped_gemm_is_per_group_dense():
             assert np.array_equal(y[i], O.gemm(row, bs[g])[0][0])
 
 
+# ---------------------------------------------------------------- grouped backward
+
+MOE_TINY_OFFSETS = np.array([0, 0, 1, 32, 65, 65, 165, 200])   # sizes 0,1,31,33,0,100,35
+
+
+@pytest.mark.parametrize("fa,fb", [("e5m2", "e4m3"), ("e4m3", "e4m3")])
+def test_grouped_wgrad_of_lossless_integers_is_the_integer_matmul(fa, fb):
+    """Integers in [-8, 8] are exact in bf16 and MX-quantize without loss in
+    both formats (at most 3 significant bits; the largest scaled value is
+    7 * 2^6 = 448 for E4M3 and 7 * 2^13 = 57344 for E5M2, each format's
+    maximum), so each expert's weight gradient must equal the int64 product
+    dY_g^T X_g over that expert's rows alone (closed form)."""
+    rng = np.random.default_rng(5)
+    total = int(MOE_TINY_OFFSETS[-1])
+    dy = rng.integers(-8, 9, size=(total, 40)).astype(np.float64)
+    x = rng.integers(-8, 9, size=(total, 72)).astype(np.float64)
+    a = O.quantize_grouped_cols(dy, MOE_TINY_OFFSETS, fa)
+    b = O.quantize_grouped_cols(x, MOE_TINY_OFFSETS, fb)
+    y, t = O.grouped_wgrad(a, b)
+    assert y.shape == (len(MOE_TINY_OFFSETS) - 1, 40, 72)
+    for g in range(len(MOE_TINY_OFFSETS) - 1):
+        lo, hi = MOE_TINY_OFFSETS[g], MOE_TINY_OFFSETS[g + 1]
+        ref = dy[lo:hi].astype(np.int64).T @ x[lo:hi].astype(np.int64)
+        assert np.array_equal(y[g], ref.astype(np.float64)), g
+        assert np.array_equal(t[g], (np.abs(dy[lo:hi]).T @ np.abs(x[lo:hi])))
+
+
+def test_grouped_col_blocks_start_at_each_group():
+    """A block spanning two groups would give the small values of group 1
+    the scale of group 0's 2^10 entries and flush them to zero; blocks that
+    start at each group's first row keep them exactly."""
+    offsets = np.array([0, 5, 45])
+    x = np.zeros((45, 32))
+    x[:5] = 2.0 ** 10
+    rng = np.random.default_rng(2)
+    x[5:] = rng.integers(1, 8, size=(40, 32)) * 2.0 ** -10
+    q = O.quantize_grouped_cols(x, offsets, "e4m3")
+    deq = O.dequantize(q[1])            # [32 columns, 64 padded tokens]
+    assert np.array_equal(deq[:, :40], x[5:].T)
+    assert np.all(deq[:, 40:] == 0)
+
+
+def test_grouped_col_partial_block_is_zero_padded():
+    """A group of 33 rows has two blocks; the second holds one real row and
+    31 zeros, so its scale is the floor rule applied to that row alone
+    (frexp closed form) and its padding codes are +0."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((33, 64)) * 3
+    q = O.quantize_grouped_cols(x, [0, 33], "e4m3")[0]
+    assert q.codes.shape == (64, 64)
+    assert np.all(q.codes[:, 33:] == 0)
+    for c in range(64):
+        _, ex = math.frexp(abs(x[32, c]))      # |x| = f * 2^ex, f in [0.5, 1)
+        assert q.scales[c, 1] == (ex - 1) - 8 + 127
+
+
+def test_stacked_weights_colwise_equal_per_expert_operands():
+    """dgrad operand of a mixture of experts: with N % 32 == 0, columnwise
+    blocks of the stacked [E*N, K] weights never span two experts, so one
+    columnwise quantization of the stack is the per-expert quantizations
+    side by side along K (columns [g*N, (g+1)*N))."""
+    rng = np.random.default_rng(4)
+    e, n, k = 3, 64, 96
+    w = rng.standard_normal((e, n, k)) * 0.02
+    whole = O.quantize(w.reshape(e * n, k), "e4m3", "col")
+    for g in range(e):
+        part = O.quantize(w[g], "e4m3", "col")
+        assert np.array_equal(whole.codes[:, g * n:(g + 1) * n], part.codes)
+        assert np.array_equal(whole.scales[:, g * n // 32:(g + 1) * n // 32], part.scales)
+
+
+def test_pack_grouped_cols_layout():
+    """Each group starts at a 128-column boundary, the segments do not
+    overlap, and unpacking returns every group's codes and scales."""
+    rng = np.random.default_rng(6)
+    total = int(MOE_TINY_OFFSETS[-1])
+    x = rng.standard_normal((total, 24))
+    qs = O.quantize_grouped_cols(x, MOE_TINY_OFFSETS, "e5m2")
+    starts = O.grouped_scale_rows(MOE_TINY_OFFSETS)
+    assert list(starts) == [0, 0, 128, 256, 384, 384, 512, 640]
+    codes, scales = O.pack_grouped_cols(qs, MOE_TINY_OFFSETS, 768)
+    for g, q in enumerate(qs):
+        s0, kp = int(starts[g]), q.codes.shape[1]
+        assert np.array_equal(codes[:, s0:s0 + kp], q.codes)
+        assert np.array_equal(scales[:, s0 // 32:(s0 + kp) // 32], q.scales)
+        assert np.all(codes[:, s0 + kp:int(starts[g + 1])] == 0)
+    with pytest.raises(ValueError):
+        O.pack_grouped_cols(qs, MOE_TINY_OFFSETS, 512)
+
+
 # ---------------------------------------------------------------- swizzle
 
 @pytest.mark.parametrize("rows,kb", [(1, 1), (128, 4), (130, 5), (300, 17), (256, 224)])
