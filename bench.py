@@ -319,6 +319,43 @@ def measure_rows(mx, peaks, dev, stream):
     gbs = xm.numel() * 3.03125 / (t * 1e-3) / 1e9
     out["moe_quantize_grouped_65536x7168"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
                                               "frac_hbm": round(gbs / hbm, 3)}
+    del ym, qa
+
+    # mixture-of-experts backward: dX_g = dY_g W_g^T (experts side by side
+    # along K) and dW_g = dY_g^T X_g (grouped along K), FP32 out
+    total = xm.shape[0]
+    dym = W.moe_grad_output(device=dev)
+    qa = mx.quantize_grouped(dym, d_off, "e5m2", stream=stream)
+    qb = mx.quantize(wm.view(e * n, k), "e4m3", "col", stream=stream)
+    dx = torch.empty((total, k), dtype=torch.float32, device=dev)
+    t = time_kernel(lambda: mx.grouped_gemm_bcat(qa, d_off, qb, "fp32", out=dx, stream=stream),
+                    stream, 10)
+    out["moe_dgrad_64x(7168x2048)_65536tok_fp32"] = {
+        "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
+        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
+    del qa, qb, dx
+    ldq = mx.mx_grouped_cols_capacity(total, e)
+    qa = mx.quantize_grouped(dym, d_off, "e5m2", axis="col", ldq=ldq, stream=stream)
+    qb = mx.quantize_grouped(xm, d_off, "e4m3", axis="col", ldq=ldq, stream=stream)
+    dw = torch.empty((e, n, k), dtype=torch.float32, device=dev)
+    t = time_kernel(lambda: mx.grouped_gemm_wgrad(qa, d_off, qb, total, "fp32", out=dw,
+                                                  stream=stream), stream, 10)
+    out["moe_wgrad_64x(2048x7168)_65536tok_fp32"] = {
+        "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
+        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
+    del dw
+
+    # grouped columnwise quantize of X (per-expert token blocks), into the
+    # buffers above; the codes of the 128-padded segments are written too
+    def qcol():
+        st = mx.mx_quantize_grouped_ex(xm.data_ptr(), 0, total, k, k, 0, 2, 0, e, d_off.data_ptr(),
+                                       None, None, qb.codes.data_ptr(), ldq,
+                                       qb.scales.data_ptr(), h)
+        assert st == 0
+    t = time_kernel(qcol, stream, 10)
+    gbs = xm.numel() * 3.03125 / (t * 1e-3) / 1e9
+    out["moe_quantize_grouped_cols_65536x7168"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
+                                                   "frac_hbm": round(gbs / hbm, 3)}
     return out
 
 

@@ -150,6 +150,37 @@ mx_status mx_quantize_grouped(const void* x, mx_dtype x_dtype, int64_t total_row
                               int32_t groups, const int32_t* d_offsets,
                               uint8_t* q, uint8_t* s, cudaStream_t stream);
 
+/* Upper bound of the token columns that the per-group padded columnwise
+ * layout of mx_quantize_grouped_ex needs for any split of total_rows into
+ * `groups` groups: 128 * (floor(total_rows / 128) + groups) (each group
+ * rounds its token count up to a multiple of 128).  0 for negative input. */
+int64_t mx_grouped_cols_capacity(int64_t total_rows, int32_t groups);
+
+/* MX quantization of routed tokens x[total_rows, cols] grouped by expert,
+ * in either or both orientations from one read (axis).
+ * ROWWISE: exactly mx_quantize_grouped (q_row, s_row).
+ * COLWISE: per group g, the 32-row blocks start at the group's first row
+ *   (no block spans two groups) and a final partial block is completed with
+ *   zeros -- the zero-padded final block of section "Scale ownership and
+ *   the GEMM dataflow".  The transposed codes of all groups share one
+ *   q_col[cols, ldq_col] matrix (K = tokens, contiguous): group g occupies
+ *   columns [P_g, P_g + ceil(m_g/128)*128), P_g = sum_{h<g} ceil(m_h/128)*128,
+ *   padding tokens holding code 0; s_col holds the swizzled scales of the
+ *   whole [cols, ldq_col] operand (mx_scale_bytes(cols, ldq_col) bytes),
+ *   padding blocks 0.  Columns past the last group are left untouched.
+ *   ldq_col % 128 == 0 and ldq_col >= P_groups (mx_grouped_cols_capacity
+ *   always suffices); a layout that does not fit is reported through
+ *   mx_device_status (MX_ERR_DEVICE_ARG) and nothing is written.  This is
+ *   the operand layout of mx_grouped_gemm_wgrad.
+ * cols % 8 == 0 (ROWWISE also cols % 32 == 0); d_offsets and groups as for
+ * mx_quantize_grouped.  Unused outputs may be NULL. */
+mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_rows,
+                                 int64_t cols, int64_t ldx, mx_fmt fmt, mx_axis axis,
+                                 mx_scale_rule rule, int32_t groups, const int32_t* d_offsets,
+                                 uint8_t* q_row, uint8_t* s_row,
+                                 uint8_t* q_col, int64_t ldq_col, uint8_t* s_col,
+                                 cudaStream_t stream);
+
 /* Block-scaled GEMM, section "Scale ownership and the GEMM dataflow":
  *   y[i, j] = sum_b S_A[i,b] S_B[j,b] sum_{k in b} A~[i,k] B~[j,k]
  * A: a[m, k] codes (row-major, K contiguous, leading dimension k) with
@@ -201,6 +232,46 @@ mx_status mx_grouped_gemm(int32_t groups, const int32_t* d_offsets, int64_t tota
                           const uint8_t* a, const uint8_t* sa, mx_fmt fa,
                           const uint8_t* b, const uint8_t* sb, mx_fmt fb,
                           void* y, mx_dtype y_dtype, cudaStream_t stream);
+
+/* Grouped GEMM with the experts' B operands side by side along K (the
+ * data-gradient GEMM of a mixture of experts, dX_g = dY_g W_g^T):
+ *   y[o_g : o_{g+1}, :] = A[o_g : o_{g+1}, :] * B_g^T,  B_g = b[:, g*k : (g+1)*k]
+ * a, sa, d_offsets, y: as for mx_grouped_gemm (a: [total_m, k] rowwise,
+ *    per-group padded scales).
+ * b: one [n, ldb] code matrix (K contiguous) with swizzled scales sb of the
+ *    whole [n, ldb] operand -- exactly what mx_quantize COLWISE writes for
+ *    the stacked expert weights viewed as [groups * k, n] (e.g. W^T of every
+ *    expert stored [groups, k, n]); 32-row blocks never span two experts
+ *    because k % 32 == 0.
+ * Constraints: k % 128 == 0 (each expert starts on a scale tile),
+ * ldb >= groups * k, ldb % 16 == 0, n % 8 == 0. */
+mx_status mx_grouped_gemm_bcat(int32_t groups, const int32_t* d_offsets, int64_t total_m,
+                               int64_t n, int64_t k,
+                               const uint8_t* a, const uint8_t* sa, mx_fmt fa,
+                               const uint8_t* b, int64_t ldb, const uint8_t* sb, mx_fmt fb,
+                               void* y, mx_dtype y_dtype, cudaStream_t stream);
+
+/* Per-expert weight gradient of a mixture of experts, a GEMM grouped along
+ * its contraction: for every group g with m_g = o_{g+1} - o_g tokens,
+ *   y[g] = A_g * B_g^T,  A_g = a[:, P_g : P_g + m_g],  B_g = b[:, P_g : P_g + m_g]
+ * contracted over that expert's tokens only (section "Scale ownership and
+ * the GEMM dataflow", with the final partial block zero-padded).
+ * a: [m, ldk] codes with swizzled scales sa of the [m, ldk] operand;
+ *    b: [n, ldk] likewise -- both as written by mx_quantize_grouped_ex
+ *    COLWISE with the same d_offsets and ldk (e.g. a from dY[tokens, m],
+ *    b from X[tokens, n], giving y[g] = dY_g^T X_g).
+ * y: [groups, m, n] row-major (group g at element g*m*n); an expert without
+ *    tokens gets zeros.
+ * d_offsets: device int32[groups + 1], 0 = o_0 <= ... <= o_groups =
+ *    total_tokens, read on the device; invalid offsets, or segments that do
+ *    not fit in ldk, are reported through mx_device_status
+ *    (MX_ERR_DEVICE_ARG) and nothing is written.
+ * Constraints: ldk % 128 == 0, n % 8 == 0, 1 <= groups <= 1000. */
+mx_status mx_grouped_gemm_wgrad(int32_t groups, const int32_t* d_offsets, int64_t total_tokens,
+                                int64_t m, int64_t n, int64_t ldk,
+                                const uint8_t* a, const uint8_t* sa, mx_fmt fa,
+                                const uint8_t* b, const uint8_t* sb, mx_fmt fb,
+                                void* y, mx_dtype y_dtype, cudaStream_t stream);
 
 /* Synchronizes `stream`, then returns and clears the device status word of
  * the current device: MX_OK, MX_ERR_TIMEOUT (a kernel's bounded pipeline wait

@@ -33,9 +33,10 @@ RULE = {"floor": 0, "ceil": 1}
 
 ACT = {"none": 0, "silu": 1}
 
-EXPORTS = ("mx_scale_bytes", "mx_grouped_scale_bytes", "mx_quantize", "mx_quantize_sr",
-           "mx_quantize_grouped",
-           "mx_gemm", "mx_gemm_bias_act", "mx_grouped_gemm", "mx_device_status", "mx_status_str",
+EXPORTS = ("mx_scale_bytes", "mx_grouped_scale_bytes", "mx_grouped_cols_capacity",
+           "mx_quantize", "mx_quantize_sr", "mx_quantize_grouped", "mx_quantize_grouped_ex",
+           "mx_gemm", "mx_gemm_bias_act", "mx_grouped_gemm", "mx_grouped_gemm_bcat",
+           "mx_grouped_gemm_wgrad", "mx_device_status", "mx_status_str",
            "mx_set_wait_timeout_ns", "mx_selftest_wait_timeout")
 
 
@@ -64,6 +65,17 @@ def _declare(lib):
     lib.mx_quantize_grouped.argtypes = [vp, c.c_int, i64, i64, i64, c.c_int, c.c_int, i32, vp,
                                         vp, vp, vp]
     lib.mx_quantize_grouped.restype = c.c_int
+    lib.mx_grouped_cols_capacity.argtypes = [i64, i32]
+    lib.mx_grouped_cols_capacity.restype = i64
+    lib.mx_quantize_grouped_ex.argtypes = [vp, c.c_int, i64, i64, i64, c.c_int, c.c_int, c.c_int,
+                                           i32, vp, vp, vp, vp, i64, vp, vp]
+    lib.mx_quantize_grouped_ex.restype = c.c_int
+    lib.mx_grouped_gemm_bcat.argtypes = [i32, vp, i64, i64, i64, vp, vp, c.c_int, vp, i64, vp,
+                                         c.c_int, vp, c.c_int, vp]
+    lib.mx_grouped_gemm_bcat.restype = c.c_int
+    lib.mx_grouped_gemm_wgrad.argtypes = [i32, vp, i64, i64, i64, i64, vp, vp, c.c_int, vp, vp,
+                                          c.c_int, vp, c.c_int, vp]
+    lib.mx_grouped_gemm_wgrad.restype = c.c_int
     lib.mx_gemm.argtypes = [i64, i64, i64, vp, vp, c.c_int, vp, vp, c.c_int, vp, c.c_int, i64, vp]
     lib.mx_gemm.restype = c.c_int
     lib.mx_gemm_bias_act.argtypes = [i64, i64, i64, vp, vp, c.c_int, vp, vp, c.c_int, vp, c.c_int,
@@ -136,6 +148,29 @@ def mx_quantize_grouped(x, x_dtype, total_rows, cols, ldx, fmt, rule, groups, d_
                         stream) -> int:
     return lib().mx_quantize_grouped(x, x_dtype, total_rows, cols, ldx, fmt, rule, groups,
                                      d_offsets, q, s, stream)
+
+
+def mx_grouped_cols_capacity(total_rows: int, groups: int) -> int:
+    return int(lib().mx_grouped_cols_capacity(total_rows, groups))
+
+
+def mx_quantize_grouped_ex(x, x_dtype, total_rows, cols, ldx, fmt, axis, rule, groups, d_offsets,
+                           q_row, s_row, q_col, ldq_col, s_col, stream) -> int:
+    return lib().mx_quantize_grouped_ex(x, x_dtype, total_rows, cols, ldx, fmt, axis, rule,
+                                        groups, d_offsets, q_row, s_row, q_col, ldq_col, s_col,
+                                        stream)
+
+
+def mx_grouped_gemm_bcat(groups, d_offsets, total_m, n, k, a, sa, fa, b, ldb, sb, fb, y, y_dtype,
+                         stream) -> int:
+    return lib().mx_grouped_gemm_bcat(groups, d_offsets, total_m, n, k, a, sa, fa, b, ldb, sb, fb,
+                                      y, y_dtype, stream)
+
+
+def mx_grouped_gemm_wgrad(groups, d_offsets, total_tokens, m, n, ldk, a, sa, fa, b, sb, fb, y,
+                          y_dtype, stream) -> int:
+    return lib().mx_grouped_gemm_wgrad(groups, d_offsets, total_tokens, m, n, ldk, a, sa, fa, b,
+                                       sb, fb, y, y_dtype, stream)
 
 
 def mx_gemm(m, n, k, a, sa, fa, b, sb, fb, y, y_dtype, ldy, stream) -> int:
@@ -230,23 +265,44 @@ def quantize(x: torch.Tensor, fmt: str = "e4m3", axis: str = "row", rule: str = 
 
 
 def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt: str = "e4m3",
-                     rule: str = "floor", stream=None) -> MxTensor:
-    """Rowwise quantization of expert-grouped tokens; offsets is a device
-    int32 tensor of groups+1 entries.  Scales use the per-group padded
-    layout that grouped_gemm reads."""
+                     rule: str = "floor", stream=None, axis: str = "row", ldq: int | None = None):
+    """MX quantization of expert-grouped tokens x[total, cols]; offsets is a
+    device int32 tensor of groups+1 entries.
+    axis 'row': MxTensor [total, cols] with the per-group padded scale layout
+    that grouped_gemm reads.  axis 'col': MxTensor [cols, ldq] holding every
+    group's columnwise codes in its own 128-padded token segment (blocks
+    start at the group's first token; the final partial block is
+    zero-padded), the operand layout of grouped_gemm_wgrad; ldq defaults to
+    mx_grouped_cols_capacity(total, groups).  axis 'both': (row, col) from
+    one read."""
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
         raise ValueError("x must be a row-major 2-D bf16 CUDA tensor")
     if offsets.dtype != torch.int32 or not offsets.is_cuda:
         raise ValueError("offsets must be a CUDA int32 tensor")
     rows, cols = x.shape
     groups = offsets.numel() - 1
-    q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
-    s = torch.zeros(max(mx_grouped_scale_bytes(rows, groups, cols), 1), dtype=torch.uint8,
-                    device=x.device)
-    st = mx_quantize_grouped(_ptr(x), DTYPE["bf16"], rows, cols, x.stride(0), FMT[fmt],
-                             RULE[rule], groups, _ptr(offsets), _ptr(q), _ptr(s), _stream(stream))
-    _check("mx_quantize_grouped", st)
-    return MxTensor(q, s, fmt)
+    q_row = s_row = q_col = s_col = None
+    if axis in ("row", "both"):
+        q_row = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+        s_row = torch.zeros(max(mx_grouped_scale_bytes(rows, groups, cols), 1), dtype=torch.uint8,
+                            device=x.device)
+    if axis in ("col", "both"):
+        if ldq is None:
+            ldq = mx_grouped_cols_capacity(rows, groups)
+        q_col = torch.zeros((cols, ldq), dtype=torch.uint8, device=x.device)
+        s_col = torch.zeros(max(mx_scale_bytes(cols, ldq), 1), dtype=torch.uint8, device=x.device)
+    if axis == "row":
+        st = mx_quantize_grouped(_ptr(x), DTYPE["bf16"], rows, cols, x.stride(0), FMT[fmt],
+                                 RULE[rule], groups, _ptr(offsets), _ptr(q_row), _ptr(s_row),
+                                 _stream(stream))
+        _check("mx_quantize_grouped", st)
+        return MxTensor(q_row, s_row, fmt)
+    st = mx_quantize_grouped_ex(_ptr(x), DTYPE["bf16"], rows, cols, x.stride(0), FMT[fmt],
+                                AXIS[axis], RULE[rule], groups, _ptr(offsets), _ptr(q_row),
+                                _ptr(s_row), _ptr(q_col), ldq or 0, _ptr(s_col), _stream(stream))
+    _check("mx_quantize_grouped_ex", st)
+    col = MxTensor(q_col, s_col, fmt)
+    return col if axis == "col" else (MxTensor(q_row, s_row, fmt), col)
 
 
 def gemm(a: MxTensor, b: MxTensor, out_dtype: str = "bf16", out: torch.Tensor | None = None,
@@ -290,6 +346,45 @@ def grouped_gemm(a: MxTensor, offsets: torch.Tensor, b: MxTensor, out_dtype: str
                          FMT[a.fmt], _ptr(b.codes), _ptr(b.scales), FMT[b.fmt], _ptr(out),
                          DTYPE[out_dtype], _stream(stream))
     _check("mx_grouped_gemm", st)
+    return out
+
+
+def grouped_gemm_bcat(a: MxTensor, offsets: torch.Tensor, b: MxTensor, out_dtype: str = "bf16",
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Per group g: y[o_g:o_{g+1}] = A[o_g:o_{g+1}] * B_g^T with B_g the
+    columns [g*k, (g+1)*k) of one [n, groups*k] operand (b from quantize(...,
+    axis="col") of the stacked [groups*k, n] expert weights); k = a's K."""
+    total_m, k = a.codes.shape
+    n, ldb = b.codes.shape
+    groups = offsets.numel() - 1
+    tdtype = torch.float32 if out_dtype == "fp32" else torch.bfloat16
+    if out is None:
+        out = torch.empty((total_m, n), dtype=tdtype, device=a.codes.device)
+    st = mx_grouped_gemm_bcat(groups, _ptr(offsets), total_m, n, k, _ptr(a.codes),
+                              _ptr(a.scales), FMT[a.fmt], _ptr(b.codes), ldb, _ptr(b.scales),
+                              FMT[b.fmt], _ptr(out), DTYPE[out_dtype], _stream(stream))
+    _check("mx_grouped_gemm_bcat", st)
+    return out
+
+
+def grouped_gemm_wgrad(a: MxTensor, offsets: torch.Tensor, b: MxTensor, total_tokens: int,
+                       out_dtype: str = "fp32", out: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """Per group g: y[g] = A_g * B_g^T over the group's tokens, with a and b
+    from quantize_grouped(..., axis="col") (same offsets and ldq).  Returns
+    [groups, m, n]; an expert without tokens gets zeros."""
+    m, ldk = a.codes.shape
+    n, ldk2 = b.codes.shape
+    groups = offsets.numel() - 1
+    if ldk != ldk2:
+        raise ValueError("A and B must share the token layout (ldq)")
+    tdtype = torch.float32 if out_dtype == "fp32" else torch.bfloat16
+    if out is None:
+        out = torch.empty((groups, m, n), dtype=tdtype, device=a.codes.device)
+    st = mx_grouped_gemm_wgrad(groups, _ptr(offsets), total_tokens, m, n, ldk, _ptr(a.codes),
+                               _ptr(a.scales), FMT[a.fmt], _ptr(b.codes), _ptr(b.scales),
+                               FMT[b.fmt], _ptr(out), DTYPE[out_dtype], _stream(stream))
+    _check("mx_grouped_gemm_wgrad", st)
     return out
 
 

@@ -23,11 +23,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // t_row: tensor-memory address of this warp's lane quarter and first
 // column; grow0/gcol0: output coordinates of that lane 0 / column 0; rows
 // >= m_end and columns >= p.n are not stored.  `release` runs once the
-// accumulator share is in registers (it must fence and arrive).
+// accumulator share is in registers (it must fence and arrive).  `zero`:
+// the tile had no K blocks (an expert without tokens), so the output is
+// zero and tensor memory is not read.
 template <int BN, bool FUSED, typename Release>
 __device__ __forceinline__ void epilogue_share(const GemmParams& p, uint32_t t_row,
                                                int64_t grow0, int64_t gcol0, int64_t m_end,
-                                               uint8_t* stage_buf, uint32_t lane,
+                                               uint8_t* stage_buf, uint32_t lane, bool zero,
                                                Release&& release) {
   constexpr int kCols = BN / 2;
   const int64_t m_end_ = m_end;
@@ -65,10 +67,15 @@ __device__ __forceinline__ void epilogue_share(const GemmParams& p, uint32_t t_r
     // Whole share as FP32 in registers; the accumulator is released
     // before any epilogue arithmetic.
     uint32_t v[kCols];
+    if (!zero) {
 #pragma unroll
-    for (int c = 0; c < kCols / 32; ++c)
-      tmem_ld_32x32b_x32(t_row + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
-    tmem_ld_wait();
+      for (int c = 0; c < kCols / 32; ++c)
+        tmem_ld_32x32b_x32(t_row + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) v[c] = 0u;
+    }
     release();
     if (p.y_fp32) {
       float* y = static_cast<float*>(p.y);
@@ -123,14 +130,19 @@ __device__ __forceinline__ void epilogue_share(const GemmParams& p, uint32_t t_r
     }
   } else {
     uint32_t w[kCols / 2];
+    if (!zero) {
 #pragma unroll
-    for (int c = 0; c < kCols / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(t_row + c * 32, r);
-      tmem_ld_wait();
+      for (int c = 0; c < kCols / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, r);
+        tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        w[c * 16 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+        for (int i = 0; i < 16; ++i)
+          w[c * 16 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kCols / 2; ++i) w[i] = 0u;
     }
     release();
     uint16_t* y = static_cast<uint16_t*>(p.y);

@@ -93,35 +93,76 @@ struct Cfg {
 };
 
 struct TileInfo {
-  int64_t m0;       // first row of A / Y
-  int64_t m_end;    // rows >= m_end are not stored
-  int64_t n0;       // first column of Y
-  int64_t b_row0;   // first row of the B tile in the [rows, k] B tensor
-  int64_t sfa_rt;   // 128-row scale tile of A (-1: this block's tile is padding)
-  int64_t sfb_rt0;  // first 128-row scale tile of B
+  int64_t m0;        // first row of the A tile
+  int64_t y_row0;    // output row of the tile's first row
+  int64_t m_end;     // output rows >= m_end are not stored
+  int64_t n0;        // first column of Y (first row of the group's B)
+  int64_t b_row0;    // first row of the B tile in the B tensor map
+  int64_t a_kx0;     // first K column of the A operand in its tensor map
+  int64_t b_kx0;     // first K column of the B operand
+  int64_t sfa_unit;  // first 512-byte scale unit of A (-1: this block's tile is padding)
+  int64_t sfb_unit;  // first scale unit of the B tile's first 128-row tile
+  int64_t sfb_step;  // scale units between consecutive 128-row tiles of B
+  int32_t k_blocks;  // 32-element K blocks of the tile's contraction
 };
 
 // Work unit u of a cluster = CM m-tiles x one n-tile; block `rank` of the
 // cluster takes m-tile CM*mu + rank.  Dense units follow a banded raster
 // (p.band_m m-tiles per band, n outer inside a band) so a band of A stays in
-// L2 while B streams once per band; grouped units walk groups, then
-// m-units, then n.
-template <int BN, bool GROUPED, int CM>
+// L2 while B streams once per band; units grouped by rows walk groups, then
+// m-units, then n; units grouped along K walk groups, then m-units, then n,
+// every group covering the whole [m, n] output of its own matrix.  Scale
+// units: 512 bytes per 128 rows x 128 K, ceil(ld / 128) per 128-row tile.
+template <int BN, int MODE, int CM>
 __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t u, int64_t n_tiles,
                                               uint32_t rank, const GroupSmem* gs) {
   TileInfo ti;
-  if constexpr (GROUPED) {
+  const int64_t a_tiles_k = (p.lda + 127) / 128;
+  const int64_t b_tiles_k = (p.ldb + 127) / 128;
+  ti.a_kx0 = 0;
+  ti.b_kx0 = 0;
+  ti.sfb_step = b_tiles_k;
+  ti.k_blocks = static_cast<int32_t>(p.k / 32);
+  if constexpr (MODE == kModeGroupM) {
     const int64_t mu = u / n_tiles;
     const int64_t n_blk = u - mu * n_tiles;
     const int g = find_group(gs->units, p.groups, static_cast<int32_t>(mu));
     const int64_t lm = (mu - gs->units[g]) * CM + rank;  // m-tile inside the group
     const int64_t g_tiles = gs->tiles[g + 1] - gs->tiles[g];
     ti.m0 = static_cast<int64_t>(gs->off[g]) + lm * BM;
+    ti.y_row0 = ti.m0;
     ti.m_end = lm < g_tiles ? static_cast<int64_t>(gs->off[g + 1]) : ti.m0;
-    ti.sfa_rt = lm < g_tiles ? gs->tiles[g] + lm : -1;
+    ti.sfa_unit = lm < g_tiles ? (gs->tiles[g] + lm) * a_tiles_k : -1;
     ti.n0 = n_blk * BN;
-    ti.b_row0 = static_cast<int64_t>(g) * p.n + ti.n0;
-    ti.sfb_rt0 = ti.b_row0 / 128;
+    if (p.b_concat) {
+      // one [n, ldb] B; expert g's operand is columns [g*k, (g+1)*k)
+      ti.b_row0 = ti.n0;
+      ti.b_kx0 = static_cast<int64_t>(g) * p.k;
+      ti.sfb_unit = (ti.n0 / 128) * b_tiles_k + static_cast<int64_t>(g) * (p.k / 128);
+    } else {
+      // [groups, n, k] B, one swizzled scale matrix per expert
+      ti.b_row0 = static_cast<int64_t>(g) * p.n + ti.n0;
+      ti.sfb_unit = (ti.b_row0 / 128) * b_tiles_k;
+    }
+  } else if constexpr (MODE == kModeGroupK) {
+    const int64_t m_tiles = (p.m + BM - 1) / BM;
+    const int64_t per_group = ((m_tiles + CM - 1) / CM) * n_tiles;
+    const int g = static_cast<int>(u / per_group);
+    const int64_t w = u - g * per_group;
+    const int64_t mu = w / n_tiles;
+    const int64_t n_blk = w - mu * n_tiles;
+    const int64_t m_blk = mu * CM + rank;
+    const int64_t kt0 = gs->tiles[g];  // the group's first 128-column K tile
+    ti.m0 = m_blk * BM;
+    ti.y_row0 = static_cast<int64_t>(g) * p.m + ti.m0;
+    ti.m_end = static_cast<int64_t>(g) * p.m + p.m;  // a padding m-tile starts past it
+    ti.sfa_unit = m_blk < m_tiles ? m_blk * a_tiles_k + kt0 : -1;
+    ti.n0 = n_blk * BN;
+    ti.b_row0 = ti.n0;
+    ti.a_kx0 = kt0 * BK;
+    ti.b_kx0 = kt0 * BK;
+    ti.sfb_unit = (ti.n0 / 128) * b_tiles_k + kt0;
+    ti.k_blocks = (gs->off[g + 1] - gs->off[g] + 31) / 32;
   } else {
     const int64_t m_tiles = (p.m + BM - 1) / BM;
     const int64_t m_units = (m_tiles + CM - 1) / CM;
@@ -134,19 +175,21 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t u, in
     const int64_t mu = band * band_units + (within - n_blk * in_band);
     const int64_t m_blk = mu * CM + rank;
     ti.m0 = m_blk * BM;
+    ti.y_row0 = ti.m0;
     ti.m_end = p.m;
-    ti.sfa_rt = m_blk < m_tiles ? m_blk : -1;
+    ti.sfa_unit = m_blk < m_tiles ? m_blk * a_tiles_k : -1;
     ti.n0 = n_blk * BN;
     ti.b_row0 = ti.n0;
-    ti.sfb_rt0 = ti.n0 / 128;
+    ti.sfb_unit = (ti.n0 / 128) * b_tiles_k;
   }
   return ti;
 }
 
-template <int BN, bool GROUPED, int CM, bool FUSED>
+template <int BN, int MODE, int CM, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+  constexpr bool GROUPED = MODE != kModeDense;
   using C = Cfg<BN, GROUPED>;
   static_assert(CM == 1 || CM == 2, "cluster size");
   constexpr uint16_t kPairMask = 0x3;
@@ -192,7 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     if constexpr (GROUPED) {
-      group_tile_prefix(p.offsets, p.groups, p.m, gs->off, gs->tiles, &gs->valid, CM, gs->units);
+      // grouped along K the offsets split the p.k tokens of the contraction
+      group_tile_prefix(p.offsets, p.groups, MODE == kModeGroupK ? p.k : p.m, gs->off, gs->tiles,
+                        &gs->valid, CM, gs->units);
     }
   }
   if (warp == 1) {
@@ -213,18 +258,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t n_tiles = (p.n + BN - 1) / BN;
   int64_t num_units;
   if constexpr (GROUPED) {
-    if (!gs->valid) {
+    // grouped along K, the 128-padded token segments must fit in A and B
+    const bool fits = MODE != kModeGroupK ||
+                      (gs->valid && static_cast<int64_t>(gs->tiles[p.groups]) * BK <= p.lda &&
+                       static_cast<int64_t>(gs->tiles[p.groups]) * BK <= p.ldb);
+    if (!gs->valid || !fits) {
       if (blockIdx.x == 0 && threadIdx.x == 0) record_device_status(p.status, MX_DEV_BAD_OFFSETS);
       num_units = 0;
+    } else if constexpr (MODE == kModeGroupK) {
+      num_units = static_cast<int64_t>(p.groups) * ((p.m + BM * CM - 1) / (BM * CM)) * n_tiles;
     } else {
       num_units = static_cast<int64_t>(gs->units[p.groups]) * n_tiles;
     }
   } else {
     num_units = ((p.m + BM * CM - 1) / (BM * CM)) * n_tiles;
   }
-  const int64_t k_tiles = (p.k + BK - 1) / BK;
-  const int32_t k_blocks = static_cast<int32_t>(p.k / 32);
-  const int64_t scale_tiles_k = k_tiles;  // 512-byte scale units per 128-row tile
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
@@ -232,19 +280,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t issued = 0;  // stage fills issued so far
     bool ok = true;
     for (int64_t u = cluster_id; u < num_units && ok; u += num_clusters) {
-      const TileInfo ti = tile_info<BN, GROUPED, CM>(p, u, n_tiles, rank, gs);
+      const TileInfo ti = tile_info<BN, MODE, CM>(p, u, n_tiles, rank, gs);
       int sfb_units = 0;
 #pragma unroll
       for (int j = 0; j < C::kSfbUnits; ++j)
         if (ti.n0 + 128 * j < p.n) ++sfb_units;
       const uint32_t tx =
-          C::kABytes + C::kBBytes + (ti.sfa_rt >= 0 ? 512u : 0u) + 512u * sfb_units;
-      const uint8_t* sfa_src = p.sa + (ti.sfa_rt >= 0 ? ti.sfa_rt : 0) * scale_tiles_k * 512;
-      const uint8_t* sfb_src = p.sb + ti.sfb_rt0 * scale_tiles_k * 512;
-      const int64_t sfb_stride = scale_tiles_k * 512;
+          C::kABytes + C::kBBytes + (ti.sfa_unit >= 0 ? 512u : 0u) + 512u * sfb_units;
+      const uint8_t* sfa_src = p.sa + (ti.sfa_unit >= 0 ? ti.sfa_unit : 0) * 512;
+      const uint8_t* sfb_src = p.sb + ti.sfb_unit * 512;
+      const int64_t sfb_stride = ti.sfb_step * 512;
       const int32_t a_row = static_cast<int32_t>(ti.m0);
       const int32_t b_row = static_cast<int32_t>(ti.b_row0 + rank * (BN / CM));
-      const int32_t kt_count = static_cast<int32_t>(k_tiles);
+      const int32_t kt_count = (ti.k_blocks + 3) / 4;
       for (int32_t kt = 0; kt < kt_count; ++kt) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) {
           ok = false;
@@ -252,16 +300,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(&full[stage], tx);
         ++issued;
-        const int32_t kx = kt * BK;
-        tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full[stage], kx, a_row);
+        const int32_t kx_a = static_cast<int32_t>(ti.a_kx0) + kt * BK;
+        const int32_t kx_b = static_cast<int32_t>(ti.b_kx0) + kt * BK;
+        tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full[stage], kx_a, a_row);
         if constexpr (CM > 1) {
           // this block's half of the shared B tile, delivered to both blocks
           tma_load_2d_multicast(sB + stage * C::kBBytes + rank * (C::kBBytes / CM), &tmap_b,
-                                &full[stage], kx, b_row, kPairMask);
+                                &full[stage], kx_b, b_row, kPairMask);
         } else {
-          tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full[stage], kx, b_row);
+          tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full[stage], kx_b, b_row);
         }
-        if (ti.sfa_rt >= 0) bulk_load(sSfa + stage * 512, sfa_src, 512, &full[stage]);
+        if (ti.sfa_unit >= 0) bulk_load(sSfa + stage * 512, sfa_src, 512, &full[stage]);
         for (int j = 0; j < sfb_units; ++j)
           bulk_load(sSfb + (stage * C::kSfbUnits + j) * 512, sfb_src + j * sfb_stride, 512,
                     &full[stage]);
@@ -292,12 +341,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sfa_lo0 = smem_desc_lo(smem_u32(sSfa), 0);
     const uint32_t sfb_lo0 = smem_desc_lo(smem_u32(sSfb), 0);
     const uint32_t idesc0 = mxf8_idesc(p.fa, p.fb, BM, BN, 0, 0);
-    const int32_t kt_count = static_cast<int32_t>(k_tiles);
-    const int32_t kt_full = k_blocks / 4;  // k-tiles with all four scale blocks
+    // Grouped along K every group has its own contraction length; a group
+    // without tokens has none (its output tile is written as zeros).
+    const uint32_t group_units =
+        static_cast<uint32_t>(((p.m + BM * CM - 1) / (BM * CM)) * n_tiles);
+    int32_t k_blocks = static_cast<int32_t>(p.k / 32);
     uint32_t stage = 0, phase = 0;
     uint32_t acc = 0, acc_phase = 0;
     bool ok = true;
     for (int64_t u = cluster_id; u < num_units && ok; u += num_clusters) {
+      if constexpr (MODE == kModeGroupK) {
+        const int g = static_cast<int>(static_cast<uint32_t>(u) / group_units);
+        k_blocks = (gs->off[g + 1] - gs->off[g] + 31) / 32;
+      }
+      const int32_t kt_count = (k_blocks + 3) / 4;
+      const int32_t kt_full = k_blocks / 4;  // k-tiles with all four scale blocks
       if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) break;
       tc_fence_after_sync();
       const uint32_t d_tmem = tmem_base + acc * BN;
@@ -344,7 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      tc_commit(&acc_full[acc]);
+      if (kt_count > 0) {
+        tc_commit(&acc_full[acc]);
+      } else {
+        mbar_arrive(&acc_full[acc]);  // nothing to accumulate: the epilogue writes zeros
+      }
       if (++acc == C::kAccStages) {
         acc = 0;
         acc_phase ^= 1u;
@@ -368,17 +430,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* stage_buf = sEpi + (warp - 2) * kEpiStageBytes;
     uint32_t acc = 0, acc_phase = 0;
     for (int64_t u = cluster_id; u < num_units; u += num_clusters) {
-      const TileInfo ti = tile_info<BN, GROUPED, CM>(p, u, n_tiles, rank, gs);
+      const TileInfo ti = tile_info<BN, MODE, CM>(p, u, n_tiles, rank, gs);
       const bool got = mbar_wait(&acc_full[acc], acc_phase, s_abort, p.status, p.wait_limit_ns);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + ((q * 32u) << 16) + acc * BN + half * kCols;
-      const int64_t grow0 = ti.m0 + q * 32;
+      const int64_t grow0 = ti.y_row0 + q * 32;
       const int64_t gcol0 = ti.n0 + half * kCols;
-      epilogue_share<BN, FUSED>(p, t_row, grow0, gcol0, ti.m_end, stage_buf, lane, [&] {
-        tc_fence_before_sync();
-        mbar_arrive(&acc_empty[acc]);
-      });
+      epilogue_share<BN, FUSED>(p, t_row, grow0, gcol0, ti.m_end, stage_buf, lane, ti.k_blocks == 0,
+                                [&] {
+                                  tc_fence_before_sync();
+                                  mbar_arrive(&acc_empty[acc]);
+                                });
       if (++acc == C::kAccStages) {
         acc = 0;
         acc_phase ^= 1u;
@@ -410,11 +473,11 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
   }
 }
 
-template <int BN, bool GROUPED, int CM, bool FUSED = false>
+template <int BN, int MODE, int CM, bool FUSED = false>
 cudaError_t launch_impl(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                         int num_sms, cudaStream_t stream) {
-  using C = Cfg<BN, GROUPED>;
-  auto kern = mx_gemm_kernel<BN, GROUPED, CM, FUSED>;
+  using C = Cfg<BN, MODE != kModeDense>;
+  auto kern = mx_gemm_kernel<BN, MODE, CM, FUSED>;
   // The attribute is per function and device; set it once per device.
   static bool attr_set[64] = {};
   int dev = 0;
@@ -427,9 +490,11 @@ cudaError_t launch_impl(const GemmParams& p, const CUtensorMap& ta, const CUtens
   }
   const int64_t n_tiles = (p.n + BN - 1) / BN;
   const int64_t m_tiles = (p.m + BM - 1) / BM;
-  // upper bound of the work units (grouped: every group may add a partial unit)
-  const int64_t units = GROUPED ? ((m_tiles + p.groups + CM - 1) / CM + p.groups) * n_tiles
-                                : ((m_tiles + CM - 1) / CM) * n_tiles;
+  // upper bound of the work units (grouped by rows: every group may add a
+  // partial unit; grouped along K: every group covers the whole output)
+  int64_t units = ((m_tiles + CM - 1) / CM) * n_tiles;
+  if (MODE == kModeGroupM) units = ((m_tiles + p.groups + CM - 1) / CM + p.groups) * n_tiles;
+  if (MODE == kModeGroupK) units *= p.groups;
   if (units == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -454,6 +519,16 @@ cudaError_t launch_impl(const GemmParams& p, const CUtensorMap& ta, const CUtens
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
 }
 
+template <int MODE>
+cudaError_t launch_mode(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                        int block_n, int cluster_m, int num_sms, cudaStream_t stream) {
+  if (block_n == 256)
+    return cluster_m == 2 ? launch_impl<256, MODE, 2>(p, ta, tb, num_sms, stream)
+                          : launch_impl<256, MODE, 1>(p, ta, tb, num_sms, stream);
+  return cluster_m == 2 ? launch_impl<128, MODE, 2>(p, ta, tb, num_sms, stream)
+                        : launch_impl<128, MODE, 1>(p, ta, tb, num_sms, stream);
+}
+
 }  // namespace
 
 int gemm_default_block_n(const GemmParams& p) {
@@ -463,27 +538,19 @@ int gemm_default_block_n(const GemmParams& p) {
 
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                         int block_n, int cluster_m, int num_sms, cudaStream_t stream) {
-  const bool grouped = p.groups > 0;
   if (p.bias != nullptr || p.act != 0) {  // fused epilogue: dense GEMMs only
-    if (grouped) return cudaErrorNotSupported;
+    if (p.mode != kModeDense) return cudaErrorNotSupported;
     if (block_n == 256)
-      return cluster_m == 2 ? launch_impl<256, false, 2, true>(p, ta, tb, num_sms, stream)
-                            : launch_impl<256, false, 1, true>(p, ta, tb, num_sms, stream);
-    return cluster_m == 2 ? launch_impl<128, false, 2, true>(p, ta, tb, num_sms, stream)
-                          : launch_impl<128, false, 1, true>(p, ta, tb, num_sms, stream);
+      return cluster_m == 2 ? launch_impl<256, kModeDense, 2, true>(p, ta, tb, num_sms, stream)
+                            : launch_impl<256, kModeDense, 1, true>(p, ta, tb, num_sms, stream);
+    return cluster_m == 2 ? launch_impl<128, kModeDense, 2, true>(p, ta, tb, num_sms, stream)
+                          : launch_impl<128, kModeDense, 1, true>(p, ta, tb, num_sms, stream);
   }
-  if (block_n == 256) {
-    if (cluster_m == 2)
-      return grouped ? launch_impl<256, true, 2>(p, ta, tb, num_sms, stream)
-                     : launch_impl<256, false, 2>(p, ta, tb, num_sms, stream);
-    return grouped ? launch_impl<256, true, 1>(p, ta, tb, num_sms, stream)
-                   : launch_impl<256, false, 1>(p, ta, tb, num_sms, stream);
-  }
-  if (cluster_m == 2)
-    return grouped ? launch_impl<128, true, 2>(p, ta, tb, num_sms, stream)
-                   : launch_impl<128, false, 2>(p, ta, tb, num_sms, stream);
-  return grouped ? launch_impl<128, true, 1>(p, ta, tb, num_sms, stream)
-                 : launch_impl<128, false, 1>(p, ta, tb, num_sms, stream);
+  if (p.mode == kModeGroupM)
+    return launch_mode<kModeGroupM>(p, ta, tb, block_n, cluster_m, num_sms, stream);
+  if (p.mode == kModeGroupK)
+    return launch_mode<kModeGroupK>(p, ta, tb, block_n, cluster_m, num_sms, stream);
+  return launch_mode<kModeDense>(p, ta, tb, block_n, cluster_m, num_sms, stream);
 }
 
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {

@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + ((q * 32u) << 16) + half * (kPairN / 2);
       epilogue_share<kPairN, FUSED>(p, t_row, t.m0 + q * 32, t.n0 + half * (kPairN / 2), p.m,
-                                    stage_buf, lane, [&] {
+                                    stage_buf, lane, false, [&] {
                                       tc_fence_before_sync();
                                       __syncwarp();
                                       if (lane == 0) mbar_arrive_cluster(acc_empty_leader);

@@ -20,10 +20,12 @@ struct QuantizeParams {
   uint8_t* s_col;      // swizzled scales of the [cols, rows] operand
   int32_t fmt;         // 0 = E4M3, 1 = E5M2
   int32_t rule;        // 0 = floor, 1 = ceil
-  const int32_t* offsets;  // grouped rowwise only: device int32[groups + 1]
+  const int32_t* offsets;  // grouped only: device int32[groups + 1]
   int32_t groups;
   uint32_t* status;    // device status word
   uint64_t wait_limit_ns;
+  int64_t ldq_col;     // columns of the q_col matrix (dense: rows; grouped: the
+                       // 128-padded token capacity, a multiple of 128)
 };
 
 // tmap_x: 2-D bf16 tensor map over x (box 128 x 128, no swizzle); tmap_r:
@@ -31,13 +33,28 @@ struct QuantizeParams {
 // nullptr for round-to-nearest-even.
 cudaError_t launch_quantize(const QuantizeParams& p, const CUtensorMap& tmap_x,
                             const CUtensorMap* tmap_r, int num_sms, cudaStream_t stream);
+// Grouped: rowwise (q_row) and/or columnwise (q_col, per-group padded
+// segments of 128 columns) quantization of token groups.
 cudaError_t launch_quantize_grouped(const QuantizeParams& p, const CUtensorMap& tmap_x,
                                     int num_sms, cudaStream_t stream);
 
+// GEMM modes: dense; grouped by rows of A (each expert owns a range of A
+// rows and its own B); grouped along K (each expert owns a 128-aligned
+// range of the K columns of A and B and its own output matrix).
+constexpr int kModeDense = 0;
+constexpr int kModeGroupM = 1;
+constexpr int kModeGroupK = 2;
+
 struct GemmParams {
-  int64_t m;           // rows of A and Y (grouped: total rows)
+  int64_t m;           // rows of A and Y (grouped by rows: total rows; grouped
+                       // along K: rows of A and of each output matrix)
   int64_t n;           // rows of each B (columns of Y)
-  int64_t k;           // contraction length, multiple of 32
+  int64_t k;           // contraction length, multiple of 32 (grouped along K:
+                       // unused, each group's length comes from the offsets)
+  int64_t lda;         // columns of the A code matrix (K-contiguous)
+  int64_t ldb;         // columns of the B code matrix
+  int32_t b_concat;    // grouped by rows: 1 = B is one [n, ldb] matrix with
+                       // expert g's operand in columns [g*k, (g+1)*k)
   const uint8_t* sa;   // swizzled scales of A (grouped: per-group padded)
   const uint8_t* sb;   // swizzled scales of B (grouped: one matrix per group)
   void* y;
@@ -47,6 +64,7 @@ struct GemmParams {
   int32_t fb;
   const int32_t* offsets;  // grouped only: device int32[groups + 1]
   int32_t groups;          // 0 for the dense GEMM
+  int32_t mode;            // kModeDense, kModeGroupM or kModeGroupK
   uint32_t* status;
   uint64_t wait_limit_ns;
   int32_t band_m;          // m-tiles per raster band (dense), a multiple of 2

@@ -130,19 +130,35 @@ int block_n_choice(const mx::GemmParams& p) {
   return mx::gemm_default_block_n(p);
 }
 
-mx_status gemm_common(int64_t m, int64_t n, int64_t k, const uint8_t* a, const uint8_t* sa,
-                      mx_fmt fa, const uint8_t* b, const uint8_t* sb, mx_fmt fb, void* y,
-                      mx_dtype y_dtype, int64_t ldy, int32_t groups, const int32_t* d_offsets,
-                      int64_t b_rows, cudaStream_t stream, const float* bias = nullptr,
+// Operand geometry of one GEMM launch: A codes [m, lda] (grouped along K:
+// [m, lda] shared by all groups), B codes [b_rows, ldb]; scales swizzled
+// over the same shapes.
+struct GemmShape {
+  int64_t m, n, k;
+  int64_t lda, ldb, b_rows;
+  int32_t groups = 0;
+  const int32_t* d_offsets = nullptr;
+  int32_t mode = mx::kModeDense;
+  int32_t b_concat = 0;
+};
+
+mx_status gemm_common(const GemmShape& g, const uint8_t* a, const uint8_t* sa, mx_fmt fa,
+                      const uint8_t* b, const uint8_t* sb, mx_fmt fb, void* y, mx_dtype y_dtype,
+                      int64_t ldy, cudaStream_t stream, const float* bias = nullptr,
                       int32_t act = 0) {
+  const int64_t m = g.m, n = g.n, k = g.k;
   if (!a || !sa || !b || !sb || !y) return MX_ERR_INVALID_ARG;
-  if (m < 0 || n <= 0 || k < 32 || k % 32 != 0 || n % 8 != 0 || ldy < n) return MX_ERR_INVALID_ARG;
+  if (m < 0 || n <= 0 || k < 0 || n % 8 != 0 || ldy < n) return MX_ERR_INVALID_ARG;
+  // grouped along K, k is the token total that the offsets split
+  if (g.mode != mx::kModeGroupK && (k < 32 || k % 32 != 0)) return MX_ERR_INVALID_ARG;
   if (!valid_fmt(fa) || !valid_fmt(fb)) return MX_ERR_INVALID_ARG;
   if (y_dtype != MX_BF16 && y_dtype != MX_FP32) return MX_ERR_INVALID_ARG;
-  if (m > INT32_MAX || b_rows > INT32_MAX || k > INT32_MAX) return MX_ERR_UNSUPPORTED;
+  if (m > INT32_MAX || g.b_rows > INT32_MAX || k > INT32_MAX || g.lda > INT32_MAX ||
+      g.ldb > INT32_MAX)
+    return MX_ERR_UNSUPPORTED;
   const int64_t elt = y_dtype == MX_FP32 ? 4 : 2;
   if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(y) ||
-      (ldy * elt) % 16 != 0)
+      (ldy * elt) % 16 != 0 || g.lda % 16 != 0 || g.ldb % 16 != 0)
     return MX_ERR_MISALIGNED;
   DeviceState* st = nullptr;
   mx_status s = device_state(&st);
@@ -153,6 +169,9 @@ mx_status gemm_common(int64_t m, int64_t n, int64_t k, const uint8_t* a, const u
   p.m = m;
   p.n = n;
   p.k = k;
+  p.lda = g.lda;
+  p.ldb = g.ldb;
+  p.b_concat = g.b_concat;
   p.sa = sa;
   p.sb = sb;
   p.y = y;
@@ -160,8 +179,9 @@ mx_status gemm_common(int64_t m, int64_t n, int64_t k, const uint8_t* a, const u
   p.y_fp32 = y_dtype == MX_FP32 ? 1 : 0;
   p.fa = fa;
   p.fb = fb;
-  p.offsets = d_offsets;
-  p.groups = groups;
+  p.offsets = g.d_offsets;
+  p.groups = g.groups;
+  p.mode = g.mode;
   p.status = st->status;
   p.wait_limit_ns = g_wait_ns;
   p.bias = bias;
@@ -172,29 +192,41 @@ mx_status gemm_common(int64_t m, int64_t n, int64_t k, const uint8_t* a, const u
     if (v >= 2 && v % 2 == 0) p.band_m = v;
   }
   const int block_n = block_n_choice(p);
-  // Dense GEMMs pair blocks (B tile multicast); grouped GEMMs measured
-  // slightly faster unpaired.  MX_GEMM_CLUSTER_M overrides (1 or 2).
-  int cluster_m = groups > 0 ? 1 : 2;
+  // Dense GEMMs and the per-expert weight gradient pair blocks (B tile
+  // multicast); GEMMs grouped by rows measured slightly faster unpaired.
+  // MX_GEMM_CLUSTER_M overrides (1 or 2).
+  int cluster_m = g.mode == mx::kModeGroupM ? 1 : 2;
   if (const char* env = std::getenv("MX_GEMM_CLUSTER_M")) cluster_m = std::atoi(env) == 1 ? 1 : 2;
 
   CUtensorMap ta, tb;
-  if ((s = encode_codes_map(&ta, a, k, m, k, 128)) != MX_OK) return s;
-  if (use_pair_kernel(groups)) {
+  if ((s = encode_codes_map(&ta, a, g.lda, m, g.lda, 128)) != MX_OK) return s;
+  if (g.mode == mx::kModeDense && use_pair_kernel(0)) {
     // block pairs: each block loads 128 rows of the 256-row B tile
     CUtensorMap tsa, tsb;
-    if ((s = encode_codes_map(&tb, b, k, b_rows, k, 128)) != MX_OK) return s;
+    if ((s = encode_codes_map(&tb, b, k, g.b_rows, k, 128)) != MX_OK) return s;
     if ((s = encode_scale_map(&tsa, sa, m, k, 1)) != MX_OK) return s;
-    if ((s = encode_scale_map(&tsb, sb, b_rows, k, 2)) != MX_OK) return s;
+    if ((s = encode_scale_map(&tsb, sb, g.b_rows, k, 2)) != MX_OK) return s;
     if (mx::launch_gemm_pair(p, ta, tb, tsa, tsb, st->num_sms, stream) != cudaSuccess)
       return MX_ERR_CUDA;
     return MX_OK;
   }
   // With block pairs each block loads half of the B tile (multicast).
   const uint32_t b_box_rows = static_cast<uint32_t>(block_n / cluster_m);
-  if ((s = encode_codes_map(&tb, b, k, b_rows, k, b_box_rows)) != MX_OK) return s;
+  if ((s = encode_codes_map(&tb, b, g.ldb, g.b_rows, g.ldb, b_box_rows)) != MX_OK) return s;
   if (mx::launch_gemm(p, ta, tb, block_n, cluster_m, st->num_sms, stream) != cudaSuccess)
     return MX_ERR_CUDA;
   return MX_OK;
+}
+
+GemmShape dense_shape(int64_t m, int64_t n, int64_t k) {
+  GemmShape g;
+  g.m = m;
+  g.n = n;
+  g.k = k;
+  g.lda = k;
+  g.ldb = k;
+  g.b_rows = n;
+  return g;
 }
 
 }  // namespace
@@ -252,6 +284,7 @@ mx_status quantize_common(const void* x, mx_dtype x_dtype, int64_t rows, int64_t
   p.rule = rule;
   p.status = st->status;
   p.wait_limit_ns = g_wait_ns;
+  p.ldq_col = rows;
   if (rows == 0 || cols == 0) return MX_OK;
   CUtensorMap tmap, tmap_r;
   if ((s = encode_bf16_map(&tmap, x, cols, rows, ldx)) != MX_OK) return s;
@@ -287,15 +320,39 @@ mx_status mx_quantize_grouped(const void* x, mx_dtype x_dtype, int64_t total_row
                               int64_t ldx, mx_fmt fmt, mx_scale_rule rule, int32_t groups,
                               const int32_t* d_offsets, uint8_t* q, uint8_t* s,
                               cudaStream_t stream) {
+  if (!q || !s) return MX_ERR_INVALID_ARG;
+  return mx_quantize_grouped_ex(x, x_dtype, total_rows, cols, ldx, fmt, MX_ROWWISE, rule, groups,
+                                d_offsets, q, s, nullptr, 0, nullptr, stream);
+}
+
+int64_t mx_grouped_cols_capacity(int64_t total_rows, int32_t groups) {
+  if (total_rows < 0 || groups < 0) return 0;
+  return (total_rows / 128 + groups) * 128;
+}
+
+mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_rows,
+                                 int64_t cols, int64_t ldx, mx_fmt fmt, mx_axis axis,
+                                 mx_scale_rule rule, int32_t groups, const int32_t* d_offsets,
+                                 uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, int64_t ldq_col,
+                                 uint8_t* s_col, cudaStream_t stream) {
   if (x_dtype != MX_BF16) return x_dtype == MX_FP32 ? MX_ERR_UNSUPPORTED : MX_ERR_INVALID_ARG;
   if (!valid_fmt(fmt) || (rule != MX_SCALE_FLOOR && rule != MX_SCALE_CEIL))
     return MX_ERR_INVALID_ARG;
-  if (!x || !q || !s || !d_offsets) return MX_ERR_INVALID_ARG;
-  if (groups < 1 || groups > 1000) return MX_ERR_INVALID_ARG;
-  if (total_rows < 0 || total_rows > INT32_MAX || cols < 0 || cols % 32 != 0 || ldx < cols)
+  if (axis != MX_ROWWISE && axis != MX_COLWISE && axis != MX_BOTH) return MX_ERR_INVALID_ARG;
+  const bool row = axis & MX_ROWWISE;
+  const bool col = axis & MX_COLWISE;
+  if (!x || !d_offsets || (row && (!q_row || !s_row)) || (col && (!q_col || !s_col)))
     return MX_ERR_INVALID_ARG;
+  if (groups < 1 || groups > 1000) return MX_ERR_INVALID_ARG;
+  if (total_rows < 0 || total_rows > INT32_MAX || cols < 0 || ldx < cols || cols % 8 != 0)
+    return MX_ERR_INVALID_ARG;
+  if (row && cols % 32 != 0) return MX_ERR_INVALID_ARG;
+  if (col && (ldq_col <= 0 || ldq_col % 128 != 0)) return MX_ERR_INVALID_ARG;
   if (ceil_div(cols, 128) > 65535) return MX_ERR_UNSUPPORTED;
-  if (!aligned16(x) || !aligned16(q) || !aligned16(s) || ldx % 8 != 0) return MX_ERR_MISALIGNED;
+  if (!aligned16(x) || ldx % 8 != 0) return MX_ERR_MISALIGNED;
+  if ((row && (!aligned16(q_row) || !aligned16(s_row))) ||
+      (col && (!aligned16(q_col) || !aligned16(s_col))))
+    return MX_ERR_MISALIGNED;
   DeviceState* st = nullptr;
   mx_status status = device_state(&st);
   if (status != MX_OK) return status;
@@ -304,8 +361,11 @@ mx_status mx_quantize_grouped(const void* x, mx_dtype x_dtype, int64_t total_row
   p.rows = total_rows;
   p.cols = cols;
   p.ldx = ldx;
-  p.q_row = q;
-  p.s_row = s;
+  p.q_row = row ? q_row : nullptr;
+  p.s_row = row ? s_row : nullptr;
+  p.q_col = col ? q_col : nullptr;
+  p.s_col = col ? s_col : nullptr;
+  p.ldq_col = col ? ldq_col : 0;
   p.fmt = fmt;
   p.rule = rule;
   p.offsets = d_offsets;
@@ -324,7 +384,7 @@ mx_status mx_quantize_grouped(const void* x, mx_dtype x_dtype, int64_t total_row
 mx_status mx_gemm(int64_t m, int64_t n, int64_t k, const uint8_t* a, const uint8_t* sa, mx_fmt fa,
                   const uint8_t* b, const uint8_t* sb, mx_fmt fb, void* y, mx_dtype y_dtype,
                   int64_t ldy, cudaStream_t stream) {
-  return gemm_common(m, n, k, a, sa, fa, b, sb, fb, y, y_dtype, ldy, 0, nullptr, n, stream);
+  return gemm_common(dense_shape(m, n, k), a, sa, fa, b, sb, fb, y, y_dtype, ldy, stream);
 }
 
 mx_status mx_gemm_bias_act(int64_t m, int64_t n, int64_t k, const uint8_t* a, const uint8_t* sa,
@@ -333,7 +393,7 @@ mx_status mx_gemm_bias_act(int64_t m, int64_t n, int64_t k, const uint8_t* a, co
                            int64_t ldy, cudaStream_t stream) {
   if (act != MX_ACT_NONE && act != MX_ACT_SILU) return MX_ERR_INVALID_ARG;
   if (bias != nullptr && !aligned16(bias)) return MX_ERR_MISALIGNED;
-  return gemm_common(m, n, k, a, sa, fa, b, sb, fb, y, y_dtype, ldy, 0, nullptr, n, stream, bias,
+  return gemm_common(dense_shape(m, n, k), a, sa, fa, b, sb, fb, y, y_dtype, ldy, stream, bias,
                      act);
 }
 
@@ -343,8 +403,51 @@ mx_status mx_grouped_gemm(int32_t groups, const int32_t* d_offsets, int64_t tota
                           mx_dtype y_dtype, cudaStream_t stream) {
   if (groups < 1 || groups > 1000 || !d_offsets) return MX_ERR_INVALID_ARG;
   if (n % 128 != 0) return MX_ERR_INVALID_ARG;
-  return gemm_common(total_m, n, k, a, sa, fa, b, sb, fb, y, y_dtype, n, groups, d_offsets,
-                     static_cast<int64_t>(groups) * n, stream);
+  GemmShape g = dense_shape(total_m, n, k);
+  g.b_rows = static_cast<int64_t>(groups) * n;
+  g.groups = groups;
+  g.d_offsets = d_offsets;
+  g.mode = mx::kModeGroupM;
+  return gemm_common(g, a, sa, fa, b, sb, fb, y, y_dtype, n, stream);
+}
+
+mx_status mx_grouped_gemm_bcat(int32_t groups, const int32_t* d_offsets, int64_t total_m,
+                               int64_t n, int64_t k, const uint8_t* a, const uint8_t* sa,
+                               mx_fmt fa, const uint8_t* b, int64_t ldb, const uint8_t* sb,
+                               mx_fmt fb, void* y, mx_dtype y_dtype, cudaStream_t stream) {
+  if (groups < 1 || groups > 1000 || !d_offsets) return MX_ERR_INVALID_ARG;
+  if (k <= 0 || k % 128 != 0 || ldb < static_cast<int64_t>(groups) * k) return MX_ERR_INVALID_ARG;
+  GemmShape g = dense_shape(total_m, n, k);
+  g.ldb = ldb;
+  g.b_rows = n;
+  g.groups = groups;
+  g.d_offsets = d_offsets;
+  g.mode = mx::kModeGroupM;
+  g.b_concat = 1;
+  return gemm_common(g, a, sa, fa, b, sb, fb, y, y_dtype, n, stream);
+}
+
+mx_status mx_grouped_gemm_wgrad(int32_t groups, const int32_t* d_offsets, int64_t total_tokens,
+                                int64_t m, int64_t n, int64_t ldk, const uint8_t* a,
+                                const uint8_t* sa, mx_fmt fa, const uint8_t* b,
+                                const uint8_t* sb, mx_fmt fb, void* y, mx_dtype y_dtype,
+                                cudaStream_t stream) {
+  if (groups < 1 || groups > 1000 || !d_offsets) return MX_ERR_INVALID_ARG;
+  if (total_tokens < 0 || total_tokens > INT32_MAX || ldk <= 0 || ldk % 128 != 0)
+    return MX_ERR_INVALID_ARG;
+  // k carries the token total for the device-side offsets check; each
+  // group contracts its own share of the tokens
+  GemmShape g;
+  g.m = m;
+  g.n = n;
+  g.k = total_tokens;
+  g.lda = ldk;
+  g.ldb = ldk;
+  g.b_rows = n;
+  g.groups = groups;
+  g.d_offsets = d_offsets;
+  g.mode = mx::kModeGroupK;
+  return gemm_common(g, a, sa, fa, b, sb, fb, y, y_dtype, n, stream);
 }
 
 mx_status mx_device_status(cudaStream_t stream) {

@@ -215,8 +215,11 @@ __device__ __forceinline__ bool group_bar_any(int group, bool pred) {
 
 // One consumer group quantizes one tile held in ring slot `xs` (128 rows of
 // 256 bytes); with SR, `rs` holds the tile's 16-bit random integers in the
-// same layout.  `lt` is the thread's index inside the group.
-template <int FMT, bool ROW, bool COL, bool SR>
+// same layout.  `lt` is the thread's index inside the group.  Grouped
+// columnwise tiles may hold rows of the next group past rows_valid: those
+// rows count as zeros (the zero-padded final block of the group), and the
+// tile's full 128 transposed columns are written, padding included.
+template <int FMT, bool ROW, bool COL, bool GROUPED, bool SR>
 __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Tile& tl,
                                               const uint8_t* xs, const uint8_t* rs, uint8_t* s_q,
                                               uint8_t* s_unit_row, uint8_t* s_unit_col,
@@ -289,6 +292,9 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
       w[r] = xw[(rb * 32 + r) * 64 + cp];
+      if constexpr (GROUPED) {
+        if (rb * 32 + r >= tl.rows_valid) w[r] = 0u;
+      }
       if constexpr (SR) rw[r] = rw_src[(rb * 32 + r) * 64 + cp];
       a2 = max_u16x2(a2, w[r] & 0x7FFF7FFFu);
     }
@@ -359,20 +365,23 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
     }
   }
   if constexpr (COL) {
-    // Transposed codes: output row (c0 + c) holds x rows [x_row0, x_row0 + 128).
+    // Transposed codes: output row (c0 + c), columns [128 * scale_rt,
+    // 128 * scale_rt + 128) (dense: x rows [x_row0, x_row0 + 128); grouped:
+    // the tile's place in the group's padded segment).
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int idx = i * kGroupThreads + lt;
       const int c = idx >> 3;
       const int j = idx & 7;
-      if (tl.c0 + c < p.cols && j * 16 < tl.rows_valid) {
+      if (tl.c0 + c < p.cols && (GROUPED || j * 16 < tl.rows_valid)) {
         const uint4 q = *reinterpret_cast<const uint4*>(s_q + c * kColPitch + j * 16);
-        *reinterpret_cast<uint4*>(p.q_col + (tl.c0 + c) * p.rows + tl.x_row0 + j * 16) = q;
+        *reinterpret_cast<uint4*>(p.q_col + (tl.c0 + c) * p.ldq_col + tl.scale_rt * kTile +
+                                  j * 16) = q;
       }
     }
     if (lt < 32) {
-      const int64_t tiles_k = (p.rows + 127) / 128;
-      const int64_t unit = (tl.c0 / 128) * tiles_k + tl.x_row0 / 128;
+      const int64_t tiles_k = (p.ldq_col + 127) / 128;
+      const int64_t unit = (tl.c0 / 128) * tiles_k + tl.scale_rt;
       reinterpret_cast<uint4*>(p.s_col + unit * 512)[lt] =
           reinterpret_cast<const uint4*>(s_unit_col)[lt];
     }
@@ -433,10 +442,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (GROUPED) group_tile_prefix(p.offsets, p.groups, p.rows, gi->off, gi->tiles, &gi->valid);
   __syncthreads();
 
+
   const int64_t col_tiles = (p.cols + kTile - 1) / kTile;
   int64_t num_tiles;
   if constexpr (GROUPED) {
-    if (!gi->valid) {
+    // columnwise: the padded segments must also fit in the q_col matrix
+    const bool fits = !COL || (gi->valid && static_cast<int64_t>(gi->tiles[p.groups]) * kTile <=
+                                                 p.ldq_col);
+    if (!gi->valid || !fits) {
       if (blockIdx.x == 0 && tid == 0) record_device_status(p.status, MX_DEV_BAD_OFFSETS);
       num_tiles = 0;
     } else {
@@ -492,8 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // scale units zeroed; a wait that gave up anywhere stops the whole group
       if (group_bar_any(group, !got)) break;
       const uint8_t* slot = smem + QSmem::kOffRing + s * QSmem::kSlotBytes;
-      quantize_tile<FMT, ROW, COL, SR>(p, tl, slot, slot + kTileBytes, s_q, s_unit_row,
-                                       s_unit_col, &empty[s], group, lt);
+      quantize_tile<FMT, ROW, COL, GROUPED, SR>(p, tl, slot, slot + kTileBytes, s_q, s_unit_row,
+                                                s_unit_col, &empty[s], group, lt);
     }
   }
 }
@@ -553,8 +566,16 @@ cudaError_t launch_quantize_grouped(const QuantizeParams& p, const CUtensorMap& 
   if (p.cols == 0) return cudaSuccess;
   // upper bound of the padded row tiles; the kernel computes the exact count
   const int64_t tiles = ((p.rows + kTile - 1) / kTile + p.groups) * ((p.cols + kTile - 1) / kTile);
-  if (p.fmt == 0) return launch_one<0, true, false, true>(p, tmap_x, tmap_x, tiles, num_sms, stream);
-  return launch_one<1, true, false, true>(p, tmap_x, tmap_x, tiles, num_sms, stream);
+  const bool row = p.q_row != nullptr;
+  const bool col = p.q_col != nullptr;
+  if (p.fmt == 0) {
+    if (row && col) return launch_one<0, true, true, true>(p, tmap_x, tmap_x, tiles, num_sms, stream);
+    if (row) return launch_one<0, true, false, true>(p, tmap_x, tmap_x, tiles, num_sms, stream);
+    return launch_one<0, false, true, true>(p, tmap_x, tmap_x, tiles, num_sms, stream);
+  }
+  if (row && col) return launch_one<1, true, true, true>(p, tmap_x, tmap_x, tiles, num_sms, stream);
+  if (row) return launch_one<1, true, false, true>(p, tmap_x, tmap_x, tiles, num_sms, stream);
+  return launch_one<1, false, true, true>(p, tmap_x, tmap_x, tiles, num_sms, stream);
 }
 
 }  // namespace mx

@@ -128,6 +128,13 @@ def moe_inputs(total=65536, experts=64, k=7168, n=2048, seed: int = 0, device="c
     return x, w, moe_offsets(sizes)
 
 
+def moe_grad_output(total=65536, n=2048, seed: int = 0, device="cpu"):
+    """Output gradient of the routed tokens dY [total, n] (concatenated by
+    expert): the dense backward recipe, N(0, 1e-3) with 0.01% spikes
+    +-U(0.1, 1)."""
+    return synth_matrix((total, n), 1e-3, 0.0001, 0.1, 1.0, seed=seed * 100 + 9, device=device)
+
+
 @dataclass(frozen=True)
 class GemmShape:
     m: int

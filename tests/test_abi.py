@@ -100,6 +100,34 @@ def test_grouped_calls_reject_bad_arguments_on_the_host(mx):
     assert qg(FAKE, 0, 64, 64, 64, 0, 0, 4, None, FAKE, FAKE, 0) == 1                  # offsets
 
 
+def test_grouped_backward_calls_reject_bad_arguments_on_the_host(mx):
+    assert mx.mx_grouped_cols_capacity(65536, 64) == (512 + 64) * 128
+    assert mx.mx_grouped_cols_capacity(200, 7) == (1 + 7) * 128
+    assert mx.mx_grouped_cols_capacity(-1, 4) == 0
+    qx = mx.mx_quantize_grouped_ex
+    # (x, dtype, total, cols, ldx, fmt, axis, rule, groups, offsets, q_row, s_row, q_col, ldq, s_col, s)
+    assert qx(FAKE, 0, 64, 64, 64, 0, 2, 0, 4, FAKE, None, None, FAKE, 200, FAKE, 0) == 1   # ldq % 128
+    assert qx(FAKE, 0, 64, 64, 64, 0, 2, 0, 4, FAKE, None, None, FAKE, 0, FAKE, 0) == 1     # ldq == 0
+    assert qx(FAKE, 0, 64, 64, 64, 0, 2, 0, 4, FAKE, None, None, None, 256, FAKE, 0) == 1  # q_col
+    assert qx(FAKE, 0, 64, 64, 64, 0, 2, 0, 4, None, None, None, FAKE, 256, FAKE, 0) == 1  # offsets
+    assert qx(FAKE, 0, 64, 64, 64, 0, 2, 0, 0, FAKE, None, None, FAKE, 256, FAKE, 0) == 1  # groups
+    assert qx(FAKE, 0, 64, 40, 40, 0, 3, 0, 4, FAKE, FAKE, FAKE, FAKE, 256, FAKE, 0) == 1  # row cols % 32
+    assert qx(FAKE, 0, 64, 64, 64, 0, 2, 0, 4, FAKE, None, None, FAKE + 8, 256, FAKE, 0) == 2  # align
+    bc = mx.mx_grouped_gemm_bcat
+    # (groups, offsets, total_m, n, k, a, sa, fa, b, ldb, sb, fb, y, y_dtype, s)
+    assert bc(4, FAKE, 64, 128, 96, FAKE, FAKE, 0, FAKE, 384, FAKE, 0, FAKE, 0, 0) == 1     # k % 128
+    assert bc(4, FAKE, 64, 128, 128, FAKE, FAKE, 0, FAKE, 384, FAKE, 0, FAKE, 0, 0) == 1    # ldb < g*k
+    assert bc(4, None, 64, 128, 128, FAKE, FAKE, 0, FAKE, 512, FAKE, 0, FAKE, 0, 0) == 1    # offsets
+    assert bc(4, FAKE, 64, 128, 128, FAKE, FAKE, 0, FAKE, 520, FAKE, 0, FAKE, 0, 0) == 2    # ldb % 16
+    wg = mx.mx_grouped_gemm_wgrad
+    # (groups, offsets, total, m, n, ldk, a, sa, fa, b, sb, fb, y, y_dtype, s)
+    assert wg(4, FAKE, 100, 64, 64, 200, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 1, 0) == 1      # ldk % 128
+    assert wg(4, FAKE, -1, 64, 64, 256, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 1, 0) == 1       # total
+    assert wg(0, FAKE, 100, 64, 64, 256, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 1, 0) == 1      # groups
+    assert wg(4, FAKE, 100, 64, 60, 256, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 1, 0) == 1      # n % 8
+    assert wg(4, FAKE, 100, 64, 64, 256, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE + 4, 1, 0) == 2  # y align
+
+
 def test_fused_epilogue_rejects_bad_arguments_on_the_host(mx):
     f = mx.mx_gemm_bias_act
     assert f(64, 64, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, None, 7, FAKE, 0, 64, 0) == 1      # act
