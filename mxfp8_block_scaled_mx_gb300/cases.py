@@ -3,6 +3,8 @@
     python -m mxfp8_block_scaled_mx_gb300.cases gemm --m 4096 --n 18432 --k 7168 [--reps 3]
     python -m mxfp8_block_scaled_mx_gb300.cases quantize --rows 16384 --cols 8192 --axis row
     python -m mxfp8_block_scaled_mx_gb300.cases grouped --tokens 16384 --experts 16
+    python -m mxfp8_block_scaled_mx_gb300.cases moe_dgrad --tokens 16384 --experts 16
+    python -m mxfp8_block_scaled_mx_gb300.cases moe_wgrad --tokens 16384 --experts 16
 
 Inputs are the seeded synthetic workloads; each case launches the kernel
 `--reps` times after building its inputs and prints the mean event time.
@@ -33,7 +35,7 @@ def _time(fn, reps):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["gemm", "quantize", "grouped"])
+    ap.add_argument("case", choices=["gemm", "quantize", "grouped", "moe_dgrad", "moe_wgrad"])
     ap.add_argument("--m", type=int, default=4096)
     ap.add_argument("--n", type=int, default=18432)
     ap.add_argument("--k", type=int, default=7168)
@@ -61,6 +63,27 @@ def main(argv=None):
         bpe = 4.0625 if a.axis == "both" else 3.03125
         print(f"quantize {a.rows}x{a.cols} {a.axis}: {ms:.4f} ms, "
               f"{a.rows * a.cols * bpe / ms / 1e6:.1f} GB/s")
+    elif a.case in ("moe_dgrad", "moe_wgrad"):
+        # mixture-of-experts backward, FP32 out: dX_g = dY_g W_g^T or dW_g = dY_g^T X_g
+        x, w, offsets = W.moe_inputs(a.tokens, a.experts, a.k, 2048, device=dev)
+        e, n, k = w.shape
+        dy = W.moe_grad_output(a.tokens, n, device=dev)
+        d_off = torch.from_numpy(offsets).to(dev)
+        if a.case == "moe_dgrad":
+            qa = mx.quantize_grouped(dy, d_off, "e5m2")
+            qb = mx.quantize(w.view(e * n, k), "e4m3", "col")
+            y = torch.empty((a.tokens, k), dtype=torch.float32, device=dev)
+            fn = lambda: mx.grouped_gemm_bcat(qa, d_off, qb, "fp32", out=y)  # noqa: E731
+        else:
+            ldq = mx.mx_grouped_cols_capacity(a.tokens, e)
+            qa = mx.quantize_grouped(dy, d_off, "e5m2", axis="col", ldq=ldq)
+            qb = mx.quantize_grouped(x, d_off, "e4m3", axis="col", ldq=ldq)
+            y = torch.empty((e, n, k), dtype=torch.float32, device=dev)
+            fn = lambda: mx.grouped_gemm_wgrad(qa, d_off, qb, a.tokens, "fp32", out=y)  # noqa: E731
+        del x, w, dy
+        ms = _time(fn, a.reps)
+        print(f"{a.case} {a.tokens} tokens x {a.experts} experts ({n}x{k}): {ms:.4f} ms, "
+              f"{2 * a.tokens * n * k / ms / 1e9:.1f} TFLOP/s")
     else:
         x, w, offsets = W.moe_inputs(a.tokens, a.experts, a.k, 2048, device=dev)
         e, n, k = w.shape

@@ -192,10 +192,9 @@ mx_status gemm_common(const GemmShape& g, const uint8_t* a, const uint8_t* sa, m
     if (v >= 2 && v % 2 == 0) p.band_m = v;
   }
   const int block_n = block_n_choice(p);
-  // Dense GEMMs and the per-expert weight gradient pair blocks (B tile
-  // multicast); GEMMs grouped by rows measured slightly faster unpaired.
-  // MX_GEMM_CLUSTER_M overrides (1 or 2).
-  int cluster_m = g.mode == mx::kModeGroupM ? 1 : 2;
+  // Dense GEMMs pair blocks (B tile multicast); the grouped GEMMs measured
+  // faster unpaired.  MX_GEMM_CLUSTER_M overrides (1 or 2).
+  int cluster_m = g.mode == mx::kModeDense ? 2 : 1;
   if (const char* env = std::getenv("MX_GEMM_CLUSTER_M")) cluster_m = std::atoi(env) == 1 ? 1 : 2;
 
   CUtensorMap ta, tb;
