@@ -58,6 +58,8 @@ import numpy as np
 
 @dataclass(frozen=True)
 class Fp8Format:
+    """An OCP element format: sign, ebits exponent bits, mbits mantissa bits
+    (FP8, and the narrower MXFP6 / MXFP4 element formats)."""
     name: str
     ebits: int       # exponent field width
     mbits: int       # mantissa field width
@@ -65,6 +67,11 @@ class Fp8Format:
     emax_elem: int   # exponent of the largest binade (floor(log2(max)))
     max_finite: float
     has_inf: bool
+    has_nan: bool = True
+
+    @property
+    def bits(self) -> int:
+        return 1 + self.ebits + self.mbits
 
     @property
     def min_normal(self) -> float:
@@ -74,14 +81,26 @@ class Fp8Format:
     def subnormal_step(self) -> float:
         return 2.0 ** (1 - self.bias - self.mbits)
 
+    @property
+    def nan_code(self) -> int:
+        """Code written for every element of a NaN/Inf block: the FP8 NaN
+        0x7F; formats without NaN encodings write 0 (the block's NaN scale
+        alone marks it)."""
+        return NAN_CODE if self.has_nan else 0
+
 
 # OCP E4M3: bias 7, max 448 = 1.75 * 2^8, no Inf, NaN at S.1111.111.
 E4M3 = Fp8Format("e4m3", 4, 3, 7, 8, 448.0, False)
 # OCP E5M2: bias 15, max 57344 = 1.75 * 2^15, IEEE-like Inf / NaN.
 E5M2 = Fp8Format("e5m2", 5, 2, 15, 15, 57344.0, True)
-FORMATS = {"e4m3": E4M3, "e5m2": E5M2}
+# OCP MX element formats without Inf or NaN ("Format taxonomy": MXFP6 uses
+# E3M2, maximum 28, or E2M3, maximum 7.5; MXFP4 uses E2M1, maximum 6).
+E2M3 = Fp8Format("e2m3", 2, 3, 1, 2, 7.5, False, False)
+E3M2 = Fp8Format("e3m2", 3, 2, 3, 4, 28.0, False, False)
+E2M1 = Fp8Format("e2m1", 2, 1, 1, 2, 6.0, False, False)
+FORMATS = {"e4m3": E4M3, "e5m2": E5M2, "e2m3": E2M3, "e3m2": E3M2, "e2m1": E2M1}
 
-NAN_CODE = 0x7F          # canonical NaN code emitted for NaN/Inf blocks
+NAN_CODE = 0x7F          # canonical NaN code emitted for NaN/Inf blocks (FP8)
 E8M0_NAN = 0xFF
 
 
@@ -95,16 +114,19 @@ def fmt_of(f) -> Fp8Format:
 
 
 def decode_code(fmt, code: int) -> float:
-    """Value of one FP8 code byte (float64; exact, the grid is dyadic)."""
+    """Value of one code (float64; exact, the grid is dyadic).  The sign is
+    the top bit of the format's width."""
     f = fmt_of(fmt)
-    sign = -1.0 if code & 0x80 else 1.0
+    if not 0 <= code < (1 << f.bits):
+        raise ValueError("code out of range")
+    sign = -1.0 if code >> (f.bits - 1) else 1.0
     e = (code >> f.mbits) & ((1 << f.ebits) - 1)
     m = code & ((1 << f.mbits) - 1)
     e_all_ones = (1 << f.ebits) - 1
     if f.has_inf:
         if e == e_all_ones:
             return sign * math.inf if m == 0 else math.nan
-    elif e == e_all_ones and m == (1 << f.mbits) - 1:
+    elif f.has_nan and e == e_all_ones and m == (1 << f.mbits) - 1:
         return math.nan
     if e == 0:
         return sign * (m / (1 << f.mbits)) * 2.0 ** (1 - f.bias)
@@ -112,8 +134,9 @@ def decode_code(fmt, code: int) -> float:
 
 
 def decode_table(fmt) -> np.ndarray:
-    """float64[256]: value of every code byte."""
-    return np.array([decode_code(fmt, c) for c in range(256)], dtype=np.float64)
+    """float64[2^bits]: value of every code."""
+    f = fmt_of(fmt)
+    return np.array([decode_code(f, c) for c in range(1 << f.bits)], dtype=np.float64)
 
 
 def decode_e8m0(code: int) -> float:
@@ -193,7 +216,7 @@ def encode_sat_sr(fmt, v: np.ndarray, rand: np.ndarray) -> np.ndarray:
     r = round_to_grid_stochastic(f, finite_v, rand)
     r = np.where(np.abs(r) > f.max_finite, np.copysign(f.max_finite, r), r)
     codes = encode_grid_value(f, r)
-    codes[nan] = NAN_CODE
+    codes[nan] = f.nan_code
     return codes
 
 
@@ -214,16 +237,17 @@ def encode_grid_value(fmt, r: np.ndarray) -> np.ndarray:
     m_field = np.where(a == 0, 0.0, m_field)
     m_int = m_field.astype(np.int64)
     assert np.all(m_int == m_field), "value is not on the format grid"
-    code = (sign << 7) | (e_field << f.mbits) | m_int
+    code = (sign << (f.bits - 1)) | (e_field << f.mbits) | m_int
     return code.astype(np.uint8)
 
 
 def encode_sat_rne(fmt, v: np.ndarray) -> np.ndarray:
-    """Saturating RNE conversion of exact float64 values to FP8 codes.
+    """Saturating RNE conversion of exact float64 values to element codes.
 
     Round first; if the rounded magnitude exceeds the maximum finite value,
     give the maximum with the input's sign.  +-Inf saturates likewise, NaN
-    gives the NaN code 0x7F.  A negative value that rounds to zero gives -0.
+    gives the format's NaN code (0x7F for FP8, 0 for the formats without
+    NaN).  A negative value that rounds to zero gives -0.
     """
     f = fmt_of(fmt)
     v = np.asarray(v, dtype=np.float64)
@@ -233,7 +257,7 @@ def encode_sat_rne(fmt, v: np.ndarray) -> np.ndarray:
     r = round_to_grid_rne(f, finite_v)
     r = np.where(np.abs(r) > f.max_finite, np.copysign(f.max_finite, r), r)
     codes = encode_grid_value(f, r)
-    codes[nan] = NAN_CODE
+    codes[nan] = f.nan_code
     return codes
 
 
@@ -314,7 +338,7 @@ def quantize_rows(x: np.ndarray, fmt, rule: str = "floor", rand=None) -> MxBlock
     else:
         r = np.asarray(rand, dtype=np.int64).reshape(rows, k // BLOCK, BLOCK)
         codes = encode_sat_sr(f, finite_scaled, r)
-    codes = np.where(bad[:, :, None], np.uint8(NAN_CODE), codes)
+    codes = np.where(bad[:, :, None], np.uint8(f.nan_code), codes)
     scales = (e + 127).astype(np.uint8)
     scales[bad] = E8M0_NAN
     return MxBlocks(codes.reshape(rows, k).astype(np.uint8), scales, f)
@@ -417,6 +441,61 @@ def swizzle_scales_grouped(scales: np.ndarray, offsets) -> np.ndarray:
         base = starts[g] // TILE_ROWS * tiles_k * TILE_BYTES
         out[base:base + part.size] = part
     return out
+
+
+# --------------------------------------------------------------------------
+# Container layout of the 6- and 4-bit element codes (tensor-core operand
+# layout; not defined by the pages)
+# --------------------------------------------------------------------------
+
+CONTAINER_ELEMS = 16      # elements per 16-byte container along K
+
+
+def pack_container(codes: np.ndarray, fmt) -> np.ndarray:
+    """One code per element [rows, K] -> the byte layout the operand takes in
+    memory.  FP8 codes are their own bytes.  For 6- and 4-bit formats every
+    run of 16 elements along K occupies 16 bytes: the 16 codes packed
+    little-endian (element i at bits [i*w, i*w + w) of the run), followed by
+    zero bytes (8 for w = 4, 4 for w = 6).  Layout only: no arithmetic on
+    values.  parity unpinned on the CPU: pinned by the tensor core consuming
+    bytes written by this function."""
+    f = fmt_of(fmt)
+    codes = np.asarray(codes, dtype=np.uint8)
+    if f.bits == 8:
+        return codes.copy()
+    rows, k = codes.shape
+    if k % CONTAINER_ELEMS:
+        raise ValueError("K must be a multiple of 16")
+    runs = codes.reshape(rows, k // CONTAINER_ELEMS, CONTAINER_ELEMS).astype(np.uint32)
+    out = np.zeros((rows, k // CONTAINER_ELEMS, 16), dtype=np.uint32)
+    for i in range(CONTAINER_ELEMS):
+        off = i * f.bits
+        byte, shift = off // 8, off % 8
+        val = runs[:, :, i] << shift          # at most 13 bits
+        out[:, :, byte] |= val & 0xFF
+        if shift + f.bits > 8:
+            out[:, :, byte + 1] |= val >> 8
+    return out.astype(np.uint8).reshape(rows, k)
+
+
+def unpack_container(buf: np.ndarray, fmt) -> np.ndarray:
+    """Inverse of pack_container (padding bytes are ignored)."""
+    f = fmt_of(fmt)
+    buf = np.asarray(buf, dtype=np.uint8)
+    if f.bits == 8:
+        return buf.copy()
+    rows, k = buf.shape
+    b = buf.reshape(rows, k // CONTAINER_ELEMS, 16).astype(np.uint32)
+    out = np.zeros((rows, k // CONTAINER_ELEMS, CONTAINER_ELEMS), dtype=np.uint32)
+    mask = (1 << f.bits) - 1
+    for i in range(CONTAINER_ELEMS):
+        off = i * f.bits
+        byte, shift = off // 8, off % 8
+        val = b[:, :, byte] >> shift
+        if shift + f.bits > 8:
+            val |= b[:, :, byte + 1] << (8 - shift)
+        out[:, :, i] = val & mask
+    return out.astype(np.uint8).reshape(rows, k)
 
 
 # --------------------------------------------------------------------------

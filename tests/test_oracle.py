@@ -504,6 +504,118 @@ def test_pack_grouped_cols_layout():
         O.pack_grouped_cols(qs, MOE_TINY_OFFSETS, 512)
 
 
+# ---------------------------------------------------------------- MXFP6 / MXFP4 element formats
+
+NARROW = ["e2m3", "e3m2", "e2m1"]
+
+
+@pytest.mark.parametrize("fmt", NARROW)
+def test_narrow_formats_from_page(golden_dir, fmt):
+    """Maxima printed on the page pin each format's (ebits, mbits, bias);
+    the grid has no Inf or NaN, 2^(bits-1) - 1 positive values, and within
+    every binade 2^mbits equal steps that double at each binade boundary."""
+    g = load(golden_dir, "mx_narrow_formats.json")
+    f = O.fmt_of(fmt)
+    t = O.decode_table(f)
+    assert len(t) == 1 << f.bits and np.isfinite(t).all()
+    assert t.max() == g[fmt]["max"] == f.max_finite and t.min() == -g[fmt]["max"]
+    pos = np.unique(t[t > 0])
+    assert len(pos) == (1 << (f.bits - 1)) - 1
+    # below the smallest normal: the subnormals k * step, k = 1 .. 2^mbits - 1
+    sub = pos[pos < f.min_normal]
+    assert np.array_equal(sub, f.subnormal_step * np.arange(1, 1 << f.mbits))
+    # every normal binade [2^e, 2^(e+1)) up to the top one: 2^mbits values
+    # spaced 2^(e - mbits), the spacing doubling from binade to binade
+    e = 1 - f.bias
+    while 2.0 ** e <= f.max_finite:
+        inside = pos[(pos >= 2.0 ** e) & (pos < 2.0 ** (e + 1))]
+        assert np.array_equal(inside, 2.0 ** e + 2.0 ** (e - f.mbits) * np.arange(1 << f.mbits))
+        e += 1
+    assert e - 1 == f.emax_elem
+    assert O.BLOCK == g["block"]
+
+
+def test_e2m1_values():
+    """E2M1 (sign, 2 exponent bits with bias 1, 1 mantissa bit): the eight
+    magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6, and their negatives."""
+    t = O.decode_table("e2m1")
+    assert list(t[:8]) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert list(t[8:]) == [-v for v in t[:8]]
+    assert np.signbit(t[8]) and not np.signbit(t[0])
+
+
+def brute_force_encode(fmt, v):
+    """Nearest finite code by exhaustive search; ties to the even code (the
+    code whose last mantissa bit is 0); a negative value that rounds to zero
+    keeps its sign."""
+    f = O.fmt_of(fmt)
+    t = O.decode_table(f)
+    codes = np.arange(len(t))
+    out = np.empty(len(v), dtype=np.uint8)
+    for i, x in enumerate(v):
+        d = np.abs(t - x)
+        best = codes[d == d.min()]
+        best = [c for c in best if (t[c] != 0 or np.signbit(t[c]) == np.signbit(x))] or list(best)
+        if len(best) > 1:
+            even = [c for c in best if c % 2 == 0]
+            best = even or best
+        out[i] = best[0]
+    return out
+
+
+@pytest.mark.parametrize("fmt", NARROW)
+def test_narrow_encode_matches_brute_force(fmt):
+    f = O.fmt_of(fmt)
+    rng = np.random.default_rng(hash(fmt) % 1000)
+    t = O.decode_table(f)
+    mids = (np.sort(np.unique(t))[1:] + np.sort(np.unique(t))[:-1]) / 2   # every tie point
+    v = np.concatenate([rng.standard_normal(3000) * f.max_finite / 3,
+                        rng.standard_normal(500) * f.subnormal_step * 4,
+                        mids, t, [f.max_finite * 1.01, -f.max_finite * 9, 1e-30, -1e-30]])
+    got = O.encode_sat_rne(f, v)
+    want = brute_force_encode(f, v)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("fmt", NARROW)
+def test_narrow_block_scale_rules(fmt):
+    """Floor rule: the scaled amax lands in the top binade [2^emax,
+    2^(emax+1)); ceil rule: brute-force smallest e with amax <= max * 2^e."""
+    f = O.fmt_of(fmt)
+    rng = np.random.default_rng(7)
+    amax = np.exp(rng.uniform(-30, 30, 2000))
+    e = O.scale_exponent_floor(f, amax)
+    scaled = amax / 2.0 ** e
+    assert np.all((scaled >= 2.0 ** f.emax_elem) & (scaled < 2.0 ** (f.emax_elem + 1)))
+    c = O.scale_exponent_ceil(f, amax)
+    for a, ec in zip(amax[:300], c[:300]):
+        want = min(k for k in range(-140, 140) if a <= f.max_finite * 2.0 ** k)
+        assert ec == want
+
+
+def test_narrow_quantize_nan_block_writes_zero_codes():
+    x = np.ones((1, 64))
+    x[0, 5] = np.nan
+    q = O.quantize(x, "e2m1", "row")
+    assert q.scales[0, 0] == 0xFF and np.all(q.codes[0, :32] == 0)
+    assert q.scales[0, 1] == 127 - 2 and np.all(O.decode_table("e2m1")[q.codes[0, 32:]] == 4.0)
+
+
+@pytest.mark.parametrize("fmt", NARROW + ["e4m3"])
+def test_container_round_trip(fmt):
+    """Packing keeps 16 codes per 16 bytes (FP8: identity) and unpacks to
+    the same codes; the padding bytes are zero."""
+    f = O.fmt_of(fmt)
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 1 << f.bits, size=(5, 64)).astype(np.uint8)
+    buf = O.pack_container(codes, f)
+    assert buf.shape == codes.shape
+    assert np.array_equal(O.unpack_container(buf, f), codes)
+    if f.bits < 8:
+        used = 2 * f.bits
+        assert np.all(buf.reshape(5, 4, 16)[:, :, used:] == 0)
+
+
 # ---------------------------------------------------------------- swizzle
 
 @pytest.mark.parametrize("rows,kb", [(1, 1), (128, 4), (130, 5), (300, 17), (256, 224)])
