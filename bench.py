@@ -247,6 +247,20 @@ def measure_rows(mx, peaks, dev, stream):
                                                "frac_hbm": round(gbs / hbm, 3),
                                                "bytes_per_elem": bpe}
         if (r, c) == (16384, 8192):
+            # MXFP4 codes (E2M1, 16-element containers: one byte per element)
+            def q4():
+                st = mx.mx_quantize(x.data_ptr(), 0, r, c, c, 4, 1, 0, qr.data_ptr(),
+                                    sr.data_ptr(), None, None, h)
+                assert st == 0
+            ms = []
+            for _ in range(20):
+                flush_l2(scrub)
+                ms.append(time_kernel(q4, stream, 1, warmup=0 if ms else 3))
+            t = statistics.median(ms)
+            gbs = r * c * 3.03125 / (t * 1e-3) / 1e9
+            out[f"quantize_{r}x{c}_row_e2m1"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
+                                                 "frac_hbm": round(gbs / hbm, 3),
+                                                 "bytes_per_elem": 3.03125}
             # stochastic rounding (E5M2, the gradient format): the 16-bit
             # random draws are an input, +2 bytes per element
             rb = W.random_bits16((r, c), seed=11, device=dev)
@@ -279,7 +293,18 @@ def measure_rows(mx, peaks, dev, stream):
     out["forward_bias_silu_16384x18432x7168_bf16"] = {
         "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
         "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
-    del xq, wq, yf, bias
+    del xq, wq, bias
+    # MXFP4 (E2M1) weights and MXFP6 (E3M2) operands through the same MMA
+    for tag, fa, fb in (("mxfp4_weights_e4m3xe2m1", "e4m3", "e2m1"),
+                        ("mxfp6_e3m2xe3m2", "e3m2", "e3m2")):
+        xq = mx.quantize(x, fa, "row", stream=stream)
+        wq = mx.quantize(w, fb, "col", stream=stream)
+        t = time_kernel(lambda: mx.gemm(xq, wq, "bf16", out=yf, stream=stream), stream, 10)
+        out[f"forward_{tag}_16384x18432x7168_bf16"] = {
+            "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
+            "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
+        del xq, wq
+    del yf
     dy = W.dense_grad_output(device=dev)
     rq = mx.quantize(dy, "e5m2", "row", stream=stream)
     wq = mx.quantize(w, "e4m3", "row", stream=stream)

@@ -66,9 +66,16 @@ typedef enum {
   MX_ERR_DEVICE_ARG = 6     /* the device found invalid data (group offsets)  */
 } mx_status;
 
-/* Element formats (OCP OFP8).  E4M3: max 448, no Inf, NaN 0x7F/0xFF.
- * E5M2: max 57344, IEEE-like Inf and NaN. */
-typedef enum { MX_E4M3 = 0, MX_E5M2 = 1 } mx_fmt;
+/* Element formats, section "Format taxonomy: range, spacing, and
+ * bitfields".  FP8 (OCP OFP8): E4M3 max 448, no Inf, NaN 0x7F/0xFF; E5M2
+ * max 57344, IEEE-like Inf and NaN.  MXFP6: E2M3 (max 7.5) and E3M2 (max
+ * 28); MXFP4: E2M1 (max 6); these three have no Inf or NaN encodings.
+ * FP8 codes are one byte per element.  The 6- and 4-bit codes use the
+ * tensor-core container layout: every run of 16 elements along K occupies
+ * 16 bytes, the 16 codes packed little-endian (element i at bits
+ * [i*w, i*w + w) of the run, w = 6 or 4) followed by zero bytes -- so a
+ * code buffer has the same size and strides as an FP8 one. */
+typedef enum { MX_E4M3 = 0, MX_E5M2 = 1, MX_E2M3 = 2, MX_E3M2 = 3, MX_E2M1 = 4 } mx_fmt;
 
 /* Wide element types: quantizer input and GEMM output. */
 typedef enum { MX_BF16 = 0, MX_FP32 = 1 } mx_dtype;

@@ -26,7 +26,7 @@ MX_OK = 0
 STATUS_NAMES = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_MISALIGNED",
                 3: "MX_ERR_UNSUPPORTED", 4: "MX_ERR_CUDA", 5: "MX_ERR_TIMEOUT",
                 6: "MX_ERR_DEVICE_ARG"}
-FMT = {"e4m3": 0, "e5m2": 1}
+FMT = {"e4m3": 0, "e5m2": 1, "e2m3": 2, "e3m2": 3, "e2m1": 4}
 DTYPE = {"bf16": 0, "fp32": 1}
 AXIS = {"row": 1, "col": 2, "both": 3}
 RULE = {"floor": 0, "ceil": 1}

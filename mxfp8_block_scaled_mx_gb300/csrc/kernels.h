@@ -18,7 +18,7 @@ struct QuantizeParams {
   uint8_t* s_row;      // swizzled scales of the [rows, cols] operand
   uint8_t* q_col;      // [cols, rows] codes or nullptr
   uint8_t* s_col;      // swizzled scales of the [cols, rows] operand
-  int32_t fmt;         // 0 = E4M3, 1 = E5M2
+  int32_t fmt;         // element format: 0 E4M3, 1 E5M2, 2 E2M3, 3 E3M2, 4 E2M1
   int32_t rule;        // 0 = floor, 1 = ceil
   const int32_t* offsets;  // grouped only: device int32[groups + 1]
   int32_t groups;
@@ -60,7 +60,7 @@ struct GemmParams {
   void* y;
   int64_t ldy;         // elements
   int32_t y_fp32;      // 1: FP32 output, 0: BF16 output
-  int32_t fa;          // 0 = E4M3, 1 = E5M2
+  int32_t fa;          // tensor-core operand type code (E4M3 0, E5M2 1, E2M3 3, E3M2 4, E2M1 5)
   int32_t fb;
   const int32_t* offsets;  // grouped only: device int32[groups + 1]
   int32_t groups;          // 0 for the dense GEMM

@@ -63,6 +63,21 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool valid_fmt(mx_fmt f) { return f == MX_E4M3 || f == MX_E5M2; }
 
+// GEMM operand formats: FP8 and the MXFP6 / MXFP4 element formats.
+bool valid_gemm_fmt(mx_fmt f) { return f >= MX_E4M3 && f <= MX_E2M1; }
+
+// Operand type code of tcgen05.mma.kind::mxf8f6f4 (instruction descriptor
+// bits 7-9 / 10-12): E4M3 0, E5M2 1, E2M3 3, E3M2 4, E2M1 5.
+int32_t mma_type_code(mx_fmt f) {
+  switch (f) {
+    case MX_E5M2: return 1;
+    case MX_E2M3: return 3;
+    case MX_E3M2: return 4;
+    case MX_E2M1: return 5;
+    default: return 0;
+  }
+}
+
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // 2-D uint8 tensor map over a [rows, inner] row-major matrix with row stride
@@ -151,7 +166,7 @@ mx_status gemm_common(const GemmShape& g, const uint8_t* a, const uint8_t* sa, m
   if (m < 0 || n <= 0 || k < 0 || n % 8 != 0 || ldy < n) return MX_ERR_INVALID_ARG;
   // grouped along K, k is the token total that the offsets split
   if (g.mode != mx::kModeGroupK && (k < 32 || k % 32 != 0)) return MX_ERR_INVALID_ARG;
-  if (!valid_fmt(fa) || !valid_fmt(fb)) return MX_ERR_INVALID_ARG;
+  if (!valid_gemm_fmt(fa) || !valid_gemm_fmt(fb)) return MX_ERR_INVALID_ARG;
   if (y_dtype != MX_BF16 && y_dtype != MX_FP32) return MX_ERR_INVALID_ARG;
   if (m > INT32_MAX || g.b_rows > INT32_MAX || k > INT32_MAX || g.lda > INT32_MAX ||
       g.ldb > INT32_MAX)
@@ -177,8 +192,8 @@ mx_status gemm_common(const GemmShape& g, const uint8_t* a, const uint8_t* sa, m
   p.y = y;
   p.ldy = ldy;
   p.y_fp32 = y_dtype == MX_FP32 ? 1 : 0;
-  p.fa = fa;
-  p.fb = fb;
+  p.fa = mma_type_code(fa);
+  p.fb = mma_type_code(fb);
   p.offsets = g.d_offsets;
   p.groups = g.groups;
   p.mode = g.mode;
@@ -251,8 +266,9 @@ mx_status quantize_common(const void* x, mx_dtype x_dtype, int64_t rows, int64_t
                           mx_axis axis, mx_scale_rule rule, uint8_t* q_row, uint8_t* s_row,
                           uint8_t* q_col, uint8_t* s_col, cudaStream_t stream) {
   if (x_dtype != MX_BF16) return x_dtype == MX_FP32 ? MX_ERR_UNSUPPORTED : MX_ERR_INVALID_ARG;
-  if (!valid_fmt(fmt) || (rule != MX_SCALE_FLOOR && rule != MX_SCALE_CEIL))
+  if (!valid_gemm_fmt(fmt) || (rule != MX_SCALE_FLOOR && rule != MX_SCALE_CEIL))
     return MX_ERR_INVALID_ARG;
+  if (rbits && !valid_fmt(fmt)) return MX_ERR_UNSUPPORTED;  // stochastic rounding: FP8 codes
   if (axis != MX_ROWWISE && axis != MX_COLWISE && axis != MX_BOTH) return MX_ERR_INVALID_ARG;
   const bool row = axis & MX_ROWWISE;
   const bool col = axis & MX_COLWISE;
@@ -335,8 +351,9 @@ mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_
                                  uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, int64_t ldq_col,
                                  uint8_t* s_col, cudaStream_t stream) {
   if (x_dtype != MX_BF16) return x_dtype == MX_FP32 ? MX_ERR_UNSUPPORTED : MX_ERR_INVALID_ARG;
-  if (!valid_fmt(fmt) || (rule != MX_SCALE_FLOOR && rule != MX_SCALE_CEIL))
+  if (!valid_gemm_fmt(fmt) || (rule != MX_SCALE_FLOOR && rule != MX_SCALE_CEIL))
     return MX_ERR_INVALID_ARG;
+  if (!valid_fmt(fmt)) return MX_ERR_UNSUPPORTED;  // grouped: FP8 codes
   if (axis != MX_ROWWISE && axis != MX_COLWISE && axis != MX_BOTH) return MX_ERR_INVALID_ARG;
   const bool row = axis & MX_ROWWISE;
   const bool col = axis & MX_COLWISE;

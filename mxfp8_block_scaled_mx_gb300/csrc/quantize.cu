@@ -58,11 +58,28 @@ __device__ __forceinline__ uint32_t amax_bits8(const uint4 v) {
   return max(m & 0xFFFFu, m >> 16);
 }
 
+// Element formats (library enum order): 0 E4M3, 1 E5M2, 2 E2M3, 3 E3M2,
+// 4 E2M1.  kEmax = exponent of the largest binade; the largest finite value
+// has significand kMaxNum / kMaxDen (1.75 for E4M3, E5M2 and E3M2, 1.875 for
+// E2M3, 1.5 for E2M1); kBits = code width.
+template <int FMT>
+struct ElemFmt {
+  static constexpr int kEmax = FMT == 0 ? 8 : FMT == 1 ? 15 : FMT == 3 ? 4 : 2;
+  static constexpr uint32_t kMaxNum = FMT == 2 ? 15u : FMT == 4 ? 3u : 7u;
+  static constexpr uint32_t kMaxDen = FMT == 2 ? 8u : FMT == 4 ? 2u : 4u;
+  static constexpr int kBits = FMT <= 1 ? 8 : FMT == 4 ? 4 : 6;
+  // code written for every element of a NaN/Inf block (4 codes per word
+  // for FP8; the narrower formats have no NaN code and write 0)
+  static constexpr uint32_t kNanWord = FMT <= 1 ? 0x7F7F7F7Fu : 0u;
+};
+
 // Scale exponent e of a block with finite amax (bit pattern `a`):
 // floor rule e = floor(log2 amax) - emax_elem; the ceil rule adds one when
-// the significand of amax exceeds 1.75 (= max / 2^emax_elem for both E4M3
-// and E5M2).  amax = 0 gives e = 0 (S = 1).  Clamped to [-127, 127].
-__device__ __forceinline__ int scale_exponent(uint32_t a, int emax, int rule) {
+// the significand of amax exceeds that of the format's maximum.  amax = 0
+// gives e = 0 (S = 1).  Clamped to [-127, 127].
+template <int FMT>
+__device__ __forceinline__ int scale_exponent(uint32_t a, int rule) {
+  using F = ElemFmt<FMT>;
   if (a == 0) return 0;
   const uint32_t ef = a >> 7;
   const uint32_t mant = a & 0x7Fu;
@@ -70,13 +87,13 @@ __device__ __forceinline__ int scale_exponent(uint32_t a, int emax, int rule) {
   bool above;
   if (ef != 0) {
     fl = static_cast<int>(ef) - 127;
-    above = mant > 0x60u;
+    above = F::kMaxDen * (128u + mant) > F::kMaxNum * 128u;   // (1 + mant/128) > max significand
   } else {  // bf16 subnormal: value = mant * 2^-133
     const int p = 31 - __clz(mant);
     fl = p - 133;
-    above = 4u * mant > (7u << p);
+    above = F::kMaxDen * mant > (F::kMaxNum << p);
   }
-  int e = fl - emax + ((rule == 1 && above) ? 1 : 0);
+  int e = fl - F::kEmax + ((rule == 1 && above) ? 1 : 0);
   return min(max(e, -127), 127);
 }
 
@@ -85,17 +102,45 @@ __device__ __forceinline__ float pow2_neg(int e) {
   return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
 }
 
-// Two floats -> two FP8 codes, RNE with saturation to the finite range;
-// `lo` lands in the low byte.
+// Two floats -> two codes, RNE with saturation to the finite range; `lo`
+// lands in the low part.  FP8 and FP6: one code per byte (16 bits; a 6-bit
+// code in the low bits of its byte); FP4: one code per nibble (8 bits).
 template <int FMT>
 __device__ __forceinline__ uint32_t cvt_pair(float lo, float hi) {
-  uint16_t r;
-  if constexpr (FMT == 0) {
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  if constexpr (FMT == 4) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
   } else {
-    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    uint16_t r;
+    if constexpr (FMT == 0) {
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    } else if constexpr (FMT == 1) {
+      asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    } else if constexpr (FMT == 2) {
+      asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    } else {
+      asm("cvt.rn.satfinite.e3m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    }
+    return r;
   }
-  return r;
+}
+
+// Four 6-bit codes, one per byte of w, packed into 24 bits (code i at bits
+// [6i, 6i + 6)).
+__device__ __forceinline__ uint32_t pack4_fp6(uint32_t w) {
+  return (w & 0x3Fu) | ((w >> 8) & 0x3Fu) << 6 | ((w >> 16) & 0x3Fu) << 12 |
+         ((w >> 24) & 0x3Fu) << 18;
+}
+
+// Sixteen 6-bit codes (one per byte of w0..w3) -> one 16-byte container:
+// the 96 packed bits, then four zero bytes.
+__device__ __forceinline__ uint4 container16_fp6(uint32_t w0, uint32_t w1, uint32_t w2,
+                                                 uint32_t w3) {
+  const uint32_t g0 = pack4_fp6(w0), g1 = pack4_fp6(w1), g2 = pack4_fp6(w2), g3 = pack4_fp6(w3);
+  return make_uint4(g0 | g1 << 24, g1 >> 8 | g2 << 16, g2 >> 16 | g3 << 8, 0u);
 }
 
 // Two bf16 packed in a word -> two codes (16 bits), after an exact scaling.
@@ -106,11 +151,19 @@ __device__ __forceinline__ uint32_t encode_word(uint32_t w, float mul) {
   return cvt_pair<FMT>(lo, hi);
 }
 
+// Eight bf16 -> eight codes: FP8 and FP6 one per byte (x: codes 0-3,
+// y: codes 4-7); FP4 packed in x (code i in bits [4i, 4i + 4)), y = 0.
 template <int FMT>
 __device__ __forceinline__ uint2 encode8(const uint4 v, float mul) {
   uint2 r;
-  r.x = encode_word<FMT>(v.x, mul) | (encode_word<FMT>(v.y, mul) << 16);
-  r.y = encode_word<FMT>(v.z, mul) | (encode_word<FMT>(v.w, mul) << 16);
+  if constexpr (FMT == 4) {
+    r.x = encode_word<FMT>(v.x, mul) | (encode_word<FMT>(v.y, mul) << 8) |
+          (encode_word<FMT>(v.z, mul) << 16) | (encode_word<FMT>(v.w, mul) << 24);
+    r.y = 0u;
+  } else {
+    r.x = encode_word<FMT>(v.x, mul) | (encode_word<FMT>(v.y, mul) << 16);
+    r.y = encode_word<FMT>(v.z, mul) | (encode_word<FMT>(v.w, mul) << 16);
+  }
   return r;
 }
 
@@ -153,7 +206,6 @@ __device__ __forceinline__ uint2 encode8_sr(const uint4 v, const uint4 r, float 
   return q;
 }
 
-constexpr uint32_t kNanCode4 = 0x7F7F7F7Fu;  // four NaN codes
 constexpr uint8_t kNanScale = 0xFF;
 
 // Byte offset of (local row r, local block c) inside a 512-byte scale unit.
@@ -224,7 +276,8 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
                                               const uint8_t* xs, const uint8_t* rs, uint8_t* s_q,
                                               uint8_t* s_unit_row, uint8_t* s_unit_col,
                                               uint64_t* empty_bar, int group, int lt) {
-  constexpr int emax = FMT == 0 ? 8 : 15;
+  using F = ElemFmt<FMT>;
+  static_assert(!SR || F::kBits == 8, "stochastic rounding is built for FP8 codes");
   const uint32_t lane = lt & 31;
 
   // Thread lt holds the 8-column chunk lt % 16 of rows lt / 16 + 16 * it.
@@ -259,16 +312,33 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
       uint2 codes;
       uint8_t sbyte;
       if (a >= 0x7F80u) {  // NaN or Inf in the block
-        codes = make_uint2(kNanCode4, kNanCode4);
+        codes = make_uint2(F::kNanWord, F::kNanWord);
         sbyte = kNanScale;
       } else {
-        const int e = scale_exponent(a, emax, p.rule);
+        const int e = scale_exponent<FMT>(a, p.rule);
         if constexpr (SR) {
           codes = encode8_sr<FMT>(v[it], rv[it], pow2_neg(e));
         } else {
           codes = encode8<FMT>(v[it], pow2_neg(e));
         }
         sbyte = static_cast<uint8_t>(e + 127);
+      }
+      if constexpr (F::kBits == 6) {  // eight codes packed into 48 bits
+        const uint32_t lo = pack4_fp6(codes.x), hi = pack4_fp6(codes.y);
+        codes = make_uint2(lo | hi << 24, hi >> 8);
+      }
+      if constexpr (F::kBits < 8) {
+        // Lanes 2j and 2j + 1 hold the two halves of one 16-element run,
+        // whose 16-byte container is the packed run then zero bytes; each
+        // lane writes the 8 bytes at its own FP8 offset.
+        const uint32_t px = __shfl_xor_sync(0xffffffffu, codes.x, 1);
+        const bool first = (ch & 1) == 0;
+        if constexpr (F::kBits == 4) {
+          codes = first ? make_uint2(codes.x, px) : make_uint2(0u, 0u);
+        } else {
+          codes = first ? make_uint2(codes.x, codes.y | px << 16)
+                        : make_uint2(codes.x >> 16 | codes.y << 16, 0u);
+        }
       }
       if (ok) {
         *reinterpret_cast<uint2*>(qp + it * q_step) = codes;
@@ -304,8 +374,8 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
     const uint32_t a_hi = a2 >> 16;
     const bool nan_lo = a_lo >= 0x7F80u;
     const bool nan_hi = a_hi >= 0x7F80u;
-    const int e_lo = nan_lo ? 0 : scale_exponent(a_lo, emax, p.rule);
-    const int e_hi = nan_hi ? 0 : scale_exponent(a_hi, emax, p.rule);
+    const int e_lo = nan_lo ? 0 : scale_exponent<FMT>(a_lo, p.rule);
+    const int e_hi = nan_hi ? 0 : scale_exponent<FMT>(a_hi, p.rule);
     const float m_lo = pow2_neg(e_lo);
     const float m_hi = pow2_neg(e_hi);
     uint32_t q_lo[8], q_hi[8];
@@ -325,8 +395,23 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
                   (cvt_pair<FMT>(lo(w2, rw[4 * i + 2]), lo(w3, rw[4 * i + 3])) << 16);
         q_hi[i] = cvt_pair<FMT>(hi(w0, rw[4 * i]), hi(w1, rw[4 * i + 1])) |
                   (cvt_pair<FMT>(hi(w2, rw[4 * i + 2]), hi(w3, rw[4 * i + 3])) << 16);
-        if (nan_lo) q_lo[i] = kNanCode4;
-        if (nan_hi) q_hi[i] = kNanCode4;
+        if (nan_lo) q_lo[i] = F::kNanWord;
+        if (nan_hi) q_hi[i] = F::kNanWord;
+        continue;
+      }
+      if constexpr (FMT == 4) {  // four 4-bit codes in 16 bits
+        q_lo[i] = cvt_pair<FMT>(__fmul_rn(__uint_as_float(w0 << 16), m_lo),
+                                __fmul_rn(__uint_as_float(w1 << 16), m_lo)) |
+                  (cvt_pair<FMT>(__fmul_rn(__uint_as_float(w2 << 16), m_lo),
+                                 __fmul_rn(__uint_as_float(w3 << 16), m_lo))
+                   << 8);
+        q_hi[i] = cvt_pair<FMT>(__fmul_rn(__uint_as_float(w0 & 0xFFFF0000u), m_hi),
+                                __fmul_rn(__uint_as_float(w1 & 0xFFFF0000u), m_hi)) |
+                  (cvt_pair<FMT>(__fmul_rn(__uint_as_float(w2 & 0xFFFF0000u), m_hi),
+                                 __fmul_rn(__uint_as_float(w3 & 0xFFFF0000u), m_hi))
+                   << 8);
+        if (nan_lo) q_lo[i] = 0u;
+        if (nan_hi) q_hi[i] = 0u;
         continue;
       }
       q_lo[i] = cvt_pair<FMT>(__fmul_rn(__uint_as_float(w0 << 16), m_lo),
@@ -339,15 +424,29 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
                 (cvt_pair<FMT>(__fmul_rn(__uint_as_float(w2 & 0xFFFF0000u), m_hi),
                                __fmul_rn(__uint_as_float(w3 & 0xFFFF0000u), m_hi))
                  << 16);
-      if (nan_lo) q_lo[i] = kNanCode4;
-      if (nan_hi) q_hi[i] = kNanCode4;
+      if (nan_lo) q_lo[i] = F::kNanWord;
+      if (nan_hi) q_hi[i] = F::kNanWord;
     }
+    // The column's 32 codes (two 16-element runs) as 32 bytes: FP8 one
+    // code per byte; FP6 / FP4 one 16-byte container per run.
     uint4* d0 = reinterpret_cast<uint4*>(s_q + (2 * cp) * kColPitch + rb * 32);
     uint4* d1 = reinterpret_cast<uint4*>(s_q + (2 * cp + 1) * kColPitch + rb * 32);
-    d0[0] = make_uint4(q_lo[0], q_lo[1], q_lo[2], q_lo[3]);
-    d0[1] = make_uint4(q_lo[4], q_lo[5], q_lo[6], q_lo[7]);
-    d1[0] = make_uint4(q_hi[0], q_hi[1], q_hi[2], q_hi[3]);
-    d1[1] = make_uint4(q_hi[4], q_hi[5], q_hi[6], q_hi[7]);
+    if constexpr (F::kBits == 8) {
+      d0[0] = make_uint4(q_lo[0], q_lo[1], q_lo[2], q_lo[3]);
+      d0[1] = make_uint4(q_lo[4], q_lo[5], q_lo[6], q_lo[7]);
+      d1[0] = make_uint4(q_hi[0], q_hi[1], q_hi[2], q_hi[3]);
+      d1[1] = make_uint4(q_hi[4], q_hi[5], q_hi[6], q_hi[7]);
+    } else if constexpr (F::kBits == 6) {
+      d0[0] = container16_fp6(q_lo[0], q_lo[1], q_lo[2], q_lo[3]);
+      d0[1] = container16_fp6(q_lo[4], q_lo[5], q_lo[6], q_lo[7]);
+      d1[0] = container16_fp6(q_hi[0], q_hi[1], q_hi[2], q_hi[3]);
+      d1[1] = container16_fp6(q_hi[4], q_hi[5], q_hi[6], q_hi[7]);
+    } else {
+      d0[0] = make_uint4(q_lo[0] | q_lo[1] << 16, q_lo[2] | q_lo[3] << 16, 0u, 0u);
+      d0[1] = make_uint4(q_lo[4] | q_lo[5] << 16, q_lo[6] | q_lo[7] << 16, 0u, 0u);
+      d1[0] = make_uint4(q_hi[0] | q_hi[1] << 16, q_hi[2] | q_hi[3] << 16, 0u, 0u);
+      d1[1] = make_uint4(q_hi[4] | q_hi[5] << 16, q_hi[6] | q_hi[7] << 16, 0u, 0u);
+    }
     if (ok) {
       s_unit_col[unit_offset(2 * cp, rb)] = nan_lo ? kNanScale : static_cast<uint8_t>(e_lo + 127);
       s_unit_col[unit_offset(2 * cp + 1, rb)] =
@@ -534,36 +633,49 @@ cudaError_t launch_one(const QuantizeParams& p, const CUtensorMap& tmap, const C
 
 }  // namespace
 
+namespace {
+
+template <int FMT>
+cudaError_t launch_dense(const QuantizeParams& p, const CUtensorMap& tmap_x,
+                         const CUtensorMap* tmap_r, int64_t tiles, int num_sms,
+                         cudaStream_t stream) {
+  const bool row = p.q_row != nullptr;
+  const bool col = p.q_col != nullptr;
+  const CUtensorMap& tr = tmap_r ? *tmap_r : tmap_x;
+  if constexpr (FMT <= 1) {
+    if (tmap_r) {  // stochastic rounding (FP8 codes)
+      if (row && col) return launch_one<FMT, true, true, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
+      if (row) return launch_one<FMT, true, false, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
+      return launch_one<FMT, false, true, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
+    }
+  } else {
+    if (tmap_r) return cudaErrorNotSupported;
+  }
+  if (row && col) return launch_one<FMT, true, true, false>(p, tmap_x, tr, tiles, num_sms, stream);
+  if (row) return launch_one<FMT, true, false, false>(p, tmap_x, tr, tiles, num_sms, stream);
+  return launch_one<FMT, false, true, false>(p, tmap_x, tr, tiles, num_sms, stream);
+}
+
+}  // namespace
+
 cudaError_t launch_quantize(const QuantizeParams& p, const CUtensorMap& tmap_x,
                             const CUtensorMap* tmap_r, int num_sms, cudaStream_t stream) {
   if (p.rows == 0 || p.cols == 0) return cudaSuccess;
-  const bool row = p.q_row != nullptr;
-  const bool col = p.q_col != nullptr;
   const int64_t tiles = ((p.rows + kTile - 1) / kTile) * ((p.cols + kTile - 1) / kTile);
-  const CUtensorMap& tr = tmap_r ? *tmap_r : tmap_x;
-  if (tmap_r) {  // stochastic rounding
-    if (p.fmt == 0) {
-      if (row && col) return launch_one<0, true, true, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
-      if (row) return launch_one<0, true, false, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
-      return launch_one<0, false, true, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
-    }
-    if (row && col) return launch_one<1, true, true, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
-    if (row) return launch_one<1, true, false, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
-    return launch_one<1, false, true, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
+  switch (p.fmt) {
+    case 0: return launch_dense<0>(p, tmap_x, tmap_r, tiles, num_sms, stream);
+    case 1: return launch_dense<1>(p, tmap_x, tmap_r, tiles, num_sms, stream);
+    case 2: return launch_dense<2>(p, tmap_x, tmap_r, tiles, num_sms, stream);
+    case 3: return launch_dense<3>(p, tmap_x, tmap_r, tiles, num_sms, stream);
+    case 4: return launch_dense<4>(p, tmap_x, tmap_r, tiles, num_sms, stream);
+    default: return cudaErrorInvalidValue;
   }
-  if (p.fmt == 0) {
-    if (row && col) return launch_one<0, true, true, false>(p, tmap_x, tr, tiles, num_sms, stream);
-    if (row) return launch_one<0, true, false, false>(p, tmap_x, tr, tiles, num_sms, stream);
-    return launch_one<0, false, true, false>(p, tmap_x, tr, tiles, num_sms, stream);
-  }
-  if (row && col) return launch_one<1, true, true, false>(p, tmap_x, tr, tiles, num_sms, stream);
-  if (row) return launch_one<1, true, false, false>(p, tmap_x, tr, tiles, num_sms, stream);
-  return launch_one<1, false, true, false>(p, tmap_x, tr, tiles, num_sms, stream);
 }
 
 cudaError_t launch_quantize_grouped(const QuantizeParams& p, const CUtensorMap& tmap_x,
                                     int num_sms, cudaStream_t stream) {
   if (p.cols == 0) return cudaSuccess;
+  if (p.fmt > 1) return cudaErrorNotSupported;  // grouped: FP8 codes
   // upper bound of the padded row tiles; the kernel computes the exact count
   const int64_t tiles = ((p.rows + kTile - 1) / kTile + p.groups) * ((p.cols + kTile - 1) / kTile);
   const bool row = p.q_row != nullptr;

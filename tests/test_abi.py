@@ -79,7 +79,7 @@ def test_gemm_rejects_bad_arguments_on_the_host(mx):
     assert g(64, 64, 48, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # k % 32
     assert g(64, 64, 0, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1       # k == 0
     assert g(64, 60, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # n % 8
-    assert g(64, 64, 64, FAKE, FAKE, 2, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # fmt
+    assert g(64, 64, 64, FAKE, FAKE, 7, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # fmt
     assert g(64, 64, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 5, 64, s) == 1      # out dtype
     assert g(64, 64, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 32, s) == 1      # ldy < n
     assert g(64, 64, 64, None, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # null
@@ -141,6 +141,18 @@ def test_stochastic_quantize_rejects_bad_arguments_on_the_host(mx):
     assert q(FAKE, 0, 64, 64, 64, FAKE, 32, 0, 1, 0, FAKE, FAKE, None, None, 0) == 1     # ldr < cols
     assert q(FAKE, 0, 64, 64, 64, FAKE + 2, 64, 0, 1, 0, FAKE, FAKE, None, None, 0) == 2  # align
     assert q(FAKE, 0, 64, 64, 64, FAKE, 68, 0, 1, 0, FAKE, FAKE, None, None, 0) == 2     # ldr % 8
+
+
+def test_narrow_formats_on_the_host(mx):
+    """MXFP6 / MXFP4 codes: accepted by the quantizer and the GEMM; not by
+    stochastic rounding or the grouped quantizer (FP8 only)."""
+    sr = mx.mx_quantize_sr
+    for fmt in (2, 3, 4):
+        assert sr(FAKE, 0, 64, 64, 64, FAKE, 64, fmt, 1, 0, FAKE, FAKE, None, None, 0) == 3
+        assert mx.mx_quantize_grouped(FAKE, 0, 64, 64, 64, fmt, 0, 4, FAKE, FAKE, FAKE, 0) == 3
+    q = mx.mx_quantize
+    assert q(FAKE, 0, 64, 64, 64, 5, 1, 0, FAKE, FAKE, None, None, 0) == 1           # no format 5
+    assert q(FAKE, 0, 64, 40, 40, 4, 1, 0, FAKE, FAKE, None, None, 0) == 1           # cols % 32
 
 
 def test_selftest_rejects_zero_limit(mx):

@@ -1,0 +1,114 @@
+"""GPU parity of the MXFP6 (E2M3, E3M2) and MXFP4 (E2M1) operands: the
+quantizer writes the 16-element container layout byte for byte like the
+oracle, and the block-scaled GEMM on such operands (alone or mixed with
+FP8) matches the oracle's block sum."""
+import numpy as np
+import pytest
+import torch
+
+from mxcheck import assert_gemm_close, canonical_scales, ensure_built, to_f64
+from oracle import mx_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+NARROW = ["e2m3", "e3m2", "e2m1"]
+
+
+@pytest.fixture(scope="module")
+def mx():
+    ensure_built()
+    import mxfp8_block_scaled_mx_gb300 as mx
+    return mx
+
+
+def inputs(rows, cols, seed):
+    """bf16 N(0,1) with spikes, exact zeros, negative zeros and bf16
+    subnormals, so every branch of the encoders is exercised."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(rows, cols, generator=g)
+    idx = torch.randperm(rows * cols, generator=g)
+    n = rows * cols // 50
+    x.view(-1)[idx[:n]] *= 1000.0
+    x.view(-1)[idx[n:2 * n]] = 0.0
+    x.view(-1)[idx[2 * n:3 * n]] = -0.0
+    x.view(-1)[idx[3 * n:4 * n]] *= 1e-39
+    x[:, :32] *= 1e-3                      # a column band of small blocks
+    return x.to(torch.bfloat16)
+
+
+def check_codes(q, x, fmt, axis, rule="floor"):
+    ref = O.quantize(to_f64(x), fmt, axis, rule)
+    want = O.pack_container(ref.codes, fmt)
+    assert torch.equal(q.codes.cpu(), torch.from_numpy(want))
+    rows, k = ref.codes.shape
+    assert np.array_equal(canonical_scales(q.scales, rows, k), ref.scales)
+    return ref
+
+
+@pytest.mark.parametrize("fmt", NARROW)
+@pytest.mark.parametrize("shape", [(256, 512), (288, 352), (32, 96)])
+@pytest.mark.parametrize("rule", ["floor", "ceil"])
+def test_narrow_quantize_matches_oracle(mx, fmt, shape, rule):
+    x = inputs(*shape, seed=shape[0] + shape[1])
+    row, col = mx.quantize(x.cuda(), fmt, "both", rule=rule)
+    assert mx.device_status() == 0
+    check_codes(row, x, fmt, "row", rule)
+    check_codes(col, x, fmt, "col", rule)
+    only_row = mx.quantize(x.cuda(), fmt, "row", rule=rule)
+    only_col = mx.quantize(x.cuda(), fmt, "col", rule=rule)
+    assert torch.equal(only_row.codes, row.codes) and torch.equal(only_col.codes, col.codes)
+    assert torch.equal(only_row.scales, row.scales) and torch.equal(only_col.scales, col.scales)
+
+
+@pytest.mark.parametrize("fmt", NARROW)
+def test_narrow_nan_and_inf_blocks(mx, fmt):
+    x = inputs(64, 128, seed=4).float()
+    x[3, 40] = float("nan")
+    x[10, 70] = float("inf")
+    x[45, 100] = float("-inf")
+    x = x.to(torch.bfloat16)
+    row, col = mx.quantize(x.cuda(), fmt, "both")
+    assert mx.device_status() == 0
+    r = check_codes(row, x, fmt, "row")
+    c = check_codes(col, x, fmt, "col")
+    assert (r.scales == 0xFF).sum() == 3 and (c.scales == 0xFF).sum() == 3
+
+
+@pytest.mark.parametrize("fa,fb", [("e2m1", "e2m1"), ("e2m3", "e3m2"), ("e4m3", "e2m1"),
+                                   ("e3m2", "e5m2"), ("e2m1", "e4m3")])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_narrow_gemm_matches_oracle(mx, fa, fb, out):
+    """X [m, k] rowwise in fa, W [k, n] columnwise in fb, on the GPU; the
+    codes match the oracle and the GEMM matches the oracle's block sum."""
+    m, n, k = 200, 264, 544
+    x = inputs(m, k, seed=11)
+    g = torch.Generator().manual_seed(12)
+    w = (torch.randn(k, n, generator=g) * 0.05).to(torch.bfloat16)
+    qa = mx.quantize(x.cuda(), fa, "row")
+    qb = mx.quantize(w.cuda(), fb, "col")
+    y = mx.gemm(qa, qb, out)
+    assert mx.device_status() == 0
+    a = check_codes(qa, x, fa, "row")
+    b = check_codes(qb, w, fb, "col")
+    y_ref, t_ref = O.gemm(a, b)
+    assert_gemm_close(y, y_ref, t_ref, out)
+
+
+def test_mxfp4_weights_full_size_sampled(mx):
+    """Forward layer 16384 x 18432 x 7168 with E4M3 activations and MXFP4
+    (E2M1) weights, BF16 out; sampled rows and columns against the oracle."""
+    from mxfp8_block_scaled_mx_gb300 import workloads as W
+    x, w = W.dense_forward(device="cuda")
+    qa = mx.quantize(x, "e4m3", "row")
+    qb = mx.quantize(w, "e2m1", "col")
+    y = mx.gemm(qa, qb, "bf16")
+    assert mx.device_status() == 0
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([[0, 1, 16383], rng.choice(16384, 13, replace=False)]))
+    cols = np.unique(np.concatenate([[0, 18431], rng.choice(18432, 30, replace=False)]))
+    rows_t, cols_t = torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()
+    a = O.quantize(to_f64(x[rows_t]), "e4m3", "row")
+    b = O.quantize(to_f64(w[:, cols_t]), "e2m1", "col")
+    assert torch.equal(qb.codes[cols_t].cpu(), torch.from_numpy(O.pack_container(b.codes, "e2m1")))
+    y_ref, t_ref = O.gemm(a, b)
+    assert_gemm_close(y[rows_t][:, cols_t], y_ref, t_ref, "bf16")
