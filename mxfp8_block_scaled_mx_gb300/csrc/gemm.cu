@@ -274,8 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     num_units = ((p.m + BM * CM - 1) / (BM * CM)) * n_tiles;
   }
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // The whole warp runs the loop and waits; one elected lane issues the
+    // copies (warp-uniform operands, see elect_one).
     uint32_t stage = 0, phase = 0;
     int64_t issued = 0;  // stage fills issued so far
     bool ok = true;
@@ -294,26 +296,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t b_row = static_cast<int32_t>(ti.b_row0 + rank * (BN / CM));
       const int32_t kt_count = (ti.k_blocks + 3) / 4;
       for (int32_t kt = 0; kt < kt_count; ++kt) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) {
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[stage], tx);
-        ++issued;
-        const int32_t kx_a = static_cast<int32_t>(ti.a_kx0) + kt * BK;
-        const int32_t kx_b = static_cast<int32_t>(ti.b_kx0) + kt * BK;
-        tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full[stage], kx_a, a_row);
-        if constexpr (CM > 1) {
-          // this block's half of the shared B tile, delivered to both blocks
-          tma_load_2d_multicast(sB + stage * C::kBBytes + rank * (C::kBBytes / CM), &tmap_b,
-                                &full[stage], kx_b, b_row, kPairMask);
-        } else {
-          tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full[stage], kx_b, b_row);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&full[stage], tx);
+          const int32_t kx_a = static_cast<int32_t>(ti.a_kx0) + kt * BK;
+          const int32_t kx_b = static_cast<int32_t>(ti.b_kx0) + kt * BK;
+          tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full[stage], kx_a, a_row);
+          if constexpr (CM > 1) {
+            // this block's half of the shared B tile, delivered to both blocks
+            tma_load_2d_multicast(sB + stage * C::kBBytes + rank * (C::kBBytes / CM), &tmap_b,
+                                  &full[stage], kx_b, b_row, kPairMask);
+          } else {
+            tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full[stage], kx_b, b_row);
+          }
+          if (ti.sfa_unit >= 0) bulk_load(sSfa + stage * 512, sfa_src, 512, &full[stage]);
+          for (int j = 0; j < sfb_units; ++j)
+            bulk_load(sSfb + (stage * C::kSfbUnits + j) * 512, sfb_src + j * sfb_stride, 512,
+                      &full[stage]);
         }
-        if (ti.sfa_unit >= 0) bulk_load(sSfa + stage * 512, sfa_src, 512, &full[stage]);
-        for (int j = 0; j < sfb_units; ++j)
-          bulk_load(sSfb + (stage * C::kSfbUnits + j) * 512, sfb_src + j * sfb_stride, 512,
-                    &full[stage]);
+        __syncwarp();
+        ++issued;
         sfa_src += 512;
         sfb_src += 512;
         if (++stage == C::kStages) {
@@ -327,13 +332,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) {
       const int64_t fills = issued > s ? (issued - s + C::kStages - 1) / C::kStages : 0;
       if (fills)
-        mbar_wait(&full[s], static_cast<uint32_t>((fills - 1) & 1), s_abort, p.status,
-                  p.wait_limit_ns, true);
+        mbar_wait_warp(&full[s], static_cast<uint32_t>((fills - 1) & 1), s_abort, p.status,
+                       p.wait_limit_ns, true);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // This one thread paces the tensor core, so its loop does only 32-bit
-    // adds: descriptor halves and instruction descriptors are precomputed.
+    // The whole warp runs this loop and computes the operands; one elected
+    // lane (always the same one, so its commits track its own MMAs) issues
+    // the scale copies, the MMAs and the commits.  Descriptor halves and
+    // instruction descriptors are precomputed; the loop does 32-bit adds.
     constexpr uint32_t kHiOperand = smem_desc_hi(1024, 2);  // 8-row groups 1 KB apart, 128B swizzle
     constexpr uint32_t kHiScale = smem_desc_hi(128, 0);     // 32 rows x 16 B, no swizzle
     const uint32_t a_lo0 = smem_desc_lo(smem_u32(sA), 16);
@@ -356,57 +363,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int32_t kt_count = (k_blocks + 3) / 4;
       const int32_t kt_full = k_blocks / 4;  // k-tiles with all four scale blocks
-      if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) break;
+      if (!mbar_wait_warp(&acc_empty[acc], acc_phase ^ 1u, s_abort, p.status, p.wait_limit_ns))
+        break;
       tc_fence_after_sync();
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int32_t kt = 0; kt < kt_count; ++kt) {
-        if (!mbar_wait(&full[stage], phase, s_abort, p.status, p.wait_limit_ns)) {
+        if (!mbar_wait_warp(&full[stage], phase, s_abort, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t sf_tmem = tmem_base + C::kSfBaseCol + stage * C::kSfSlotCols;
-        tc_cp_32x128b_warpx4_lohi(sf_tmem, sfa_lo0 + stage * (512 >> 4), kHiScale);
-#pragma unroll
-        for (int j = 0; j < C::kSfbUnits; ++j)
-          tc_cp_32x128b_warpx4_lohi(sf_tmem + C::kSfaCols + 4 * j,
-                                    sfb_lo0 + (stage * C::kSfbUnits + j) * (512 >> 4), kHiScale);
         const uint32_t a_lo = a_lo0 + stage * (C::kABytes >> 4);
         const uint32_t b_lo = b_lo0 + stage * (C::kBBytes >> 4);
+        const uint32_t sfa_lo = sfa_lo0 + stage * (512 >> 4);
+        const uint32_t sfb_lo = sfb_lo0 + stage * C::kSfbUnits * (512 >> 4);
         const uint32_t sfb_tmem = sf_tmem + C::kSfaCols;
-        // +32 bytes along K inside the 128-byte swizzled row = +2 in the
-        // 16-byte address field; block kb's scales are byte kb of the
-        // scale columns (scale-factor ids in the instruction descriptor).
-        if (kt < kt_full) {
-          tc_mma_mxf8_lohi(d_tmem, a_lo, kHiOperand, b_lo, kHiOperand, idesc0, sf_tmem, sfb_tmem,
-                           kt > 0 ? 1u : 0u);
+        if (elect_one()) {
+          tc_cp_32x128b_warpx4_lohi(sf_tmem, sfa_lo, kHiScale);
 #pragma unroll
-          for (uint32_t kb = 1; kb < 4; ++kb)
-            tc_mma_mxf8_lohi(d_tmem, a_lo + 2u * kb, kHiOperand, b_lo + 2u * kb, kHiOperand,
-                             idesc0 | (kb << 4) | (kb << 29), sf_tmem, sfb_tmem, 1u);
-        } else {
-          const uint32_t kb_here = static_cast<uint32_t>(k_blocks - kt * 4);
-          for (uint32_t kb = 0; kb < kb_here; ++kb)
-            tc_mma_mxf8_lohi(d_tmem, a_lo + 2u * kb, kHiOperand, b_lo + 2u * kb, kHiOperand,
-                             idesc0 | (kb << 4) | (kb << 29), sf_tmem, sfb_tmem,
-                             (kt > 0 || kb > 0) ? 1u : 0u);
+          for (int j = 0; j < C::kSfbUnits; ++j)
+            tc_cp_32x128b_warpx4_lohi(sfb_tmem + 4 * j, sfb_lo + j * (512 >> 4), kHiScale);
+          // +32 bytes along K inside the 128-byte swizzled row = +2 in the
+          // 16-byte address field; block kb's scales are byte kb of the
+          // scale columns (scale-factor ids in the instruction descriptor).
+          if (kt < kt_full) {
+            tc_mma_mxf8_lohi(d_tmem, a_lo, kHiOperand, b_lo, kHiOperand, idesc0, sf_tmem,
+                             sfb_tmem, kt > 0 ? 1u : 0u);
+#pragma unroll
+            for (uint32_t kb = 1; kb < 4; ++kb)
+              tc_mma_mxf8_lohi(d_tmem, a_lo + 2u * kb, kHiOperand, b_lo + 2u * kb, kHiOperand,
+                               idesc0 | (kb << 4) | (kb << 29), sf_tmem, sfb_tmem, 1u);
+          } else {
+            const uint32_t kb_here = static_cast<uint32_t>(k_blocks - kt * 4);
+            for (uint32_t kb = 0; kb < kb_here; ++kb)
+              tc_mma_mxf8_lohi(d_tmem, a_lo + 2u * kb, kHiOperand, b_lo + 2u * kb, kHiOperand,
+                               idesc0 | (kb << 4) | (kb << 29), sf_tmem, sfb_tmem,
+                               (kt > 0 || kb > 0) ? 1u : 0u);
+          }
+          if constexpr (CM > 1) {
+            tc_commit_multicast(&empty[stage], kPairMask);
+          } else {
+            tc_commit(&empty[stage]);
+          }
         }
-        if constexpr (CM > 1) {
-          tc_commit_multicast(&empty[stage], kPairMask);
-        } else {
-          tc_commit(&empty[stage]);
-        }
+        __syncwarp();
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      if (kt_count > 0) {
-        tc_commit(&acc_full[acc]);
-      } else {
-        mbar_arrive(&acc_full[acc]);  // nothing to accumulate: the epilogue writes zeros
+      if (elect_one()) {
+        if (kt_count > 0) {
+          tc_commit(&acc_full[acc]);
+        } else {
+          mbar_arrive(&acc_full[acc]);  // nothing to accumulate: the epilogue writes zeros
+        }
       }
+      __syncwarp();
       if (++acc == C::kAccStages) {
         acc = 0;
         acc_phase ^= 1u;
@@ -414,8 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Every issued tensor-core operation must finish before tensor memory
     // is released.
-    tc_commit(mma_done);
-    mbar_wait(mma_done, 0, s_abort, p.status, p.wait_limit_ns, true);
+    if (elect_one()) {
+      tc_commit(mma_done);
+      mbar_wait(mma_done, 0, s_abort, p.status, p.wait_limit_ns, true);
+    }
+    __syncwarp();
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     // Eight warps: warp w reads lane quarter w % 4 (rows 32*(w%4) ..) and

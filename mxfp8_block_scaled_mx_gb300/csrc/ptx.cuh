@@ -85,6 +85,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// One lane of a fully active warp (the same lane every time).  Tensor-core
+// and TMA instructions are issued by this lane while the whole warp computes
+// their operands, so the operands are warp-uniform and no per-instruction
+// conversion into uniform registers is needed.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// mbar_wait by every lane of a warp; the verdict is made warp-uniform (a
+// lane that gave up makes the whole warp give up).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               volatile uint32_t* abort_flag, uint32_t* status,
+                                               uint64_t limit_ns, bool drain = false) {
+  const bool got = mbar_wait(bar, parity, abort_flag, status, limit_ns, drain);
+  return __all_sync(0xffffffffu, got);
+}
+
 // ---------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
