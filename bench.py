@@ -442,11 +442,11 @@ def run_reference(args):
 
 
 def gemm_traffic_record():
-    """DRAM bytes per launch of the forward GEMM from the committed ncu
-    summary, valid only while gemm.cu is unchanged (its sha256 recorded
-    beside the figure)."""
-    path = os.path.join(ROOT, "profiles", "mx_gemm_forward_16384x18432x7168_dram.md")
-    src = os.path.join(ROOT, "mxfp8_block_scaled_mx_gb300", "csrc", "gemm.cu")
+    """DRAM bytes per launch of the forward GEMM (the block-pair kernel) from
+    the committed ncu summary, valid only while gemm_pair.cu is unchanged
+    (its sha256 recorded beside the figure)."""
+    path = os.path.join(ROOT, "profiles", "mx_gemm_pair_forward_16384x18432x7168_dram.md")
+    src = os.path.join(ROOT, "mxfp8_block_scaled_mx_gb300", "csrc", "gemm_pair.cu")
     try:
         text = open(path).read()
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
@@ -457,7 +457,7 @@ def gemm_traffic_record():
         if ":" in line and line.strip().startswith("- "):
             key, val = line.strip()[2:].split(":", 1)
             rec[key.strip()] = val.strip().strip("`")
-    if rec.get("gemm.cu sha256") != sha:
+    if rec.get("gemm_pair.cu sha256") != sha:
         return None
     try:
         return float(rec["dram bytes per full-size launch"])
@@ -583,7 +583,7 @@ def run_gpu(args):
         "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp8_peak, 4), "traffic": traffic,
-                     "kernel": "mx_gemm_kernel (forward, BF16 out)",
+                     "kernel": "mx_gemm_pair_kernel (cta_group::2 block pairs, forward, BF16 out)",
                      "peak_source": f"{peak_src} bf16 burst {peaks['bf16_tflops']} TFLOP/s x "
                                     f"{NOMINAL_FP8_OVER_BF16} (nominal dense fp8/bf16 ratio)",
                      "frac_of_sustained": round(

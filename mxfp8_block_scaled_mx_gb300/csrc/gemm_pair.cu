@@ -152,8 +152,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const int32_t k_tiles = static_cast<int32_t>((p.k + kBK - 1) / kBK);
   const int32_t k_blocks = static_cast<int32_t>(p.k / 32);
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Whole warp; one elected lane issues (warp-uniform operands).
     const uint32_t full_leader0 = cluster_map(&full[0], 0);
     uint32_t stage = 0, phase = 0;
     int64_t issued = 0;
@@ -161,17 +162,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
     for (int64_t u = cluster_id; u < num_units && ok; u += num_clusters) {
       const PairTile t = pair_tile(p, u, n_tiles, rank);
       for (int32_t kt = 0; kt < k_tiles; ++kt) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) {
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
         }
-        if (leader) mbar_arrive_expect_tx(&full[stage], C::kPairTx);
-        const uint32_t bar = full_leader0 + stage * 8u;
-        const int32_t kx = kt * kBK;
-        tma_load_2d_pair(sA + stage * C::kABytes, &tmap_a, bar, kx, static_cast<int32_t>(t.m0));
-        tma_load_2d_pair(sB + stage * C::kBBytes, &tmap_b, bar, kx, t.b_row);
-        tma_load_3d_pair(sSfa + stage * C::kSfaBytes, &tmap_sa, bar, 0, kt, t.sfa_rt);
-        tma_load_3d_pair(sSfb + stage * C::kSfbBytes, &tmap_sb, bar, 0, kt, t.sfb_rt0);
+        if (elect_one()) {
+          if (leader) mbar_arrive_expect_tx(&full[stage], C::kPairTx);
+          const uint32_t bar = full_leader0 + stage * 8u;
+          const int32_t kx = kt * kBK;
+          tma_load_2d_pair(sA + stage * C::kABytes, &tmap_a, bar, kx, static_cast<int32_t>(t.m0));
+          tma_load_2d_pair(sB + stage * C::kBBytes, &tmap_b, bar, kx, t.b_row);
+          tma_load_3d_pair(sSfa + stage * C::kSfaBytes, &tmap_sa, bar, 0, kt, t.sfa_rt);
+          tma_load_3d_pair(sSfb + stage * C::kSfbBytes, &tmap_sb, bar, 0, kt, t.sfb_rt0);
+        }
+        __syncwarp();
         ++issued;
         if (++stage == kPStages) {
           stage = 0;
@@ -184,11 +188,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     for (int s = 0; s < kPStages; ++s) {
       const int64_t fills = issued > s ? (issued - s + kPStages - 1) / kPStages : 0;
       if (fills)
-        mbar_wait(&empty[s], static_cast<uint32_t>((fills - 1) & 1), s_abort, p.status,
-                  p.wait_limit_ns, true);
+        mbar_wait_warp(&empty[s], static_cast<uint32_t>((fills - 1) & 1), s_abort, p.status,
+                       p.wait_limit_ns, true);
     }
-  } else if (warp == 1 && lane == 0 && leader) {
+  } else if (warp == 1 && leader) {
     // ------------------------------------------------------------ MMA issuer (block 0)
+    // Whole warp computes the operands; one elected lane issues.
     constexpr uint32_t kHiOperand = smem_desc_hi(1024, 2);
     constexpr uint32_t kHiScale = smem_desc_hi(128, 0);
     const uint32_t a_lo0 = smem_desc_lo(smem_u32(sA), 16);
@@ -200,44 +205,52 @@ __global__ void __launch_bounds__(kPThreads, 1)
     uint32_t stage = 0, phase = 0, acc_phase = 0;
     bool ok = true;
     for (int64_t u = cluster_id; u < num_units && ok; u += num_clusters) {
-      if (!mbar_wait(acc_empty, acc_phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) break;
+      if (!mbar_wait_warp(acc_empty, acc_phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) break;
       tc_fence_after_sync();
       for (int32_t kt = 0; kt < k_tiles; ++kt) {
-        if (!mbar_wait(&full[stage], phase, s_abort, p.status, p.wait_limit_ns)) {
+        if (!mbar_wait_warp(&full[stage], phase, s_abort, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t sf_tmem = tmem_base + C::kSfBaseCol + stage * C::kSfSlotCols;
-        tc_cp_pair_32x128b_warpx4(sf_tmem, sfa_lo0 + stage * (C::kSfaBytes >> 4), kHiScale);
-        tc_cp_pair_32x128b_warpx4(sf_tmem + 4, sfb_lo0 + stage * (C::kSfbBytes >> 4), kHiScale);
-        tc_cp_pair_32x128b_warpx4(sf_tmem + 8, sfb_lo0 + stage * (C::kSfbBytes >> 4) + (512 >> 4),
-                                  kHiScale);
+        const uint32_t sfa_lo = sfa_lo0 + stage * (C::kSfaBytes >> 4);
+        const uint32_t sfb_lo = sfb_lo0 + stage * (C::kSfbBytes >> 4);
         const uint32_t a_lo = a_lo0 + stage * (C::kABytes >> 4);
         const uint32_t b_lo = b_lo0 + stage * (C::kBBytes >> 4);
         const uint32_t kb_here =
             kt < kt_full ? 4u : static_cast<uint32_t>(k_blocks - kt * 4);
+        if (elect_one()) {
+          tc_cp_pair_32x128b_warpx4(sf_tmem, sfa_lo, kHiScale);
+          tc_cp_pair_32x128b_warpx4(sf_tmem + 4, sfb_lo, kHiScale);
+          tc_cp_pair_32x128b_warpx4(sf_tmem + 8, sfb_lo + (512 >> 4), kHiScale);
 #pragma unroll
-        for (uint32_t kb = 0; kb < 4; ++kb) {
-          if (kb < kb_here)
-            tc_mma_pair_mxf8(tmem_base, a_lo + 2u * kb, kHiOperand, b_lo + 2u * kb, kHiOperand,
-                             idesc0 | (kb << 4) | (kb << 29), sf_tmem, sf_tmem + 4,
-                             (kt > 0 || kb > 0) ? 1u : 0u);
+          for (uint32_t kb = 0; kb < 4; ++kb) {
+            if (kb < kb_here)
+              tc_mma_pair_mxf8(tmem_base, a_lo + 2u * kb, kHiOperand, b_lo + 2u * kb, kHiOperand,
+                               idesc0 | (kb << 4) | (kb << 29), sf_tmem, sf_tmem + 4,
+                               (kt > 0 || kb > 0) ? 1u : 0u);
+          }
+          tc_commit_pair_multicast(&empty[stage], kBoth);
         }
-        tc_commit_pair_multicast(&empty[stage], kBoth);
+        __syncwarp();
         if (++stage == kPStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      tc_commit_pair_multicast(acc_full, kBoth);
+      if (elect_one()) tc_commit_pair_multicast(acc_full, kBoth);
+      __syncwarp();
       acc_phase ^= 1u;
     }
     // Every MMA (they also write block 1's tensor memory) completes before
     // either block releases tensor memory.
-    tc_commit_pair_multicast(mma_done, kLeaderOnly);
-    mbar_wait(mma_done, 0, s_abort, p.status, p.wait_limit_ns, true);
+    if (elect_one()) {
+      tc_commit_pair_multicast(mma_done, kLeaderOnly);
+      mbar_wait(mma_done, 0, s_abort, p.status, p.wait_limit_ns, true);
+    }
+    __syncwarp();
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue (both blocks)
     const uint32_t q = warp & 3u;

@@ -130,10 +130,13 @@ mx_status encode_scale_map(CUtensorMap* map, const void* base, int64_t rows, int
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
+// Dense GEMMs run on block pairs (cta_group::2, 256x256 pair tiles) unless
+// MX_GEMM_PAIR=0 selects the one-block kernel; grouped GEMMs use the
+// one-block kernel.
 bool use_pair_kernel(int32_t groups) {
   if (groups > 0) return false;
   const char* env = std::getenv("MX_GEMM_PAIR");
-  return env != nullptr && std::atoi(env) == 1;
+  return env == nullptr || std::atoi(env) != 0;
 }
 
 int block_n_choice(const mx::GemmParams& p) {

@@ -26,12 +26,14 @@ def mx():
 @pytest.fixture(params=[("128", "1"), ("256", "1"), ("128", "2"), ("256", "2"), ("256", "pair")],
                 ids=["bn128-c1", "bn256-c1", "bn128-c2", "bn256-c2", "pair"])
 def block_n(request, monkeypatch):
-    """Tile width along N and cluster size (1, or 2 = block pairs sharing B
-    by multicast), or the cta_group::2 block-pair kernel."""
+    """The cta_group::2 block-pair kernel (the dense default), or the
+    one-block kernel with its tile width along N and cluster size (1, or 2 =
+    blocks sharing B by multicast)."""
     monkeypatch.setenv("MX_GEMM_BLOCK_N", request.param[0])
     if request.param[1] == "pair":
         monkeypatch.setenv("MX_GEMM_PAIR", "1")
     else:
+        monkeypatch.setenv("MX_GEMM_PAIR", "0")
         monkeypatch.setenv("MX_GEMM_CLUSTER_M", request.param[1])
     return int(request.param[0])
 
