@@ -48,23 +48,17 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "status.cuh"
+#include "tiles.cuh"
 
 namespace mx {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BK = 128;            // K elements (bytes) per pipeline stage = 4 scale blocks
+constexpr int BM = kTileM;
+constexpr int BK = kTileK;
 constexpr int kEpiWarps = 8;       // two per tensor-memory lane quarter
 constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr int kEpiStageBytes = 2048;  // per epilogue warp: 32 rows x 64 bytes
 constexpr uint32_t kTmemCols = 512;
-
-struct GroupSmem {
-  int32_t off[kMaxGroups + 1];
-  int32_t tiles[kMaxGroups + 1];   // 128-row tiles before each group
-  int32_t units[kMaxGroups + 1];   // cluster units (CM tiles) before each group
-  int32_t valid;
-};
 
 template <int BN, bool GROUPED>
 struct Cfg {
@@ -91,99 +85,6 @@ struct Cfg {
       kOffGroup + (GROUPED ? int(sizeof(GroupSmem)) : 0) + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
-
-struct TileInfo {
-  int64_t m0;        // first row of the A tile
-  int64_t y_row0;    // output row of the tile's first row
-  int64_t m_end;     // output rows >= m_end are not stored
-  int64_t n0;        // first column of Y (first row of the group's B)
-  int64_t b_row0;    // first row of the B tile in the B tensor map
-  int64_t a_kx0;     // first K column of the A operand in its tensor map
-  int64_t b_kx0;     // first K column of the B operand
-  int64_t sfa_unit;  // first 512-byte scale unit of A (-1: this block's tile is padding)
-  int64_t sfb_unit;  // first scale unit of the B tile's first 128-row tile
-  int64_t sfb_step;  // scale units between consecutive 128-row tiles of B
-  int32_t k_blocks;  // 32-element K blocks of the tile's contraction
-};
-
-// Work unit u of a cluster = CM m-tiles x one n-tile; block `rank` of the
-// cluster takes m-tile CM*mu + rank.  Dense units follow a banded raster
-// (p.band_m m-tiles per band, n outer inside a band) so a band of A stays in
-// L2 while B streams once per band; units grouped by rows walk groups, then
-// m-units, then n; units grouped along K walk groups, then m-units, then n,
-// every group covering the whole [m, n] output of its own matrix.  Scale
-// units: 512 bytes per 128 rows x 128 K, ceil(ld / 128) per 128-row tile.
-template <int BN, int MODE, int CM>
-__device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t u, int64_t n_tiles,
-                                              uint32_t rank, const GroupSmem* gs) {
-  TileInfo ti;
-  const int64_t a_tiles_k = (p.lda + 127) / 128;
-  const int64_t b_tiles_k = (p.ldb + 127) / 128;
-  ti.a_kx0 = 0;
-  ti.b_kx0 = 0;
-  ti.sfb_step = b_tiles_k;
-  ti.k_blocks = static_cast<int32_t>(p.k / 32);
-  if constexpr (MODE == kModeGroupM) {
-    const int64_t mu = u / n_tiles;
-    const int64_t n_blk = u - mu * n_tiles;
-    const int g = find_group(gs->units, p.groups, static_cast<int32_t>(mu));
-    const int64_t lm = (mu - gs->units[g]) * CM + rank;  // m-tile inside the group
-    const int64_t g_tiles = gs->tiles[g + 1] - gs->tiles[g];
-    ti.m0 = static_cast<int64_t>(gs->off[g]) + lm * BM;
-    ti.y_row0 = ti.m0;
-    ti.m_end = lm < g_tiles ? static_cast<int64_t>(gs->off[g + 1]) : ti.m0;
-    ti.sfa_unit = lm < g_tiles ? (gs->tiles[g] + lm) * a_tiles_k : -1;
-    ti.n0 = n_blk * BN;
-    if (p.b_concat) {
-      // one [n, ldb] B; expert g's operand is columns [g*k, (g+1)*k)
-      ti.b_row0 = ti.n0;
-      ti.b_kx0 = static_cast<int64_t>(g) * p.k;
-      ti.sfb_unit = (ti.n0 / 128) * b_tiles_k + static_cast<int64_t>(g) * (p.k / 128);
-    } else {
-      // [groups, n, k] B, one swizzled scale matrix per expert
-      ti.b_row0 = static_cast<int64_t>(g) * p.n + ti.n0;
-      ti.sfb_unit = (ti.b_row0 / 128) * b_tiles_k;
-    }
-  } else if constexpr (MODE == kModeGroupK) {
-    const int64_t m_tiles = (p.m + BM - 1) / BM;
-    const int64_t per_group = ((m_tiles + CM - 1) / CM) * n_tiles;
-    const int g = static_cast<int>(u / per_group);
-    const int64_t w = u - g * per_group;
-    const int64_t mu = w / n_tiles;
-    const int64_t n_blk = w - mu * n_tiles;
-    const int64_t m_blk = mu * CM + rank;
-    const int64_t kt0 = gs->tiles[g];  // the group's first 128-column K tile
-    ti.m0 = m_blk * BM;
-    ti.y_row0 = static_cast<int64_t>(g) * p.m + ti.m0;
-    ti.m_end = static_cast<int64_t>(g) * p.m + p.m;  // a padding m-tile starts past it
-    ti.sfa_unit = m_blk < m_tiles ? m_blk * a_tiles_k + kt0 : -1;
-    ti.n0 = n_blk * BN;
-    ti.b_row0 = ti.n0;
-    ti.a_kx0 = kt0 * BK;
-    ti.b_kx0 = kt0 * BK;
-    ti.sfb_unit = (ti.n0 / 128) * b_tiles_k + kt0;
-    ti.k_blocks = (gs->off[g + 1] - gs->off[g] + 31) / 32;
-  } else {
-    const int64_t m_tiles = (p.m + BM - 1) / BM;
-    const int64_t m_units = (m_tiles + CM - 1) / CM;
-    const int64_t band_units = p.band_m / CM;
-    const int64_t band_size = band_units * n_tiles;
-    const int64_t band = u / band_size;
-    const int64_t within = u - band * band_size;
-    const int64_t in_band = ::min(band_units, m_units - band * band_units);
-    const int64_t n_blk = within / in_band;
-    const int64_t mu = band * band_units + (within - n_blk * in_band);
-    const int64_t m_blk = mu * CM + rank;
-    ti.m0 = m_blk * BM;
-    ti.y_row0 = ti.m0;
-    ti.m_end = p.m;
-    ti.sfa_unit = m_blk < m_tiles ? m_blk * a_tiles_k : -1;
-    ti.n0 = n_blk * BN;
-    ti.b_row0 = ti.n0;
-    ti.sfb_unit = (ti.n0 / 128) * b_tiles_k;
-  }
-  return ti;
-}
 
 template <int BN, int MODE, int CM, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)

@@ -6,44 +6,54 @@
 // of the two blocks of a cluster: M = 256 per instruction, block r holding
 // rows 128r..128r+127 of A and of the accumulator, and half of the B tile
 // (N rows 128r..128r+127) in its shared memory.  Per block and stage that is
-// 32 KB of operands instead of 48 KB, so six stages fit, and one thread in
-// block 0 issues the MMAs of both SMs.
+// 32 KB of operands instead of 48 KB, so six stages fit (five next to the
+// group table of the grouped modes), and one warp of block 0 issues the
+// MMAs of both SMs.
 //
 //   warp 0 (both blocks)  TMA producer: A, B half, A scales, B scales into
 //                         this block's ring; every copy completes on block
 //                         0's `full` barrier (cta_group::2 tensor copies).
 //   warp 1                both blocks allocate tensor memory together; in
-//                         block 0 one lane copies scales to tensor memory and
-//                         issues the pair MMAs, then multicasts the stage
-//                         release to both blocks' `empty` barriers.
+//                         block 0 the warp copies scales to tensor memory and
+//                         issues the pair MMAs (one elected lane), then
+//                         multicasts the stage release to both blocks'
+//                         `empty` barriers.
 //   warps 2..9 (both)     epilogue on the block's own 128 accumulator rows,
 //                         releasing the accumulator to block 0's barrier.
-// All waits are bounded; a final cluster barrier keeps either block alive
-// until its partner no longer touches its memory.
+// The work decomposition (tiles.cuh) is the one-block kernel's with two
+// blocks per cluster, in the same three modes: dense, grouped by rows of A
+// (mixture-of-experts forward and data gradient) and grouped along K (the
+// per-expert weight gradient).  All waits are bounded; a final cluster
+// barrier keeps either block alive until its partner no longer touches its
+// memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 #include "epilogue.cuh"
+#include "groups.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "status.cuh"
+#include "tiles.cuh"
 
 namespace mx {
 namespace {
 
 constexpr int kRowsPerBlock = 128;   // accumulator rows per block (256 per pair)
 constexpr int kPairN = 256;          // columns of a pair tile
-constexpr int kBK = 128;             // K per stage = four scale blocks
-constexpr int kPStages = 6;
+constexpr int kBK = kTileK;          // K per stage = four scale blocks
 constexpr int kPEpiWarps = 8;
 constexpr int kPThreads = 64 + kPEpiWarps * 32;
 constexpr uint32_t kPTmemCols = 512;
 constexpr uint16_t kBoth = 0x3;
 constexpr uint16_t kLeaderOnly = 0x1;
+static_assert(kRowsPerBlock == kTileM, "tile rows");
 
+template <bool GROUPED>
 struct PairCfg {
+  static constexpr int kStages = GROUPED ? 5 : 6;
   static constexpr int kABytes = kRowsPerBlock * kBK;    // 16 KB
   static constexpr int kBBytes = (kPairN / 2) * kBK;     // 16 KB, this block's half of B
   static constexpr int kSfaBytes = 512;                  // this block's 128 rows x 4 blocks
@@ -51,55 +61,30 @@ struct PairCfg {
   static constexpr uint32_t kPairTx = 2u * (kABytes + kBBytes + kSfaBytes + kSfbBytes);
   static constexpr int kSfSlotCols = 4 + 8;
   static constexpr int kSfBaseCol = kPairN;              // after the accumulator
-  static_assert(kSfBaseCol + kPStages * kSfSlotCols <= int(kPTmemCols), "tensor memory budget");
+  static_assert(kSfBaseCol + kStages * kSfSlotCols <= int(kPTmemCols), "tensor memory budget");
   static constexpr int kOffA = 0;
-  static constexpr int kOffB = kOffA + kPStages * kABytes;
-  static constexpr int kOffSfa = kOffB + kPStages * kBBytes;
-  static constexpr int kOffSfb = kOffSfa + kPStages * kSfaBytes;
-  static constexpr int kOffEpi = kOffSfb + kPStages * kSfbBytes;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffSfa = kOffB + kStages * kBBytes;
+  static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
+  static constexpr int kOffEpi = kOffSfb + kStages * kSfbBytes;
   static constexpr int kOffBar = kOffEpi + kPEpiWarps * 2048;
-  static constexpr int kNumBars = 2 * kPStages + 3;
+  static constexpr int kNumBars = 2 * kStages + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+  static constexpr int kOffGroup = kOffMisc + 64;
+  static constexpr int kSmemBytes =
+      kOffGroup + (GROUPED ? int(sizeof(GroupSmem)) : 0) + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
-struct PairTile {
-  int64_t m0;       // this block's first accumulator row
-  int64_t n0;       // first column of the pair tile
-  int32_t b_row;    // first row of this block's half of the B tile
-  int32_t sfa_rt;   // 128-row scale tile of this block's A rows
-  int32_t sfb_rt0;  // first of the two 128-row scale tiles of B
-};
-
-// Pair unit u: banded raster over 256-row m-units (band_m / 2 units per
-// band, n outer inside a band) so a band of A stays in L2 while B streams.
-__device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int64_t u, int64_t n_tiles,
-                                              uint32_t rank) {
-  const int64_t m_units = (p.m + 2 * kRowsPerBlock - 1) / (2 * kRowsPerBlock);
-  const int64_t band_units = p.band_m / 2 > 0 ? p.band_m / 2 : 1;
-  const int64_t band_size = band_units * n_tiles;
-  const int64_t band = u / band_size;
-  const int64_t within = u - band * band_size;
-  const int64_t in_band = ::min(band_units, m_units - band * band_units);
-  const int64_t n_blk = within / in_band;
-  const int64_t mu = band * band_units + (within - n_blk * in_band);
-  PairTile t;
-  t.m0 = mu * 2 * kRowsPerBlock + rank * kRowsPerBlock;
-  t.n0 = n_blk * kPairN;
-  t.b_row = static_cast<int32_t>(t.n0 + rank * (kPairN / 2));
-  t.sfa_rt = static_cast<int32_t>(mu * 2 + rank);
-  t.sfb_rt0 = static_cast<int32_t>(t.n0 / 128);
-  return t;
-}
-
-template <bool FUSED>
+template <int MODE, bool FUSED>
 __global__ void __launch_bounds__(kPThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_sa,
                         const __grid_constant__ CUtensorMap tmap_sb, const GemmParams p) {
-  using C = PairCfg;
+  constexpr bool GROUPED = MODE != kModeDense;
+  using C = PairCfg<GROUPED>;
+  constexpr int kPStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -115,6 +100,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint64_t* mma_done = acc_empty + 1;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
+  GroupSmem* gs = reinterpret_cast<GroupSmem*>(smem + C::kOffGroup);
 
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
@@ -123,45 +109,74 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const int64_t cluster_id = blockIdx.x / 2;
   const int64_t num_clusters = gridDim.x / 2;
 
-  if (warp == 0 && lane == 0) {
-    for (int s = 0; s < kPStages; ++s) {
-      mbar_init(&full[s], 1);   // block 0's: its producer's arrive + both blocks' bytes
-      mbar_init(&empty[s], 1);  // one multicast commit per use
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int s = 0; s < kPStages; ++s) {
+        mbar_init(&full[s], 1);   // block 0's: its producer's arrive + both blocks' bytes
+        mbar_init(&empty[s], 1);  // one multicast commit per use
+      }
+      mbar_init(acc_full, 1);
+      mbar_init(acc_empty, 2 * kPEpiWarps);  // one arrival per epilogue warp of the pair
+      mbar_init(mma_done, 1);
+      *s_abort = 0u;
+      fence_mbarrier_init();
+      tma_prefetch_desc(&tmap_a);
+      tma_prefetch_desc(&tmap_b);
+      tma_prefetch_desc(&tmap_sa);
+      tma_prefetch_desc(&tmap_sb);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 2 * kPEpiWarps);  // one arrival per epilogue warp of the pair
-    mbar_init(mma_done, 1);
-    *s_abort = 0u;
-    fence_mbarrier_init();
-    tma_prefetch_desc(&tmap_a);
-    tma_prefetch_desc(&tmap_b);
-    tma_prefetch_desc(&tmap_sa);
-    tma_prefetch_desc(&tmap_sb);
+    __syncwarp();
+    if constexpr (GROUPED) {
+      // grouped along K the offsets split the p.k tokens of the contraction
+      group_tile_prefix(p.offsets, p.groups, MODE == kModeGroupK ? p.k : p.m, gs->off, gs->tiles,
+                        &gs->valid, 2, gs->units);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(s_tmem, kPTmemCols);
     tmem_relinquish_pair();
   }
   tc_fence_before_sync();
-  cluster_sync();  // barriers of both blocks exist before any cross-block use
+  cluster_sync();  // barriers and group tables of both blocks exist before any cross-block use
   tc_fence_after_sync();
   const uint32_t tmem_base = *s_tmem;
 
   const int64_t n_tiles = (p.n + kPairN - 1) / kPairN;
-  const int64_t num_units = ((p.m + 2 * kRowsPerBlock - 1) / (2 * kRowsPerBlock)) * n_tiles;
-  const int32_t k_tiles = static_cast<int32_t>((p.k + kBK - 1) / kBK);
-  const int32_t k_blocks = static_cast<int32_t>(p.k / 32);
+  const int64_t m_units = (p.m + 2 * kRowsPerBlock - 1) / (2 * kRowsPerBlock);
+  int64_t num_units;
+  if constexpr (GROUPED) {
+    // grouped along K, the 128-padded token segments must fit in A and B
+    const bool fits = MODE != kModeGroupK ||
+                      (gs->valid && static_cast<int64_t>(gs->tiles[p.groups]) * kBK <= p.lda &&
+                       static_cast<int64_t>(gs->tiles[p.groups]) * kBK <= p.ldb);
+    if (!gs->valid || !fits) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) record_device_status(p.status, MX_DEV_BAD_OFFSETS);
+      num_units = 0;
+    } else if constexpr (MODE == kModeGroupK) {
+      num_units = static_cast<int64_t>(p.groups) * m_units * n_tiles;
+    } else {
+      num_units = static_cast<int64_t>(gs->units[p.groups]) * n_tiles;
+    }
+  } else {
+    num_units = m_units * n_tiles;
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Whole warp; one elected lane issues (warp-uniform operands).
+    // Whole warp; one elected lane issues (warp-uniform operands).  Every
+    // block always issues all four copies with full boxes (padding rows and
+    // out-of-range scale tiles are zero-filled or never stored), so block
+    // 0's expected byte count is the same for every stage.
     const uint32_t full_leader0 = cluster_map(&full[0], 0);
     uint32_t stage = 0, phase = 0;
     int64_t issued = 0;
     bool ok = true;
     for (int64_t u = cluster_id; u < num_units && ok; u += num_clusters) {
-      const PairTile t = pair_tile(p, u, n_tiles, rank);
-      for (int32_t kt = 0; kt < k_tiles; ++kt) {
+      const TileInfo ti = tile_info<kPairN, MODE, 2>(p, u, n_tiles, rank, gs);
+      const int32_t a_row = static_cast<int32_t>(ti.m0);
+      const int32_t b_row = static_cast<int32_t>(ti.b_row0 + rank * (kPairN / 2));
+      const int32_t kt_count = (ti.k_blocks + 3) / 4;
+      for (int32_t kt = 0; kt < kt_count; ++kt) {
         if (!mbar_wait_warp(&empty[stage], phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
@@ -169,11 +184,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (elect_one()) {
           if (leader) mbar_arrive_expect_tx(&full[stage], C::kPairTx);
           const uint32_t bar = full_leader0 + stage * 8u;
-          const int32_t kx = kt * kBK;
-          tma_load_2d_pair(sA + stage * C::kABytes, &tmap_a, bar, kx, static_cast<int32_t>(t.m0));
-          tma_load_2d_pair(sB + stage * C::kBBytes, &tmap_b, bar, kx, t.b_row);
-          tma_load_3d_pair(sSfa + stage * C::kSfaBytes, &tmap_sa, bar, 0, kt, t.sfa_rt);
-          tma_load_3d_pair(sSfb + stage * C::kSfbBytes, &tmap_sb, bar, 0, kt, t.sfb_rt0);
+          tma_load_2d_pair(sA + stage * C::kABytes, &tmap_a, bar,
+                           static_cast<int32_t>(ti.a_kx0) + kt * kBK, a_row);
+          tma_load_2d_pair(sB + stage * C::kBBytes, &tmap_b, bar,
+                           static_cast<int32_t>(ti.b_kx0) + kt * kBK, b_row);
+          tma_load_3d_pair(sSfa + stage * C::kSfaBytes, &tmap_sa, bar, 0, ti.sfa_kt0 + kt,
+                           ti.sfa_rt);
+          tma_load_3d_pair(sSfb + stage * C::kSfbBytes, &tmap_sb, bar, 0, ti.sfb_kt0 + kt,
+                           ti.sfb_rt);
         }
         __syncwarp();
         ++issued;
@@ -201,13 +219,23 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t sfa_lo0 = smem_desc_lo(smem_u32(sSfa), 0);
     const uint32_t sfb_lo0 = smem_desc_lo(smem_u32(sSfb), 0);
     const uint32_t idesc0 = mxf8_idesc(p.fa, p.fb, 2 * kRowsPerBlock, kPairN, 0, 0);
-    const int32_t kt_full = k_blocks / 4;
+    const uint32_t acc_full_peer = cluster_map(acc_full, 1);
+    // Grouped along K every group has its own contraction length; a group
+    // without tokens has none (its output tile is written as zeros).
+    const uint32_t group_units = static_cast<uint32_t>(m_units * n_tiles);
+    int32_t k_blocks = static_cast<int32_t>(p.k / 32);
     uint32_t stage = 0, phase = 0, acc_phase = 0;
     bool ok = true;
     for (int64_t u = cluster_id; u < num_units && ok; u += num_clusters) {
+      if constexpr (MODE == kModeGroupK) {
+        const int g = static_cast<int>(static_cast<uint32_t>(u) / group_units);
+        k_blocks = (gs->off[g + 1] - gs->off[g] + 31) / 32;
+      }
+      const int32_t kt_count = (k_blocks + 3) / 4;
+      const int32_t kt_full = k_blocks / 4;
       if (!mbar_wait_warp(acc_empty, acc_phase ^ 1u, s_abort, p.status, p.wait_limit_ns)) break;
       tc_fence_after_sync();
-      for (int32_t kt = 0; kt < k_tiles; ++kt) {
+      for (int32_t kt = 0; kt < kt_count; ++kt) {
         if (!mbar_wait_warp(&full[stage], phase, s_abort, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
@@ -240,7 +268,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
       }
       if (!ok) break;
-      if (elect_one()) tc_commit_pair_multicast(acc_full, kBoth);
+      if (elect_one()) {
+        if (kt_count > 0) {
+          tc_commit_pair_multicast(acc_full, kBoth);
+        } else {
+          // nothing to accumulate: both epilogues write zeros
+          mbar_arrive(acc_full);
+          mbar_arrive_cluster(acc_full_peer);
+        }
+      }
       __syncwarp();
       acc_phase ^= 1u;
     }
@@ -259,13 +295,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t acc_empty_leader = cluster_map(acc_empty, 0);
     uint32_t acc_phase = 0;
     for (int64_t u = cluster_id; u < num_units; u += num_clusters) {
-      const PairTile t = pair_tile(p, u, n_tiles, rank);
+      const TileInfo ti = tile_info<kPairN, MODE, 2>(p, u, n_tiles, rank, gs);
       const bool got = mbar_wait(acc_full, acc_phase, s_abort, p.status, p.wait_limit_ns);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + ((q * 32u) << 16) + half * (kPairN / 2);
-      epilogue_share<kPairN, FUSED>(p, t_row, t.m0 + q * 32, t.n0 + half * (kPairN / 2), p.m,
-                                    stage_buf, lane, false, [&] {
+      epilogue_share<kPairN, FUSED>(p, t_row, ti.y_row0 + q * 32, ti.n0 + half * (kPairN / 2),
+                                    ti.m_end, stage_buf, lane, ti.k_blocks == 0, [&] {
                                       tc_fence_before_sync();
                                       __syncwarp();
                                       if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
@@ -284,23 +320,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
 }
 
-template <bool FUSED>
+template <int MODE, bool FUSED>
 cudaError_t launch_pair_impl(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                              const CUtensorMap& tsa, const CUtensorMap& tsb, int num_sms,
                              cudaStream_t stream) {
-  auto kern = mx_gemm_pair_kernel<FUSED>;
+  using C = PairCfg<MODE != kModeDense>;
+  auto kern = mx_gemm_pair_kernel<MODE, FUSED>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               PairCfg::kSmemBytes);
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  const int64_t units =
-      ((p.m + 2 * kRowsPerBlock - 1) / (2 * kRowsPerBlock)) * ((p.n + kPairN - 1) / kPairN);
+  const int64_t n_tiles = (p.n + kPairN - 1) / kPairN;
+  const int64_t m_tiles = (p.m + kRowsPerBlock - 1) / kRowsPerBlock;
+  // upper bound of the pair units (grouped by rows: every group may add a
+  // partial unit; grouped along K: every group covers the whole output)
+  int64_t units = ((m_tiles + 1) / 2) * n_tiles;
+  if (MODE == kModeGroupM) units = ((m_tiles + p.groups + 1) / 2 + p.groups) * n_tiles;
+  if (MODE == kModeGroupK) units *= p.groups;
   if (units == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -309,7 +350,7 @@ cudaError_t launch_pair_impl(const GemmParams& p, const CUtensorMap& ta, const C
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kPThreads);
-  cfg.dynamicSmemBytes = PairCfg::kSmemBytes;
+  cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -328,10 +369,18 @@ cudaError_t launch_pair_impl(const GemmParams& p, const CUtensorMap& ta, const C
 cudaError_t launch_gemm_pair(const GemmParams& p, const CUtensorMap& tmap_a,
                              const CUtensorMap& tmap_b, const CUtensorMap& tmap_sa,
                              const CUtensorMap& tmap_sb, int num_sms, cudaStream_t stream) {
-  if (p.groups > 0) return cudaErrorNotSupported;
-  if (p.bias != nullptr || p.act != 0)
-    return launch_pair_impl<true>(p, tmap_a, tmap_b, tmap_sa, tmap_sb, num_sms, stream);
-  return launch_pair_impl<false>(p, tmap_a, tmap_b, tmap_sa, tmap_sb, num_sms, stream);
+  if (p.bias != nullptr || p.act != 0) {  // fused epilogue: dense GEMMs only
+    if (p.mode != kModeDense) return cudaErrorNotSupported;
+    return launch_pair_impl<kModeDense, true>(p, tmap_a, tmap_b, tmap_sa, tmap_sb, num_sms,
+                                              stream);
+  }
+  if (p.mode == kModeGroupM)
+    return launch_pair_impl<kModeGroupM, false>(p, tmap_a, tmap_b, tmap_sa, tmap_sb, num_sms,
+                                                stream);
+  if (p.mode == kModeGroupK)
+    return launch_pair_impl<kModeGroupK, false>(p, tmap_a, tmap_b, tmap_sa, tmap_sb, num_sms,
+                                                stream);
+  return launch_pair_impl<kModeDense, false>(p, tmap_a, tmap_b, tmap_sa, tmap_sb, num_sms, stream);
 }
 
 }  // namespace mx

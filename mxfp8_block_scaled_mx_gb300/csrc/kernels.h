@@ -80,7 +80,7 @@ int gemm_default_block_n(const GemmParams& p);
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                         int block_n, int cluster_m, int num_sms, cudaStream_t stream);
 
-// Block-pair GEMM (cta_group::2, 256 x 256 pair tiles; dense only).
+// Block-pair GEMM (cta_group::2, 256 x 256 pair tiles), all three modes.
 // tmap_a / tmap_b: codes, box 128 rows; tmap_sa / tmap_sb: the swizzled
 // scale buffers viewed as uint32 [row_tiles][k_tiles][128], boxes of one
 // (A) and two (B) 512-byte units.

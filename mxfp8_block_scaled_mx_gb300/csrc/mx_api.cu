@@ -130,13 +130,15 @@ mx_status encode_scale_map(CUtensorMap* map, const void* base, int64_t rows, int
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
-// Dense GEMMs run on block pairs (cta_group::2, 256x256 pair tiles) unless
-// MX_GEMM_PAIR=0 selects the one-block kernel; grouped GEMMs use the
-// one-block kernel.
-bool use_pair_kernel(int32_t groups) {
-  if (groups > 0) return false;
+// Dense GEMMs and GEMMs grouped by rows run on block pairs (cta_group::2,
+// 256x256 pair tiles); the weight gradient grouped along K, whose tiles are
+// short (a few K-tiles per expert) and whose FP32 stores are heavy, measured
+// faster on the one-block kernel with its quicker accumulator handoff.
+// MX_GEMM_PAIR=1 / 0 forces either kernel.
+bool use_pair_kernel(int32_t mode) {
   const char* env = std::getenv("MX_GEMM_PAIR");
-  return env == nullptr || std::atoi(env) != 0;
+  if (env != nullptr) return std::atoi(env) != 0;
+  return mode != mx::kModeGroupK;
 }
 
 int block_n_choice(const mx::GemmParams& p) {
@@ -217,15 +219,19 @@ mx_status gemm_common(const GemmShape& g, const uint8_t* a, const uint8_t* sa, m
 
   CUtensorMap ta, tb;
   if ((s = encode_codes_map(&ta, a, g.lda, m, g.lda, 128)) != MX_OK) return s;
-  if (g.mode == mx::kModeDense && use_pair_kernel(0)) {
-    // block pairs: each block loads 128 rows of the 256-row B tile
+  if (use_pair_kernel(g.mode)) {
+    // block pairs: each block loads 128 rows of the 256-row B tile; the
+    // scale buffers are viewed as grids of 512-byte units, A's with the
+    // per-group padded row bound when grouped by rows
     CUtensorMap tsa, tsb;
-    if ((s = encode_codes_map(&tb, b, k, g.b_rows, k, 128)) != MX_OK) return s;
-    if ((s = encode_scale_map(&tsa, sa, m, k, 1)) != MX_OK) return s;
-    if ((s = encode_scale_map(&tsb, sb, g.b_rows, k, 2)) != MX_OK) return s;
-    if (mx::launch_gemm_pair(p, ta, tb, tsa, tsb, st->num_sms, stream) != cudaSuccess)
-      return MX_ERR_CUDA;
-    return MX_OK;
+    const int64_t a_scale_rows =
+        g.mode == mx::kModeGroupM ? (ceil_div(m, 128) + g.groups) * 128 : m;
+    if ((s = encode_codes_map(&tb, b, g.ldb, g.b_rows, g.ldb, 128)) != MX_OK) return s;
+    if ((s = encode_scale_map(&tsa, sa, a_scale_rows, g.lda, 1)) != MX_OK) return s;
+    if ((s = encode_scale_map(&tsb, sb, g.b_rows, g.ldb, 2)) != MX_OK) return s;
+    const cudaError_t err = mx::launch_gemm_pair(p, ta, tb, tsa, tsb, st->num_sms, stream);
+    if (err == cudaErrorNotSupported) return MX_ERR_UNSUPPORTED;
+    return err == cudaSuccess ? MX_OK : MX_ERR_CUDA;
   }
   // With block pairs each block loads half of the B tile (multicast).
   const uint32_t b_box_rows = static_cast<uint32_t>(block_n / cluster_m);

@@ -17,12 +17,17 @@ def mx():
     return mx
 
 
-@pytest.fixture(params=[("128", "1"), ("256", "1"), ("128", "2"), ("256", "2")],
-                ids=["bn128-c1", "bn256-c1", "bn128-c2", "bn256-c2"])
+@pytest.fixture(params=[("256", "pair"), ("128", "1"), ("256", "1"), ("128", "2"), ("256", "2")],
+                ids=["pair", "bn128-c1", "bn256-c1", "bn128-c2", "bn256-c2"])
 def block_n(request, monkeypatch):
-    """Tile width along N and cluster size (1, or 2 = block pairs sharing B)."""
+    """The block-pair kernel (the default), or the one-block kernel with its
+    tile width along N and cluster size (1, or 2 = blocks sharing B)."""
     monkeypatch.setenv("MX_GEMM_BLOCK_N", request.param[0])
-    monkeypatch.setenv("MX_GEMM_CLUSTER_M", request.param[1])
+    if request.param[1] == "pair":
+        monkeypatch.setenv("MX_GEMM_PAIR", "1")
+    else:
+        monkeypatch.setenv("MX_GEMM_PAIR", "0")
+        monkeypatch.setenv("MX_GEMM_CLUSTER_M", request.param[1])
     return int(request.param[0])
 
 
