@@ -37,8 +37,6 @@ namespace {
 
 constexpr int kTile = 128;                    // rows and columns of x per tile
 constexpr int kGroupThreads = 256;            // one consumer group: 8 warps
-constexpr int kGroups = 2;                    // consumer groups (round-robin tiles)
-constexpr int kThreads = kGroups * kGroupThreads + 32;  // + one producer warp
 constexpr int kTileBytes = kTile * kTile * 2; // 32 KB
 constexpr int kColPitch = 144;                // bytes per transposed code row in smem
 
@@ -491,6 +489,10 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
 // buffer (columnwise modes only) and two scale units.
 template <bool COL, bool SR = false>
 struct QSmem {
+  // consumer groups (round-robin tiles): three for the rowwise-only ring
+  // of six slots, two otherwise
+  static constexpr int kGroups = (!COL && !SR) ? 3 : 2;
+  static constexpr int kThreads = kGroups * kGroupThreads + 32;  // + one producer warp
   // a slot holds the bf16 tile, plus its 16-bit random integers with SR
   static constexpr int kSlotBytes = SR ? 2 * kTileBytes : kTileBytes;
   static constexpr int kStages = SR ? 2 : (COL ? 4 : 6);   // tile slots in flight
@@ -511,7 +513,7 @@ struct QSmem {
 };
 
 template <int FMT, bool ROW, bool COL, bool GROUPED, bool SR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(QSmem<COL, SR>::kThreads, 1)
     quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     const __grid_constant__ CUtensorMap tmap_r, const QuantizeParams p) {
   using QSmem = mx::QSmem<COL, SR>;
@@ -526,6 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  constexpr int kGroups = QSmem::kGroups;
   constexpr int kProducerWarp = kGroups * kGroupThreads / 32;
 
   if (warp == kProducerWarp && lane == 0) {
@@ -627,7 +630,7 @@ cudaError_t launch_one(const QuantizeParams& p, const CUtensorMap& tmap, const C
   }
   const int64_t grid = tiles < num_sms ? tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
-  kern<<<static_cast<unsigned>(grid), kThreads, QSmem::kBytes, stream>>>(tmap, tmap_r, p);
+  kern<<<static_cast<unsigned>(grid), QSmem::kThreads, QSmem::kBytes, stream>>>(tmap, tmap_r, p);
   return cudaGetLastError();
 }
 
