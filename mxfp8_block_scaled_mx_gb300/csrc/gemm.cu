@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int s = 0; s < C::kAccStages; ++s) {
         mbar_init(&acc_full[s], 1);
-        mbar_init(&acc_empty[s], kEpiWarps * 32);
+        mbar_init(&acc_empty[s], kEpiWarps);  // one arrival per epilogue warp
       }
       mbar_init(mma_done, 1);
       *s_abort = 0u;
@@ -359,7 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       epilogue_share<BN, FUSED>(p, t_row, grow0, gcol0, ti.m_end, stage_buf, lane, ti.k_blocks == 0,
                                 [&] {
                                   tc_fence_before_sync();
-                                  mbar_arrive(&acc_empty[acc]);
+                                  __syncwarp();
+                                  if (lane == 0) mbar_arrive_relaxed(&acc_empty[acc]);
                                 });
       if (++acc == C::kAccStages) {
         acc = 0;

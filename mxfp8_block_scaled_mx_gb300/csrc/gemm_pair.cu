@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                     ti.m_end, stage_buf, lane, ti.k_blocks == 0, [&] {
                                       tc_fence_before_sync();
                                       __syncwarp();
-                                      if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+                                      if (lane == 0) mbar_arrive_relaxed_cluster(acc_empty_leader);
                                     });
       acc_phase ^= 1u;
     }

@@ -130,15 +130,11 @@ mx_status encode_scale_map(CUtensorMap* map, const void* base, int64_t rows, int
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
-// Dense GEMMs and GEMMs grouped by rows run on block pairs (cta_group::2,
-// 256x256 pair tiles); the weight gradient grouped along K, whose tiles are
-// short (a few K-tiles per expert) and whose FP32 stores are heavy, measured
-// faster on the one-block kernel with its quicker accumulator handoff.
-// MX_GEMM_PAIR=1 / 0 forces either kernel.
-bool use_pair_kernel(int32_t mode) {
+// GEMMs run on block pairs (cta_group::2, 256x256 pair tiles), in every
+// mode; MX_GEMM_PAIR=0 selects the one-block kernel.
+bool use_pair_kernel() {
   const char* env = std::getenv("MX_GEMM_PAIR");
-  if (env != nullptr) return std::atoi(env) != 0;
-  return mode != mx::kModeGroupK;
+  return env == nullptr || std::atoi(env) != 0;
 }
 
 int block_n_choice(const mx::GemmParams& p) {
@@ -219,7 +215,7 @@ mx_status gemm_common(const GemmShape& g, const uint8_t* a, const uint8_t* sa, m
 
   CUtensorMap ta, tb;
   if ((s = encode_codes_map(&ta, a, g.lda, m, g.lda, 128)) != MX_OK) return s;
-  if (use_pair_kernel(g.mode)) {
+  if (use_pair_kernel()) {
     // block pairs: each block loads 128 rows of the 256-row B tile; the
     // scale buffers are viewed as grids of 512-byte units, A's with the
     // per-group padded row bound when grouped by rows

@@ -322,6 +322,21 @@ __device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
   return r;
 }
 
+// Arrive without memory-ordering semantics: for releasing tensor memory
+// that this thread finished reading with tcgen05.ld + tcgen05.wait::ld and
+// a tcgen05.fence::before_thread_sync.  A release arrive would also wait
+// until this thread's earlier global stores are visible, which the
+// accumulator handoff does not need.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_relaxed_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
 // Arrive (count one) on an mbarrier given by its cluster address.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
