@@ -6,25 +6,29 @@
 //     Y[i,j] = sum_b S_A[i,b] S_B[j,b] sum_{k in b} A~[i,k] B~[j,k],
 // and block-scaled matrix instructions consume the scale operands directly.
 // Here that instruction is tcgen05.mma.kind::mxf8f6f4.block_scale: one MMA
-// covers K = 32 (one scale block), takes E4M3/E5M2 operands from shared
-// memory and E8M0 scales from tensor memory, and accumulates in FP32 in
-// tensor memory.
+// covers K = 32 (one scale block), takes E4M3/E5M2 (or E2M3/E3M2/E2M1)
+// operands from shared memory and E8M0 scales from tensor memory, and
+// accumulates in FP32 in tensor memory.  This is the one-block kernel; the
+// default for every mode is the block-pair kernel of gemm_pair.cu, which
+// shares the work decomposition (tiles.cuh) and the epilogue.
 //
 // Structure (one persistent block of 10 warps per SM):
 //   warp 0      TMA producer: A and B code tiles (128-byte swizzle) with
 //               cp.async.bulk.tensor, the 512-byte scale units with
 //               cp.async.bulk, into a ring of kStages shared-memory slots
 //               guarded by full/empty mbarriers.
-//   warp 1      allocates tensor memory; one lane issues tcgen05.cp
-//               (scales -> tensor memory) and tcgen05.mma, and releases each
-//               slot with tcgen05.commit.
+//   warp 1      allocates tensor memory; issues tcgen05.cp (scales ->
+//               tensor memory) and tcgen05.mma, and releases each slot with
+//               tcgen05.commit.
+//   Both run as warp-wide loops in which one elected lane issues the copies
+//   and tensor-core instructions, so their operands are warp-uniform.
 //   warps 2..9  epilogue: tcgen05.ld of the FP32 accumulator into registers
 //               (two warps per 32-lane quarter, half the columns each), early
-//               release of the accumulator, then (optionally) the FP32
-//               bias and SiLU of the kernel contract's epilogue, conversion
-//               to FP32/BF16 (RNE), staging through shared memory and
-//               coalesced 64-byte row segments, masked at the matrix (or
-//               group) edge.
+//               release of the accumulator (one relaxed arrive per warp),
+//               then (optionally) the FP32 bias and SiLU of the kernel
+//               contract's epilogue, conversion to FP32/BF16 (RNE), staging
+//               through shared memory and coalesced 64-byte row segments,
+//               masked at the matrix (or group) edge.
 // With 128-wide tiles the accumulator is double-buffered in tensor memory
 // so the epilogue of one tile overlaps the main loop of the next.
 //
@@ -34,7 +38,7 @@
 // only when both blocks' MMAs are done with it (the MMA commit arrives on
 // the empty barrier of both blocks).
 //
-// Grouped (mixture-of-experts) mode walks (group, m-tile, n-tile) triples;
+// Grouped (mixture-of-experts) modes walk (group, m-tile, n-tile) triples;
 // group offsets are read on the device and turned into a tile prefix by
 // every block, so the host never synchronizes.
 #include <cuda.h>
