@@ -20,6 +20,9 @@
 //                         `empty` barriers.
 //   warps 2..9 (both)     epilogue on the block's own 128 accumulator rows,
 //                         releasing the accumulator to block 0's barrier.
+//                         With the fused epilogue: warps 4..11, warps 2 and
+//                         3 idle (they complete the first warpgroup, whose
+//                         registers go to the epilogue warpgroups).
 // The work decomposition (tiles.cuh) is the one-block kernel's with two
 // blocks per cluster, in the same three modes: dense, grouped by rows of A
 // (mixture-of-experts forward and data gradient) and grouped along K (the
@@ -45,7 +48,28 @@ constexpr int kRowsPerBlock = 128;   // accumulator rows per block (256 per pair
 constexpr int kPairN = 256;          // columns of a pair tile
 constexpr int kBK = kTileK;          // K per stage = four scale blocks
 constexpr int kPEpiWarps = 8;
-constexpr int kPThreads = 64 + kPEpiWarps * 32;
+// Warp layout.  Plain epilogue: warp 0 producer, warp 1 MMA, warps 2-9
+// epilogue, ten warps.  Either way a block has three warps on some of the
+// SM's four sub-partition register files (16384 registers each), so a
+// thread gets at most 168 at launch, which the plain kernels need and the
+// fused epilogue (128 FP32 accumulator values plus bias and activation)
+// exceeds.  Fused epilogue: twelve warps; the first warpgroup (producer,
+// MMA, two idle warps) gives registers up and the two epilogue warpgroups
+// take them, within the block's launch allocation.  (The grouped modes
+// measured slower in the twelve-warp form, so it is kept to the fused,
+// dense kernel.)
+template <bool FUSED>
+struct PairWarps {
+  static constexpr int kFirstEpi = FUSED ? 4 : 2;
+  static constexpr int kThreads = (kFirstEpi + kPEpiWarps) * 32;
+};
+constexpr int kPLaunchRegs = 168;
+constexpr int kPLowRegs = 88;
+constexpr int kPHighRegs = 208;
+static_assert(kPLaunchRegs * 3 * 32 <= 16384, "launch registers per sub-partition");
+static_assert(4 * 32 * kPLowRegs + kPEpiWarps * 32 * kPHighRegs <=
+                  PairWarps<true>::kThreads * kPLaunchRegs,
+              "register reallocation within the launch allocation");
 constexpr uint32_t kPTmemCols = 512;
 constexpr uint16_t kBoth = 0x3;
 constexpr uint16_t kLeaderOnly = 0x1;
@@ -77,7 +101,7 @@ struct PairCfg {
 };
 
 template <int MODE, bool FUSED>
-__global__ void __launch_bounds__(kPThreads, 1)
+__global__ void __launch_bounds__(PairWarps<FUSED>::kThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_sa,
@@ -85,6 +109,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   constexpr bool GROUPED = MODE != kModeDense;
   using C = PairCfg<GROUPED>;
   constexpr int kPStages = C::kStages;
+  constexpr int kFirstEpi = PairWarps<FUSED>::kFirstEpi;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -161,6 +186,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
     num_units = m_units * n_tiles;
   }
 
+  // Each role's code sits under its own register reallocation, so the
+  // compiler allocates it within that role's share.
+  if constexpr (FUSED) {
+    if (warp < kFirstEpi) setmaxnreg_dec<kPLowRegs>();
+  }
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // Whole warp; one elected lane issues (warp-uniform operands).  Every
@@ -287,11 +317,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_wait(mma_done, 0, s_abort, p.status, p.wait_limit_ns, true);
     }
     __syncwarp();
-  } else if (warp >= 2) {
+  } else if (warp >= kFirstEpi) {
     // ------------------------------------------------------------ epilogue (both blocks)
+    if constexpr (FUSED) setmaxnreg_inc<kPHighRegs>();
     const uint32_t q = warp & 3u;
-    const uint32_t half = (warp - 2) >> 2;
-    uint8_t* stage_buf = sEpi + (warp - 2) * 2048;
+    const uint32_t half = (warp - kFirstEpi) >> 2;
+    uint8_t* stage_buf = sEpi + (warp - kFirstEpi) * 2048;
     const uint32_t acc_empty_leader = cluster_map(acc_empty, 0);
     uint32_t acc_phase = 0;
     for (int64_t u = cluster_id; u < num_units; u += num_clusters) {
@@ -331,6 +362,15 @@ cudaError_t launch_pair_impl(const GemmParams& p, const CUtensorMap& ta, const C
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    // The register increase in the kernel waits for registers the first
+    // warpgroup returns; it only completes if the block is launched with
+    // the allocation the shares were computed for.
+    if (FUSED) {
+      cudaFuncAttributes fa;
+      err = cudaFuncGetAttributes(&fa, kern);
+      if (err != cudaSuccess) return err;
+      if (fa.numRegs != kPLaunchRegs) return cudaErrorInvalidConfiguration;
+    }
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
@@ -349,7 +389,7 @@ cudaError_t launch_pair_impl(const GemmParams& p, const CUtensorMap& ta, const C
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kPThreads);
+  cfg.blockDim = dim3(PairWarps<FUSED>::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;

@@ -97,6 +97,22 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Register reallocation between the warpgroups of a block: every warp of a
+// warpgroup executes the same instruction.  A decrease returns registers to
+// the block's pool; an increase waits until the pool holds them, so the
+// warpgroups' new shares must sum to at most the block's launch allocation
+// (threads x registers per thread at launch).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  static_assert(N >= 24 && N <= 256 && N % 8 == 0, "register count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  static_assert(N >= 24 && N <= 256 && N % 8 == 0, "register count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // mbar_wait by every lane of a warp; the verdict is made warp-uniform (a
 // lane that gave up makes the whole warp give up).
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
