@@ -447,15 +447,28 @@ def run_reference(args):
     return 0
 
 
+PAIR_KERNEL_SOURCES = ("gemm_pair.cu", "epilogue.cuh", "tiles.cuh", "groups.cuh", "ptx.cuh",
+                       "kernels.h")
+
+
+def pair_kernel_sources_sha() -> str:
+    """sha256 over the block-pair GEMM's source files, in a fixed order."""
+    h = hashlib.sha256()
+    for name in PAIR_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "mxfp8_block_scaled_mx_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def gemm_traffic_record():
     """DRAM bytes per launch of the forward GEMM (the block-pair kernel) from
-    the committed ncu summary, valid only while gemm_pair.cu is unchanged
-    (its sha256 recorded beside the figure)."""
+    the committed ncu summary, valid only while the kernel's sources are
+    unchanged (the sha256 of their concatenation recorded beside the
+    figure)."""
     path = os.path.join(ROOT, "profiles", "mx_gemm_pair_forward_16384x18432x7168_dram.md")
-    src = os.path.join(ROOT, "mxfp8_block_scaled_mx_gb300", "csrc", "gemm_pair.cu")
     try:
         text = open(path).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        sha = pair_kernel_sources_sha()
     except OSError:
         return None
     rec = {}
@@ -463,7 +476,7 @@ def gemm_traffic_record():
         if ":" in line and line.strip().startswith("- "):
             key, val = line.strip()[2:].split(":", 1)
             rec[key.strip()] = val.strip().strip("`")
-    if rec.get("gemm_pair.cu sha256") != sha:
+    if rec.get("pair kernel sources sha256") != sha:
         return None
     try:
         return float(rec["dram bytes per full-size launch"])

@@ -1,6 +1,6 @@
 """Run one hot-path kernel on one shape a few times (for profilers).
 
-    python -m mxfp8_block_scaled_mx_gb300.cases gemm --m 4096 --n 18432 --k 7168 [--reps 3]
+    python -m mxfp8_block_scaled_mx_gb300.cases gemm --m 4096 --n 18432 --k 7168 [--reps 3] [--fused]
     python -m mxfp8_block_scaled_mx_gb300.cases quantize --rows 16384 --cols 8192 --axis row
     python -m mxfp8_block_scaled_mx_gb300.cases grouped --tokens 16384 --experts 16
     python -m mxfp8_block_scaled_mx_gb300.cases moe_dgrad --tokens 16384 --experts 16
@@ -46,6 +46,7 @@ def main(argv=None):
     ap.add_argument("--experts", type=int, default=16)
     ap.add_argument("--out", default="bf16", choices=["bf16", "fp32"])
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--fused", action="store_true", help="gemm: FP32 bias + SiLU epilogue")
     a = ap.parse_args(argv)
     dev = torch.device("cuda", 0)
     if a.case == "gemm":
@@ -55,8 +56,13 @@ def main(argv=None):
         del x, w
         y = torch.empty((a.m, a.n), dtype=torch.bfloat16 if a.out == "bf16" else torch.float32,
                         device=dev)
-        ms = _time(lambda: mx.gemm(qa, qb, a.out, out=y), a.reps)
-        print(f"gemm {a.m}x{a.n}x{a.k}: {ms:.4f} ms, {2 * a.m * a.n * a.k / ms / 1e9:.1f} TFLOP/s")
+        if a.fused:  # FP32 bias + SiLU epilogue
+            bias = torch.randn(a.n, generator=torch.Generator().manual_seed(3)).to(dev)
+            ms = _time(lambda: mx.gemm(qa, qb, a.out, out=y, bias=bias, act="silu"), a.reps)
+        else:
+            ms = _time(lambda: mx.gemm(qa, qb, a.out, out=y), a.reps)
+        print(f"gemm {a.m}x{a.n}x{a.k}{' bias+silu' if a.fused else ''}: {ms:.4f} ms, "
+              f"{2 * a.m * a.n * a.k / ms / 1e9:.1f} TFLOP/s")
     elif a.case == "quantize":
         x = W.quantize_sweep((a.rows, a.cols), seed=1, device=dev)
         ms = _time(lambda: mx.quantize(x, "e4m3", a.axis), a.reps)

@@ -53,11 +53,12 @@ __device__ __forceinline__ void epilogue_share(const GemmParams& p, uint32_t t_r
         float z = __fadd_rn(__uint_as_float(vals[c4 * 4 + e]), bb[e]);
         if (p.act == 1) {
           // FP32 outputs use the accurate exponential and division; BF16
-          // outputs (8 significant bits) the hardware approximations,
-          // whose ~1e-6 relative error is far below one BF16 ulp.
-          // exp overflow gives 1/inf = 0, so very negative z gives -0.
+          // outputs (8 significant bits) the fast exponential and the fast
+          // division (approximate reciprocal times z), whose ~1e-6
+          // relative error is far below one BF16 ulp.  exp overflow gives
+          // z / inf = -0 for very negative z (both forms).
           z = p.y_fp32 ? __fdiv_rn(z, __fadd_rn(1.0f, expf(-z)))
-                       : __fmul_rn(z, __frcp_rn(__fadd_rn(1.0f, __expf(-z))));
+                       : __fdividef(z, __fadd_rn(1.0f, __expf(-z)));
         }
         vals[c4 * 4 + e] = __float_as_uint(z);
       }
