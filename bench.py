@@ -210,6 +210,45 @@ def flush_l2(buf):
     buf.add_(1)
 
 
+def time_after_flush(fn, stream, scrub, reps: int = 20, read_pass=None):
+    """Median duration (ms) of fn() launched right behind an L2 flush on the
+    same stream: `scrub` (a buffer larger than L2) is written, then, with
+    `read_pass`, a second such buffer is read, so that the flush's dirty
+    lines go back to HBM before the timed launch instead of during it.
+    Flush and launch are enqueued back to back with no host synchronization
+    between them, so the host's launch latency is not timed."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    events = []
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            flush_l2(scrub)
+            if read_pass is not None:
+                read_pass.sum()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            events.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in events)
+
+
+def bandwidth_row(fn, stream, scrub, clean, nbytes: float, hbm: float, bpe: float) -> dict:
+    """A bandwidth row: timed after the write flush, and after the write
+    flush plus a read pass (clean L2)."""
+    t = time_after_flush(fn, stream, scrub)
+    tc = time_after_flush(fn, stream, scrub, read_pass=clean)
+    gbs = nbytes / (t * 1e-3) / 1e9
+    gbc = nbytes / (tc * 1e-3) / 1e9
+    return {"ms": round(t, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3),
+            "bytes_per_elem": bpe,
+            "clean_l2": {"ms": round(tc, 4), "GB/s": round(gbc, 1), "frac_hbm": round(gbc / hbm, 3)}}
+
+
 # ---------------------------------------------------------------- per-row measurements
 
 def measure_rows(mx, peaks, dev, stream):
@@ -221,6 +260,7 @@ def measure_rows(mx, peaks, dev, stream):
     hbm = peaks["hbm_gbs"]
     fp8_peak = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
     scrub = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    clean = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
     # quantize bandwidth sweep: 4096x4096 (fits in L2: flush between runs) and 16384x8192
     for (r, c), seed in (((4096, 4096), 0), ((16384, 8192), 1)):
@@ -237,30 +277,16 @@ def measure_rows(mx, peaks, dev, stream):
                                     qc.data_ptr() if axis & 2 else None,
                                     sc.data_ptr() if axis & 2 else None, h)
                 assert st == 0
-            ms = []
-            for _ in range(20):
-                flush_l2(scrub)
-                ms.append(time_kernel(q, stream, 1, warmup=0 if ms else 3))
-            t = statistics.median(ms)
-            gbs = r * c * bpe / (t * 1e-3) / 1e9
-            out[f"quantize_{r}x{c}_{mode}"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
-                                               "frac_hbm": round(gbs / hbm, 3),
-                                               "bytes_per_elem": bpe}
+            out[f"quantize_{r}x{c}_{mode}"] = bandwidth_row(q, stream, scrub, clean,
+                                                            r * c * bpe, hbm, bpe)
         if (r, c) == (16384, 8192):
             # MXFP4 codes (E2M1, 16-element containers: one byte per element)
             def q4():
                 st = mx.mx_quantize(x.data_ptr(), 0, r, c, c, 4, 1, 0, qr.data_ptr(),
                                     sr.data_ptr(), None, None, h)
                 assert st == 0
-            ms = []
-            for _ in range(20):
-                flush_l2(scrub)
-                ms.append(time_kernel(q4, stream, 1, warmup=0 if ms else 3))
-            t = statistics.median(ms)
-            gbs = r * c * 3.03125 / (t * 1e-3) / 1e9
-            out[f"quantize_{r}x{c}_row_e2m1"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
-                                                 "frac_hbm": round(gbs / hbm, 3),
-                                                 "bytes_per_elem": 3.03125}
+            out[f"quantize_{r}x{c}_row_e2m1"] = bandwidth_row(q4, stream, scrub, clean,
+                                                              r * c * 3.03125, hbm, 3.03125)
             # stochastic rounding (E5M2, the gradient format): the 16-bit
             # random draws are an input, +2 bytes per element
             rb = W.random_bits16((r, c), seed=11, device=dev)
@@ -269,15 +295,8 @@ def measure_rows(mx, peaks, dev, stream):
                 st = mx.mx_quantize_sr(x.data_ptr(), 0, r, c, c, rb.data_ptr(), c, 1, 1, 0,
                                        qr.data_ptr(), sr.data_ptr(), None, None, h)
                 assert st == 0
-            ms = []
-            for _ in range(20):
-                flush_l2(scrub)
-                ms.append(time_kernel(qsr, stream, 1, warmup=0 if ms else 3))
-            t = statistics.median(ms)
-            gbs = r * c * 5.03125 / (t * 1e-3) / 1e9
-            out[f"quantize_{r}x{c}_row_sr_e5m2"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
-                                                   "frac_hbm": round(gbs / hbm, 3),
-                                                   "bytes_per_elem": 5.03125}
+            out[f"quantize_{r}x{c}_row_sr_e5m2"] = bandwidth_row(qsr, stream, scrub, clean,
+                                                                 r * c * 5.03125, hbm, 5.03125)
             del rb
         del x, qr, sr, qc, sc
 
