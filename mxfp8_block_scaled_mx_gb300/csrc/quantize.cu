@@ -141,12 +141,25 @@ __device__ __forceinline__ uint4 container16_fp6(uint32_t w0, uint32_t w1, uint3
   return make_uint4(g0 | g1 << 24, g1 >> 8 | g2 << 16, g2 >> 16 | g3 << 8, 0u);
 }
 
+// The two bf16 of a word (low half first) as FP32, each times its own
+// power-of-two factor, in one packed FP32x2 multiply.  The products are
+// exact (an 8-bit significand times a power of two, far from the FP32
+// range limits), so they equal the scalar products bit for bit.
+__device__ __forceinline__ float2 scale_pair(uint32_t w, float m_lo, float m_hi) {
+  uint64_t x, m, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(w << 16), "r"(w & 0xFFFF0000u));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(m) : "f"(m_lo), "f"(m_hi));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(m));
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+
 // Two bf16 packed in a word -> two codes (16 bits), after an exact scaling.
 template <int FMT>
 __device__ __forceinline__ uint32_t encode_word(uint32_t w, float mul) {
-  const float lo = __fmul_rn(__uint_as_float(w << 16), mul);
-  const float hi = __fmul_rn(__uint_as_float(w & 0xFFFF0000u), mul);
-  return cvt_pair<FMT>(lo, hi);
+  const float2 v = scale_pair(w, mul, mul);
+  return cvt_pair<FMT>(v.x, v.y);
 }
 
 // Eight bf16 -> eight codes: FP8 and FP6 one per byte (x: codes 0-3,
@@ -191,6 +204,7 @@ __device__ __forceinline__ float sr_to_grid(float v, uint32_t r16) {
 // Two bf16 of a word with their two 16-bit random integers -> two codes.
 template <int FMT>
 __device__ __forceinline__ uint32_t encode_word_sr(uint32_t w, uint32_t r, float mul) {
+  // scalar multiplies: the packed form measured slower here
   const float lo = __fmul_rn(__uint_as_float(w << 16), mul);
   const float hi = __fmul_rn(__uint_as_float(w & 0xFFFF0000u), mul);
   return cvt_pair<FMT>(sr_to_grid<FMT>(lo, r & 0xFFFFu), sr_to_grid<FMT>(hi, r >> 16));
@@ -379,49 +393,35 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
     uint32_t q_lo[8], q_hi[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint32_t w0 = w[4 * i], w1 = w[4 * i + 1], w2 = w[4 * i + 2], w3 = w[4 * i + 3];
+      // rows 4i..4i+3: .x = column 2cp (scale m_lo), .y = column 2cp + 1 (m_hi)
+      const float2 s0 = scale_pair(w[4 * i], m_lo, m_hi);
+      const float2 s1 = scale_pair(w[4 * i + 1], m_lo, m_hi);
+      const float2 s2 = scale_pair(w[4 * i + 2], m_lo, m_hi);
+      const float2 s3 = scale_pair(w[4 * i + 3], m_lo, m_hi);
       if constexpr (SR) {
         // the random integer of column 2cp sits in the low half of the
         // random word, that of column 2cp + 1 in the high half
-        auto lo = [&](uint32_t x, uint32_t r) {
-          return sr_to_grid<FMT>(__fmul_rn(__uint_as_float(x << 16), m_lo), r & 0xFFFFu);
-        };
-        auto hi = [&](uint32_t x, uint32_t r) {
-          return sr_to_grid<FMT>(__fmul_rn(__uint_as_float(x & 0xFFFF0000u), m_hi), r >> 16);
-        };
-        q_lo[i] = cvt_pair<FMT>(lo(w0, rw[4 * i]), lo(w1, rw[4 * i + 1])) |
-                  (cvt_pair<FMT>(lo(w2, rw[4 * i + 2]), lo(w3, rw[4 * i + 3])) << 16);
-        q_hi[i] = cvt_pair<FMT>(hi(w0, rw[4 * i]), hi(w1, rw[4 * i + 1])) |
-                  (cvt_pair<FMT>(hi(w2, rw[4 * i + 2]), hi(w3, rw[4 * i + 3])) << 16);
+        const uint32_t r0 = rw[4 * i], r1 = rw[4 * i + 1], r2 = rw[4 * i + 2], r3 = rw[4 * i + 3];
+        q_lo[i] = cvt_pair<FMT>(sr_to_grid<FMT>(s0.x, r0 & 0xFFFFu),
+                                sr_to_grid<FMT>(s1.x, r1 & 0xFFFFu)) |
+                  (cvt_pair<FMT>(sr_to_grid<FMT>(s2.x, r2 & 0xFFFFu),
+                                 sr_to_grid<FMT>(s3.x, r3 & 0xFFFFu)) << 16);
+        q_hi[i] = cvt_pair<FMT>(sr_to_grid<FMT>(s0.y, r0 >> 16), sr_to_grid<FMT>(s1.y, r1 >> 16)) |
+                  (cvt_pair<FMT>(sr_to_grid<FMT>(s2.y, r2 >> 16), sr_to_grid<FMT>(s3.y, r3 >> 16))
+                   << 16);
         if (nan_lo) q_lo[i] = F::kNanWord;
         if (nan_hi) q_hi[i] = F::kNanWord;
         continue;
       }
       if constexpr (FMT == 4) {  // four 4-bit codes in 16 bits
-        q_lo[i] = cvt_pair<FMT>(__fmul_rn(__uint_as_float(w0 << 16), m_lo),
-                                __fmul_rn(__uint_as_float(w1 << 16), m_lo)) |
-                  (cvt_pair<FMT>(__fmul_rn(__uint_as_float(w2 << 16), m_lo),
-                                 __fmul_rn(__uint_as_float(w3 << 16), m_lo))
-                   << 8);
-        q_hi[i] = cvt_pair<FMT>(__fmul_rn(__uint_as_float(w0 & 0xFFFF0000u), m_hi),
-                                __fmul_rn(__uint_as_float(w1 & 0xFFFF0000u), m_hi)) |
-                  (cvt_pair<FMT>(__fmul_rn(__uint_as_float(w2 & 0xFFFF0000u), m_hi),
-                                 __fmul_rn(__uint_as_float(w3 & 0xFFFF0000u), m_hi))
-                   << 8);
+        q_lo[i] = cvt_pair<FMT>(s0.x, s1.x) | (cvt_pair<FMT>(s2.x, s3.x) << 8);
+        q_hi[i] = cvt_pair<FMT>(s0.y, s1.y) | (cvt_pair<FMT>(s2.y, s3.y) << 8);
         if (nan_lo) q_lo[i] = 0u;
         if (nan_hi) q_hi[i] = 0u;
         continue;
       }
-      q_lo[i] = cvt_pair<FMT>(__fmul_rn(__uint_as_float(w0 << 16), m_lo),
-                              __fmul_rn(__uint_as_float(w1 << 16), m_lo)) |
-                (cvt_pair<FMT>(__fmul_rn(__uint_as_float(w2 << 16), m_lo),
-                               __fmul_rn(__uint_as_float(w3 << 16), m_lo))
-                 << 16);
-      q_hi[i] = cvt_pair<FMT>(__fmul_rn(__uint_as_float(w0 & 0xFFFF0000u), m_hi),
-                              __fmul_rn(__uint_as_float(w1 & 0xFFFF0000u), m_hi)) |
-                (cvt_pair<FMT>(__fmul_rn(__uint_as_float(w2 & 0xFFFF0000u), m_hi),
-                               __fmul_rn(__uint_as_float(w3 & 0xFFFF0000u), m_hi))
-                 << 16);
+      q_lo[i] = cvt_pair<FMT>(s0.x, s1.x) | (cvt_pair<FMT>(s2.x, s3.x) << 16);
+      q_hi[i] = cvt_pair<FMT>(s0.y, s1.y) | (cvt_pair<FMT>(s2.y, s3.y) << 16);
       if (nan_lo) q_lo[i] = F::kNanWord;
       if (nan_hi) q_hi[i] = F::kNanWord;
     }
