@@ -166,6 +166,31 @@ def test_forward_full_size_sampled(mx):
     assert mx.device_status() == 0
 
 
+def test_fused_forward_full_size_sampled(mx):
+    """The fused epilogue in the bench's launch configuration: dense forward
+    M=16384, N=18432, K=7168 with an FP32 bias and SiLU, BF16 out, checked on
+    sampled rows and columns (GPU-written codes and scales, verified by
+    test_forward_full_size_sampled) against the oracle's epilogue."""
+    from mxfp8_block_scaled_mx_gb300 import workloads as W
+    x, w = W.dense_forward(device="cuda")
+    qa = mx.quantize(x, "e4m3", "row")
+    qb = mx.quantize(w, "e4m3", "col")
+    del x, w
+    n = qb.codes.shape[0]
+    bias = torch.randn(n, generator=torch.Generator().manual_seed(21)) * 0.5
+    y = mx.gemm(qa, qb, "bf16", bias=bias.cuda(), act="silu")
+    assert mx.device_status() == 0
+    m, k = qa.codes.shape
+    rows, cols = stripes(m), stripes(n)
+    sa = canonical_scales(qa.scales, m, k)
+    sb = canonical_scales(qb.scales, n, k)
+    a = O.MxBlocks(qa.codes[rows.cuda()].cpu().numpy(), sa[rows.numpy()], O.FORMATS[qa.fmt])
+    b = O.MxBlocks(qb.codes[cols.cuda()].cpu().numpy(), sb[cols.numpy()], O.FORMATS[qb.fmt])
+    out_ref, z_ref, t_ref = O.gemm_bias_act(a, b, bias.double().numpy()[cols.numpy()], "silu")
+    r = fused_error_ratio(y[rows.cuda()][:, cols.cuda()], out_ref, z_ref, t_ref, "bf16")
+    assert r <= 1.0, f"fused epilogue error {r:.3g} x bound"
+
+
 def test_dgrad_and_wgrad_full_size_sampled(mx):
     """Backward GEMMs of the same layer: dgrad dX = dY W^T with dY E5M2
     (blocks along N) and W E4M3 (blocks along N); wgrad dW = X^T dY over
