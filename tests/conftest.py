@@ -17,3 +17,24 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return GOLDEN
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Observed GEMM accuracy of the parity tests that ran: the worst error
+    as a fraction of the allowed bound and as a fraction of T = sum |a*b|,
+    per test file and output type."""
+    from mxcheck import ERROR_LOG
+    if not ERROR_LOG:
+        return
+    worst = {}
+    for test, dtype, ratio, rel_t, n in ERROR_LOG:
+        key = (test.split("::")[0], dtype)
+        w = worst.setdefault(key, [0.0, 0.0, 0])
+        w[0] = max(w[0], ratio)
+        w[1] = max(w[1], rel_t)
+        w[2] += n
+    terminalreporter.write_sep("-", "observed GEMM accuracy (max over checked outputs)")
+    for (path, dtype), (ratio, rel_t, n) in sorted(worst.items()):
+        terminalreporter.write_line(
+            f"{path} {dtype}: error/bound {ratio:.3g}, max |y - y_ref| / T {rel_t:.3g}, "
+            f"{n} outputs")

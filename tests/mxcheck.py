@@ -55,6 +55,12 @@ def bf16_ulp(y: np.ndarray) -> np.ndarray:
     return np.where(a > 0, 2.0 ** (e - 7), 2.0 ** -133)
 
 
+# Observed GEMM accuracy, one record per checked block of outputs:
+# (test id, output dtype, max error / allowed bound, max |y - y_ref| / T over
+# entries with T > 0, entries checked).  conftest prints a summary.
+ERROR_LOG: list = []
+
+
 def gemm_error_ratio(y_gpu: torch.Tensor, y_ref: np.ndarray, t_ref: np.ndarray,
                      out_dtype: str) -> float:
     """max |y - y_ref| / allowed over all entries (<= 1 passes)."""
@@ -65,7 +71,12 @@ def gemm_error_ratio(y_gpu: torch.Tensor, y_ref: np.ndarray, t_ref: np.ndarray,
     allowed = np.maximum(allowed, 1e-300)
     err = np.abs(y - y_ref)
     assert np.isfinite(y).all(), "non-finite GEMM output"
-    return float((err / allowed).max()) if err.size else 0.0
+    ratio = float((err / allowed).max()) if err.size else 0.0
+    pos = t_ref > 0
+    rel_t = float((err[pos] / t_ref[pos]).max()) if pos.any() else 0.0
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    ERROR_LOG.append((test, out_dtype, ratio, rel_t, int(err.size)))
+    return ratio
 
 
 def assert_gemm_close(y_gpu, y_ref, t_ref, out_dtype):
