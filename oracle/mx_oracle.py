@@ -31,7 +31,7 @@ states.  Sources (page title, section):
   MX specification):
   S = 2^(floor(log2 amax) - emax_elem), emax_elem = 8 (E4M3) or 15 (E5M2).
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 * A block holding NaN or +-Inf gets scale byte 0xFF (NaN) and every code in
   it is the NaN code 0x7F.
