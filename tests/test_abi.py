@@ -91,7 +91,7 @@ def test_gemm_rejects_bad_arguments_on_the_host(mx):
 def test_grouped_calls_reject_bad_arguments_on_the_host(mx):
     gg = mx.mx_grouped_gemm
     assert gg(0, FAKE, 64, 128, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 0) == 1      # groups
-    assert gg(2000, FAKE, 64, 128, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 0) == 1   # > 1024
+    assert gg(2000, FAKE, 64, 128, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 0) == 1   # > 1000
     assert gg(4, None, 64, 128, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 0) == 1      # offsets
     assert gg(4, FAKE, 64, 136, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 0) == 1      # n % 128
     qg = mx.mx_quantize_grouped
