@@ -43,6 +43,15 @@
  *  - Padding entries (rows >= rows, blocks >= K/32) are written as 0x00 by
  *    the quantizer and never influence a valid GEMM output.
  *  - A scale byte c encodes 2^(c - 127); 0xFF is NaN.
+ *
+ * GEMM kernel selection (environment, read at every GEMM call; for
+ * comparisons and tests -- the defaults are the measured best):
+ *  - MX_GEMM_PAIR=0 selects the one-block kernel (one CTA per 128-row
+ *    tile) instead of the default block-pair kernel (tcgen05 cta_group::2,
+ *    256x256 tiles over two SMs).  Results agree within the stated bound.
+ *  - One-block kernel only: MX_GEMM_BLOCK_N=128|256 (tile width along N),
+ *    MX_GEMM_CLUSTER_M=1|2 (2 = two blocks share the B tile by multicast).
+ *  - MX_GEMM_BAND_M=<even m-tiles per raster band> (dense GEMMs; default 32).
  */
 #ifndef MX_H_
 #define MX_H_

@@ -207,9 +207,11 @@ mx_status gemm_common(const GemmShape& g, const uint8_t* a, const uint8_t* sa, m
     const int v = std::atoi(env);
     if (v >= 2 && v % 2 == 0) p.band_m = v;
   }
+  // One-block kernel only (MX_GEMM_PAIR=0): tile width along N, and
+  // clusters of two blocks sharing the B tile by multicast for dense GEMMs
+  // (its grouped GEMMs measured faster unpaired); MX_GEMM_BLOCK_N and
+  // MX_GEMM_CLUSTER_M override.
   const int block_n = block_n_choice(p);
-  // Dense GEMMs pair blocks (B tile multicast); the grouped GEMMs measured
-  // faster unpaired.  MX_GEMM_CLUSTER_M overrides (1 or 2).
   int cluster_m = g.mode == mx::kModeDense ? 2 : 1;
   if (const char* env = std::getenv("MX_GEMM_CLUSTER_M")) cluster_m = std::atoi(env) == 1 ? 1 : 2;
 
