@@ -251,6 +251,47 @@ def bandwidth_row(fn, stream, scrub, clean, nbytes: float, hbm: float, bpe: floa
 
 # ---------------------------------------------------------------- per-row measurements
 
+def moe_roofline(sizes, n: int, k: int, kind: str, flops_peak: float, hbm_gbs: float) -> dict:
+    """Roofline of a mixture-of-experts GEMM.  Per expert with t tokens
+    (codes 1 byte and scales 1/32 byte per element):
+      forward  y[t, n] = x[t, k] w_g[n, k]^T, BF16 out
+      dgrad    dx[t, k] = dy[t, n] w_g[n, k], FP32 out
+      wgrad    dw_g[n, k] = dy[t, n]^T x[t, k], FP32 out (written for every
+               expert, zeros without tokens)
+    time_ms is the lower bound max(sum FLOP / tensor peak, sum bytes / HBM)
+    for a kernel that overlaps experts freely; per_expert_ms is the sum over
+    experts of max(FLOP_g / peak, bytes_g / HBM), the bound when experts run
+    one after another (small experts bound by their weight or output bytes).
+    flops_peak in TFLOP/s, hbm_gbs in GB/s."""
+    sc = 1.0 + 1.0 / 32.0
+    flops_sum = bytes_sum = per_expert = 0.0
+    for t in sizes:
+        t = int(t)
+        flops = 2.0 * t * n * k
+        if kind == "forward":
+            nbytes = (t * k + n * k) * sc + t * n * 2 if t else 0.0
+        elif kind == "dgrad":
+            nbytes = (t * n + n * k) * sc + t * k * 4 if t else 0.0
+        elif kind == "wgrad":
+            nbytes = (t * n + t * k) * sc + n * k * 4
+        else:
+            raise ValueError(kind)
+        flops_sum += flops
+        bytes_sum += nbytes
+        per_expert += max(flops / (flops_peak * 1e12), nbytes / (hbm_gbs * 1e9))
+    tc = flops_sum / (flops_peak * 1e12)
+    tm = bytes_sum / (hbm_gbs * 1e9)
+    return {"bound": "tensor" if tc >= tm else "hbm", "time_ms": round(max(tc, tm) * 1e3, 4),
+            "tensor_ms": round(tc * 1e3, 4), "hbm_ms": round(tm * 1e3, 4),
+            "bytes": int(bytes_sum), "per_expert_ms": round(per_expert * 1e3, 4)}
+
+
+def with_roofline(row: dict, roof: dict) -> dict:
+    row["roofline"] = dict(roof, frac=round(roof["time_ms"] / row["ms"], 3),
+                           per_expert_frac=round(roof["per_expert_ms"] / row["ms"], 3))
+    return row
+
+
 def measure_rows(mx, peaks, dev, stream):
     """Per-kernel measurements of the other hot-path rows (rank 0, N=1)."""
     import torch
@@ -355,10 +396,11 @@ def measure_rows(mx, peaks, dev, stream):
                     stream, 10)
     fl = 2 * xm.shape[0] * n * k
     sizes = [int(v) for v in (offsets[1:] - offsets[:-1])]
-    out["moe_grouped_64x(2048x7168)_65536tok_bf16"] = {
+    out["moe_grouped_64x(2048x7168)_65536tok_bf16"] = with_roofline({
         "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
         "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3),
-        "group_sizes_min_max": [min(sizes), max(sizes)], "empty_groups": sizes.count(0)}
+        "group_sizes_min_max": [min(sizes), max(sizes)], "empty_groups": sizes.count(0)},
+        moe_roofline(sizes, n, k, "forward", fp8_peak, hbm))
     # grouped rowwise quantize into the buffers above (the C call: no
     # allocation inside the timed launches)
     def qrow():
@@ -380,9 +422,10 @@ def measure_rows(mx, peaks, dev, stream):
     dx = torch.empty((total, k), dtype=torch.float32, device=dev)
     t = time_kernel(lambda: mx.grouped_gemm_bcat(qa, d_off, qb, "fp32", out=dx, stream=stream),
                     stream, 10)
-    out["moe_dgrad_64x(7168x2048)_65536tok_fp32"] = {
+    out["moe_dgrad_64x(7168x2048)_65536tok_fp32"] = with_roofline({
         "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
-        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
+        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)},
+        moe_roofline(sizes, n, k, "dgrad", fp8_peak, hbm))
     del qa, qb, dx
     ldq = mx.mx_grouped_cols_capacity(total, e)
     qa = mx.quantize_grouped(dym, d_off, "e5m2", axis="col", ldq=ldq, stream=stream)
@@ -390,9 +433,10 @@ def measure_rows(mx, peaks, dev, stream):
     dw = torch.empty((e, n, k), dtype=torch.float32, device=dev)
     t = time_kernel(lambda: mx.grouped_gemm_wgrad(qa, d_off, qb, total, "fp32", out=dw,
                                                   stream=stream), stream, 10)
-    out["moe_wgrad_64x(2048x7168)_65536tok_fp32"] = {
+    out["moe_wgrad_64x(2048x7168)_65536tok_fp32"] = with_roofline({
         "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
-        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
+        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)},
+        moe_roofline(sizes, n, k, "wgrad", fp8_peak, hbm))
     del dw
 
     # grouped columnwise quantize of X (per-expert token blocks), into the

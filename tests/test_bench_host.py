@@ -86,3 +86,23 @@ def test_peaks_file_is_read_or_falls_back():
     d, src = bench.read_peaks()
     assert src in ("measured", "fallback")
     assert d["hbm_gbs"] > 1000 and d["bf16_tflops"] > 100
+
+
+def test_moe_roofline_bounds():
+    """The MoE roofline: one large expert is tensor-bound with time = FLOP /
+    peak; experts without tokens cost nothing in the forward but their FP32
+    zero outputs in the weight gradient; the per-expert sum of maxima is
+    never below the overall bound."""
+    n, k, peak, bw = 2048, 7168, 4000.0, 8000.0
+    r = bench.moe_roofline([65536], n, k, "forward", peak, bw)
+    assert r["bound"] == "tensor"
+    assert abs(r["time_ms"] - 2 * 65536 * n * k / (peak * 1e12) * 1e3) < 1e-3
+    assert bench.moe_roofline([0, 0, 0], n, k, "forward", peak, bw)["time_ms"] == 0.0
+    w = bench.moe_roofline([0] * 64, n, k, "wgrad", peak, bw)
+    assert w["bound"] == "hbm" and w["bytes"] == 64 * n * k * 4
+    assert abs(w["time_ms"] - 64 * n * k * 4 / (bw * 1e9) * 1e3) < 1e-3
+    for kind in ("forward", "dgrad", "wgrad"):
+        m = bench.moe_roofline([0, 1, 31, 500, 20000, 45004], n, k, kind, peak, bw)
+        assert m["per_expert_ms"] >= m["time_ms"] - 1e-9
+        row = bench.with_roofline({"ms": 2 * m["time_ms"]}, m)
+        assert row["roofline"]["frac"] == 0.5
