@@ -1,7 +1,8 @@
 """Run one hot-path kernel on one shape a few times (for profilers).
 
     python -m mxfp8_block_scaled_mx_gb300.cases gemm --m 4096 --n 18432 --k 7168 [--reps 3] [--fused]
-    python -m mxfp8_block_scaled_mx_gb300.cases quantize --rows 16384 --cols 8192 --axis row
+    python -m mxfp8_block_scaled_mx_gb300.cases quantize --rows 16384 --cols 8192 --axis row [--sr]
+    python -m mxfp8_block_scaled_mx_gb300.cases moe_quantize --tokens 65536 --experts 64 --axis col
     python -m mxfp8_block_scaled_mx_gb300.cases grouped --tokens 16384 --experts 16
     python -m mxfp8_block_scaled_mx_gb300.cases moe_dgrad --tokens 16384 --experts 16
     python -m mxfp8_block_scaled_mx_gb300.cases moe_wgrad --tokens 16384 --experts 16
@@ -35,7 +36,8 @@ def _time(fn, reps):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["gemm", "quantize", "grouped", "moe_dgrad", "moe_wgrad"])
+    ap.add_argument("case", choices=["gemm", "quantize", "grouped", "moe_dgrad", "moe_wgrad",
+                                     "moe_quantize"])
     ap.add_argument("--m", type=int, default=4096)
     ap.add_argument("--n", type=int, default=18432)
     ap.add_argument("--k", type=int, default=7168)
@@ -47,6 +49,7 @@ def main(argv=None):
     ap.add_argument("--out", default="bf16", choices=["bf16", "fp32"])
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--fused", action="store_true", help="gemm: FP32 bias + SiLU epilogue")
+    ap.add_argument("--sr", action="store_true", help="quantize: stochastic rounding (E5M2)")
     a = ap.parse_args(argv)
     dev = torch.device("cuda", 0)
     if a.case == "gemm":
@@ -65,10 +68,29 @@ def main(argv=None):
               f"{2 * a.m * a.n * a.k / ms / 1e9:.1f} TFLOP/s")
     elif a.case == "quantize":
         x = W.quantize_sweep((a.rows, a.cols), seed=1, device=dev)
-        ms = _time(lambda: mx.quantize(x, "e4m3", a.axis), a.reps)
         bpe = 4.0625 if a.axis == "both" else 3.03125
-        print(f"quantize {a.rows}x{a.cols} {a.axis}: {ms:.4f} ms, "
+        if a.sr:  # stochastic rounding to E5M2: the random draws are a second input
+            rb = W.random_bits16((a.rows, a.cols), seed=11, device=dev)
+            ms = _time(lambda: mx.quantize(x, "e5m2", a.axis, rand=rb), a.reps)
+            bpe += 2.0
+        else:
+            ms = _time(lambda: mx.quantize(x, "e4m3", a.axis), a.reps)
+        print(f"quantize {a.rows}x{a.cols} {a.axis}{' sr' if a.sr else ''}: {ms:.4f} ms, "
               f"{a.rows * a.cols * bpe / ms / 1e6:.1f} GB/s")
+    elif a.case == "moe_quantize":
+        # the routed tokens [tokens, k], per-expert groups: rowwise (forward
+        # operand) or columnwise into 128-padded token segments (weight
+        # gradient operand)
+        x, _, offsets = W.moe_inputs(a.tokens, a.experts, a.k, 128, device=dev)
+        d_off = torch.from_numpy(offsets).to(dev)
+        if a.axis == "col":
+            ldq = mx.mx_grouped_cols_capacity(a.tokens, a.experts)
+            fn = lambda: mx.quantize_grouped(x, d_off, "e4m3", axis="col", ldq=ldq)  # noqa: E731
+        else:
+            fn = lambda: mx.quantize_grouped(x, d_off, "e4m3")  # noqa: E731
+        ms = _time(fn, a.reps)
+        print(f"moe_quantize {a.tokens}x{a.k} {a.axis} ({a.experts} experts): {ms:.4f} ms, "
+              f"{a.tokens * a.k * 3.03125 / ms / 1e6:.1f} GB/s")
     elif a.case in ("moe_dgrad", "moe_wgrad"):
         # mixture-of-experts backward, FP32 out: dX_g = dY_g W_g^T or dW_g = dY_g^T X_g
         x, w, offsets = W.moe_inputs(a.tokens, a.experts, a.k, 2048, device=dev)
