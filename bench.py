@@ -188,7 +188,13 @@ class ForwardLayer:
     launches_per_step = 3
 
 
-def time_kernel(fn, stream, reps: int, warmup: int = 3) -> float:
+# Per-row kernel timings: warm-up launches, then the median of this many
+# timed launches.
+ROW_WARMUP = 10
+ROW_REPS = 50
+
+
+def time_kernel(fn, stream, reps: int, warmup: int = ROW_WARMUP) -> float:
     """Mean duration (ms) of fn() over reps launches, CUDA events on `stream`."""
     import torch
     for _ in range(warmup):
@@ -210,7 +216,7 @@ def flush_l2(buf):
     buf.add_(1)
 
 
-def time_after_flush(fn, stream, scrub, reps: int = 20, read_pass=None):
+def time_after_flush(fn, stream, scrub, reps: int = ROW_REPS, read_pass=None):
     """Median duration (ms) of fn() launched right behind an L2 flush on the
     same stream: `scrub` (a buffer larger than L2) is written, then, with
     `read_pass`, a second such buffer is read, so that the flush's dirty
@@ -218,7 +224,7 @@ def time_after_flush(fn, stream, scrub, reps: int = 20, read_pass=None):
     Flush and launch are enqueued back to back with no host synchronization
     between them, so the host's launch latency is not timed."""
     import torch
-    for _ in range(3):
+    for _ in range(ROW_WARMUP):
         fn()
     torch.cuda.synchronize()
     events = []
@@ -348,7 +354,7 @@ def measure_rows(mx, peaks, dev, stream):
     bias = torch.randn(w.shape[1], device=dev, dtype=torch.float32)
     yf = torch.empty((x.shape[0], w.shape[1]), dtype=torch.bfloat16, device=dev)
     t = time_kernel(lambda: mx.gemm(xq, wq, "bf16", out=yf, stream=stream, bias=bias, act="silu"),
-                    stream, 10)
+                    stream, ROW_REPS)
     fl = 2 * x.shape[0] * w.shape[1] * x.shape[1]
     out["forward_bias_silu_16384x18432x7168_bf16"] = {
         "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
@@ -359,7 +365,7 @@ def measure_rows(mx, peaks, dev, stream):
                         ("mxfp6_e3m2xe3m2", "e3m2", "e3m2")):
         xq = mx.quantize(x, fa, "row", stream=stream)
         wq = mx.quantize(w, fb, "col", stream=stream)
-        t = time_kernel(lambda: mx.gemm(xq, wq, "bf16", out=yf, stream=stream), stream, 10)
+        t = time_kernel(lambda: mx.gemm(xq, wq, "bf16", out=yf, stream=stream), stream, ROW_REPS)
         out[f"forward_{tag}_16384x18432x7168_bf16"] = {
             "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
             "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
@@ -369,7 +375,7 @@ def measure_rows(mx, peaks, dev, stream):
     rq = mx.quantize(dy, "e5m2", "row", stream=stream)
     wq = mx.quantize(w, "e4m3", "row", stream=stream)
     dx = torch.empty((dy.shape[0], w.shape[0]), dtype=torch.float32, device=dev)
-    t = time_kernel(lambda: mx.gemm(rq, wq, "fp32", out=dx, stream=stream), stream, 10)
+    t = time_kernel(lambda: mx.gemm(rq, wq, "fp32", out=dx, stream=stream), stream, ROW_REPS)
     fl = 2 * dy.shape[0] * w.shape[0] * dy.shape[1]
     out["dgrad_16384x7168x18432_e5m2xe4m3_fp32"] = {
         "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
@@ -378,7 +384,7 @@ def measure_rows(mx, peaks, dev, stream):
     xq = mx.quantize(x, "e4m3", "col", stream=stream)
     dq = mx.quantize(dy, "e5m2", "col", stream=stream)
     dw = torch.empty((x.shape[1], dy.shape[1]), dtype=torch.float32, device=dev)
-    t = time_kernel(lambda: mx.gemm(xq, dq, "fp32", out=dw, stream=stream), stream, 10)
+    t = time_kernel(lambda: mx.gemm(xq, dq, "fp32", out=dw, stream=stream), stream, ROW_REPS)
     fl = 2 * x.shape[1] * dy.shape[1] * x.shape[0]
     out["wgrad_7168x18432x16384_e4m3xe5m2_fp32"] = {
         "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
@@ -393,7 +399,7 @@ def measure_rows(mx, peaks, dev, stream):
     qb = mx.MxTensor(qw.codes.view(e, n, k), qw.scales, "e4m3")
     ym = torch.empty((xm.shape[0], n), dtype=torch.bfloat16, device=dev)
     t = time_kernel(lambda: mx.grouped_gemm(qa, d_off, qb, "bf16", out=ym, stream=stream),
-                    stream, 10)
+                    stream, ROW_REPS)
     fl = 2 * xm.shape[0] * n * k
     sizes = [int(v) for v in (offsets[1:] - offsets[:-1])]
     out["moe_grouped_64x(2048x7168)_65536tok_bf16"] = with_roofline({
@@ -407,7 +413,7 @@ def measure_rows(mx, peaks, dev, stream):
         st = mx.mx_quantize_grouped(xm.data_ptr(), 0, xm.shape[0], k, k, 0, 0, e,
                                     d_off.data_ptr(), qa.codes.data_ptr(), qa.scales.data_ptr(), h)
         assert st == 0
-    t = time_kernel(qrow, stream, 10)
+    t = time_kernel(qrow, stream, ROW_REPS)
     gbs = xm.numel() * 3.03125 / (t * 1e-3) / 1e9
     out["moe_quantize_grouped_65536x7168"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
                                               "frac_hbm": round(gbs / hbm, 3)}
@@ -421,7 +427,7 @@ def measure_rows(mx, peaks, dev, stream):
     qb = mx.quantize(wm.view(e * n, k), "e4m3", "col", stream=stream)
     dx = torch.empty((total, k), dtype=torch.float32, device=dev)
     t = time_kernel(lambda: mx.grouped_gemm_bcat(qa, d_off, qb, "fp32", out=dx, stream=stream),
-                    stream, 10)
+                    stream, ROW_REPS)
     out["moe_dgrad_64x(7168x2048)_65536tok_fp32"] = with_roofline({
         "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
         "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)},
@@ -432,7 +438,7 @@ def measure_rows(mx, peaks, dev, stream):
     qb = mx.quantize_grouped(xm, d_off, "e4m3", axis="col", ldq=ldq, stream=stream)
     dw = torch.empty((e, n, k), dtype=torch.float32, device=dev)
     t = time_kernel(lambda: mx.grouped_gemm_wgrad(qa, d_off, qb, total, "fp32", out=dw,
-                                                  stream=stream), stream, 10)
+                                                  stream=stream), stream, ROW_REPS)
     out["moe_wgrad_64x(2048x7168)_65536tok_fp32"] = with_roofline({
         "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
         "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)},
@@ -446,7 +452,7 @@ def measure_rows(mx, peaks, dev, stream):
                                        None, None, qb.codes.data_ptr(), ldq,
                                        qb.scales.data_ptr(), h)
         assert st == 0
-    t = time_kernel(qcol, stream, 10)
+    t = time_kernel(qcol, stream, ROW_REPS)
     gbs = xm.numel() * 3.03125 / (t * 1e-3) / 1e9
     out["moe_quantize_grouped_cols_65536x7168"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
                                                    "frac_hbm": round(gbs / hbm, 3)}
@@ -605,8 +611,8 @@ def run_gpu(args):
         value = world * flops_step / (ms_per_step * 1e-3) / 1e12
 
         # quantize kernels timed alone (same buffers) for their GB/s
-        tq_x = time_kernel(layer.quantize_x, stream, 20)
-        tq_w = time_kernel(layer.quantize_w, stream, 20)
+        tq_x = time_kernel(layer.quantize_x, stream, ROW_REPS)
+        tq_w = time_kernel(layer.quantize_w, stream, ROW_REPS)
 
         # ---------------- end to end: host buffers through the C ABI
         hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
