@@ -122,6 +122,39 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+# The C ABI takes raw pointers and cannot see buffer sizes: the tensor API
+# checks them before every call, so that no kernel reads or writes past a
+# caller's tensor.
+
+def _require_codes(t: torch.Tensor, shape, what: str):
+    if (t.dtype != torch.uint8 or not t.is_cuda or tuple(t.shape) != tuple(shape)
+            or not t.is_contiguous()):
+        raise ValueError(f"{what}: codes must be a contiguous CUDA uint8 tensor of shape "
+                         f"{tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+
+
+def _require_scales(t: torch.Tensor, nbytes: int, what: str):
+    if t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous() or t.numel() < nbytes:
+        raise ValueError(f"{what}: scales must be a contiguous CUDA uint8 tensor of at least "
+                         f"{nbytes} bytes, got {t.numel()}")
+
+
+def _require_out(out: torch.Tensor, shape, dtype, contiguous: bool):
+    if out.dtype != dtype or not out.is_cuda or tuple(out.shape) != tuple(shape):
+        raise ValueError(f"out must be a CUDA {dtype} tensor of shape {tuple(shape)}, got "
+                         f"{out.dtype} {tuple(out.shape)}")
+    if out.stride(-1) != 1 or (contiguous and not out.is_contiguous()):
+        raise ValueError("out must have unit column stride" +
+                         (" and be contiguous" if contiguous else ""))
+
+
+def _require_offsets(offsets: torch.Tensor) -> int:
+    if offsets.dtype != torch.int32 or not offsets.is_cuda or offsets.dim() != 1 or \
+            not offsets.is_contiguous() or offsets.numel() < 2:
+        raise ValueError("offsets must be a contiguous 1-D CUDA int32 tensor of groups + 1 entries")
+    return offsets.numel() - 1
+
+
 # ---------------------------------------------------------------- C-named calls
 
 def mx_scale_bytes(rows: int, k: int) -> int:
@@ -313,9 +346,14 @@ def gemm(a: MxTensor, b: MxTensor, out_dtype: str = "bf16", out: torch.Tensor | 
     n, k2 = b.codes.shape
     if k != k2:
         raise ValueError("K mismatch")
+    _require_codes(a.codes, (m, k), "a")
+    _require_codes(b.codes, (n, k), "b")
+    _require_scales(a.scales, mx_scale_bytes(m, k), "a")
+    _require_scales(b.scales, mx_scale_bytes(n, k), "b")
     tdtype = torch.float32 if out_dtype == "fp32" else torch.bfloat16
     if out is None:
         out = torch.empty((m, n), dtype=tdtype, device=a.codes.device)
+    _require_out(out, (m, n), tdtype, contiguous=False)
     if bias is None and act == "none":
         st = mx_gemm(m, n, k, _ptr(a.codes), _ptr(a.scales), FMT[a.fmt], _ptr(b.codes),
                      _ptr(b.scales), FMT[b.fmt], _ptr(out), DTYPE[out_dtype], out.stride(0),
@@ -337,11 +375,16 @@ def grouped_gemm(a: MxTensor, offsets: torch.Tensor, b: MxTensor, out_dtype: str
     [groups, n, k]; b.scales holds groups consecutive swizzled matrices."""
     total_m, k = a.codes.shape
     groups, n, k2 = b.codes.shape
-    if k != k2 or offsets.numel() != groups + 1:
+    if k != k2 or _require_offsets(offsets) != groups:
         raise ValueError("shape mismatch")
+    _require_codes(a.codes, (total_m, k), "a")
+    _require_codes(b.codes, (groups, n, k), "b")
+    _require_scales(a.scales, mx_grouped_scale_bytes(total_m, groups, k), "a")
+    _require_scales(b.scales, groups * mx_scale_bytes(n, k), "b")
     tdtype = torch.float32 if out_dtype == "fp32" else torch.bfloat16
     if out is None:
         out = torch.empty((total_m, n), dtype=tdtype, device=a.codes.device)
+    _require_out(out, (total_m, n), tdtype, contiguous=True)
     st = mx_grouped_gemm(groups, _ptr(offsets), total_m, n, k, _ptr(a.codes), _ptr(a.scales),
                          FMT[a.fmt], _ptr(b.codes), _ptr(b.scales), FMT[b.fmt], _ptr(out),
                          DTYPE[out_dtype], _stream(stream))
@@ -356,10 +399,15 @@ def grouped_gemm_bcat(a: MxTensor, offsets: torch.Tensor, b: MxTensor, out_dtype
     axis="col") of the stacked [groups*k, n] expert weights); k = a's K."""
     total_m, k = a.codes.shape
     n, ldb = b.codes.shape
-    groups = offsets.numel() - 1
+    groups = _require_offsets(offsets)
+    _require_codes(a.codes, (total_m, k), "a")
+    _require_codes(b.codes, (n, ldb), "b")
+    _require_scales(a.scales, mx_grouped_scale_bytes(total_m, groups, k), "a")
+    _require_scales(b.scales, mx_scale_bytes(n, ldb), "b")
     tdtype = torch.float32 if out_dtype == "fp32" else torch.bfloat16
     if out is None:
         out = torch.empty((total_m, n), dtype=tdtype, device=a.codes.device)
+    _require_out(out, (total_m, n), tdtype, contiguous=True)
     st = mx_grouped_gemm_bcat(groups, _ptr(offsets), total_m, n, k, _ptr(a.codes),
                               _ptr(a.scales), FMT[a.fmt], _ptr(b.codes), ldb, _ptr(b.scales),
                               FMT[b.fmt], _ptr(out), DTYPE[out_dtype], _stream(stream))
@@ -375,12 +423,17 @@ def grouped_gemm_wgrad(a: MxTensor, offsets: torch.Tensor, b: MxTensor, total_to
     [groups, m, n]; an expert without tokens gets zeros."""
     m, ldk = a.codes.shape
     n, ldk2 = b.codes.shape
-    groups = offsets.numel() - 1
+    groups = _require_offsets(offsets)
     if ldk != ldk2:
         raise ValueError("A and B must share the token layout (ldq)")
+    _require_codes(a.codes, (m, ldk), "a")
+    _require_codes(b.codes, (n, ldk), "b")
+    _require_scales(a.scales, mx_scale_bytes(m, ldk), "a")
+    _require_scales(b.scales, mx_scale_bytes(n, ldk), "b")
     tdtype = torch.float32 if out_dtype == "fp32" else torch.bfloat16
     if out is None:
         out = torch.empty((groups, m, n), dtype=tdtype, device=a.codes.device)
+    _require_out(out, (groups, m, n), tdtype, contiguous=True)
     st = mx_grouped_gemm_wgrad(groups, _ptr(offsets), total_tokens, m, n, ldk, _ptr(a.codes),
                                _ptr(a.scales), FMT[a.fmt], _ptr(b.codes), _ptr(b.scales),
                                FMT[b.fmt], _ptr(out), DTYPE[out_dtype], _stream(stream))
