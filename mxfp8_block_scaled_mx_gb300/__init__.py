@@ -310,10 +310,8 @@ def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt: str = "e4m3",
     one read."""
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
         raise ValueError("x must be a row-major 2-D bf16 CUDA tensor")
-    if offsets.dtype != torch.int32 or not offsets.is_cuda:
-        raise ValueError("offsets must be a CUDA int32 tensor")
+    groups = _require_offsets(offsets)
     rows, cols = x.shape
-    groups = offsets.numel() - 1
     q_row = s_row = q_col = s_col = None
     if axis in ("row", "both"):
         q_row = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
