@@ -133,3 +133,40 @@ def test_largest_group_count(mx, kernel):
         be = O.quantize(to_f64(w[e]), "e4m3", "row")
         y_ref, t_ref = O.gemm(O.MxBlocks(a.codes[lo:hi], a.scales[lo:hi], a.fmt), be)
         assert_gemm_close(y[lo:hi], y_ref, t_ref, "fp32")
+
+
+def test_buffers_beyond_2_gib_of_elements(mx):
+    """Operands and outputs with more than 2^31 elements (64-bit offsets in
+    every kernel): a rowwise quantize of 40960 x 57344 bf16 (2.35 G
+    elements) checked on its last rows and first rows, and a GEMM whose
+    65536 x 36864 output (2.4 G elements) is checked on its last rows and
+    columns."""
+    rows, cols = 40960, 57344
+    g = torch.Generator(device="cuda").manual_seed(12)
+    x = (torch.randn(rows, cols, generator=g, device="cuda") * 3).to(torch.bfloat16)
+    q = mx.quantize(x, "e4m3", "row")
+    assert mx.device_status() == 0
+    for lo in (0, rows - 128):
+        ref = O.quantize(to_f64(x[lo:lo + 128, :4096]), "e4m3", "row")
+        assert torch.equal(q.codes[lo:lo + 128, :4096].cpu(), torch.from_numpy(ref.codes))
+        tail = O.quantize(to_f64(x[lo:lo + 128, cols - 4096:]), "e4m3", "row")
+        assert torch.equal(q.codes[lo:lo + 128, cols - 4096:].cpu(), torch.from_numpy(tail.codes))
+    kb = cols // 32
+    r, c = np.meshgrid(np.arange(rows - 128, rows), np.arange(kb - 128, kb), indexing="ij")
+    got = q.scales.cpu().numpy()[O.swizzle_offset(r, c, kb)]
+    assert np.array_equal(got, tail.scales)
+    del x, q
+    torch.cuda.empty_cache()
+    m, n, k = 65536, 36864, 64
+    a = (torch.randn(m, k, generator=g, device="cuda")).to(torch.bfloat16)
+    b = (torch.randn(k, n, generator=g, device="cuda") * 0.1).to(torch.bfloat16)
+    qa = mx.quantize(a, "e4m3", "row")
+    qb = mx.quantize(b, "e4m3", "col")
+    y = mx.gemm(qa, qb, "bf16")
+    assert mx.device_status() == 0
+    ra = O.quantize(to_f64(a[m - 64:]), "e4m3", "row")
+    rb = O.quantize(to_f64(b[:, n - 256:]), "e4m3", "col")
+    y_ref, t_ref = O.gemm(ra, rb)
+    assert_gemm_close(y[m - 64:, n - 256:], y_ref, t_ref, "bf16")
+    del a, b, qa, qb, y
+    torch.cuda.empty_cache()
