@@ -22,7 +22,9 @@
  *    CUDA device; the caller allocates and owns every buffer.  The library
  *    allocates no device memory.
  *  - Work is enqueued on `stream` (0 = legacy default stream).  No entry
- *    point synchronizes the stream or the device.
+ *    point synchronizes the stream or the device (except mx_device_status),
+ *    and none keeps per-call device scratch, so the calls may be captured
+ *    into CUDA graphs and issued on several streams concurrently.
  *  - Arguments are validated on the host before anything is launched; a
  *    non-MX_OK status means nothing was enqueued.
  *  - Faults detected on the device (a pipeline wait that timed out, invalid
