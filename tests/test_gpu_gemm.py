@@ -3,7 +3,6 @@
 Bound (FP32 accumulation, implementation-defined order):
 |y - y_ref| <= 1e-4 * sum_k |a_hat b_hat|, plus one BF16 ulp of y_ref for
 BF16 outputs.  Integer-valued cases must match bit for bit."""
-import os
 
 import numpy as np
 import pytest
