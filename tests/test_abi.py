@@ -157,3 +157,25 @@ def test_narrow_formats_on_the_host(mx):
 
 def test_selftest_rejects_zero_limit(mx):
     assert mx.mx_selftest_wait_timeout(0, 0) == 1
+
+
+def test_no_cpu_fallback(monkeypatch):
+    """Without the built library every entry point raises, and the tensor
+    API refuses CPU tensors instead of computing anything on the host."""
+    import torch
+    import mxfp8_block_scaled_mx_gb300 as mx
+    monkeypatch.setattr(mx, "_lib", None)
+    monkeypatch.setattr(mx, "LIB_PATH", os.path.join(ROOT, "no-such-libmx.so"))
+    with pytest.raises(RuntimeError):
+        mx.mx_scale_bytes(128, 128)
+    with pytest.raises(RuntimeError):
+        mx.device_status()
+    x = torch.zeros(64, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        mx.quantize(x, "e4m3", "row")
+    codes = torch.zeros(64, 64, dtype=torch.uint8)
+    t = mx.MxTensor(codes, torch.zeros(1024, dtype=torch.uint8), "e4m3")
+    with pytest.raises(ValueError):
+        mx.gemm(t, t, "fp32")
+    with pytest.raises(ValueError):
+        mx.quantize_grouped(x, torch.tensor([0, 64], dtype=torch.int32))
