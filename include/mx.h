@@ -19,17 +19,24 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Pointers marked "device" must point to device memory of the current
- *    CUDA device; the caller allocates and owns every buffer.  The library
- *    allocates no device memory.
+ *    CUDA device (memory of cudaMalloc or of a memory pool on that device);
+ *    the caller allocates and owns every buffer.  Every entry point checks
+ *    this with cudaPointerGetAttributes and returns MX_ERR_INVALID_ARG,
+ *    launching nothing, for host memory (pageable, pinned or mapped),
+ *    managed memory or another device's memory.  The library allocates no
+ *    device memory.
  *  - Work is enqueued on `stream` (0 = legacy default stream).  No entry
  *    point synchronizes the stream or the device (except mx_device_status),
  *    and none keeps per-call device scratch, so the calls may be captured
- *    into CUDA graphs and issued on several streams concurrently.
+ *    into CUDA graphs and issued on several streams and from several host
+ *    threads concurrently.
  *  - Arguments are validated on the host before anything is launched; a
  *    non-MX_OK status means nothing was enqueued.
  *  - Faults detected on the device (a pipeline wait that timed out, invalid
- *    group offsets) are recorded in a per-process device status word and
- *    reported by mx_device_status(), which synchronizes `stream`.
+ *    group offsets) are recorded in one status word per device, shared by
+ *    every stream and host thread of the process, and reported by
+ *    mx_device_status().  A fault of a kernel on any stream is therefore
+ *    reported to whichever caller queries the device first.
  *  - Every device pointer must be 16-byte aligned, and every leading
  *    dimension must span a multiple of 16 bytes (MX_ERR_MISALIGNED).
  *
@@ -46,14 +53,10 @@
  *    the quantizer and never influence a valid GEMM output.
  *  - A scale byte c encodes 2^(c - 127); 0xFF is NaN.
  *
- * GEMM kernel selection (environment, read at every GEMM call; for
- * comparisons and tests -- the defaults are the measured best):
- *  - MX_GEMM_PAIR=0 selects the one-block kernel (one CTA per 128-row
- *    tile) instead of the default block-pair kernel (tcgen05 cta_group::2,
- *    256x256 tiles over two SMs).  Results agree within the stated bound.
- *  - One-block kernel only: MX_GEMM_BLOCK_N=128|256 (tile width along N),
- *    MX_GEMM_CLUSTER_M=1|2 (2 = two blocks share the B tile by multicast).
- *  - MX_GEMM_BAND_M=<even m-tiles per raster band> (dense GEMMs; default 32).
+ * Kernels: quantization runs in one persistent kernel (one block per SM,
+ * tiles streamed by TMA); every GEMM runs in one block-pair kernel
+ * (tcgen05 cta_group::2, 256x256 output tiles over two SMs).  No
+ * environment variable changes what the library does.
  */
 #ifndef MX_H_
 #define MX_H_
@@ -105,8 +108,13 @@ typedef enum { MX_ROWWISE = 1, MX_COLWISE = 2, MX_BOTH = 3 } mx_axis;
  * MX_SCALE_CEIL: S = 2^ceil(log2(amax / max)), the conservative rule the
  *   two-row experiment uses; no element saturates.
  * Both: exponent clamped to [-127, 127]; an all-zero block takes S = 1; a
- * block holding NaN or Inf takes scale 0xFF and the NaN code 0x7F for every
- * element. */
+ * block holding NaN or Inf takes scale 0xFF and, for every element, the NaN
+ * code 0x7F of E4M3 / E5M2, or code 0 for E2M3, E3M2 and E2M1 (which have
+ * no NaN encoding).  MX_SCALE_CEIL is the rule some documents call RCEIL
+ * ("round the scale up"); with amax = m * 2^E, m in [1, 2), it equals the
+ * floor rule's exponent plus one exactly when m exceeds the significand of
+ * the format's maximum (1.75 for E4M3, E5M2 and E3M2; 1.875 for E2M3; 1.5
+ * for E2M1). */
 typedef enum { MX_SCALE_FLOOR = 0, MX_SCALE_CEIL = 1 } mx_scale_rule;
 
 /* Bytes of the swizzled scale buffer of a [rows, k] operand:
@@ -205,7 +213,9 @@ mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_
  *    swizzled scales sa of the [m, k] operand -- e.g. X quantized ROWWISE.
  * B: b[n, k] codes (K contiguous, leading dimension k) with swizzled scales
  *    sb of the [n, k] operand -- e.g. W[k, n] quantized COLWISE (= W^T).
- * fa, fb: E4M3 or E5M2, any combination.
+ * fa, fb: any of the five element formats (MX_E4M3, MX_E5M2, MX_E2M3,
+ *    MX_E3M2, MX_E2M1), in any combination; 6- and 4-bit codes in the
+ *    container layout described with mx_fmt.
  * y: device, [m, n] row-major with leading dimension ldy (elements),
  *    FP32 or BF16 (RNE from the FP32 accumulator).
  * Constraints: k % 32 == 0, k >= 32, n % 8 == 0, ldy >= n.
@@ -291,10 +301,13 @@ mx_status mx_grouped_gemm_wgrad(int32_t groups, const int32_t* d_offsets, int64_
                                 const uint8_t* b, const uint8_t* sb, mx_fmt fb,
                                 void* y, mx_dtype y_dtype, cudaStream_t stream);
 
-/* Synchronizes `stream`, then returns and clears the device status word of
- * the current device: MX_OK, MX_ERR_TIMEOUT (a kernel's bounded pipeline wait
- * gave up; its outputs are undefined) or MX_ERR_DEVICE_ARG (invalid group
- * offsets).  MX_ERR_CUDA if the synchronization itself failed. */
+/* Synchronizes `stream`, then reads the device status word of the current
+ * device and clears the bits it read: MX_OK, MX_ERR_TIMEOUT (a kernel's
+ * bounded pipeline wait gave up; its outputs are undefined) or
+ * MX_ERR_DEVICE_ARG (invalid group offsets).  The word is shared by all
+ * streams of the device, so the fault may come from a kernel on another
+ * stream; a bit that such a kernel sets after the read stays set for the
+ * next call.  MX_ERR_CUDA if the synchronization itself failed. */
 mx_status mx_device_status(cudaStream_t stream);
 
 /* Static string naming a status code. */

@@ -124,9 +124,20 @@ def _ptr(t) -> int | None:
 
 # The C ABI takes raw pointers and cannot see buffer sizes: the tensor API
 # checks them before every call, so that no kernel reads or writes past a
-# caller's tensor.
+# caller's tensor.  Every tensor must also live on the current CUDA device
+# (the device whose stream the call is enqueued on); the C ABI refuses
+# other devices' memory too.
+
+def _on_current_device(t: torch.Tensor, what: str):
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor, got {t.device}")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{what} must be on the current CUDA device "
+                         f"(cuda:{torch.cuda.current_device()}), got {t.device}")
+
 
 def _require_codes(t: torch.Tensor, shape, what: str):
+    _on_current_device(t, what)
     if (t.dtype != torch.uint8 or not t.is_cuda or tuple(t.shape) != tuple(shape)
             or not t.is_contiguous()):
         raise ValueError(f"{what}: codes must be a contiguous CUDA uint8 tensor of shape "
@@ -134,12 +145,14 @@ def _require_codes(t: torch.Tensor, shape, what: str):
 
 
 def _require_scales(t: torch.Tensor, nbytes: int, what: str):
+    _on_current_device(t, what)
     if t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous() or t.numel() < nbytes:
         raise ValueError(f"{what}: scales must be a contiguous CUDA uint8 tensor of at least "
                          f"{nbytes} bytes, got {t.numel()}")
 
 
 def _require_out(out: torch.Tensor, shape, dtype, contiguous: bool):
+    _on_current_device(out, "out")
     if out.dtype != dtype or not out.is_cuda or tuple(out.shape) != tuple(shape):
         raise ValueError(f"out must be a CUDA {dtype} tensor of shape {tuple(shape)}, got "
                          f"{out.dtype} {tuple(out.shape)}")
@@ -149,6 +162,7 @@ def _require_out(out: torch.Tensor, shape, dtype, contiguous: bool):
 
 
 def _require_offsets(offsets: torch.Tensor) -> int:
+    _on_current_device(offsets, "offsets")
     if offsets.dtype != torch.int32 or not offsets.is_cuda or offsets.dim() != 1 or \
             not offsets.is_contiguous() or offsets.numel() < 2:
         raise ValueError("offsets must be a contiguous 1-D CUDA int32 tensor of groups + 1 entries")
@@ -263,6 +277,7 @@ def quantize(x: torch.Tensor, fmt: str = "e4m3", axis: str = "row", rule: str = 
     stochastic rounding."""
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda:
         raise ValueError("x must be a 2-D bf16 CUDA tensor")
+    _on_current_device(x, "x")
     if x.stride(1) != 1:
         raise ValueError("x must be row-major with unit column stride")
     rows, cols = x.shape
@@ -282,6 +297,7 @@ def quantize(x: torch.Tensor, fmt: str = "e4m3", axis: str = "row", rule: str = 
     else:
         if rand.dtype != torch.int16 or rand.shape != x.shape or not rand.is_cuda:
             raise ValueError("rand must be a CUDA int16 tensor shaped like x")
+        _on_current_device(rand, "rand")
         if rand.stride(1) != 1:
             raise ValueError("rand must have unit column stride")
         st = mx_quantize_sr(_ptr(x), DTYPE["bf16"], rows, cols, x.stride(0), _ptr(rand),
@@ -310,6 +326,7 @@ def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt: str = "e4m3",
     one read."""
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
         raise ValueError("x must be a row-major 2-D bf16 CUDA tensor")
+    _on_current_device(x, "x")
     groups = _require_offsets(offsets)
     rows, cols = x.shape
     q_row = s_row = q_col = s_col = None
@@ -360,6 +377,8 @@ def gemm(a: MxTensor, b: MxTensor, out_dtype: str = "bf16", out: torch.Tensor | 
         return out
     if bias is not None and (bias.dtype != torch.float32 or bias.numel() != n or not bias.is_cuda):
         raise ValueError("bias must be a CUDA float32 tensor of n elements")
+    if bias is not None:
+        _on_current_device(bias, "bias")
     st = mx_gemm_bias_act(m, n, k, _ptr(a.codes), _ptr(a.scales), FMT[a.fmt], _ptr(b.codes),
                           _ptr(b.scales), FMT[b.fmt], _ptr(bias), ACT[act], _ptr(out),
                           DTYPE[out_dtype], out.stride(0), _stream(stream))

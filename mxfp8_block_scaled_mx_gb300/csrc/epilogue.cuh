@@ -3,7 +3,7 @@
 // registers, release of the accumulator (callback), optional fused bias and
 // SiLU in FP32, conversion to FP32/BF16 (RNE), staging through 2 KB of
 // shared memory and coalesced 64-byte row segments to global memory, masked
-// at the matrix edge.  Shared by the one-block and the block-pair GEMMs.
+// at the matrix edge.
 #pragma once
 
 #include <cstdint>

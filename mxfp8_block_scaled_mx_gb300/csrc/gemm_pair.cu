@@ -1,9 +1,12 @@
 // gemm_pair.cu -- block-scaled MXFP8 GEMM on block pairs (tcgen05 cta_group::2).
 //
-// Same computation as gemm.cu ("Low-Precision GPU Programming", section
-// "Scale ownership and the GEMM dataflow": each 32-element K block keeps its
-// scale product inside the outer sum), but every MMA spans the tensor cores
-// of the two blocks of a cluster: M = 256 per instruction, block r holding
+// "Low-Precision GPU Programming", section "Scale ownership and the GEMM
+// dataflow": Y = sum over 32-element K blocks b of S_A[i,b] S_B[j,b] times
+// the block's dot product, each block's scale product kept inside the outer
+// sum and applied by the tensor core (kind::mxf8f6f4.block_scale, E8M0
+// scales from tensor memory), FP32 accumulation in tensor memory, FP32 or
+// BF16 epilogue.  Every MMA spans the tensor cores of the two blocks of a
+// cluster: M = 256 per instruction, block r holding
 // rows 128r..128r+127 of A and of the accumulator, and half of the B tile
 // (N rows 128r..128r+127) in its shared memory.  Per block and stage that is
 // 32 KB of operands instead of 48 KB, so six stages fit (five next to the
@@ -23,8 +26,7 @@
 //                         With the fused epilogue: warps 4..11, warps 2 and
 //                         3 idle (they complete the first warpgroup, whose
 //                         registers go to the epilogue warpgroups).
-// The work decomposition (tiles.cuh) is the one-block kernel's with two
-// blocks per cluster, in the same three modes: dense, grouped by rows of A
+// The work decomposition (tiles.cuh) has three modes: dense, grouped by rows of A
 // (mixture-of-experts forward and data gradient) and grouped along K (the
 // per-expert weight gradient).  All waits are bounded; a final cluster
 // barrier keeps either block alive until its partner no longer touches its
@@ -357,24 +359,20 @@ cudaError_t launch_pair_impl(const GemmParams& p, const CUtensorMap& ta, const C
                              cudaStream_t stream) {
   using C = PairCfg<MODE != kModeDense>;
   auto kern = mx_gemm_pair_kernel<MODE, FUSED>;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+  static PerDeviceOnce setup;
+  cudaError_t err = setup.run([&]() -> cudaError_t {
     // The register increase in the kernel waits for registers the first
     // warpgroup returns; it only completes if the block is launched with
     // the allocation the shares were computed for.
     if (FUSED) {
       cudaFuncAttributes fa;
-      err = cudaFuncGetAttributes(&fa, kern);
-      if (err != cudaSuccess) return err;
+      const cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
       if (fa.numRegs != kPLaunchRegs) return cudaErrorInvalidConfiguration;
     }
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  });
+  if (err != cudaSuccess) return err;
   const int64_t n_tiles = (p.n + kPairN - 1) / kPairN;
   const int64_t m_tiles = (p.m + kRowsPerBlock - 1) / kRowsPerBlock;
   // upper bound of the pair units (grouped by rows: every group may add a

@@ -1,13 +1,40 @@
 // kernels.h -- launch interface between the C-ABI layer (mx_api.cu) and the
-// CUDA kernels (quantize.cu, gemm.cu).  Not part of the public ABI.
+// CUDA kernels (quantize.cu, gemm_pair.cu, status.cu).  Not part of the
+// public ABI.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 namespace mx {
+
+// One-time set-up of a kernel per device (its dynamic shared-memory limit):
+// `fn` runs until it first succeeds on the current device.  The flags are
+// guarded by a mutex, so concurrent first calls from several host threads
+// are safe.
+class PerDeviceOnce {
+ public:
+  template <typename Fn>
+  cudaError_t run(Fn&& fn) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDev) return fn();
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev]) return cudaSuccess;
+    err = fn();
+    if (err == cudaSuccess) done_[dev] = true;
+    return err;
+  }
+
+ private:
+  static constexpr int kMaxDev = 64;
+  std::mutex mu_;
+  bool done_[kMaxDev] = {};
+};
 
 struct QuantizeParams {
   const uint16_t* x;   // bf16 bit patterns, [rows, cols], leading dimension ldx
@@ -72,14 +99,6 @@ struct GemmParams {
   int32_t act;             // fused epilogue: 0 none, 1 SiLU
 };
 
-// Tile width along N of the GEMM kernel: 128 (double-buffered accumulator)
-// or 256 (single accumulator).
-int gemm_default_block_n(const GemmParams& p);
-
-// cluster_m: 1, or 2 for block pairs sharing (multicasting) the B tile.
-cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                        int block_n, int cluster_m, int num_sms, cudaStream_t stream);
-
 // Block-pair GEMM (cta_group::2, 256 x 256 pair tiles), all three modes.
 // tmap_a / tmap_b: codes, box 128 rows; tmap_sa / tmap_sb: the swizzled
 // scale buffers viewed as uint32 [row_tiles][k_tiles][128], boxes of one
@@ -87,6 +106,10 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tmap_a, const CU
 cudaError_t launch_gemm_pair(const GemmParams& p, const CUtensorMap& tmap_a,
                              const CUtensorMap& tmap_b, const CUtensorMap& tmap_sa,
                              const CUtensorMap& tmap_sb, int num_sms, cudaStream_t stream);
+
+// Clears the bits `bits` of the device status word (atomically, so bits
+// set meanwhile by kernels on other streams survive).
+cudaError_t launch_status_clear(uint32_t* status, uint32_t bits, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 

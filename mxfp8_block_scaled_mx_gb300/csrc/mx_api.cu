@@ -5,9 +5,10 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdint>
-#include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "kernels.h"
@@ -23,6 +24,7 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 struct DeviceState {
   bool ready = false;
+  int device = 0;
   int num_sms = 0;
   uint32_t* status = nullptr;  // device address of g_status_word on this device
 };
@@ -30,7 +32,10 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-uint64_t g_wait_ns = kDefaultWaitNs;
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+// Dense GEMMs walk their output tiles in bands of this many 128-row tiles
+// (n-tiles outer inside a band), so a band of A stays in L2 while B streams.
+constexpr int32_t kBandM = 32;
 
 mx_status device_state(DeviceState** out) {
   int dev = 0;
@@ -44,6 +49,7 @@ mx_status device_state(DeviceState** out) {
     if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return MX_ERR_CUDA;
     st.status = static_cast<uint32_t*>(addr);
     if (cudaMemset(st.status, 0, sizeof(uint32_t)) != cudaSuccess) return MX_ERR_CUDA;
+    st.device = dev;
     st.ready = true;
   }
   if (!g_encode) {
@@ -60,6 +66,24 @@ mx_status device_state(DeviceState** out) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Every non-null pointer of the list points into device memory of device
+// `dev` (memory of cudaMalloc or a memory pool on that device).  Host memory
+// (pinned, mapped or unregistered), managed memory and the memory of other
+// devices -- all reachable through unified addressing -- are refused, so
+// the kernels and their tensor copies only ever read this GPU's own memory.
+bool all_on_device(int dev, std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs) {
+    if (p == nullptr) continue;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+      (void)cudaGetLastError();  // clear the (non-sticky) error of the query
+      return false;
+    }
+    if (a.type != cudaMemoryTypeDevice || a.device != dev) return false;
+  }
+  return true;
+}
 
 bool valid_fmt(mx_fmt f) { return f == MX_E4M3 || f == MX_E5M2; }
 
@@ -130,22 +154,6 @@ mx_status encode_scale_map(CUtensorMap* map, const void* base, int64_t rows, int
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
-// GEMMs run on block pairs (cta_group::2, 256x256 pair tiles), in every
-// mode; MX_GEMM_PAIR=0 selects the one-block kernel.
-bool use_pair_kernel() {
-  const char* env = std::getenv("MX_GEMM_PAIR");
-  return env == nullptr || std::atoi(env) != 0;
-}
-
-int block_n_choice(const mx::GemmParams& p) {
-  const char* env = std::getenv("MX_GEMM_BLOCK_N");
-  if (env) {
-    const int v = std::atoi(env);
-    if (v == 128 || v == 256) return v;
-  }
-  return mx::gemm_default_block_n(p);
-}
-
 // Operand geometry of one GEMM launch: A codes [m, lda] (grouped along K:
 // [m, lda] shared by all groups), B codes [b_rows, ldb]; scales swizzled
 // over the same shapes.
@@ -180,6 +188,7 @@ mx_status gemm_common(const GemmShape& g, const uint8_t* a, const uint8_t* sa, m
   mx_status s = device_state(&st);
   if (s != MX_OK) return s;
   if (m == 0) return MX_OK;
+  if (!all_on_device(st->device, {a, sa, b, sb, y, bias, g.d_offsets})) return MX_ERR_INVALID_ARG;
 
   mx::GemmParams p{};
   p.m = m;
@@ -199,44 +208,24 @@ mx_status gemm_common(const GemmShape& g, const uint8_t* a, const uint8_t* sa, m
   p.groups = g.groups;
   p.mode = g.mode;
   p.status = st->status;
-  p.wait_limit_ns = g_wait_ns;
+  p.wait_limit_ns = g_wait_ns.load(std::memory_order_relaxed);
   p.bias = bias;
   p.act = act;
-  p.band_m = 32;
-  if (const char* env = std::getenv("MX_GEMM_BAND_M")) {
-    const int v = std::atoi(env);
-    if (v >= 2 && v % 2 == 0) p.band_m = v;
-  }
-  // One-block kernel only (MX_GEMM_PAIR=0): tile width along N, and
-  // clusters of two blocks sharing the B tile by multicast for dense GEMMs
-  // (its grouped GEMMs measured faster unpaired); MX_GEMM_BLOCK_N and
-  // MX_GEMM_CLUSTER_M override.
-  const int block_n = block_n_choice(p);
-  int cluster_m = g.mode == mx::kModeDense ? 2 : 1;
-  if (const char* env = std::getenv("MX_GEMM_CLUSTER_M")) cluster_m = std::atoi(env) == 1 ? 1 : 2;
+  p.band_m = kBandM;
 
-  CUtensorMap ta, tb;
+  // Block pairs (cta_group::2, 256x256 pair tiles): each block loads 128
+  // rows of A and 128 of the 256 rows of the B tile; the scale buffers are
+  // viewed as grids of 512-byte units, A's with the per-group padded row
+  // bound when grouped by rows.
+  CUtensorMap ta, tb, tsa, tsb;
+  const int64_t a_scale_rows = g.mode == mx::kModeGroupM ? (ceil_div(m, 128) + g.groups) * 128 : m;
   if ((s = encode_codes_map(&ta, a, g.lda, m, g.lda, 128)) != MX_OK) return s;
-  if (use_pair_kernel()) {
-    // block pairs: each block loads 128 rows of the 256-row B tile; the
-    // scale buffers are viewed as grids of 512-byte units, A's with the
-    // per-group padded row bound when grouped by rows
-    CUtensorMap tsa, tsb;
-    const int64_t a_scale_rows =
-        g.mode == mx::kModeGroupM ? (ceil_div(m, 128) + g.groups) * 128 : m;
-    if ((s = encode_codes_map(&tb, b, g.ldb, g.b_rows, g.ldb, 128)) != MX_OK) return s;
-    if ((s = encode_scale_map(&tsa, sa, a_scale_rows, g.lda, 1)) != MX_OK) return s;
-    if ((s = encode_scale_map(&tsb, sb, g.b_rows, g.ldb, 2)) != MX_OK) return s;
-    const cudaError_t err = mx::launch_gemm_pair(p, ta, tb, tsa, tsb, st->num_sms, stream);
-    if (err == cudaErrorNotSupported) return MX_ERR_UNSUPPORTED;
-    return err == cudaSuccess ? MX_OK : MX_ERR_CUDA;
-  }
-  // With block pairs each block loads half of the B tile (multicast).
-  const uint32_t b_box_rows = static_cast<uint32_t>(block_n / cluster_m);
-  if ((s = encode_codes_map(&tb, b, g.ldb, g.b_rows, g.ldb, b_box_rows)) != MX_OK) return s;
-  if (mx::launch_gemm(p, ta, tb, block_n, cluster_m, st->num_sms, stream) != cudaSuccess)
-    return MX_ERR_CUDA;
-  return MX_OK;
+  if ((s = encode_codes_map(&tb, b, g.ldb, g.b_rows, g.ldb, 128)) != MX_OK) return s;
+  if ((s = encode_scale_map(&tsa, sa, a_scale_rows, g.lda, 1)) != MX_OK) return s;
+  if ((s = encode_scale_map(&tsb, sb, g.b_rows, g.ldb, 2)) != MX_OK) return s;
+  const cudaError_t err = mx::launch_gemm_pair(p, ta, tb, tsa, tsb, st->num_sms, stream);
+  if (err == cudaErrorNotSupported) return MX_ERR_UNSUPPORTED;
+  return err == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
 GemmShape dense_shape(int64_t m, int64_t n, int64_t k) {
@@ -305,9 +294,11 @@ mx_status quantize_common(const void* x, mx_dtype x_dtype, int64_t rows, int64_t
   p.fmt = fmt;
   p.rule = rule;
   p.status = st->status;
-  p.wait_limit_ns = g_wait_ns;
+  p.wait_limit_ns = g_wait_ns.load(std::memory_order_relaxed);
   p.ldq_col = rows;
   if (rows == 0 || cols == 0) return MX_OK;
+  if (!all_on_device(st->device, {x, rbits, p.q_row, p.s_row, p.q_col, p.s_col}))
+    return MX_ERR_INVALID_ARG;
   CUtensorMap tmap, tmap_r;
   if ((s = encode_bf16_map(&tmap, x, cols, rows, ldx)) != MX_OK) return s;
   // the random integers are 16-bit like bf16: the same tile geometry
@@ -394,8 +385,10 @@ mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_
   p.offsets = d_offsets;
   p.groups = groups;
   p.status = st->status;
-  p.wait_limit_ns = g_wait_ns;
+  p.wait_limit_ns = g_wait_ns.load(std::memory_order_relaxed);
   if (cols == 0) return MX_OK;
+  if (!all_on_device(st->device, {x, d_offsets, p.q_row, p.s_row, p.q_col, p.s_col}))
+    return MX_ERR_INVALID_ARG;
   CUtensorMap tmap;
   // an empty token set still needs a valid map (1 row) for the offsets check
   if ((status = encode_bf16_map(&tmap, x, cols, total_rows > 0 ? total_rows : 1, ldx)) != MX_OK)
@@ -481,15 +474,20 @@ mx_status mx_device_status(cudaStream_t stream) {
   uint32_t word = 0;
   if (cudaMemcpy(&word, st->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
     return MX_ERR_CUDA;
-  if (word != 0 && cudaMemset(st->status, 0, sizeof(word)) != cudaSuccess) return MX_ERR_CUDA;
+  if (word != 0) {
+    // clear only the bits read here (a kernel on another stream may set one
+    // meanwhile; it then stays for the next query)
+    if (mx::launch_status_clear(st->status, word, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+      return MX_ERR_CUDA;
+  }
   if (word & 1u) return MX_ERR_TIMEOUT;
   if (word & 2u) return MX_ERR_DEVICE_ARG;
   return MX_OK;
 }
 
 mx_status mx_set_wait_timeout_ns(uint64_t ns) {
-  std::lock_guard<std::mutex> lock(g_mu);
-  g_wait_ns = ns == 0 ? kDefaultWaitNs : ns;
+  g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);
   return MX_OK;
 }
 

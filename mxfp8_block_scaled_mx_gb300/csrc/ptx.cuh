@@ -154,49 +154,7 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, ui
       : "memory");
 }
 
-// 2-D tiled load multicast to the blocks of `cta_mask` in the cluster: the
-// tile lands at the same shared-memory offset in each of them and completes
-// on the mbarrier at the same offset in each.
-__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const void* tmap,
-                                                      uint64_t* bar, int32_t x, int32_t y,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
-
-// Plain bulk copy global -> shared (16-byte aligned addresses, size a
-// multiple of 16), completing on `bar`.
-__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05
-
-// Allocate `ncols` (power of two >= 32) tensor-memory columns; the base
-// address is written to *slot.  Executed by one full warp.
-__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(slot)),
-               "r"(ncols)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
 
 __device__ __forceinline__ void tc_fence_before_sync() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -204,74 +162,6 @@ __device__ __forceinline__ void tc_fence_before_sync() {
 
 __device__ __forceinline__ void tc_fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Make `bar` arrive (count one) once every tcgen05 operation issued so far
-// by this thread has completed.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-// As tc_commit, but the arrival goes to the mbarrier at the same offset in
-// every block of `cta_mask` in the cluster.
-__device__ __forceinline__ void tc_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
-// Copy a 32-row x 128-bit shared-memory matrix into tensor memory at
-// `taddr`, replicated into all four 32-lane quarters (warpx4).
-__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-               : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T with per-32-K block scales from tensor
-// memory (kind::mxf8f6f4, E8M0 scales, one scale per 32 K-elements).
-__device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
-      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-      : "memory");
-}
-
-// Same MMA with each shared-memory descriptor given as two 32-bit halves
-// (the low half carries the start address, the high half is constant per
-// operand), so the issuing thread only does 32-bit adds per MMA.
-__device__ __forceinline__ void tc_mma_mxf8_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
-                                                 uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
-                                                 uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                                 uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
-      "mov.b64 da, {%1, %2};\n\t"
-      "mov.b64 db, {%3, %4};\n\t"
-      "setp.ne.b32 p, %8, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
-      " [%0], da, db, %5, [%6], [%7], p;\n\t}" ::"r"(d_tmem),
-      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
-      "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_cp_32x128b_warpx4_lohi(uint32_t taddr, uint32_t lo,
-                                                          uint32_t hi) {
-  asm volatile(
-      "{\n\t.reg .b64 d;\n\tmov.b64 d, {%1, %2};\n\t"
-      "tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], d;\n\t}" ::"r"(taddr),
-      "r"(lo), "r"(hi)
-      : "memory");
 }
 
 // Load 32 consecutive 32-bit columns of this warp's 32 tensor-memory lanes:
@@ -296,21 +186,11 @@ __device__ __forceinline__ void tmem_ld_wait() {
 
 // ---------------------------------------------------------------- descriptors
 
-// Shared-memory matrix descriptor (tcgen05 format): start address, leading
-// and stride byte offsets (16-byte units), version 1 at bit 46, swizzle
-// mode in bits 61..63 (0 none, 2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
-                                              uint32_t sbo_bytes, uint32_t swizzle_mode) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= 1ull << 46;
-  d |= static_cast<uint64_t>(swizzle_mode & 0x7u) << 61;
-  return d;
-}
-
-// Low / high 32-bit halves of smem_desc (same fields).
+// Shared-memory matrix descriptor of the tcgen05 instructions, as two
+// 32-bit halves.  Low half: start address and leading byte offset (16-byte
+// units); high half: stride byte offset (16-byte units), version 1 (bit 46
+// of the 64-bit descriptor) and the swizzle mode in bits 61..63 (0 none,
+// 2 = 128-byte swizzle).
 __device__ __forceinline__ uint32_t smem_desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
   return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
 }
@@ -320,7 +200,7 @@ __host__ __device__ constexpr uint32_t smem_desc_hi(uint32_t sbo_bytes, uint32_t
 
 // Instruction descriptor of kind::mxf8f6f4 with block scaling: K-major A
 // and B, dense, E8M0 scale format, scale-factor byte ids for A and B.
-// fmt codes: 0 = E4M3, 1 = E5M2.
+// fmt codes: 0 = E4M3, 1 = E5M2, 3 = E2M3, 4 = E3M2, 5 = E2M1.
 __host__ __device__ constexpr uint32_t mxf8_idesc(uint32_t fa, uint32_t fb, uint32_t m,
                                                   uint32_t n, uint32_t sfa_id, uint32_t sfb_id) {
   return (sfb_id & 3u) << 4 | (fa & 7u) << 7 | (fb & 7u) << 10 | ((n >> 3) & 0x3Fu) << 17 |
@@ -343,11 +223,6 @@ __device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
 // a tcgen05.fence::before_thread_sync.  A release arrive would also wait
 // until this thread's earlier global stores are visible, which the
 // accumulator handoff does not need.
-__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_relaxed_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");

@@ -618,16 +618,11 @@ cudaError_t launch_one(const QuantizeParams& p, const CUtensorMap& tmap, const C
                        int64_t tiles, int num_sms, cudaStream_t stream) {
   auto kern = quantize_kernel<FMT, ROW, COL, GROUPED, SR>;
   using QSmem = mx::QSmem<COL, SR>;
-  // The attribute is per function and device; set it once per device.
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  static PerDeviceOnce setup;
+  const cudaError_t err = setup.run([&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QSmem::kBytes);
+  });
   if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QSmem::kBytes);
-    if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
   const int64_t grid = tiles < num_sms ? tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
   kern<<<static_cast<unsigned>(grid), QSmem::kThreads, QSmem::kBytes, stream>>>(tmap, tmap_r, p);

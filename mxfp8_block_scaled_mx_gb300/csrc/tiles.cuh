@@ -1,8 +1,7 @@
-// tiles.cuh -- work decomposition shared by the one-block and the
-// block-pair GEMM kernels: the shared-memory group table, and the mapping
-// of a linear work unit to one block's output tile, operand coordinates and
-// scale units in the three GEMM modes (dense; grouped by rows of A; grouped
-// along K).
+// tiles.cuh -- work decomposition of the block-pair GEMM kernel: the
+// shared-memory group table, and the mapping of a linear work unit to one
+// block's output tile, operand coordinates and scale units in the three
+// GEMM modes (dense; grouped by rows of A; grouped along K).
 #pragma once
 
 #include <cstdint>

@@ -18,12 +18,6 @@ def mx():
     return mx
 
 
-@pytest.fixture(params=["1", "0"], ids=["pair", "one-block"])
-def kernel(request, monkeypatch):
-    monkeypatch.setenv("MX_GEMM_PAIR", request.param)
-    return request.param
-
-
 def h():
     return int(torch.cuda.current_stream().cuda_stream)
 
@@ -55,7 +49,7 @@ def test_smallest_quantize_shapes(mx, shape, axis):
 
 
 @pytest.mark.parametrize("m,n,k", [(1, 8, 32), (2, 16, 32), (1, 264, 32), (300, 8, 64)])
-def test_smallest_gemm_shapes(mx, kernel, m, n, k):
+def test_smallest_gemm_shapes(mx, m, n, k):
     g = torch.Generator().manual_seed(m + n + k)
     x = torch.randn(m, k, generator=g).to(torch.bfloat16)
     w = (torch.randn(k, n, generator=g) * 0.1).to(torch.bfloat16)
@@ -70,7 +64,7 @@ def test_smallest_gemm_shapes(mx, kernel, m, n, k):
         assert_gemm_close(y, y_ref, t_ref, out)
 
 
-def test_gemm_with_no_rows_launches_nothing(mx, kernel):
+def test_gemm_with_no_rows_launches_nothing(mx):
     y = torch.full((8, 8), 3.0, device="cuda")
     codes = torch.zeros(8, 32, dtype=torch.uint8, device="cuda")
     scales = torch.zeros(512, dtype=torch.uint8, device="cuda")
@@ -80,7 +74,7 @@ def test_gemm_with_no_rows_launches_nothing(mx, kernel):
     assert (y == 3.0).all()
 
 
-def test_grouped_gemms_with_every_group_empty(mx, kernel):
+def test_grouped_gemms_with_every_group_empty(mx):
     """No tokens at all: the row-grouped GEMMs write nothing, the weight
     gradient writes zeros for every expert."""
     groups, n, k = 5, 128, 128
@@ -108,7 +102,7 @@ def test_grouped_gemms_with_every_group_empty(mx, kernel):
     assert int((dw != 0).sum()) == 0
 
 
-def test_largest_group_count(mx, kernel):
+def test_largest_group_count(mx):
     """1000 groups (the library's maximum), most of them empty, a few with
     ragged sizes: the device group table covers them all."""
     groups, n, k = 1000, 128, 64

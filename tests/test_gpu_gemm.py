@@ -22,21 +22,6 @@ def mx():
     return mx
 
 
-@pytest.fixture(params=[("128", "1"), ("256", "1"), ("128", "2"), ("256", "2"), ("256", "pair")],
-                ids=["bn128-c1", "bn256-c1", "bn128-c2", "bn256-c2", "pair"])
-def block_n(request, monkeypatch):
-    """The cta_group::2 block-pair kernel (the dense default), or the
-    one-block kernel with its tile width along N and cluster size (1, or 2 =
-    blocks sharing B by multicast)."""
-    monkeypatch.setenv("MX_GEMM_BLOCK_N", request.param[0])
-    if request.param[1] == "pair":
-        monkeypatch.setenv("MX_GEMM_PAIR", "1")
-    else:
-        monkeypatch.setenv("MX_GEMM_PAIR", "0")
-        monkeypatch.setenv("MX_GEMM_CLUSTER_M", request.param[1])
-    return int(request.param[0])
-
-
 def random_mx(rng, rows, k, fmt, lo=118, hi=136):
     t = O.decode_table(fmt)
     finite = np.array([c for c in range(256) if np.isfinite(t[c])], dtype=np.uint8)
@@ -52,7 +37,7 @@ SHAPES = [(128, 128, 128), (256, 256, 512), (200, 136, 96), (1, 8, 32), (300, 26
 @pytest.mark.parametrize("m,n,k", SHAPES)
 @pytest.mark.parametrize("fa,fb", [("e4m3", "e4m3"), ("e5m2", "e4m3"), ("e4m3", "e5m2"),
                                    ("e5m2", "e5m2")])
-def test_gemm_on_oracle_operands(mx, block_n, m, n, k, fa, fb):
+def test_gemm_on_oracle_operands(mx, m, n, k, fa, fb):
     """Oracle-quantized codes with non-uniform per-block scales fed straight
     to the GPU GEMM: pins descriptors, scale layout and the block-scaled sum."""
     rng = np.random.default_rng(m * 1000 + n + k)
@@ -66,7 +51,7 @@ def test_gemm_on_oracle_operands(mx, block_n, m, n, k, fa, fb):
 
 
 @pytest.mark.parametrize("m,n,k", [(128, 128, 128), (256, 384, 640), (77, 136, 4096)])
-def test_gemm_integer_case_is_bit_exact(mx, block_n, m, n, k):
+def test_gemm_integer_case_is_bit_exact(mx, m, n, k):
     """Codes of small integers with power-of-two scales: every partial sum
     is an integer multiple of a power of two far below 2^24, so FP32
     accumulation is exact in any order and the GPU must match exactly."""
@@ -110,7 +95,7 @@ def test_output_leading_dimension(mx):
     assert torch.isnan(big[:, :16]).all() and torch.isnan(big[:, 152:]).all()
 
 
-def test_pr1_reference_end_to_end(mx, block_n):
+def test_pr1_reference_end_to_end(mx):
     """The small reference configuration: X 256x512 with spikes and a 1e-3
     row, W 512x256; GPU quantize then GPU GEMM, FP32 out."""
     from mxfp8_block_scaled_mx_gb300 import workloads as W
@@ -235,7 +220,7 @@ def fused_error_ratio(y_gpu, out_ref, z_ref, t_ref, out_dtype):
 @pytest.mark.parametrize("m,n,k", [(128, 256, 256), (300, 264, 1056), (77, 520, 160)])
 @pytest.mark.parametrize("act", ["none", "silu"])
 @pytest.mark.parametrize("with_bias", [True, False])
-def test_fused_bias_act_epilogue(mx, block_n, m, n, k, act, with_bias):
+def test_fused_bias_act_epilogue(mx, m, n, k, act, with_bias):
     """The kernel contract's epilogue: act(acc + bias[col]) in FP32, one
     rounding to BF16 / FP32."""
     if not with_bias and act == "none":

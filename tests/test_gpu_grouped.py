@@ -17,20 +17,6 @@ def mx():
     return mx
 
 
-@pytest.fixture(params=[("256", "pair"), ("128", "1"), ("256", "1"), ("128", "2"), ("256", "2")],
-                ids=["pair", "bn128-c1", "bn256-c1", "bn128-c2", "bn256-c2"])
-def block_n(request, monkeypatch):
-    """The block-pair kernel (the default), or the one-block kernel with its
-    tile width along N and cluster size (1, or 2 = blocks sharing B)."""
-    monkeypatch.setenv("MX_GEMM_BLOCK_N", request.param[0])
-    if request.param[1] == "pair":
-        monkeypatch.setenv("MX_GEMM_PAIR", "1")
-    else:
-        monkeypatch.setenv("MX_GEMM_PAIR", "0")
-        monkeypatch.setenv("MX_GEMM_CLUSTER_M", request.param[1])
-    return int(request.param[0])
-
-
 def run_grouped(mx, sizes, n, k, out, seed=0, fa="e4m3", fb="e4m3"):
     offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
     groups, total = len(sizes), int(offsets[-1])
@@ -58,11 +44,11 @@ def run_grouped(mx, sizes, n, k, out, seed=0, fa="e4m3", fb="e4m3"):
 
 @pytest.mark.parametrize("sizes", [[0, 1, 31, 200, 0, 128, 129, 5], [300], [0, 0, 77],
                                    [1] * 9, [256, 0, 384]])
-def test_grouped_gemm_matches_oracle(mx, block_n, sizes):
+def test_grouped_gemm_matches_oracle(mx, sizes):
     run_grouped(mx, sizes, 256, 256, "bf16", seed=len(sizes))
 
 
-def test_grouped_gemm_fp32_long_k(mx, block_n):
+def test_grouped_gemm_fp32_long_k(mx):
     run_grouped(mx, [0, 3, 130, 64, 0, 250], 384, 1056, "fp32", seed=7)
 
 

@@ -20,20 +20,6 @@ def mx():
     return mx
 
 
-@pytest.fixture(params=[("256", "pair"), ("128", "1"), ("256", "1"), ("128", "2"), ("256", "2")],
-                ids=["pair", "bn128-c1", "bn256-c1", "bn128-c2", "bn256-c2"])
-def tiles(request, monkeypatch):
-    """The block-pair kernel (the default), or the one-block kernel with its
-    tile width along N and cluster size (1, or 2 = blocks sharing B)."""
-    monkeypatch.setenv("MX_GEMM_BLOCK_N", request.param[0])
-    if request.param[1] == "pair":
-        monkeypatch.setenv("MX_GEMM_PAIR", "1")
-    else:
-        monkeypatch.setenv("MX_GEMM_PAIR", "0")
-        monkeypatch.setenv("MX_GEMM_CLUSTER_M", request.param[1])
-    return request.param
-
-
 def offsets_of(sizes):
     return np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
 
@@ -143,11 +129,11 @@ def run_dgrad(mx, sizes, n_model, n_expert, out, seed=0):
 
 
 @pytest.mark.parametrize("sizes", [[0, 1, 31, 200, 0, 128, 129, 5], [300], [0, 0, 77]])
-def test_grouped_dgrad_bcat_matches_oracle(mx, tiles, sizes):
+def test_grouped_dgrad_bcat_matches_oracle(mx, sizes):
     run_dgrad(mx, sizes, 264, 256, "fp32", seed=len(sizes))
 
 
-def test_grouped_dgrad_bcat_bf16_long_k(mx, tiles):
+def test_grouped_dgrad_bcat_bf16_long_k(mx):
     run_dgrad(mx, [3, 0, 250, 64], 384, 1152, "bf16", seed=11)
 
 
@@ -178,11 +164,11 @@ def run_wgrad(mx, sizes, m, n, out, seed=0, ldq=None):
 
 @pytest.mark.parametrize("sizes", [[0, 1, 31, 33, 0, 100, 35], [300], [0, 0, 77], [1] * 9,
                                    [129, 0, 640]])
-def test_grouped_wgrad_matches_oracle(mx, tiles, sizes):
+def test_grouped_wgrad_matches_oracle(mx, sizes):
     run_wgrad(mx, sizes, 256, 264, "fp32", seed=len(sizes))
 
 
-def test_grouped_wgrad_bf16_and_ragged_m(mx, tiles):
+def test_grouped_wgrad_bf16_and_ragged_m(mx):
     run_wgrad(mx, [5, 0, 300, 40], 328, 128, "bf16", seed=13)
 
 
