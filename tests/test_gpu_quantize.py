@@ -136,6 +136,43 @@ def test_two_row_fixture_on_gpu_reproduces_page_scales(mx):
     check_row(mx, x, "e4m3", "floor")
 
 
+@pytest.mark.parametrize("variant", ["zero_small_row", "spike_in_small_row"])
+@pytest.mark.parametrize("rule", ["ceil", "floor"])
+def test_troubleshooting_fixtures_on_gpu(mx, variant, rule):
+    """The page's troubleshooting changes to the two-row fixture ("Troubleshooting
+    numerical failures"): the small row all zeros, or 500 in the small row's
+    block (x[0, 3] = 500), each projected by the original W and by a column
+    selecting only the spike (padded with zero columns to n = 16).  Codes
+    and scales bit-exact against the oracle; the projections are exact sums
+    of a few dyadic products, so the FP32 outputs must match exactly."""
+    small = [0.001, 0.03, 0.117, 0.5, 1.0, -0.25, 0.0625, -0.015625] * 4
+    large = [4.0, 16.0, 64.0, 500.0, -2.0, -8.0, -32.0, -250.0] * 4
+    x = torch.tensor([small, large], dtype=torch.float32)
+    if variant == "zero_small_row":
+        x[0] = 0.0
+    else:
+        x[0, 3] = 500.0
+    x = x.to(torch.bfloat16)
+    check_row(mx, x, "e4m3", rule)
+    w = torch.zeros(32, 16)
+    w[:, 1] = torch.tensor([0.5, -0.25, 0.125, -0.0625, 0.03125, -0.5, 0.25, -0.125] * 4)
+    w[3, 0] = 1.0                                   # the selector
+    w = w.to(torch.bfloat16)
+    check_col(mx, w, "e4m3", rule)
+    qx = mx.quantize(x.cuda(), "e4m3", "row", rule)
+    qw = mx.quantize(w.cuda(), "e4m3", "col", rule)
+    y = mx.gemm(qx, qw, "fp32").cpu().double().numpy()
+    ox, _ = oracle_quant(x, "e4m3", "row", rule)
+    ow, _ = oracle_quant(w, "e4m3", "col", rule)
+    y_ref, _ = O.gemm(ox, ow)
+    assert np.array_equal(y, y_ref)
+    spike = 512.0 if rule == "ceil" else 448.0
+    small_sel = 0.0 if variant == "zero_small_row" else spike
+    assert y[:, 0].tolist() == [small_sel, spike]
+    assert (y[:, 2:] == 0).all()
+    assert mx.device_status() == 0
+
+
 def test_pr1_reference_inputs(mx):
     from mxfp8_block_scaled_mx_gb300 import workloads as W
     x, w = W.pr1_reference()

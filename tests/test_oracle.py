@@ -315,6 +315,97 @@ def test_two_row_experiment_floor_rule_saturates_spike(golden_dir):
     assert y.ravel().tolist() == [0.6015625, 23.75]
 
 
+# The three changes to the two-row fixture proposed in "Troubleshooting
+# numerical failures" (same page).  The page prints no numbers for them;
+# every expected value below is derived by hand from the format grid and
+# the two scale rules, not by the oracle.
+#  (1) the small row all zeros;
+#  (2) 500 moved into the small row's (only) 32-value group: the reading
+#      taken is x[0, 3] := 500, replacing the 0.5 at the column where the
+#      spike sits in the large row; the large row is left as it is;
+#  (3) W replaced by a column that selects only the spike (column 3).
+
+def selector_w():
+    sel = np.zeros((32, 1))
+    sel[3, 0] = 1.0
+    return sel
+
+
+@pytest.mark.parametrize("rule", ["ceil", "floor"])
+def test_troubleshooting_zero_small_row(golden_dir, rule):
+    g = load(golden_dir, "two_row_fixture.json")
+    x, w = two_row_fixture(g)
+    x[0, :] = 0.0
+    qx = O.quantize(x, "e4m3", "row", rule=rule)
+    # an all-zero block takes S = 1 (byte 127) and every code is +0
+    assert qx.scales[0, 0] == 127 and not qx.codes[0].any()
+    # the spike row keeps its scale: 2 (ceil) or 1 (floor)
+    assert O.decode_e8m0(int(qx.scales[1, 0])) == (2.0 if rule == "ceil" else 1.0)
+    y, t = O.gemm(qx, O.quantize(w, "e4m3", "col", rule=rule))
+    # nothing to lose in row 0: its projection is exactly 0
+    assert y[0, 0] == 0.0 and t[0, 0] == 0.0
+    assert y[1, 0] == (7.75 if rule == "ceil" else 23.75)
+
+
+# Reconstructed small row (one period of the 8-value pattern) after 500
+# joins its block, worked out by hand:
+#  ceil rule: S = 2^ceil(log2(500/448)) = 2; 0.001/2 = 0.0005 is below half
+#    the smallest subnormal 2^-9, so it becomes 0; 0.03/2 = 0.015 rounds to
+#    2^-6 (8 subnormal steps of 2^-9); 0.117/2 = 0.0585 rounds to 15 * 2^-8;
+#    500/2 = 250 rounds to 256 (spacing 16 in [128, 256)); the rest are
+#    exact multiples of their spacing.
+#  floor rule: S = 2^(floor(log2 500) - 8) = 1; 0.001 is above 2^-10, so it
+#    becomes 2^-9; 0.03 rounds to 15 * 2^-9; 0.117 to 15 * 2^-7; 500
+#    saturates to 448.
+SPIKED_SMALL_ROW = {
+    "ceil": (2.0, [0.0, 2 * 2.0 ** -6, 2 * 15 * 2.0 ** -8, 512.0,
+                   1.0, -0.25, 0.0625, -0.015625]),
+    "floor": (1.0, [2.0 ** -9, 15 * 2.0 ** -9, 15 * 2.0 ** -7, 448.0,
+                    1.0, -0.25, 0.0625, -0.015625]),
+}
+
+
+@pytest.mark.parametrize("rule", ["ceil", "floor"])
+def test_troubleshooting_spike_moved_into_small_row(golden_dir, rule):
+    g = load(golden_dir, "two_row_fixture.json")
+    x, w = two_row_fixture(g)
+    x[0, 3] = 500.0
+    qx = O.quantize(x, "e4m3", "row", rule=rule)
+    scale, period = SPIKED_SMALL_ROW[rule]
+    assert O.decode_e8m0(int(qx.scales[0, 0])) == scale
+    xh = O.dequantize(qx)
+    assert xh[0, :8].tolist() == period
+    # columns 11, 19, 27 still hold the pattern's 0.5 (exact under either scale)
+    assert xh[0, 8:].tolist() == (period[:3] + [0.5] + period[4:]) * 3
+    # the page's lesson: 0.001 shares a scale with 500 and loses its precision
+    # (original fixture, ceil rule: 0.00097656, 2.3 % off)
+    assert abs(xh[0, 0] - 0.001) / 0.001 > 0.9
+    # the large row is untouched
+    assert np.array_equal(qx.codes[1], O.quantize(two_row_fixture(g)[0], "e4m3", "row",
+                                                   rule=rule).codes[1])
+    # the selector exposes the spike's reconstruction in both rows
+    ys, _ = O.gemm(qx, O.quantize(selector_w(), "e4m3", "col", rule=rule))
+    spike = 512.0 if rule == "ceil" else 448.0
+    assert ys.ravel().tolist() == [spike, spike]
+
+
+@pytest.mark.parametrize("rule", ["ceil", "floor"])
+def test_troubleshooting_selector_column(golden_dir, rule):
+    """The selector column quantizes exactly (amax 1: S = 2^-8 under both
+    rules, 1/S = 256 on the grid) and returns column 3 of X-hat: the page
+    prints [0.5, 512] for the ceil rule; the floor rule saturates to 448."""
+    g = load(golden_dir, "two_row_fixture.json")
+    x, _ = two_row_fixture(g)
+    qs = O.quantize(selector_w(), "e4m3", "col", rule=rule)
+    assert O.decode_e8m0(int(qs.scales[0, 0])) == 2.0 ** -8
+    assert O.dequantize(qs).ravel().tolist() == selector_w().ravel().tolist()
+    ys, _ = O.gemm(O.quantize(x, "e4m3", "row", rule=rule), qs)
+    if rule == "ceil":
+        assert ys.ravel().tolist() == g["ceil_rule"]["selector_mx"]
+    else:
+        assert ys.ravel().tolist() == [0.5, 448.0]
+
+
 # ---------------------------------------------------------------- GEMM
 
 def int_operands(rng, rows, k, fmt, lim):
