@@ -53,23 +53,40 @@ def read_peaks():
 
 # ---------------------------------------------------------------- clocks
 
-CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+def _sample_time(field: str):
+    """Host epoch seconds of an nvidia-smi timestamp ("2026/12/03 05:29:22.123"),
+    or None."""
+    try:
+        day, clock = field.strip().split(" ")
+        hms, _, frac = clock.partition(".")
+        t = time.mktime(time.strptime(f"{day} {hms}", "%Y/%m/%d %H:%M:%S"))
+        return t + (float("0." + frac) if frac else 0.0)
+    except ValueError:
+        return None
 
 
 class ClockSampler:
-    """nvidia-smi sampling every 100 ms while the timed region runs."""
+    """nvidia-smi sampling (every `period_ms`) while the timed regions run.
+    Every sample carries nvidia-smi's timestamp, so a measurement can take
+    the median SM clock of the samples inside its own host-time window."""
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 100):
         self.gpu = gpu_index
+        self.period_ms = period_ms
         self.proc = None
+        self.lines = []
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={CLOCK_FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -89,21 +106,39 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
         return False
 
-    def summary(self):
+    @staticmethod
+    def _parse(line: str):
+        """(epoch seconds or None, sm MHz, max MHz, active reasons) or None."""
+        parts = [p.strip() for p in line.split(",")]
+        t = None
+        if parts and "/" in parts[0]:          # leading timestamp field
+            t = _sample_time(parts[0])
+            parts = parts[1:]
+        if len(parts) < 9:
+            return None
+        try:
+            sm, mx_ = float(parts[1]), float(parts[2])
+        except ValueError:
+            return None
+        reasons = {name for name, val in zip(REASONS, parts[5:9])
+                   if val.lower() in ("active", "0x1", "1", "yes")}
+        return t, sm, mx_, reasons
+
+    def summary(self, t0: float | None = None, t1: float | None = None):
+        """Median SM clock under load (samples at >= half the highest one),
+        highest max clock and the throttle reasons seen; with t0, t1 (host
+        epoch seconds) only the samples inside that window."""
         sm, mx_, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in getattr(self, "lines", []):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+        for line in self.lines:
+            rec = self._parse(line)
+            if rec is None:
                 continue
-            try:
-                sm.append(float(parts[1]))
-                mx_.append(float(parts[2]))
-            except ValueError:
+            t, s_, m_, r_ = rec
+            if t0 is not None and (t is None or t < t0 or t > t1):
                 continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() in ("active", "0x1", "1", "yes"):
-                    reasons.add(name)
+            sm.append(s_)
+            mx_.append(m_)
+            reasons |= r_
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         busy = [s for s in sm if s >= 0.5 * max(sm)] or sm
@@ -188,71 +223,153 @@ class ForwardLayer:
     launches_per_step = 3
 
 
-# Per-row kernel timings: warm-up launches, then the median of this many
-# timed launches.
+# Per-row kernel timings: warm-up launches, then the median of timed
+# launches; each row's timed region lasts at least ROW_SECONDS so that
+# several clock samples fall inside it.
 ROW_WARMUP = 10
 ROW_REPS = 50
+ROW_MAX_REPS = 4000
+ROW_SECONDS = 0.25
+SM_MAX_MHZ = 2070.0
 
 
-def time_kernel(fn, stream, reps: int, warmup: int = ROW_WARMUP) -> float:
-    """Mean duration (ms) of fn() over reps launches, CUDA events on `stream`."""
+def _reps_for(one_ms: float, reps: int | None) -> int:
+    if reps is not None:
+        return reps
+    return int(min(ROW_MAX_REPS, max(ROW_REPS, ROW_SECONDS * 1e3 / max(one_ms, 1e-4))))
+
+
+def _estimate_ms(fn, stream) -> float:
     import torch
-    for _ in range(warmup):
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(5):
         fn()
+    b.record(stream)
     torch.cuda.synchronize()
-    times = []
-    for _ in range(reps):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        fn()
-        b.record(stream)
-        times.append((a, b))
-    torch.cuda.synchronize()
-    return statistics.median(a.elapsed_time(b) for a, b in times)
+    return a.elapsed_time(b) / 5
 
 
-def flush_l2(buf):
-    buf.add_(1)
-
-
-def time_after_flush(fn, stream, scrub, reps: int = ROW_REPS, read_pass=None):
-    """Median duration (ms) of fn() launched right behind an L2 flush on the
-    same stream: `scrub` (a buffer larger than L2) is written, then, with
-    `read_pass`, a second such buffer is read, so that the flush's dirty
-    lines go back to HBM before the timed launch instead of during it.
-    Flush and launch are enqueued back to back with no host synchronization
-    between them, so the host's launch latency is not timed."""
+def timed_launches(fn, stream, reps: int | None = None, warmup: int = ROW_WARMUP, pre=None):
+    """Median duration (ms) of fn() over timed launches, each between two
+    CUDA events on `stream`, and the host-time window (epoch seconds) of the
+    timed region.  `pre` (e.g. an L2 flush) is enqueued before each launch,
+    outside its events; nothing synchronizes the host between `pre`, the
+    launch and the events, so the host's launch latency is not timed."""
     import torch
-    for _ in range(ROW_WARMUP):
-        fn()
-    torch.cuda.synchronize()
-    events = []
     with torch.cuda.stream(stream):
-        for _ in range(reps):
-            flush_l2(scrub)
-            if read_pass is not None:
-                read_pass.sum()
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        n = _reps_for(_estimate_ms(fn, stream) + (_estimate_ms(pre, stream) if pre else 0.0),
+                      reps)
+        events = []
+        t0 = time.time()
+        for _ in range(n):
+            if pre is not None:
+                pre()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
             b.record(stream)
             events.append((a, b))
-    torch.cuda.synchronize()
-    return statistics.median(a.elapsed_time(b) for a, b in events)
+        torch.cuda.synchronize()
+        t1 = time.time()
+    return statistics.median(a.elapsed_time(b) for a, b in events), (t0, t1)
 
 
-def bandwidth_row(fn, stream, scrub, clean, nbytes: float, hbm: float, bpe: float) -> dict:
-    """A bandwidth row: timed after the write flush, and after the write
-    flush plus a read pass (clean L2)."""
-    t = time_after_flush(fn, stream, scrub)
-    tc = time_after_flush(fn, stream, scrub, read_pass=clean)
+def time_kernel(fn, stream, reps: int | None = ROW_REPS, warmup: int = ROW_WARMUP) -> float:
+    """Median duration (ms) of fn() over reps launches, CUDA events on `stream`."""
+    return timed_launches(fn, stream, reps, warmup)[0]
+
+
+def timed_graph(call, nbuf: int, stream, launches: int):
+    """Steady-state duration (ms) per launch: `launches` calls (call(i) runs
+    on `stream` with buffer set i % nbuf) captured in one CUDA graph and
+    replayed, timed by CUDA events around the replays.  Consecutive launches
+    touch different buffer sets totalling more than four times the L2, so
+    every launch reads its input from HBM."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(nbuf):
+            call(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(launches):
+                call(i % nbuf)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        one = a.elapsed_time(b)
+        n = int(min(200, max(3, ROW_SECONDS * 1e3 / max(one, 1e-3))))
+        t0 = time.time()
+        a.record(stream)
+        for _ in range(n):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+    del g
+    return a.elapsed_time(b) / (n * launches), (t0, t1)
+
+
+class RowClocks:
+    """The host-time window of every row's timed region; once the clock
+    sampler has stopped, each row gets the median SM clock of the samples
+    in its window and its throughput scaled to the maximum SM clock."""
+
+    def __init__(self):
+        self.windows = []
+
+    def mark(self, row: dict, window, key: str):
+        self.windows.append((row, window, key))
+
+    def fill(self, sampler):
+        for row, (t0, t1), key in self.windows:
+            c = sampler.summary(t0, t1)
+            row["sm_mhz_median"] = c["sm_mhz"]
+            row["clock_samples"] = c["samples"]
+            if c["sm_mhz"] and key in row:
+                row["clock_normalized"] = {
+                    key: round(row[key] * SM_MAX_MHZ / c["sm_mhz"], 1),
+                    "def": f"{key} x {SM_MAX_MHZ:.0f} / median SM MHz of the row"}
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def bandwidth_row(fn, stream, scrub, clean, nbytes: float, hbm: float, bpe: float,
+                  clocks: RowClocks, steady=None) -> dict:
+    """A bandwidth row: one launch timed right behind an L2 write flush, and
+    behind the write flush plus a read pass (clean L2); with `steady`
+    (call(i), buffer sets, launches per graph), also the steady-state time
+    per launch of back-to-back launches over rotating buffers."""
+    t, win = timed_launches(fn, stream, pre=lambda: flush_l2(scrub))
+    tc, _ = timed_launches(fn, stream, pre=lambda: (flush_l2(scrub), clean.sum()))
     gbs = nbytes / (t * 1e-3) / 1e9
     gbc = nbytes / (tc * 1e-3) / 1e9
-    return {"ms": round(t, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3),
-            "bytes_per_elem": bpe,
-            "clean_l2": {"ms": round(tc, 4), "GB/s": round(gbc, 1), "frac_hbm": round(gbc / hbm, 3)}}
+    row = {"ms": round(t, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3),
+           "bytes_per_elem": bpe,
+           "clean_l2": {"ms": round(tc, 4), "GB/s": round(gbc, 1), "frac_hbm": round(gbc / hbm, 3)}}
+    if steady is not None:
+        call, nbuf, launches = steady
+        ts, _ = timed_graph(call, nbuf, stream, launches)
+        gss = nbytes / (ts * 1e-3) / 1e9
+        row["steady"] = {"ms": round(ts, 4), "GB/s": round(gss, 1), "frac_hbm": round(gss / hbm, 3),
+                         "form": f"CUDA graph of {launches} launches over {nbuf} buffer sets "
+                                 "(> 4x L2), replayed; time per launch"}
+    clocks.mark(row, win, "GB/s")
+    return row
 
 
 # ---------------------------------------------------------------- per-row measurements
@@ -298,8 +415,23 @@ def with_roofline(row: dict, roof: dict) -> dict:
     return row
 
 
-def measure_rows(mx, peaks, dev, stream):
-    """Per-kernel measurements of the other hot-path rows (rank 0, N=1)."""
+def measure_rows(mx, peaks, dev, stream, local: int = 0):
+    """Per-kernel measurements of the other hot-path rows (rank 0, N=1), with
+    the SM clock sampled during each row."""
+    import torch
+    with ClockSampler(local, period_ms=50) as sampler:
+        clocks = RowClocks()
+        out = _measure_rows(mx, peaks, dev, stream, clocks)
+    clocks.fill(sampler)
+    return out
+
+
+def _gemm_row(fl: float, t: float, fp8_peak: float) -> dict:
+    return {"ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
+            "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
+
+
+def _measure_rows(mx, peaks, dev, stream, clocks: RowClocks):
     import torch
     from mxfp8_block_scaled_mx_gb300 import workloads as W
     h = int(stream.cuda_stream)
@@ -308,32 +440,73 @@ def measure_rows(mx, peaks, dev, stream):
     fp8_peak = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
     scrub = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     clean = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
 
-    # quantize bandwidth sweep: 4096x4096 (fits in L2: flush between runs) and 16384x8192
+    def gemm_row(name, fn, fl, extra=None):
+        t, win = timed_launches(fn, stream)
+        row = _gemm_row(fl, t, fp8_peak)
+        if extra:
+            row.update(extra)
+        clocks.mark(row, win, "TFLOP/s")
+        out[name] = row
+        return row
+
+    # quantize bandwidth sweep: 4096x4096 and 16384x8192.  Each launch is
+    # timed alone right behind an L2 write flush (and behind a flush plus a
+    # read pass), and back to back over rotating buffer sets in a CUDA graph.
     for (r, c), seed in (((4096, 4096), 0), ((16384, 8192), 1)):
-        x = W.quantize_sweep((r, c), seed=seed, device=dev)
-        qr = torch.empty((r, c), dtype=torch.uint8, device=dev)
-        sr = torch.empty(mx.mx_scale_bytes(r, c), dtype=torch.uint8, device=dev)
+        set_bytes = r * c * 2 + r * c + mx.mx_scale_bytes(r, c)
+        nbuf = max(2, -(-4 * l2_bytes // set_bytes) + 1)
+        xs = [W.quantize_sweep((r, c), seed=seed, device=dev)]
+        xs += [xs[0].roll(i, 0) for i in range(1, nbuf)]          # distinct buffers, same data
+        x = xs[0]
+        qrs = [torch.empty((r, c), dtype=torch.uint8, device=dev) for _ in range(nbuf)]
+        srs = [torch.empty(mx.mx_scale_bytes(r, c), dtype=torch.uint8, device=dev) for _ in range(nbuf)]
+        qr, sr = qrs[0], srs[0]
         qc = torch.empty((c, r), dtype=torch.uint8, device=dev)
         sc = torch.empty(mx.mx_scale_bytes(c, r), dtype=torch.uint8, device=dev)
         for mode, axis, bpe in (("row", 1, 3.03125), ("col", 2, 3.03125), ("both", 3, 4.0625)):
-            def q():
+            def q(axis=axis):
                 st = mx.mx_quantize(x.data_ptr(), 0, r, c, c, 0, axis, 0,
                                     qr.data_ptr() if axis & 1 else None,
                                     sr.data_ptr() if axis & 1 else None,
                                     qc.data_ptr() if axis & 2 else None,
                                     sc.data_ptr() if axis & 2 else None, h)
                 assert st == 0
+            steady = None
+            if mode == "row":
+                def qi(i):
+                    st = mx.mx_quantize(xs[i].data_ptr(), 0, r, c, c, 0, 1, 0, qrs[i].data_ptr(),
+                                        srs[i].data_ptr(), None, None, h)
+                    assert st == 0
+                steady = (qi, nbuf, 4 * nbuf)
             out[f"quantize_{r}x{c}_{mode}"] = bandwidth_row(q, stream, scrub, clean,
-                                                            r * c * bpe, hbm, bpe)
+                                                            r * c * bpe, hbm, bpe, clocks, steady)
         if (r, c) == (16384, 8192):
+            # the page's conservative (ceil) scale rule, rowwise E4M3
+            def qceil():
+                st = mx.mx_quantize(x.data_ptr(), 0, r, c, c, 0, 1, 1, qr.data_ptr(),
+                                    sr.data_ptr(), None, None, h)
+                assert st == 0
+            out[f"quantize_{r}x{c}_row_ceil"] = bandwidth_row(qceil, stream, scrub, clean,
+                                                              r * c * 3.03125, hbm, 3.03125, clocks)
             # MXFP4 codes (E2M1, 16-element containers: one byte per element)
             def q4():
                 st = mx.mx_quantize(x.data_ptr(), 0, r, c, c, 4, 1, 0, qr.data_ptr(),
                                     sr.data_ptr(), None, None, h)
                 assert st == 0
             out[f"quantize_{r}x{c}_row_e2m1"] = bandwidth_row(q4, stream, scrub, clean,
-                                                              r * c * 3.03125, hbm, 3.03125)
+                                                              r * c * 3.03125, hbm, 3.03125, clocks)
+            # the same codes in packed storage (two per byte): 2 + 1/2 + 1/32 B per element
+            q4p_codes = torch.empty((r, c // 2), dtype=torch.uint8, device=dev)
+
+            def q4p():
+                st = mx.mx_quantize(x.data_ptr(), 0, r, c, c, 7, 1, 0, q4p_codes.data_ptr(),
+                                    sr.data_ptr(), None, None, h)
+                assert st == 0
+            out[f"quantize_{r}x{c}_row_e2m1_packed"] = bandwidth_row(
+                q4p, stream, scrub, clean, r * c * 2.53125, hbm, 2.53125, clocks)
+            del q4p_codes
             # stochastic rounding (E5M2, the gradient format): the 16-bit
             # random draws are an input, +2 bytes per element
             rb = W.random_bits16((r, c), seed=11, device=dev)
@@ -343,52 +516,46 @@ def measure_rows(mx, peaks, dev, stream):
                                        qr.data_ptr(), sr.data_ptr(), None, None, h)
                 assert st == 0
             out[f"quantize_{r}x{c}_row_sr_e5m2"] = bandwidth_row(qsr, stream, scrub, clean,
-                                                                 r * c * 5.03125, hbm, 5.03125)
+                                                                 r * c * 5.03125, hbm, 5.03125,
+                                                                 clocks)
             del rb
-        del x, qr, sr, qc, sc
+        del x, xs, qr, sr, qrs, srs, qc, sc
 
-    # backward GEMMs (FP32 out), the fused bias+SiLU forward, the MoE grouped GEMM
+    # backward GEMMs (FP32 out), the fused bias+SiLU forward, MXFP4/6 operands
     x, w = W.dense_forward(device=dev)
     xq = mx.quantize(x, "e4m3", "row", stream=stream)
     wq = mx.quantize(w, "e4m3", "col", stream=stream)
     bias = torch.randn(w.shape[1], device=dev, dtype=torch.float32)
     yf = torch.empty((x.shape[0], w.shape[1]), dtype=torch.bfloat16, device=dev)
-    t = time_kernel(lambda: mx.gemm(xq, wq, "bf16", out=yf, stream=stream, bias=bias, act="silu"),
-                    stream, ROW_REPS)
     fl = 2 * x.shape[0] * w.shape[1] * x.shape[1]
-    out["forward_bias_silu_16384x18432x7168_bf16"] = {
-        "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
-        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
+    gemm_row("forward_16384x18432x7168_bf16",
+             lambda: mx.gemm(xq, wq, "bf16", out=yf, stream=stream), fl)
+    gemm_row("forward_bias_silu_16384x18432x7168_bf16",
+             lambda: mx.gemm(xq, wq, "bf16", out=yf, stream=stream, bias=bias, act="silu"), fl)
     del xq, wq, bias
-    # MXFP4 (E2M1) weights and MXFP6 (E3M2) operands through the same MMA
     for tag, fa, fb in (("mxfp4_weights_e4m3xe2m1", "e4m3", "e2m1"),
+                        ("mxfp4_packed_weights_e4m3xe2m1", "e4m3", "e2m1_packed"),
                         ("mxfp6_e3m2xe3m2", "e3m2", "e3m2")):
         xq = mx.quantize(x, fa, "row", stream=stream)
         wq = mx.quantize(w, fb, "col", stream=stream)
-        t = time_kernel(lambda: mx.gemm(xq, wq, "bf16", out=yf, stream=stream), stream, ROW_REPS)
-        out[f"forward_{tag}_16384x18432x7168_bf16"] = {
-            "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
-            "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
+        gemm_row(f"forward_{tag}_16384x18432x7168_bf16",
+                 lambda: mx.gemm(xq, wq, "bf16", out=yf, stream=stream), fl)
         del xq, wq
     del yf
     dy = W.dense_grad_output(device=dev)
     rq = mx.quantize(dy, "e5m2", "row", stream=stream)
     wq = mx.quantize(w, "e4m3", "row", stream=stream)
     dx = torch.empty((dy.shape[0], w.shape[0]), dtype=torch.float32, device=dev)
-    t = time_kernel(lambda: mx.gemm(rq, wq, "fp32", out=dx, stream=stream), stream, ROW_REPS)
-    fl = 2 * dy.shape[0] * w.shape[0] * dy.shape[1]
-    out["dgrad_16384x7168x18432_e5m2xe4m3_fp32"] = {
-        "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
-        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
+    gemm_row("dgrad_16384x7168x18432_e5m2xe4m3_fp32",
+             lambda: mx.gemm(rq, wq, "fp32", out=dx, stream=stream),
+             2 * dy.shape[0] * w.shape[0] * dy.shape[1])
     del rq, wq, dx
     xq = mx.quantize(x, "e4m3", "col", stream=stream)
     dq = mx.quantize(dy, "e5m2", "col", stream=stream)
     dw = torch.empty((x.shape[1], dy.shape[1]), dtype=torch.float32, device=dev)
-    t = time_kernel(lambda: mx.gemm(xq, dq, "fp32", out=dw, stream=stream), stream, ROW_REPS)
-    fl = 2 * x.shape[1] * dy.shape[1] * x.shape[0]
-    out["wgrad_7168x18432x16384_e4m3xe5m2_fp32"] = {
-        "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
-        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
+    gemm_row("wgrad_7168x18432x16384_e4m3xe5m2_fp32",
+             lambda: mx.gemm(xq, dq, "fp32", out=dw, stream=stream),
+             2 * x.shape[1] * dy.shape[1] * x.shape[0])
     del xq, dq, dw, x, w, dy
 
     xm, wm, offsets = W.moe_inputs(device=dev)
@@ -398,25 +565,25 @@ def measure_rows(mx, peaks, dev, stream):
     qw = mx.quantize(wm.view(e * n, k), "e4m3", "row", stream=stream)
     qb = mx.MxTensor(qw.codes.view(e, n, k), qw.scales, "e4m3")
     ym = torch.empty((xm.shape[0], n), dtype=torch.bfloat16, device=dev)
-    t = time_kernel(lambda: mx.grouped_gemm(qa, d_off, qb, "bf16", out=ym, stream=stream),
-                    stream, ROW_REPS)
     fl = 2 * xm.shape[0] * n * k
     sizes = [int(v) for v in (offsets[1:] - offsets[:-1])]
-    out["moe_grouped_64x(2048x7168)_65536tok_bf16"] = with_roofline({
-        "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
-        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3),
-        "group_sizes_min_max": [min(sizes), max(sizes)], "empty_groups": sizes.count(0)},
-        moe_roofline(sizes, n, k, "forward", fp8_peak, hbm))
+    row = gemm_row("moe_grouped_64x(2048x7168)_65536tok_bf16",
+                   lambda: mx.grouped_gemm(qa, d_off, qb, "bf16", out=ym, stream=stream), fl,
+                   {"group_sizes_min_max": [min(sizes), max(sizes)],
+                    "empty_groups": sizes.count(0)})
+    with_roofline(row, moe_roofline(sizes, n, k, "forward", fp8_peak, hbm))
+
     # grouped rowwise quantize into the buffers above (the C call: no
-    # allocation inside the timed launches)
+    # allocation inside the timed launches; inputs 940 MB, larger than L2)
     def qrow():
         st = mx.mx_quantize_grouped(xm.data_ptr(), 0, xm.shape[0], k, k, 0, 0, e,
                                     d_off.data_ptr(), qa.codes.data_ptr(), qa.scales.data_ptr(), h)
         assert st == 0
-    t = time_kernel(qrow, stream, ROW_REPS)
+    t, win = timed_launches(qrow, stream)
     gbs = xm.numel() * 3.03125 / (t * 1e-3) / 1e9
-    out["moe_quantize_grouped_65536x7168"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
-                                              "frac_hbm": round(gbs / hbm, 3)}
+    row = {"ms": round(t, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
+    clocks.mark(row, win, "GB/s")
+    out["moe_quantize_grouped_65536x7168"] = row
     del ym, qa
 
     # mixture-of-experts backward: dX_g = dY_g W_g^T (experts side by side
@@ -426,23 +593,18 @@ def measure_rows(mx, peaks, dev, stream):
     qa = mx.quantize_grouped(dym, d_off, "e5m2", stream=stream)
     qb = mx.quantize(wm.view(e * n, k), "e4m3", "col", stream=stream)
     dx = torch.empty((total, k), dtype=torch.float32, device=dev)
-    t = time_kernel(lambda: mx.grouped_gemm_bcat(qa, d_off, qb, "fp32", out=dx, stream=stream),
-                    stream, ROW_REPS)
-    out["moe_dgrad_64x(7168x2048)_65536tok_fp32"] = with_roofline({
-        "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
-        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)},
-        moe_roofline(sizes, n, k, "dgrad", fp8_peak, hbm))
+    row = gemm_row("moe_dgrad_64x(7168x2048)_65536tok_fp32",
+                   lambda: mx.grouped_gemm_bcat(qa, d_off, qb, "fp32", out=dx, stream=stream), fl)
+    with_roofline(row, moe_roofline(sizes, n, k, "dgrad", fp8_peak, hbm))
     del qa, qb, dx
     ldq = mx.mx_grouped_cols_capacity(total, e)
     qa = mx.quantize_grouped(dym, d_off, "e5m2", axis="col", ldq=ldq, stream=stream)
     qb = mx.quantize_grouped(xm, d_off, "e4m3", axis="col", ldq=ldq, stream=stream)
     dw = torch.empty((e, n, k), dtype=torch.float32, device=dev)
-    t = time_kernel(lambda: mx.grouped_gemm_wgrad(qa, d_off, qb, total, "fp32", out=dw,
-                                                  stream=stream), stream, ROW_REPS)
-    out["moe_wgrad_64x(2048x7168)_65536tok_fp32"] = with_roofline({
-        "ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
-        "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)},
-        moe_roofline(sizes, n, k, "wgrad", fp8_peak, hbm))
+    row = gemm_row("moe_wgrad_64x(2048x7168)_65536tok_fp32",
+                   lambda: mx.grouped_gemm_wgrad(qa, d_off, qb, total, "fp32", out=dw,
+                                                 stream=stream), fl)
+    with_roofline(row, moe_roofline(sizes, n, k, "wgrad", fp8_peak, hbm))
     del dw
 
     # grouped columnwise quantize of X (per-expert token blocks), into the
@@ -452,10 +614,11 @@ def measure_rows(mx, peaks, dev, stream):
                                        None, None, qb.codes.data_ptr(), ldq,
                                        qb.scales.data_ptr(), h)
         assert st == 0
-    t = time_kernel(qcol, stream, ROW_REPS)
+    t, win = timed_launches(qcol, stream)
     gbs = xm.numel() * 3.03125 / (t * 1e-3) / 1e9
-    out["moe_quantize_grouped_cols_65536x7168"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
-                                                   "frac_hbm": round(gbs / hbm, 3)}
+    row = {"ms": round(t, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
+    clocks.mark(row, win, "GB/s")
+    out["moe_quantize_grouped_cols_65536x7168"] = row
     return out
 
 
@@ -485,6 +648,65 @@ def oracle_sample(rows: int = 4096, cols: int = 4096):
 
 def cpu_threads():
     return os.cpu_count() or 1
+
+
+def oracle_parts(gemm_rows: int, quant: bool = True) -> dict:
+    """The oracle's pieces timed on the host: quantization of the full
+    4096x4096 tensor of the quantize sweep (rowwise and columnwise, GB/s on
+    the algorithmic 3.03125 B/element), and the block-scaled GEMM of a
+    `gemm_rows`-row slice of the forward layer (full N = 18432, K = 7168)
+    with its time extrapolated to all 16384 rows."""
+    import numpy as np
+    from mxfp8_block_scaled_mx_gb300 import workloads as W
+    from oracle import mx_oracle as O
+    out = {}
+    if quant:
+        x = W.quantize_sweep((4096, 4096), seed=0).float().double().numpy()
+        for axis in ("row", "col"):
+            t0 = time.perf_counter()
+            O.quantize(x, "e4m3", axis)
+            dt = time.perf_counter() - t0
+            out[f"quantize_4096x4096_{axis}_GB/s"] = round(4096 * 4096 * 3.03125 / dt / 1e9, 4)
+    m, n, k = FWD["m"], FWD["n"], FWD["k"]
+    rng = np.random.default_rng(5)
+    # operands of the layer's formats and block structure (E4M3 codes with
+    # per-block scales near 2^0); the GEMM's cost does not depend on the values
+    fin = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    a = O.MxBlocks(rng.choice(fin, (gemm_rows, k)), rng.integers(120, 134, (gemm_rows, k // 32),
+                                                                 dtype=np.uint8), O.FORMATS["e4m3"])
+    b = O.MxBlocks(rng.choice(fin, (n, k)), rng.integers(120, 134, (n, k // 32), dtype=np.uint8),
+                   O.FORMATS["e4m3"])
+    t0 = time.perf_counter()
+    O.gemm(a, b)
+    dt = time.perf_counter() - t0
+    out["gemm_slice"] = f"{gemm_rows}x{n}x{k}"
+    out["gemm_slice_s"] = round(dt, 3)
+    out["gemm_TFLOP/s"] = round(2 * gemm_rows * n * k / dt / 1e12, 6)
+    out["gemm_full_16384_rows_s_extrapolated"] = round(dt * m / gemm_rows, 1)
+    return out
+
+
+def oracle_one_thread() -> dict:
+    """oracle_parts in a child process limited to one thread (BLAS and
+    OpenMP pools of one), on a smaller GEMM slice."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               NUMEXPR_NUM_THREADS="1")
+    res = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-one-thread"],
+                         capture_output=True, text=True, env=env, timeout=600)
+    if res.returncode != 0:
+        return {"error": res.stderr.strip().splitlines()[-1:] or ["failed"]}
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline_record() -> dict:
+    """The reported CPU baseline: the oracle, as it stands, on bounded
+    samples (about half a minute of host work in all)."""
+    v, dt, desc = oracle_sample(2048, 4096)
+    rec = {"value": v, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle", "sample": desc,
+           "seconds": round(dt, 2)}
+    rec["all_threads"] = dict(oracle_parts(128), threads=cpu_threads())
+    rec["one_thread"] = dict(oracle_one_thread(), threads=1)
+    return rec
 
 
 # ---------------------------------------------------------------- main arms
@@ -706,7 +928,7 @@ def run_gpu(args):
         rows = None
         if rank == 0 and world == 1 and not args.no_rows:
             del hx, hw, hy
-            rows = measure_rows(mx, peaks, dev, stream)
+            rows = measure_rows(mx, peaks, dev, stream, local)
 
     if rank != 0:
         return 0
@@ -754,9 +976,7 @@ def run_gpu(args):
     if rows is not None:
         line["rows"] = rows
     if world == 1 and not args.no_cpu_baseline:
-        v, dt, desc = oracle_sample()
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                                "sample": desc, "seconds": round(dt, 2)}
+        line["cpu_baseline"] = cpu_baseline_record()
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -772,7 +992,11 @@ def main(argv=None):
     ap.add_argument("--impl", default="mx", choices=["mx", "reference"])
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row extra kernels")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-one-thread", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
+    if args.oracle_one_thread:
+        print(json.dumps(oracle_parts(16)), flush=True)
+        return 0
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -84,12 +84,26 @@ typedef enum {
  * bitfields".  FP8 (OCP OFP8): E4M3 max 448, no Inf, NaN 0x7F/0xFF; E5M2
  * max 57344, IEEE-like Inf and NaN.  MXFP6: E2M3 (max 7.5) and E3M2 (max
  * 28); MXFP4: E2M1 (max 6); these three have no Inf or NaN encodings.
- * FP8 codes are one byte per element.  The 6- and 4-bit codes use the
- * tensor-core container layout: every run of 16 elements along K occupies
- * 16 bytes, the 16 codes packed little-endian (element i at bits
- * [i*w, i*w + w) of the run, w = 6 or 4) followed by zero bytes -- so a
- * code buffer has the same size and strides as an FP8 one. */
-typedef enum { MX_E4M3 = 0, MX_E5M2 = 1, MX_E2M3 = 2, MX_E3M2 = 3, MX_E2M1 = 4 } mx_fmt;
+ * FP8 codes are one byte per element.  The 6- and 4-bit codes come in two
+ * storage layouts:
+ *  - MX_E2M3, MX_E3M2, MX_E2M1: the tensor-core container layout: every run
+ *    of 16 elements along K occupies 16 bytes, the 16 codes packed
+ *    little-endian (element i at bits [i*w, i*w + w) of the run, w = 6 or
+ *    4) followed by zero bytes -- a code buffer has the size and strides of
+ *    an FP8 one (one byte per element).
+ *  - MX_E2M3_PACKED, MX_E3M2_PACKED, MX_E2M1_PACKED: the same codes densely
+ *    packed, the payload the page counts for narrow elements: a row of K
+ *    elements is one little-endian bit string of K*w/8 bytes, element i at
+ *    bits [i*w, i*w + w) (E2M1: two codes per byte, element 2i in the low
+ *    nibble; E2M3 and E3M2: four codes per three bytes).  The GEMM reads
+ *    them with the tensor copy's unpacking element types, which place each
+ *    16-element run in the container layout in shared memory.  A GEMM
+ *    operand in packed storage needs K % 128 == 0 and a 32-byte aligned code
+ *    pointer. */
+typedef enum {
+  MX_E4M3 = 0, MX_E5M2 = 1, MX_E2M3 = 2, MX_E3M2 = 3, MX_E2M1 = 4,
+  MX_E2M3_PACKED = 5, MX_E3M2_PACKED = 6, MX_E2M1_PACKED = 7
+} mx_fmt;
 
 /* Wide element types: quantizer input and GEMM output. */
 typedef enum { MX_BF16 = 0, MX_FP32 = 1 } mx_dtype;
@@ -137,6 +151,8 @@ size_t mx_grouped_scale_bytes(int64_t total_rows, int32_t groups, int64_t k);
  *    leading dimension rows -- and s_col = swizzled scales of the
  *    [cols, rows] operand (mx_scale_bytes(cols, rows) bytes).
  *  BOTH: both of the above from one read of x.
+ *  Packed formats (MX_*_PACKED): a code row of n elements takes n*w/8 bytes
+ *    (q_row: rows x cols*w/8 bytes; q_col: cols x rows*w/8 bytes).
  *
  * x, q_*, s_* are device pointers; unused outputs may be NULL.
  * cols % 8 == 0, ldx % 8 == 0, ldx >= cols.  x_dtype must be MX_BF16.
@@ -213,9 +229,9 @@ mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_
  *    swizzled scales sa of the [m, k] operand -- e.g. X quantized ROWWISE.
  * B: b[n, k] codes (K contiguous, leading dimension k) with swizzled scales
  *    sb of the [n, k] operand -- e.g. W[k, n] quantized COLWISE (= W^T).
- * fa, fb: any of the five element formats (MX_E4M3, MX_E5M2, MX_E2M3,
- *    MX_E3M2, MX_E2M1), in any combination; 6- and 4-bit codes in the
- *    container layout described with mx_fmt.
+ * fa, fb: any element format of mx_fmt, in any combination; 6- and 4-bit
+ *    codes in either storage layout described with mx_fmt (packed storage:
+ *    k % 128 == 0, code pointer 32-byte aligned, row stride k*w/8 bytes).
  * y: device, [m, n] row-major with leading dimension ldy (elements),
  *    FP32 or BF16 (RNE from the FP32 accumulator).
  * Constraints: k % 32 == 0, k >= 32, n % 8 == 0, ldy >= n.

@@ -26,7 +26,21 @@ MX_OK = 0
 STATUS_NAMES = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_MISALIGNED",
                 3: "MX_ERR_UNSUPPORTED", 4: "MX_ERR_CUDA", 5: "MX_ERR_TIMEOUT",
                 6: "MX_ERR_DEVICE_ARG"}
-FMT = {"e4m3": 0, "e5m2": 1, "e2m3": 2, "e3m2": 3, "e2m1": 4}
+FMT = {"e4m3": 0, "e5m2": 1, "e2m3": 2, "e3m2": 3, "e2m1": 4,
+       "e2m3_packed": 5, "e3m2_packed": 6, "e2m1_packed": 7}
+# bits of storage per element: 8 for FP8 and the container layout of the
+# narrow formats, the code width for packed storage
+STORAGE_BITS = {"e2m3_packed": 6, "e3m2_packed": 6, "e2m1_packed": 4}
+
+
+def storage_bytes(fmt: str, elems: int) -> int:
+    """Bytes that `elems` consecutive codes of `fmt` occupy along K."""
+    return elems * STORAGE_BITS.get(fmt, 8) // 8
+
+
+def storage_elems(fmt: str, nbytes: int) -> int:
+    """Codes of `fmt` held by `nbytes` bytes along K."""
+    return nbytes * 8 // STORAGE_BITS.get(fmt, 8)
 DTYPE = {"bf16": 0, "fp32": 1}
 AXIS = {"row": 1, "col": 2, "both": 3}
 RULE = {"floor": 0, "ceil": 1}
@@ -266,7 +280,8 @@ class MxTensor:
 
     @property
     def k(self) -> int:
-        return self.codes.shape[-1]
+        """Elements along K (packed storage holds fewer bytes than elements)."""
+        return storage_elems(self.fmt, self.codes.shape[-1])
 
 
 def quantize(x: torch.Tensor, fmt: str = "e4m3", axis: str = "row", rule: str = "floor",
@@ -284,10 +299,10 @@ def quantize(x: torch.Tensor, fmt: str = "e4m3", axis: str = "row", rule: str = 
     dev = x.device
     q_row = s_row = q_col = s_col = None
     if axis in ("row", "both"):
-        q_row = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+        q_row = torch.empty((rows, storage_bytes(fmt, cols)), dtype=torch.uint8, device=dev)
         s_row = torch.empty(max(mx_scale_bytes(rows, cols), 1), dtype=torch.uint8, device=dev)
     if axis in ("col", "both"):
-        q_col = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+        q_col = torch.empty((cols, storage_bytes(fmt, rows)), dtype=torch.uint8, device=dev)
         s_col = torch.empty(max(mx_scale_bytes(cols, rows), 1), dtype=torch.uint8, device=dev)
     if rand is None:
         st = mx_quantize(_ptr(x), DTYPE["bf16"], rows, cols, x.stride(0), FMT[fmt], AXIS[axis],
@@ -357,12 +372,12 @@ def gemm(a: MxTensor, b: MxTensor, out_dtype: str = "bf16", out: torch.Tensor | 
          stream=None, bias: torch.Tensor | None = None, act: str = "none") -> torch.Tensor:
     """y[m, n] = block-scaled A[m, k] * B[n, k]^T; with `bias` (FP32 [n]) or
     `act` ("silu") the fused epilogue computes act(y + bias)."""
-    m, k = a.codes.shape
-    n, k2 = b.codes.shape
+    m, k = a.codes.shape[0], a.k
+    n, k2 = b.codes.shape[0], b.k
     if k != k2:
         raise ValueError("K mismatch")
-    _require_codes(a.codes, (m, k), "a")
-    _require_codes(b.codes, (n, k), "b")
+    _require_codes(a.codes, (m, storage_bytes(a.fmt, k)), "a")
+    _require_codes(b.codes, (n, storage_bytes(b.fmt, k)), "b")
     _require_scales(a.scales, mx_scale_bytes(m, k), "a")
     _require_scales(b.scales, mx_scale_bytes(n, k), "b")
     tdtype = torch.float32 if out_dtype == "fp32" else torch.bfloat16
@@ -390,12 +405,12 @@ def grouped_gemm(a: MxTensor, offsets: torch.Tensor, b: MxTensor, out_dtype: str
                  out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Per group g: y[o_g:o_{g+1}] = A[o_g:o_{g+1}] * B_g^T.  b.codes is
     [groups, n, k]; b.scales holds groups consecutive swizzled matrices."""
-    total_m, k = a.codes.shape
-    groups, n, k2 = b.codes.shape
+    total_m, k = a.codes.shape[0], a.k
+    groups, n, k2 = b.codes.shape[0], b.codes.shape[1], b.k
     if k != k2 or _require_offsets(offsets) != groups:
         raise ValueError("shape mismatch")
-    _require_codes(a.codes, (total_m, k), "a")
-    _require_codes(b.codes, (groups, n, k), "b")
+    _require_codes(a.codes, (total_m, storage_bytes(a.fmt, k)), "a")
+    _require_codes(b.codes, (groups, n, storage_bytes(b.fmt, k)), "b")
     _require_scales(a.scales, mx_grouped_scale_bytes(total_m, groups, k), "a")
     _require_scales(b.scales, groups * mx_scale_bytes(n, k), "b")
     tdtype = torch.float32 if out_dtype == "fp32" else torch.bfloat16
@@ -414,11 +429,11 @@ def grouped_gemm_bcat(a: MxTensor, offsets: torch.Tensor, b: MxTensor, out_dtype
     """Per group g: y[o_g:o_{g+1}] = A[o_g:o_{g+1}] * B_g^T with B_g the
     columns [g*k, (g+1)*k) of one [n, groups*k] operand (b from quantize(...,
     axis="col") of the stacked [groups*k, n] expert weights); k = a's K."""
-    total_m, k = a.codes.shape
-    n, ldb = b.codes.shape
+    total_m, k = a.codes.shape[0], a.k
+    n, ldb = b.codes.shape[0], b.k
     groups = _require_offsets(offsets)
-    _require_codes(a.codes, (total_m, k), "a")
-    _require_codes(b.codes, (n, ldb), "b")
+    _require_codes(a.codes, (total_m, storage_bytes(a.fmt, k)), "a")
+    _require_codes(b.codes, (n, storage_bytes(b.fmt, ldb)), "b")
     _require_scales(a.scales, mx_grouped_scale_bytes(total_m, groups, k), "a")
     _require_scales(b.scales, mx_scale_bytes(n, ldb), "b")
     tdtype = torch.float32 if out_dtype == "fp32" else torch.bfloat16
@@ -438,13 +453,13 @@ def grouped_gemm_wgrad(a: MxTensor, offsets: torch.Tensor, b: MxTensor, total_to
     """Per group g: y[g] = A_g * B_g^T over the group's tokens, with a and b
     from quantize_grouped(..., axis="col") (same offsets and ldq).  Returns
     [groups, m, n]; an expert without tokens gets zeros."""
-    m, ldk = a.codes.shape
-    n, ldk2 = b.codes.shape
+    m, ldk = a.codes.shape[0], a.k
+    n, ldk2 = b.codes.shape[0], b.k
     groups = _require_offsets(offsets)
     if ldk != ldk2:
         raise ValueError("A and B must share the token layout (ldq)")
-    _require_codes(a.codes, (m, ldk), "a")
-    _require_codes(b.codes, (n, ldk), "b")
+    _require_codes(a.codes, (m, storage_bytes(a.fmt, ldk)), "a")
+    _require_codes(b.codes, (n, storage_bytes(b.fmt, ldk)), "b")
     _require_scales(a.scales, mx_scale_bytes(m, ldk), "a")
     _require_scales(b.scales, mx_scale_bytes(n, ldk), "b")
     tdtype = torch.float32 if out_dtype == "fp32" else torch.bfloat16

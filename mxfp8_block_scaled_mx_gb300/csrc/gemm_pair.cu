@@ -84,7 +84,14 @@ struct PairCfg {
   static constexpr int kBBytes = (kPairN / 2) * kBK;     // 16 KB, this block's half of B
   static constexpr int kSfaBytes = 512;                  // this block's 128 rows x 4 blocks
   static constexpr int kSfbBytes = 1024;                 // all 256 columns x 4 blocks
-  static constexpr uint32_t kPairTx = 2u * (kABytes + kBBytes + kSfaBytes + kSfbBytes);
+  // bytes one stage's four tensor copies of both blocks deliver, with the A
+  // and B codes stored in a_bits / b_bits per element (8, or 4 / 6 packed:
+  // an unpacking copy counts the bytes it reads, not the padded container
+  // bytes it writes to shared memory)
+  static __device__ __forceinline__ uint32_t pair_tx(int32_t a_bits, int32_t b_bits) {
+    return 2u * (static_cast<uint32_t>(kABytes * a_bits / 8) +
+                 static_cast<uint32_t>(kBBytes * b_bits / 8) + kSfaBytes + kSfbBytes);
+  }
   static constexpr int kSfSlotCols = 4 + 8;
   static constexpr int kSfBaseCol = kPairN;              // after the accumulator
   static_assert(kSfBaseCol + kStages * kSfSlotCols <= int(kPTmemCols), "tensor memory budget");
@@ -154,6 +161,7 @@ __global__ void __launch_bounds__(PairWarps<FUSED>::kThreads, 1)
     }
     __syncwarp();
     if constexpr (GROUPED) {
+      pdl_wait();  // the offsets may be written by the previous kernel
       // grouped along K the offsets split the p.k tokens of the contraction
       group_tile_prefix(p.offsets, p.groups, MODE == kModeGroupK ? p.k : p.m, gs->off, gs->tiles,
                         &gs->valid, 2, gs->units);
@@ -167,6 +175,8 @@ __global__ void __launch_bounds__(PairWarps<FUSED>::kThreads, 1)
   cluster_sync();  // barriers and group tables of both blocks exist before any cross-block use
   tc_fence_after_sync();
   const uint32_t tmem_base = *s_tmem;
+  pdl_wait();  // operands and output may belong to the previous kernel of the stream
+  pdl_launch_dependents();
 
   const int64_t n_tiles = (p.n + kPairN - 1) / kPairN;
   const int64_t m_units = (p.m + 2 * kRowsPerBlock - 1) / (2 * kRowsPerBlock);
@@ -200,6 +210,7 @@ __global__ void __launch_bounds__(PairWarps<FUSED>::kThreads, 1)
     // out-of-range scale tiles are zero-filled or never stored), so block
     // 0's expected byte count is the same for every stage.
     const uint32_t full_leader0 = cluster_map(&full[0], 0);
+    const uint32_t stage_tx = C::pair_tx(p.a_bits, p.b_bits);
     uint32_t stage = 0, phase = 0;
     int64_t issued = 0;
     bool ok = true;
@@ -214,7 +225,7 @@ __global__ void __launch_bounds__(PairWarps<FUSED>::kThreads, 1)
           break;
         }
         if (elect_one()) {
-          if (leader) mbar_arrive_expect_tx(&full[stage], C::kPairTx);
+          if (leader) mbar_arrive_expect_tx(&full[stage], stage_tx);
           const uint32_t bar = full_leader0 + stage * 8u;
           tma_load_2d_pair(sA + stage * C::kABytes, &tmap_a, bar,
                            static_cast<int32_t>(ti.a_kx0) + kt * kBK, a_row);
@@ -382,16 +393,17 @@ cudaError_t launch_pair_impl(const GemmParams& p, const CUtensorMap& ta, const C
   if (MODE == kModeGroupK) units *= p.groups;
   if (units == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.blockDim = dim3(PairWarps<FUSED>::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // the occupancy query below sees the cluster shape only
   int max_clusters = num_sms / 2;
   cfg.gridDim = dim3(static_cast<unsigned>(max_clusters * 2));
   int active = 0;
@@ -399,6 +411,7 @@ cudaError_t launch_pair_impl(const GemmParams& p, const CUtensorMap& ta, const C
     max_clusters = ::min(max_clusters, active);
   const int64_t clusters = units < max_clusters ? units : max_clusters;
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * 2));
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, p);
 }
 

@@ -15,6 +15,16 @@ namespace mx {
 // `fn` runs until it first succeeds on the current device.  The flags are
 // guarded by a mutex, so concurrent first calls from several host threads
 // are safe.
+// Launch attribute of every kernel of the library: programmatic stream
+// serialization (the kernels wait for their predecessor with griddepcontrol
+// before touching global memory).
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 class PerDeviceOnce {
  public:
   template <typename Fn>
@@ -45,7 +55,8 @@ struct QuantizeParams {
   uint8_t* s_row;      // swizzled scales of the [rows, cols] operand
   uint8_t* q_col;      // [cols, rows] codes or nullptr
   uint8_t* s_col;      // swizzled scales of the [cols, rows] operand
-  int32_t fmt;         // element format: 0 E4M3, 1 E5M2, 2 E2M3, 3 E3M2, 4 E2M1
+  int32_t fmt;         // element format: 0 E4M3, 1 E5M2, 2 E2M3, 3 E3M2, 4 E2M1; 5-7 the
+                       // last three in packed storage
   int32_t rule;        // 0 = floor, 1 = ceil
   const int32_t* offsets;  // grouped only: device int32[groups + 1]
   int32_t groups;
@@ -97,6 +108,8 @@ struct GemmParams {
   int32_t band_m;          // m-tiles per raster band (dense), a multiple of 2
   const float* bias;       // fused epilogue: FP32 bias per output column, or nullptr
   int32_t act;             // fused epilogue: 0 none, 1 SiLU
+  int32_t a_bits;          // bits of global storage per A / B code: 8, or 4 / 6 when
+  int32_t b_bits;          // packed (the tensor copy counts the global bytes it reads)
 };
 
 // Block-pair GEMM (cta_group::2, 256 x 256 pair tiles), all three modes.

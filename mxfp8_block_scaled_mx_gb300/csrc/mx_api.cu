@@ -87,17 +87,29 @@ bool all_on_device(int dev, std::initializer_list<const void*> ptrs) {
 
 bool valid_fmt(mx_fmt f) { return f == MX_E4M3 || f == MX_E5M2; }
 
-// GEMM operand formats: FP8 and the MXFP6 / MXFP4 element formats.
-bool valid_gemm_fmt(mx_fmt f) { return f >= MX_E4M3 && f <= MX_E2M1; }
+// GEMM operand formats: FP8 and the MXFP6 / MXFP4 element formats, the
+// latter in container or packed storage.
+bool valid_gemm_fmt(mx_fmt f) { return f >= MX_E4M3 && f <= MX_E2M1_PACKED; }
+
+bool is_packed(mx_fmt f) { return f >= MX_E2M3_PACKED; }
+
+// Code width in bits.
+int code_bits(mx_fmt f) {
+  switch (f) {
+    case MX_E2M3: case MX_E3M2: case MX_E2M3_PACKED: case MX_E3M2_PACKED: return 6;
+    case MX_E2M1: case MX_E2M1_PACKED: return 4;
+    default: return 8;
+  }
+}
 
 // Operand type code of tcgen05.mma.kind::mxf8f6f4 (instruction descriptor
-// bits 7-9 / 10-12): E4M3 0, E5M2 1, E2M3 3, E3M2 4, E2M1 5.
+// bits 7-9 / 10-12): E4M3 0, E5M2 1, E2M3 3, E3M2 4, E2M1 5 (either storage).
 int32_t mma_type_code(mx_fmt f) {
   switch (f) {
     case MX_E5M2: return 1;
-    case MX_E2M3: return 3;
-    case MX_E3M2: return 4;
-    case MX_E2M1: return 5;
+    case MX_E2M3: case MX_E2M3_PACKED: return 3;
+    case MX_E3M2: case MX_E3M2_PACKED: return 4;
+    case MX_E2M1: case MX_E2M1_PACKED: return 5;
     default: return 0;
   }
 }
@@ -133,6 +145,33 @@ mx_status encode_bf16_map(CUtensorMap* map, const void* base, int64_t cols, int6
                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
+// 2-D tensor map over packed 6- or 4-bit codes [rows, inner elements] with
+// row stride `stride` bytes, read with the unpacking element type: each run
+// of 16 codes lands in 16 bytes of shared memory (the container layout the
+// MMA reads), so the shared-memory tile equals that of a container-layout
+// operand.  Box {128 elements, box_rows}, 128-byte swizzle, zero fill.
+mx_status encode_packed_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows,
+                            int64_t stride, uint32_t box_rows, int bits) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride)};
+  cuuint32_t box[2] = {128u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  const CUtensorMapDataType type =
+      bits == 4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B;
+  CUresult r = g_encode(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
+// Tensor map of a GEMM code operand [rows, ld elements] in its storage.
+mx_status encode_operand_map(CUtensorMap* map, const void* base, mx_fmt f, int64_t ld,
+                             int64_t rows) {
+  if (is_packed(f))
+    return encode_packed_map(map, base, ld, rows, ld * code_bits(f) / 8, 128, code_bits(f));
+  return encode_codes_map(map, base, ld, rows, ld, 128);
 }
 
 // The swizzled scale buffer of a [rows, k] operand viewed as uint32
@@ -184,6 +223,14 @@ mx_status gemm_common(const GemmShape& g, const uint8_t* a, const uint8_t* sa, m
   if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(y) ||
       (ldy * elt) % 16 != 0 || g.lda % 16 != 0 || g.ldb % 16 != 0)
     return MX_ERR_MISALIGNED;
+  // packed operands: whole 128-element K tiles (the unpacking tensor copy
+  // reads rows of a multiple of 128 elements) and 32-byte aligned rows
+  if ((is_packed(fa) && (g.lda % 128 != 0 || (g.mode != mx::kModeGroupK && k % 128 != 0))) ||
+      (is_packed(fb) && (g.ldb % 128 != 0 || (g.mode != mx::kModeGroupK && k % 128 != 0))))
+    return MX_ERR_INVALID_ARG;
+  if ((is_packed(fa) && (reinterpret_cast<uintptr_t>(a) & 31u) != 0) ||
+      (is_packed(fb) && (reinterpret_cast<uintptr_t>(b) & 31u) != 0))
+    return MX_ERR_MISALIGNED;
   DeviceState* st = nullptr;
   mx_status s = device_state(&st);
   if (s != MX_OK) return s;
@@ -212,6 +259,8 @@ mx_status gemm_common(const GemmShape& g, const uint8_t* a, const uint8_t* sa, m
   p.bias = bias;
   p.act = act;
   p.band_m = kBandM;
+  p.a_bits = is_packed(fa) ? code_bits(fa) : 8;
+  p.b_bits = is_packed(fb) ? code_bits(fb) : 8;
 
   // Block pairs (cta_group::2, 256x256 pair tiles): each block loads 128
   // rows of A and 128 of the 256 rows of the B tile; the scale buffers are
@@ -219,8 +268,8 @@ mx_status gemm_common(const GemmShape& g, const uint8_t* a, const uint8_t* sa, m
   // bound when grouped by rows.
   CUtensorMap ta, tb, tsa, tsb;
   const int64_t a_scale_rows = g.mode == mx::kModeGroupM ? (ceil_div(m, 128) + g.groups) * 128 : m;
-  if ((s = encode_codes_map(&ta, a, g.lda, m, g.lda, 128)) != MX_OK) return s;
-  if ((s = encode_codes_map(&tb, b, g.ldb, g.b_rows, g.ldb, 128)) != MX_OK) return s;
+  if ((s = encode_operand_map(&ta, a, fa, g.lda, m)) != MX_OK) return s;
+  if ((s = encode_operand_map(&tb, b, fb, g.ldb, g.b_rows)) != MX_OK) return s;
   if ((s = encode_scale_map(&tsa, sa, a_scale_rows, g.lda, 1)) != MX_OK) return s;
   if ((s = encode_scale_map(&tsb, sb, g.b_rows, g.ldb, 2)) != MX_OK) return s;
   const cudaError_t err = mx::launch_gemm_pair(p, ta, tb, tsa, tsb, st->num_sms, stream);

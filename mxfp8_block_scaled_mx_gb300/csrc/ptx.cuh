@@ -122,6 +122,21 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
   return __all_sync(0xffffffffu, got);
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// The library's kernels are launched with programmatic stream serialization:
+// a kernel may start (on SMs its predecessor in the stream has left) while
+// that predecessor is still running, so its set-up (barriers, tensor memory,
+// descriptor prefetch) overlaps the predecessor's tail.  pdl_wait() blocks
+// until the predecessor has completed and its memory operations are
+// visible; every kernel calls it before its first global memory access.
+// pdl_launch_dependents() allows the next kernel of the stream to start
+// launching.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -183,22 +183,30 @@ __device__ __forceinline__ uint2 encode8(const uint4 v, float mul) {
 // neighbouring grid values, |v| goes to u iff the element's 16-bit random
 // integer r is below floor(frac * 2^16), frac = (|v| - l) / (u - l).  The
 // result is a grid value (or one step past the maximum, which the
-// saturating conversion then clamps).  All arithmetic is exact: |v| has at
-// most 8 significant bits and every factor is a power of two.
+// saturating conversion then clamps).  v is exact (a bf16 times a power of
+// two), and so is every step below: the one rounded addition only drops
+// bits below those the comparison reads.
 template <int FMT>
 __device__ __forceinline__ float sr_to_grid(float v, uint32_t r16) {
   constexpr int kMantBits = FMT == 0 ? 3 : 2;
   constexpr int kMinNormalExp = FMT == 0 ? -6 : -14;
+  constexpr int kDrop = 23 - kMantBits;  // FP32 significand bits below the format's grid
+  // In the format's normal range the grid keeps the top kMantBits of the
+  // FP32 significand: l is |v| with the dropped bits cleared, u = l plus one
+  // step (a carry into the exponent gives the next binade's first value),
+  // and the top 16 of the dropped bits are floor(frac * 2^16).  Below the
+  // smallest normal m = 2^kMinNormalExp the step is the subnormal quantum,
+  // which is also the step of the binade [m, 2m): there |v| + m (rounded
+  // toward zero, which keeps the top 16 dropped bits exact) is rounded the
+  // same way and m is taken off again (exact: both are multiples of the step).
+  const float m = __uint_as_float(static_cast<uint32_t>(127 + kMinNormalExp) << 23);
   const float a = fabsf(v);
-  const int ex = static_cast<int>(__float_as_uint(a) >> 23) - 127;  // floor(log2 a), normal a
-  const int qe = max(ex, kMinNormalExp) - kMantBits;                // exponent of the grid step
-  // |v| in units of 2^-16 grid steps: below 2^(kMantBits + 17), exact
-  const float w = __fmul_rn(a, __uint_as_float(static_cast<uint32_t>(127 + 16 - qe) << 23));
-  const uint32_t steps16 = static_cast<uint32_t>(w);
-  const uint32_t units = (steps16 >> 16) + (r16 < (steps16 & 0xFFFFu) ? 1u : 0u);
-  const float res =
-      __fmul_rn(static_cast<float>(units), __uint_as_float(static_cast<uint32_t>(127 + qe) << 23));
-  return copysignf(res, v);
+  const bool small = a < m;
+  const uint32_t bits = __float_as_uint(small ? __fadd_rz(a, m) : a);
+  const uint32_t frac16 = (bits >> (kDrop - 16)) & 0xFFFFu;
+  const uint32_t low = bits & ~((1u << kDrop) - 1u);
+  const float r = __uint_as_float(low + (r16 < frac16 ? (1u << kDrop) : 0u));
+  return copysignf(small ? __fsub_rn(r, m) : r, v);
 }
 
 // Two bf16 of a word with their two 16-bit random integers -> two codes.
@@ -283,7 +291,7 @@ __device__ __forceinline__ bool group_bar_any(int group, bool pred) {
 // columnwise tiles may hold rows of the next group past rows_valid: those
 // rows count as zeros (the zero-padded final block of the group), and the
 // tile's full 128 transposed columns are written, padding included.
-template <int FMT, bool ROW, bool COL, bool GROUPED, bool SR>
+template <int FMT, bool ROW, bool COL, bool GROUPED, bool SR, bool PACKED>
 __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Tile& tl,
                                               const uint8_t* xs, const uint8_t* rs, uint8_t* s_q,
                                               uint8_t* s_unit_row, uint8_t* s_unit_col,
@@ -339,10 +347,12 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
         const uint32_t lo = pack4_fp6(codes.x), hi = pack4_fp6(codes.y);
         codes = make_uint2(lo | hi << 24, hi >> 8);
       }
-      if constexpr (F::kBits < 8) {
-        // Lanes 2j and 2j + 1 hold the two halves of one 16-element run,
-        // whose 16-byte container is the packed run then zero bytes; each
-        // lane writes the 8 bytes at its own FP8 offset.
+      if constexpr (F::kBits < 8 && !(PACKED && F::kBits == 4)) {
+        // Lanes 2j and 2j + 1 hold the two halves of one 16-element run.
+        // Its 16-byte container is the packed run then zero bytes: each
+        // lane writes the 8 bytes at its own FP8 offset.  Packed 6-bit
+        // storage keeps the run's first 12 bytes: the first lane writes
+        // bytes 0-7, the second bytes 8-11.
         const uint32_t px = __shfl_xor_sync(0xffffffffu, codes.x, 1);
         const bool first = (ch & 1) == 0;
         if constexpr (F::kBits == 4) {
@@ -353,7 +363,22 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
         }
       }
       if (ok) {
-        *reinterpret_cast<uint2*>(qp + it * q_step) = codes;
+        if constexpr (PACKED) {
+          // packed row: element e at bit e * w; this thread's 8 elements
+          // start at byte gc * w / 8
+          uint8_t* rp = p.q_row + (tl.x_row0 + lr) * (p.cols * F::kBits / 8);
+          if constexpr (F::kBits == 4) {
+            *reinterpret_cast<uint32_t*>(rp + gc / 2) = codes.x;
+          } else if ((ch & 1) == 0) {
+            uint32_t* d = reinterpret_cast<uint32_t*>(rp + gc * 3 / 4);
+            d[0] = codes.x;
+            d[1] = codes.y;
+          } else {
+            *reinterpret_cast<uint32_t*>(rp + gc * 3 / 4 + 2) = codes.x;
+          }
+        } else {
+          *reinterpret_cast<uint2*>(qp + it * q_step) = codes;
+        }
         if ((lt & 3) == 0) s_unit_row[unit_offset(lr, ch >> 2)] = sbyte;
       }
     }
@@ -426,10 +451,34 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
       if (nan_hi) q_hi[i] = F::kNanWord;
     }
     // The column's 32 codes (two 16-element runs) as 32 bytes: FP8 one
-    // code per byte; FP6 / FP4 one 16-byte container per run.
+    // code per byte; FP6 / FP4 one 16-byte container per run; packed
+    // storage 16 (FP4) or 24 (FP6) bytes.
     uint4* d0 = reinterpret_cast<uint4*>(s_q + (2 * cp) * kColPitch + rb * 32);
     uint4* d1 = reinterpret_cast<uint4*>(s_q + (2 * cp + 1) * kColPitch + rb * 32);
-    if constexpr (F::kBits == 8) {
+    if constexpr (PACKED && F::kBits == 4) {
+      uint4* e0 = reinterpret_cast<uint4*>(s_q + (2 * cp) * kColPitch + rb * 16);
+      uint4* e1 = reinterpret_cast<uint4*>(s_q + (2 * cp + 1) * kColPitch + rb * 16);
+      *e0 = make_uint4(q_lo[0] | q_lo[1] << 16, q_lo[2] | q_lo[3] << 16, q_lo[4] | q_lo[5] << 16,
+                       q_lo[6] | q_lo[7] << 16);
+      *e1 = make_uint4(q_hi[0] | q_hi[1] << 16, q_hi[2] | q_hi[3] << 16, q_hi[4] | q_hi[5] << 16,
+                       q_hi[6] | q_hi[7] << 16);
+    } else if constexpr (PACKED) {
+      // eight groups of four 6-bit codes, 24 bits each, in 24 bytes
+      uint2* e0 = reinterpret_cast<uint2*>(s_q + (2 * cp) * kColPitch + rb * 24);
+      uint2* e1 = reinterpret_cast<uint2*>(s_q + (2 * cp + 1) * kColPitch + rb * 24);
+      uint32_t gl[8], gh[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        gl[i] = pack4_fp6(q_lo[i]);
+        gh[i] = pack4_fp6(q_hi[i]);
+      }
+      e0[0] = make_uint2(gl[0] | gl[1] << 24, gl[1] >> 8 | gl[2] << 16);
+      e0[1] = make_uint2(gl[2] >> 16 | gl[3] << 8, gl[4] | gl[5] << 24);
+      e0[2] = make_uint2(gl[5] >> 8 | gl[6] << 16, gl[6] >> 16 | gl[7] << 8);
+      e1[0] = make_uint2(gh[0] | gh[1] << 24, gh[1] >> 8 | gh[2] << 16);
+      e1[1] = make_uint2(gh[2] >> 16 | gh[3] << 8, gh[4] | gh[5] << 24);
+      e1[2] = make_uint2(gh[5] >> 8 | gh[6] << 16, gh[6] >> 16 | gh[7] << 8);
+    } else if constexpr (F::kBits == 8) {
       d0[0] = make_uint4(q_lo[0], q_lo[1], q_lo[2], q_lo[3]);
       d0[1] = make_uint4(q_lo[4], q_lo[5], q_lo[6], q_lo[7]);
       d1[0] = make_uint4(q_hi[0], q_hi[1], q_hi[2], q_hi[3]);
@@ -461,7 +510,41 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
           reinterpret_cast<const uint4*>(s_unit_row)[lt];
     }
   }
+  if constexpr (COL && PACKED) {
+    // Packed transposed codes: output row (c0 + c) holds x rows
+    // [x_row0, x_row0 + rows_valid) at bytes [scale_rt * kRowBytes, ...),
+    // written in 16-byte (FP4) or 8-byte (FP6) pieces.
+    constexpr int kRowBytes = kTile * F::kBits / 8;
+    constexpr int kPiece = F::kBits == 4 ? 16 : 8;
+    constexpr int kPieces = kRowBytes / kPiece;
+    const int64_t ldq_bytes = p.ldq_col * F::kBits / 8;
+    const int valid_bytes = static_cast<int>(tl.rows_valid) * F::kBits / 8;
+#pragma unroll
+    for (int i = 0; i < kTile * kPieces / kGroupThreads; ++i) {
+      const int idx = i * kGroupThreads + lt;
+      const int c = idx / kPieces;
+      const int j = idx - c * kPieces;
+      if (tl.c0 + c < p.cols && j * kPiece < valid_bytes) {
+        uint8_t* dst = p.q_col + (tl.c0 + c) * ldq_bytes + tl.scale_rt * kRowBytes + j * kPiece;
+        if constexpr (kPiece == 16) {
+          *reinterpret_cast<uint4*>(dst) =
+              *reinterpret_cast<const uint4*>(s_q + c * kColPitch + j * kPiece);
+        } else {
+          *reinterpret_cast<uint2*>(dst) =
+              *reinterpret_cast<const uint2*>(s_q + c * kColPitch + j * kPiece);
+        }
+      }
+    }
+  }
   if constexpr (COL) {
+    if (lt < 32) {
+      const int64_t tiles_k = (p.ldq_col + 127) / 128;
+      const int64_t unit = (tl.c0 / 128) * tiles_k + tl.scale_rt;
+      reinterpret_cast<uint4*>(p.s_col + unit * 512)[lt] =
+          reinterpret_cast<const uint4*>(s_unit_col)[lt];
+    }
+  }
+  if constexpr (COL && !PACKED) {
     // Transposed codes: output row (c0 + c), columns [128 * scale_rt,
     // 128 * scale_rt + 128) (dense: x rows [x_row0, x_row0 + 128); grouped:
     // the tile's place in the group's padded segment).
@@ -475,12 +558,6 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
         *reinterpret_cast<uint4*>(p.q_col + (tl.c0 + c) * p.ldq_col + tl.scale_rt * kTile +
                                   j * 16) = q;
       }
-    }
-    if (lt < 32) {
-      const int64_t tiles_k = (p.ldq_col + 127) / 128;
-      const int64_t unit = (tl.c0 / 128) * tiles_k + tl.scale_rt;
-      reinterpret_cast<uint4*>(p.s_col + unit * 512)[lt] =
-          reinterpret_cast<const uint4*>(s_unit_col)[lt];
     }
   }
 }
@@ -512,7 +589,7 @@ struct QSmem {
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
-template <int FMT, bool ROW, bool COL, bool GROUPED, bool SR>
+template <int FMT, bool ROW, bool COL, bool GROUPED, bool SR, bool PACKED>
 __global__ void __launch_bounds__(QSmem<COL, SR>::kThreads, 1)
     quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     const __grid_constant__ CUtensorMap tmap_r, const QuantizeParams p) {
@@ -541,6 +618,8 @@ __global__ void __launch_bounds__(QSmem<COL, SR>::kThreads, 1)
     tma_prefetch_desc(&tmap_x);
     if constexpr (SR) tma_prefetch_desc(&tmap_r);
   }
+  pdl_wait();  // the input, the offsets and the outputs may belong to the previous kernel
+  pdl_launch_dependents();
   if constexpr (GROUPED) group_tile_prefix(p.offsets, p.groups, p.rows, gi->off, gi->tiles, &gi->valid);
   __syncthreads();
 
@@ -607,16 +686,16 @@ __global__ void __launch_bounds__(QSmem<COL, SR>::kThreads, 1)
       // scale units zeroed; a wait that gave up anywhere stops the whole group
       if (group_bar_any(group, !got)) break;
       const uint8_t* slot = smem + QSmem::kOffRing + s * QSmem::kSlotBytes;
-      quantize_tile<FMT, ROW, COL, GROUPED, SR>(p, tl, slot, slot + kTileBytes, s_q, s_unit_row,
+      quantize_tile<FMT, ROW, COL, GROUPED, SR, PACKED>(p, tl, slot, slot + kTileBytes, s_q, s_unit_row,
                                                 s_unit_col, &empty[s], group, lt);
     }
   }
 }
 
-template <int FMT, bool ROW, bool COL, bool GROUPED, bool SR = false>
+template <int FMT, bool ROW, bool COL, bool GROUPED, bool SR = false, bool PACKED = false>
 cudaError_t launch_one(const QuantizeParams& p, const CUtensorMap& tmap, const CUtensorMap& tmap_r,
                        int64_t tiles, int num_sms, cudaStream_t stream) {
-  auto kern = quantize_kernel<FMT, ROW, COL, GROUPED, SR>;
+  auto kern = quantize_kernel<FMT, ROW, COL, GROUPED, SR, PACKED>;
   using QSmem = mx::QSmem<COL, SR>;
   static PerDeviceOnce setup;
   const cudaError_t err = setup.run([&] {
@@ -625,15 +704,22 @@ cudaError_t launch_one(const QuantizeParams& p, const CUtensorMap& tmap, const C
   if (err != cudaSuccess) return err;
   const int64_t grid = tiles < num_sms ? tiles : num_sms;
   if (grid <= 0) return cudaSuccess;
-  kern<<<static_cast<unsigned>(grid), QSmem::kThreads, QSmem::kBytes, stream>>>(tmap, tmap_r, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(QSmem::kThreads);
+  cfg.dynamicSmemBytes = QSmem::kBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmap, tmap_r, p);
 }
 
 }  // namespace
 
 namespace {
 
-template <int FMT>
+template <int FMT, bool PACKED = false>
 cudaError_t launch_dense(const QuantizeParams& p, const CUtensorMap& tmap_x,
                          const CUtensorMap* tmap_r, int64_t tiles, int num_sms,
                          cudaStream_t stream) {
@@ -649,9 +735,11 @@ cudaError_t launch_dense(const QuantizeParams& p, const CUtensorMap& tmap_x,
   } else {
     if (tmap_r) return cudaErrorNotSupported;
   }
-  if (row && col) return launch_one<FMT, true, true, false>(p, tmap_x, tr, tiles, num_sms, stream);
-  if (row) return launch_one<FMT, true, false, false>(p, tmap_x, tr, tiles, num_sms, stream);
-  return launch_one<FMT, false, true, false>(p, tmap_x, tr, tiles, num_sms, stream);
+  if (row && col)
+    return launch_one<FMT, true, true, false, false, PACKED>(p, tmap_x, tr, tiles, num_sms, stream);
+  if (row)
+    return launch_one<FMT, true, false, false, false, PACKED>(p, tmap_x, tr, tiles, num_sms, stream);
+  return launch_one<FMT, false, true, false, false, PACKED>(p, tmap_x, tr, tiles, num_sms, stream);
 }
 
 }  // namespace
@@ -666,6 +754,10 @@ cudaError_t launch_quantize(const QuantizeParams& p, const CUtensorMap& tmap_x,
     case 2: return launch_dense<2>(p, tmap_x, tmap_r, tiles, num_sms, stream);
     case 3: return launch_dense<3>(p, tmap_x, tmap_r, tiles, num_sms, stream);
     case 4: return launch_dense<4>(p, tmap_x, tmap_r, tiles, num_sms, stream);
+    // packed storage of the 6- and 4-bit codes
+    case 5: return launch_dense<2, true>(p, tmap_x, tmap_r, tiles, num_sms, stream);
+    case 6: return launch_dense<3, true>(p, tmap_x, tmap_r, tiles, num_sms, stream);
+    case 7: return launch_dense<4, true>(p, tmap_x, tmap_r, tiles, num_sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }

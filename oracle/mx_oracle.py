@@ -498,6 +498,52 @@ def unpack_container(buf: np.ndarray, fmt) -> np.ndarray:
     return out.astype(np.uint8).reshape(rows, k)
 
 
+def pack_dense(codes: np.ndarray, fmt) -> np.ndarray:
+    """One code per element [rows, K] -> packed storage [rows, K * w / 8]:
+    the row is one little-endian bit string with element i at bits
+    [i*w, i*w + w), w = 4 or 6 (two E2M1 codes per byte, four E2M3 / E3M2
+    codes per three bytes) -- the payload the page counts for narrow MX
+    elements, with none of the container's padding.  Layout only: no
+    arithmetic on values."""
+    f = fmt_of(fmt)
+    codes = np.asarray(codes, dtype=np.uint8)
+    if f.bits == 8:
+        return codes.copy()
+    rows, k = codes.shape
+    if (k * f.bits) % 8:
+        raise ValueError("K * w must fill whole bytes")
+    out = np.zeros((rows, k * f.bits // 8), dtype=np.uint32)
+    for i in range(k):
+        off = i * f.bits
+        byte, shift = off // 8, off % 8
+        val = codes[:, i].astype(np.uint32) << shift
+        out[:, byte] |= val & 0xFF
+        if shift + f.bits > 8:
+            out[:, byte + 1] |= val >> 8
+    return out.astype(np.uint8)
+
+
+def unpack_dense(buf: np.ndarray, fmt) -> np.ndarray:
+    """Inverse of pack_dense."""
+    f = fmt_of(fmt)
+    buf = np.asarray(buf, dtype=np.uint8)
+    if f.bits == 8:
+        return buf.copy()
+    rows, nbytes = buf.shape
+    k = nbytes * 8 // f.bits
+    b = buf.astype(np.uint32)
+    out = np.zeros((rows, k), dtype=np.uint32)
+    mask = (1 << f.bits) - 1
+    for i in range(k):
+        off = i * f.bits
+        byte, shift = off // 8, off % 8
+        val = b[:, byte] >> shift
+        if shift + f.bits > 8:
+            val |= b[:, byte + 1] << (8 - shift)
+        out[:, i] = val & mask
+    return out.astype(np.uint8)
+
+
 # --------------------------------------------------------------------------
 # Block-scaled GEMM
 # --------------------------------------------------------------------------

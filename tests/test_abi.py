@@ -56,7 +56,7 @@ def test_quantize_rejects_bad_arguments_on_the_host(mx):
     # rows not a multiple of 32 for colwise
     assert q(FAKE, 0, 40, 64, 64, 0, 2, 0, None, None, FAKE, FAKE, s) == 1
     # bad enums
-    assert q(FAKE, 0, 64, 64, 64, 7, 1, 0, FAKE, FAKE, None, None, s) == 1
+    assert q(FAKE, 0, 64, 64, 64, 8, 1, 0, FAKE, FAKE, None, None, s) == 1
     assert q(FAKE, 0, 64, 64, 64, 0, 4, 0, FAKE, FAKE, None, None, s) == 1
     assert q(FAKE, 0, 64, 64, 64, 0, 1, 9, FAKE, FAKE, None, None, s) == 1
     # fp32 input is a valid type but not implemented
@@ -151,8 +151,27 @@ def test_narrow_formats_on_the_host(mx):
         assert sr(FAKE, 0, 64, 64, 64, FAKE, 64, fmt, 1, 0, FAKE, FAKE, None, None, 0) == 3
         assert mx.mx_quantize_grouped(FAKE, 0, 64, 64, 64, fmt, 0, 4, FAKE, FAKE, FAKE, 0) == 3
     q = mx.mx_quantize
-    assert q(FAKE, 0, 64, 64, 64, 5, 1, 0, FAKE, FAKE, None, None, 0) == 1           # no format 5
+    assert q(FAKE, 0, 64, 64, 64, 8, 1, 0, FAKE, FAKE, None, None, 0) == 1           # no format 8
     assert q(FAKE, 0, 64, 40, 40, 4, 1, 0, FAKE, FAKE, None, None, 0) == 1           # cols % 32
+
+
+def test_packed_formats_on_the_host(mx):
+    """Packed 6- and 4-bit storage (formats 5-7): the GEMM wants K % 128 and
+    32-byte aligned packed code pointers; stochastic rounding and the
+    grouped quantizer stay FP8 only."""
+    g = mx.mx_gemm
+    for fmt in (5, 6, 7):
+        assert g(64, 64, 96, FAKE, FAKE, fmt, FAKE, FAKE, 0, FAKE, 0, 64, 0) == 1        # k % 128
+        assert g(64, 64, 96, FAKE, FAKE, 0, FAKE, FAKE, fmt, FAKE, 0, 64, 0) == 1
+        assert g(64, 64, 128, FAKE + 16, FAKE, fmt, FAKE, FAKE, 0, FAKE, 0, 64, 0) == 2  # a % 32
+        assert g(64, 64, 128, FAKE, FAKE, 0, FAKE + 16, FAKE, fmt, FAKE, 0, 64, 0) == 2  # b % 32
+        assert mx.mx_quantize_sr(FAKE, 0, 64, 64, 64, FAKE, 64, fmt, 1, 0, FAKE, FAKE, None, None,
+                                 0) == 3
+        assert mx.mx_quantize_grouped(FAKE, 0, 64, 64, 64, fmt, 0, 4, FAKE, FAKE, FAKE, 0) == 3
+    assert mx.storage_bytes("e2m1_packed", 128) == 64
+    assert mx.storage_bytes("e3m2_packed", 128) == 96
+    assert mx.storage_bytes("e2m1", 128) == 128
+    assert mx.storage_elems("e2m3_packed", 96) == 128
 
 
 def test_selftest_rejects_zero_limit(mx):

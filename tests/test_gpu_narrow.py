@@ -112,3 +112,91 @@ def test_mxfp4_weights_full_size_sampled(mx):
     assert torch.equal(qb.codes[cols_t].cpu(), torch.from_numpy(O.pack_container(b.codes, "e2m1")))
     y_ref, t_ref = O.gemm(a, b)
     assert_gemm_close(y[rows_t][:, cols_t], y_ref, t_ref, "bf16")
+
+
+# ---------------------------------------------------------------- packed storage
+
+PACKED = ["e2m3_packed", "e3m2_packed", "e2m1_packed"]
+
+
+def base_fmt(fmt):
+    return fmt.replace("_packed", "")
+
+
+def check_packed(q, x, fmt, axis, rule="floor"):
+    ref = O.quantize(to_f64(x), base_fmt(fmt), axis, rule)
+    want = O.pack_dense(ref.codes, base_fmt(fmt))
+    assert torch.equal(q.codes.cpu(), torch.from_numpy(want))
+    rows, k = ref.codes.shape
+    assert np.array_equal(canonical_scales(q.scales, rows, k), ref.scales)
+    return ref
+
+
+@pytest.mark.parametrize("fmt", PACKED)
+@pytest.mark.parametrize("shape", [(256, 512), (288, 352), (32, 96)])
+@pytest.mark.parametrize("rule", ["floor", "ceil"])
+def test_packed_quantize_matches_oracle(mx, fmt, shape, rule):
+    """Packed 6- and 4-bit storage (K * w / 8 bytes per code row), both
+    orientations, bit-exact against the oracle's dense packing; the same
+    codes as the container layout with its padding removed."""
+    x = inputs(*shape, seed=shape[0] * 3 + shape[1])
+    row, col = mx.quantize(x.cuda(), fmt, "both", rule=rule)
+    assert mx.device_status() == 0
+    assert row.k == shape[1] and col.k == shape[0]
+    check_packed(row, x, fmt, "row", rule)
+    check_packed(col, x, fmt, "col", rule)
+    only_row = mx.quantize(x.cuda(), fmt, "row", rule=rule)
+    only_col = mx.quantize(x.cuda(), fmt, "col", rule=rule)
+    assert torch.equal(only_row.codes, row.codes) and torch.equal(only_col.codes, col.codes)
+    cont = mx.quantize(x.cuda(), base_fmt(fmt), "row", rule=rule)
+    w = 4 if fmt == "e2m1_packed" else 6
+    runs = cont.codes.view(shape[0], -1, 16)[:, :, :2 * w].reshape(shape[0], -1)
+    assert torch.equal(runs, row.codes)
+    assert torch.equal(cont.scales, row.scales)
+
+
+@pytest.mark.parametrize("fa,fb", [("e2m1_packed", "e2m1_packed"), ("e4m3", "e2m1_packed"),
+                                   ("e2m3_packed", "e3m2_packed"), ("e3m2_packed", "e5m2"),
+                                   ("e2m1_packed", "e3m2")])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_packed_gemm_matches_oracle(mx, fa, fb, out):
+    """GEMM on packed operands (read through the unpacking tensor copy):
+    the oracle's block sum within the bound, and bit for bit the result of
+    the same codes in the container layout."""
+    m, n, k = 200, 264, 640
+    x = inputs(m, k, seed=21)
+    g = torch.Generator().manual_seed(22)
+    w = (torch.randn(k, n, generator=g) * 0.05).to(torch.bfloat16)
+    qa = mx.quantize(x.cuda(), fa, "row")
+    qb = mx.quantize(w.cuda(), fb, "col")
+    y = mx.gemm(qa, qb, out)
+    assert mx.device_status() == 0
+    a = O.quantize(to_f64(x), base_fmt(fa), "row")
+    b = O.quantize(to_f64(w), base_fmt(fb), "col")
+    y_ref, t_ref = O.gemm(a, b)
+    assert_gemm_close(y, y_ref, t_ref, out)
+    y_cont = mx.gemm(mx.quantize(x.cuda(), base_fmt(fa), "row"),
+                     mx.quantize(w.cuda(), base_fmt(fb), "col"), out)
+    assert torch.equal(y, y_cont)
+
+
+def test_packed_mxfp4_weights_full_size_sampled(mx):
+    """Forward layer 16384 x 18432 x 7168 with E4M3 activations and MXFP4
+    weights in packed storage (half the container's weight bytes), BF16 out;
+    sampled rows and columns against the oracle."""
+    from mxfp8_block_scaled_mx_gb300 import workloads as W
+    x, w = W.dense_forward(device="cuda")
+    qa = mx.quantize(x, "e4m3", "row")
+    qb = mx.quantize(w, "e2m1_packed", "col")
+    assert qb.codes.shape == (18432, 3584)
+    y = mx.gemm(qa, qb, "bf16")
+    assert mx.device_status() == 0
+    rng = np.random.default_rng(6)
+    rows = np.unique(np.concatenate([[0, 16383], rng.choice(16384, 10, replace=False)]))
+    cols = np.unique(np.concatenate([[0, 18431], rng.choice(18432, 20, replace=False)]))
+    rows_t, cols_t = torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()
+    a = O.quantize(to_f64(x[rows_t]), "e4m3", "row")
+    b = O.quantize(to_f64(w[:, cols_t]), "e2m1", "col")
+    assert torch.equal(qb.codes[cols_t].cpu(), torch.from_numpy(O.pack_dense(b.codes, "e2m1")))
+    y_ref, t_ref = O.gemm(a, b)
+    assert_gemm_close(y[rows_t][:, cols_t], y_ref, t_ref, "bf16")

@@ -709,6 +709,35 @@ def test_container_round_trip(fmt):
 
 # ---------------------------------------------------------------- swizzle
 
+@pytest.mark.parametrize("fmt", ["e2m3", "e3m2", "e2m1"])
+def test_dense_packing(fmt):
+    """Packed storage of the narrow codes: every code comes back out
+    (round trip over random codes of every value), the byte count is the
+    page's payload (K * w / 8 per row), the E2M1 nibble order is element 2i
+    in the low nibble of byte i, and each 16-element run's packed bytes are
+    exactly the container's first 8 (E2M1) or 12 (E2M3, E3M2) bytes."""
+    f = O.fmt_of(fmt)
+    rng = np.random.default_rng(17)
+    codes = rng.integers(0, 1 << f.bits, size=(5, 128), dtype=np.uint8)
+    packed = O.pack_dense(codes, fmt)
+    assert packed.shape == (5, 128 * f.bits // 8)
+    assert np.array_equal(O.unpack_dense(packed, fmt), codes)
+    runs = O.pack_container(codes, fmt).reshape(5, 8, 16)[:, :, :2 * f.bits]
+    assert np.array_equal(runs.reshape(5, -1), packed)
+    if f.bits == 4:
+        assert np.array_equal(packed & 0xF, codes[:, 0::2])
+        assert np.array_equal(packed >> 4, codes[:, 1::2])
+    else:  # four 6-bit codes a, b, c, d in three bytes, little-endian
+        a, b, c, d = (codes[:, i::4].astype(np.uint32) for i in range(4))
+        assert np.array_equal(packed[:, 0::3], (a | (b & 3) << 6).astype(np.uint8))
+        assert np.array_equal(packed[:, 1::3], (b >> 2 | (c & 15) << 4).astype(np.uint8))
+        assert np.array_equal(packed[:, 2::3], (c >> 4 | d << 2).astype(np.uint8))
+    # every code value in every position of a 16-element run
+    allc = np.array([[(v + i) % (1 << f.bits) for i in range(16)] for v in range(1 << f.bits)],
+                    dtype=np.uint8)
+    assert np.array_equal(O.unpack_dense(O.pack_dense(allc, fmt), fmt), allc)
+
+
 @pytest.mark.parametrize("rows,kb", [(1, 1), (128, 4), (130, 5), (300, 17), (256, 224)])
 def test_swizzle_is_a_bijection_and_round_trips(rows, kb):
     size = O.scale_bytes(rows, kb)
