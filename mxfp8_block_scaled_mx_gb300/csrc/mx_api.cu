@@ -133,16 +133,17 @@ mx_status encode_codes_map(CUtensorMap* map, const void* base, int64_t inner, in
 }
 
 // 2-D bf16 tensor map over x[rows, cols] (leading dimension ldx elements),
-// tile box 128 x 128, no swizzle, zero fill outside the matrix.
+// box 64 columns x 128 rows (128-byte rows, two boxes per 128 x 128 tile),
+// 128-byte swizzle, zero fill outside the matrix.
 mx_status encode_bf16_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
                           int64_t ldx) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx * 2)};
-  cuuint32_t box[2] = {128u, 128u};
+  cuuint32_t box[2] = {64u, 128u};
   cuuint32_t estr[2] = {1u, 1u};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }

@@ -233,6 +233,27 @@ __device__ __forceinline__ int unit_offset(int r, int c) {
   return (r & 31) * 16 + (r >> 5) * 4 + c;
 }
 
+// Offset in a ring slot of byte `byte` (0..255) of tile row r.  The tensor
+// copy writes the 128 x 128 bf16 tile as two 64-column halves of 128 rows x
+// 128 bytes with the 128-byte swizzle: 16-byte chunk c of row r lands at
+// chunk c ^ (r % 8) of its row.  Then a warp reading one 64-byte block from
+// each of eight rows (rowwise) or one 128-byte row segment (columnwise)
+// touches every shared-memory bank the same number of times.
+__device__ __forceinline__ int tile_offset(int r, int byte) {
+  return (byte >> 7) * (kTile * 128) + r * 128 + ((((byte >> 4) & 7) ^ (r & 7)) << 4) + (byte & 15);
+}
+
+// Largest magnitude bit pattern (sign cleared) among the 32 bf16 of v.
+__device__ __forceinline__ uint32_t amax_bits32(const uint4 (&v)[4]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    m = max_u16x2(m, max_u16x2(v[j].x & 0x7FFF7FFFu, v[j].y & 0x7FFF7FFFu));
+    m = max_u16x2(m, max_u16x2(v[j].z & 0x7FFF7FFFu, v[j].w & 0x7FFF7FFFu));
+  }
+  return max(m & 0xFFFFu, m >> 16);
+}
+
 struct Tile {
   int64_t x_row0;       // first row of x in the tile
   int64_t c0;           // first column of x in the tile
@@ -300,87 +321,90 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
   static_assert(!SR || F::kBits == 8, "stochastic rounding is built for FP8 codes");
   const uint32_t lane = lt & 31;
 
-  // Thread lt holds the 8-column chunk lt % 16 of rows lt / 16 + 16 * it.
-  const int ch = lt & 15;
-  const int lr0 = lt >> 4;
-  const int64_t gc = tl.c0 + ch * 8;
-  const bool col_ok = gc < p.cols;
-
   if constexpr (ROW) {
-    uint4 v[8];
-    uint4 rv[SR ? 8 : 1];
+    // Thread lt quantizes the 32-element block lt % 4 of tile rows lt / 4
+    // and lt / 4 + 64: it holds the whole block, so the amax needs no
+    // shuffles and the scale exponent is derived once per block.
+    const int bq = lt & 3;
+    const int lr0 = lt >> 2;
+    const int64_t gcb = tl.c0 + bq * 32;  // first column of the block
+    const bool blk_ok = gcb < p.cols;     // cols % 32 == 0: a block is whole or absent
+    uint4 v[2][4];
+    uint4 rv[SR ? 2 : 1][4];
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      v[it] = *reinterpret_cast<const uint4*>(xs + (lr0 + it * 16) * (kTile * 2) + ch * 16);
-      if constexpr (SR)
-        rv[it] = *reinterpret_cast<const uint4*>(rs + (lr0 + it * 16) * (kTile * 2) + ch * 16);
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int off = tile_offset(lr0 + 64 * h, bq * 64 + j * 16);
+        v[h][j] = *reinterpret_cast<const uint4*>(xs + off);
+        if constexpr (SR) rv[h][j] = *reinterpret_cast<const uint4*>(rs + off);
+      }
     }
     if constexpr (!COL) {
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar);  // slot fully read by this warp
     }
-    uint8_t* qp = p.q_row + (tl.x_row0 + lr0) * p.cols + gc;
-    const int64_t q_step = 16 * p.cols;
+    // bytes per code row: one per element, or w / 8 in packed storage
+    const int64_t row_bytes = PACKED ? p.cols * F::kBits / 8 : p.cols;
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int lr = lr0 + it * 16;
-      const bool ok = col_ok && lr < tl.rows_valid;
-      // the four lanes holding one 32-element block share its amax
-      uint32_t a = amax_bits8(v[it]);
-      a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
-      a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
-      uint2 codes;
+    for (int h = 0; h < 2; ++h) {
+      const int lr = lr0 + 64 * h;
+      uint2 c[4];
       uint8_t sbyte;
+      const uint32_t a = amax_bits32(v[h]);
       if (a >= 0x7F80u) {  // NaN or Inf in the block
-        codes = make_uint2(F::kNanWord, F::kNanWord);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) c[j] = make_uint2(F::kNanWord, F::kNanWord);
         sbyte = kNanScale;
       } else {
         const int e = scale_exponent<FMT>(a, p.rule);
-        if constexpr (SR) {
-          codes = encode8_sr<FMT>(v[it], rv[it], pow2_neg(e));
-        } else {
-          codes = encode8<FMT>(v[it], pow2_neg(e));
+        const float mul = pow2_neg(e);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if constexpr (SR) {
+            c[j] = encode8_sr<FMT>(v[h][j], rv[SR ? h : 0][j], mul);
+          } else {
+            c[j] = encode8<FMT>(v[h][j], mul);
+          }
         }
         sbyte = static_cast<uint8_t>(e + 127);
       }
-      if constexpr (F::kBits == 6) {  // eight codes packed into 48 bits
-        const uint32_t lo = pack4_fp6(codes.x), hi = pack4_fp6(codes.y);
-        codes = make_uint2(lo | hi << 24, hi >> 8);
-      }
-      if constexpr (F::kBits < 8 && !(PACKED && F::kBits == 4)) {
-        // Lanes 2j and 2j + 1 hold the two halves of one 16-element run.
-        // Its 16-byte container is the packed run then zero bytes: each
-        // lane writes the 8 bytes at its own FP8 offset.  Packed 6-bit
-        // storage keeps the run's first 12 bytes: the first lane writes
-        // bytes 0-7, the second bytes 8-11.
-        const uint32_t px = __shfl_xor_sync(0xffffffffu, codes.x, 1);
-        const bool first = (ch & 1) == 0;
-        if constexpr (F::kBits == 4) {
-          codes = first ? make_uint2(codes.x, px) : make_uint2(0u, 0u);
-        } else {
-          codes = first ? make_uint2(codes.x, codes.y | px << 16)
-                        : make_uint2(codes.x >> 16 | codes.y << 16, 0u);
-        }
-      }
-      if (ok) {
+      if (!blk_ok || lr >= tl.rows_valid) continue;
+      uint8_t* rowp = p.q_row + (tl.x_row0 + lr) * row_bytes;
+      if constexpr (F::kBits == 8) {
+        *reinterpret_cast<uint4*>(rowp + gcb) = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
+        *reinterpret_cast<uint4*>(rowp + gcb + 16) = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
+      } else if constexpr (F::kBits == 4) {
+        // eight codes per 32-bit word (code i in bits [4i, 4i + 4))
         if constexpr (PACKED) {
-          // packed row: element e at bit e * w; this thread's 8 elements
-          // start at byte gc * w / 8
-          uint8_t* rp = p.q_row + (tl.x_row0 + lr) * (p.cols * F::kBits / 8);
-          if constexpr (F::kBits == 4) {
-            *reinterpret_cast<uint32_t*>(rp + gc / 2) = codes.x;
-          } else if ((ch & 1) == 0) {
-            uint32_t* d = reinterpret_cast<uint32_t*>(rp + gc * 3 / 4);
-            d[0] = codes.x;
-            d[1] = codes.y;
-          } else {
-            *reinterpret_cast<uint32_t*>(rp + gc * 3 / 4 + 2) = codes.x;
-          }
-        } else {
-          *reinterpret_cast<uint2*>(qp + it * q_step) = codes;
+          *reinterpret_cast<uint4*>(rowp + gcb / 2) = make_uint4(c[0].x, c[1].x, c[2].x, c[3].x);
+        } else {  // two 16-element runs, each 8 bytes of codes then 8 zero bytes
+          *reinterpret_cast<uint4*>(rowp + gcb) = make_uint4(c[0].x, c[1].x, 0u, 0u);
+          *reinterpret_cast<uint4*>(rowp + gcb + 16) = make_uint4(c[2].x, c[3].x, 0u, 0u);
         }
-        if ((lt & 3) == 0) s_unit_row[unit_offset(lr, ch >> 2)] = sbyte;
+      } else {
+        // 6-bit codes: each run of 16 is 96 packed bits (12 bytes)
+        uint32_t g[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          g[2 * j] = pack4_fp6(c[j].x);
+          g[2 * j + 1] = pack4_fp6(c[j].y);
+        }
+        const uint32_t w0 = g[0] | g[1] << 24, w1 = g[1] >> 8 | g[2] << 16,
+                       w2 = g[2] >> 16 | g[3] << 8;
+        const uint32_t w3 = g[4] | g[5] << 24, w4 = g[5] >> 8 | g[6] << 16,
+                       w5 = g[6] >> 16 | g[7] << 8;
+        if constexpr (PACKED) {
+          uint2* d = reinterpret_cast<uint2*>(rowp + gcb * 3 / 4);
+          d[0] = make_uint2(w0, w1);
+          d[1] = make_uint2(w2, w3);
+          d[2] = make_uint2(w4, w5);
+        } else {  // each run's 12 bytes, then 4 zero bytes
+          *reinterpret_cast<uint4*>(rowp + gcb) = make_uint4(w0, w1, w2, 0u);
+          *reinterpret_cast<uint4*>(rowp + gcb + 16) = make_uint4(w3, w4, w5, 0u);
+        }
       }
+      s_unit_row[unit_offset(lr, bq)] = sbyte;
     }
   }
 
@@ -388,21 +412,20 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
     // Thread lt: columns 2*(lt % 64) and 2*(lt % 64) + 1, 32-row block
     // lt / 64.  One 32-bit shared load gives both columns of a row, so the
     // amax of the two column blocks is one SIMD max per row.
-    const uint32_t* xw = reinterpret_cast<const uint32_t*>(xs);
     const int cp = lt & 63;
     const int rb = lt >> 6;
     const bool ok = tl.c0 + 2 * cp < p.cols && rb * 32 < tl.rows_valid;
-    const uint32_t* rw_src = reinterpret_cast<const uint32_t*>(rs);
     uint32_t w[32];
     uint32_t rw[SR ? 32 : 1];
     uint32_t a2 = 0;
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
-      w[r] = xw[(rb * 32 + r) * 64 + cp];
+      const int off = tile_offset(rb * 32 + r, cp * 4);
+      w[r] = *reinterpret_cast<const uint32_t*>(xs + off);
       if constexpr (GROUPED) {
         if (rb * 32 + r >= tl.rows_valid) w[r] = 0u;
       }
-      if constexpr (SR) rw[r] = rw_src[(rb * 32 + r) * 64 + cp];
+      if constexpr (SR) rw[r] = *reinterpret_cast<const uint32_t*>(rs + off);
       a2 = max_u16x2(a2, w[r] & 0x7FFF7FFFu);
     }
     __syncwarp();
@@ -650,11 +673,14 @@ __global__ void __launch_bounds__(QSmem<COL, SR>::kThreads, 1)
         const Tile tl = tile_of<GROUPED>(p, t, col_tiles, gi);
         mbar_arrive_expect_tx(&full[s], QSmem::kSlotBytes);
         uint8_t* slot = smem + QSmem::kOffRing + s * QSmem::kSlotBytes;
-        tma_load_2d(slot, &tmap_x, &full[s], static_cast<int32_t>(tl.c0),
-                    static_cast<int32_t>(tl.x_row0));
-        if constexpr (SR)
-          tma_load_2d(slot + kTileBytes, &tmap_r, &full[s], static_cast<int32_t>(tl.c0),
-                      static_cast<int32_t>(tl.x_row0));
+        // two 64-column halves (128-byte swizzle), also for the random integers
+        for (int half = 0; half < 2; ++half) {
+          const int32_t cx = static_cast<int32_t>(tl.c0) + 64 * half;
+          const int32_t ry = static_cast<int32_t>(tl.x_row0);
+          tma_load_2d(slot + half * (kTileBytes / 2), &tmap_x, &full[s], cx, ry);
+          if constexpr (SR)
+            tma_load_2d(slot + kTileBytes + half * (kTileBytes / 2), &tmap_r, &full[s], cx, ry);
+        }
       }
       // every issued copy lands before the block exits
       for (int s = 0; s < kStages; ++s) {
