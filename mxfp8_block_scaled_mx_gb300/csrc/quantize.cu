@@ -47,15 +47,6 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   return r;
 }
 
-// Largest magnitude bit pattern (sign cleared) among the 8 bf16 of v.  For
-// non-NaN bf16 the unsigned order of these patterns is the order of |x|;
-// NaN patterns sort above +Inf (0x7F80).
-__device__ __forceinline__ uint32_t amax_bits8(const uint4 v) {
-  uint32_t m = max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
-  m = max_u16x2(m, max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-  return max(m & 0xFFFFu, m >> 16);
-}
-
 // Element formats (library enum order): 0 E4M3, 1 E5M2, 2 E2M3, 3 E3M2,
 // 4 E2M1.  kEmax = exponent of the largest binade; the largest finite value
 // has significand kMaxNum / kMaxDen (1.75 for E4M3, E5M2 and E3M2, 1.875 for
@@ -243,7 +234,9 @@ __device__ __forceinline__ int tile_offset(int r, int byte) {
   return (byte >> 7) * (kTile * 128) + r * 128 + ((((byte >> 4) & 7) ^ (r & 7)) << 4) + (byte & 15);
 }
 
-// Largest magnitude bit pattern (sign cleared) among the 32 bf16 of v.
+// Largest magnitude bit pattern (sign cleared) among the 32 bf16 of v.  For
+// non-NaN bf16 the unsigned order of these patterns is the order of |x|;
+// NaN patterns sort above +Inf (0x7F80).
 __device__ __forceinline__ uint32_t amax_bits32(const uint4 (&v)[4]) {
   uint32_t m = 0;
 #pragma unroll

@@ -168,6 +168,31 @@ def test_grouped_wgrad_matches_oracle(mx, sizes):
     run_wgrad(mx, sizes, 256, 264, "fp32", seed=len(sizes))
 
 
+@pytest.mark.parametrize("sizes", [[1000, 0, 37, 2000, 5, 800, 64], [900, 1], [3000]])
+def test_grouped_wgrad_long_and_short_experts(mx, sizes):
+    """Experts with many tokens (long contractions over many K stages)
+    beside experts with a few tokens or none, with several m- and n-tiles
+    per expert."""
+    run_wgrad(mx, sizes, 512, 520, "fp32", seed=sum(sizes) % 97)
+
+
+def test_grouped_wgrad_is_deterministic(mx):
+    """Repeated calls agree bit for bit (each output tile's contraction
+    order is fixed)."""
+    sizes = [1500, 3, 0, 700, 41, 2100, 9]
+    offsets = offsets_of(sizes)
+    total = int(offsets[-1])
+    dy = tokens(total, 768, 5, std=1e-3).cuda()
+    x = tokens(total, 512, 6).cuda()
+    d_off = torch.from_numpy(offsets).cuda()
+    qa = mx.quantize_grouped(dy, d_off, "e5m2", axis="col")
+    qb = mx.quantize_grouped(x, d_off, "e4m3", axis="col")
+    first = mx.grouped_gemm_wgrad(qa, d_off, qb, total, "fp32")
+    for _ in range(3):
+        assert torch.equal(first, mx.grouped_gemm_wgrad(qa, d_off, qb, total, "fp32"))
+    assert mx.device_status() == 0
+
+
 def test_grouped_wgrad_bf16_and_ragged_m(mx):
     run_wgrad(mx, [5, 0, 300, 40], 328, 128, "bf16", seed=13)
 
