@@ -230,7 +230,6 @@ ROW_WARMUP = 10
 ROW_REPS = 50
 ROW_MAX_REPS = 4000
 ROW_SECONDS = 0.25
-SM_MAX_MHZ = 2070.0
 
 
 def _reps_for(one_ms: float, reps: int | None) -> int:
@@ -285,6 +284,31 @@ def time_kernel(fn, stream, reps: int | None = ROW_REPS, warmup: int = ROW_WARMU
     return timed_launches(fn, stream, reps, warmup)[0]
 
 
+BURST_IDLE_S = 0.5
+BURST_LAUNCHES = 8
+
+
+def timed_burst(fn, stream, launches: int = BURST_LAUNCHES, idle_s: float = BURST_IDLE_S) -> float:
+    """Median duration (ms) of `launches` back-to-back launches of an
+    already warmed-up fn(), started after the GPU has idled for `idle_s`
+    seconds: the kernel timed alone, before the power cap lowers the clock
+    (the counterpart of the measured burst peak)."""
+    import torch
+    torch.cuda.synchronize()
+    time.sleep(idle_s)
+    with torch.cuda.stream(stream):
+        events = []
+        for _ in range(launches):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            events.append((a, b))
+        torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in events)
+
+
 def timed_graph(call, nbuf: int, stream, launches: int):
     """Steady-state duration (ms) per launch: `launches` calls (call(i) runs
     on `stream` with buffer set i % nbuf) captured in one CUDA graph and
@@ -325,7 +349,9 @@ def timed_graph(call, nbuf: int, stream, launches: int):
 class RowClocks:
     """The host-time window of every row's timed region; once the clock
     sampler has stopped, each row gets the median SM clock of the samples
-    in its window and its throughput scaled to the maximum SM clock."""
+    in its window.  (No throughput is scaled by it: under the power cap the
+    sampled clock reads well below the clock the kernels effectively ran
+    at, so GEMM rows carry a burst time instead, see gemm rows.)"""
 
     def __init__(self):
         self.windows = []
@@ -334,14 +360,10 @@ class RowClocks:
         self.windows.append((row, window, key))
 
     def fill(self, sampler):
-        for row, (t0, t1), key in self.windows:
+        for row, (t0, t1), _key in self.windows:
             c = sampler.summary(t0, t1)
             row["sm_mhz_median"] = c["sm_mhz"]
             row["clock_samples"] = c["samples"]
-            if c["sm_mhz"] and key in row:
-                row["clock_normalized"] = {
-                    key: round(row[key] * SM_MAX_MHZ / c["sm_mhz"], 1),
-                    "def": f"{key} x {SM_MAX_MHZ:.0f} / median SM MHz of the row"}
 
 
 def flush_l2(buf):
@@ -412,6 +434,8 @@ def moe_roofline(sizes, n: int, k: int, kind: str, flops_peak: float, hbm_gbs: f
 def with_roofline(row: dict, roof: dict) -> dict:
     row["roofline"] = dict(roof, frac=round(roof["time_ms"] / row["ms"], 3),
                            per_expert_frac=round(roof["per_expert_ms"] / row["ms"], 3))
+    if "burst" in row:
+        row["burst"]["roofline_frac"] = round(roof["time_ms"] / row["burst"]["ms"], 3)
     return row
 
 
@@ -426,9 +450,19 @@ def measure_rows(mx, peaks, dev, stream, local: int = 0):
     return out
 
 
-def _gemm_row(fl: float, t: float, fp8_peak: float) -> dict:
-    return {"ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
-            "frac_fp8_peak": round(fl / (t * 1e-3) / 1e12 / fp8_peak, 3)}
+def _gemm_row(fl: float, t: float, tb: float, fp8_peak: float, fp8_sustained: float) -> dict:
+    """A GEMM row: `t` the median over a >= 0.25 s loop of launches (the
+    power cap active, compared with the sustained peak as well), `tb` the
+    burst time after an idle pause (compared with the burst peak)."""
+    tf = fl / (t * 1e-3) / 1e12
+    tfb = fl / (tb * 1e-3) / 1e12
+    return {"ms": round(t, 4), "TFLOP/s": round(tf, 1),
+            "frac_fp8_peak": round(tf / fp8_peak, 3),
+            "frac_fp8_sustained_peak": round(tf / fp8_sustained, 3),
+            "burst": {"ms": round(tb, 4), "TFLOP/s": round(tfb, 1),
+                      "frac_fp8_peak": round(tfb / fp8_peak, 3),
+                      "form": f"median of {BURST_LAUNCHES} back-to-back launches after "
+                              f"{BURST_IDLE_S:g} s idle"}}
 
 
 def _measure_rows(mx, peaks, dev, stream, clocks: RowClocks):
@@ -438,13 +472,15 @@ def _measure_rows(mx, peaks, dev, stream, clocks: RowClocks):
     out = {}
     hbm = peaks["hbm_gbs"]
     fp8_peak = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
+    fp8_sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * NOMINAL_FP8_OVER_BF16
     scrub = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     clean = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
 
     def gemm_row(name, fn, fl, extra=None):
         t, win = timed_launches(fn, stream)
-        row = _gemm_row(fl, t, fp8_peak)
+        tb = timed_burst(fn, stream)
+        row = _gemm_row(fl, t, tb, fp8_peak, fp8_sustained)
         if extra:
             row.update(extra)
         clocks.mark(row, win, "TFLOP/s")
