@@ -220,6 +220,15 @@ mx_status gemm_common(const GemmShape& g, const uint8_t* a, const uint8_t* sa, m
   if (m > INT32_MAX || g.b_rows > INT32_MAX || k > INT32_MAX || g.lda > INT32_MAX ||
       g.ldb > INT32_MAX)
     return MX_ERR_UNSUPPORTED;
+  // the kernels index their 256x256 work units in 32 bits
+  {
+    const int64_t m_tiles = ceil_div(m, 128);
+    int64_t units = g.mode == mx::kModeGroupM ? (m_tiles + g.groups + 1) / 2 + g.groups
+                                              : (m_tiles + 1) / 2;
+    units *= ceil_div(n, 256);
+    if (g.mode == mx::kModeGroupK) units *= g.groups;
+    if (units > INT32_MAX) return MX_ERR_UNSUPPORTED;
+  }
   const int64_t elt = y_dtype == MX_FP32 ? 4 : 2;
   if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(y) ||
       (ldy * elt) % 16 != 0 || g.lda % 16 != 0 || g.ldb % 16 != 0)

@@ -46,6 +46,9 @@ struct TileInfo {
 // m-units, then n; units grouped along K walk groups, then m-units, then n,
 // every group covering the whole [m, n] output of its own matrix.  Scale
 // units: 512 bytes per 128 rows x 128 K, ceil(ld / 128) per 128-row tile.
+// The host keeps the unit count below 2^31, so the unit index arithmetic
+// runs in 32 bits (a 64-bit division by a run-time value costs several
+// hundred cycles on the epilogue's path between two tiles).
 template <int BN, int MODE, int CM>
 __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t u, int64_t n_tiles,
                                               uint32_t rank, const GroupSmem* gs) {
@@ -56,9 +59,12 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t u, in
   ti.b_kx0 = 0;
   ti.sfb_step = b_tiles_k;
   ti.k_blocks = static_cast<int32_t>(p.k / 32);
+  const uint32_t u32 = static_cast<uint32_t>(u);
+  const uint32_t nt32 = static_cast<uint32_t>(n_tiles);
   if constexpr (MODE == kModeGroupM) {
-    const int64_t mu = u / n_tiles;
-    const int64_t n_blk = u - mu * n_tiles;
+    const uint32_t mu32 = u32 / nt32;
+    const int64_t mu = mu32;
+    const int64_t n_blk = u32 - mu32 * nt32;
     const int g = find_group(gs->units, p.groups, static_cast<int32_t>(mu));
     const int64_t lm = (mu - gs->units[g]) * CM + rank;  // m-tile inside the group
     const int64_t g_tiles = gs->tiles[g + 1] - gs->tiles[g];
@@ -84,11 +90,12 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t u, in
     ti.sfb_unit = ti.sfb_rt * b_tiles_k + ti.sfb_kt0;
   } else if constexpr (MODE == kModeGroupK) {
     const int64_t m_tiles = (p.m + kTileM - 1) / kTileM;
-    const int64_t per_group = ((m_tiles + CM - 1) / CM) * n_tiles;
-    const int g = static_cast<int>(u / per_group);
-    const int64_t w = u - g * per_group;
-    const int64_t mu = w / n_tiles;
-    const int64_t n_blk = w - mu * n_tiles;
+    const uint32_t per_group = static_cast<uint32_t>((m_tiles + CM - 1) / CM) * nt32;
+    const int g = static_cast<int>(u32 / per_group);
+    const uint32_t w = u32 - static_cast<uint32_t>(g) * per_group;
+    const uint32_t mu32 = w / nt32;
+    const int64_t mu = mu32;
+    const int64_t n_blk = w - mu32 * nt32;
     const int64_t m_blk = mu * CM + rank;
     const int64_t kt0 = gs->tiles[g];  // the group's first 128-column K tile
     ti.m0 = m_blk * kTileM;
@@ -108,13 +115,15 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t u, in
   } else {
     const int64_t m_tiles = (p.m + kTileM - 1) / kTileM;
     const int64_t m_units = (m_tiles + CM - 1) / CM;
-    const int64_t band_units = p.band_m / CM;
-    const int64_t band_size = band_units * n_tiles;
-    const int64_t band = u / band_size;
-    const int64_t within = u - band * band_size;
-    const int64_t in_band = ::min(band_units, m_units - band * band_units);
-    const int64_t n_blk = within / in_band;
-    const int64_t mu = band * band_units + (within - n_blk * in_band);
+    const uint32_t band_units = static_cast<uint32_t>(p.band_m / CM);
+    const uint32_t band_size = band_units * nt32;
+    const uint32_t band = u32 / band_size;
+    const uint32_t within = u32 - band * band_size;
+    const uint32_t in_band =
+        static_cast<uint32_t>(::min(static_cast<int64_t>(band_units), m_units - band * band_units));
+    const uint32_t n_blk32 = within / in_band;
+    const int64_t n_blk = n_blk32;
+    const int64_t mu = static_cast<int64_t>(band) * band_units + (within - n_blk32 * in_band);
     const int64_t m_blk = mu * CM + rank;
     ti.m0 = m_blk * kTileM;
     ti.y_row0 = ti.m0;
