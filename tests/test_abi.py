@@ -85,6 +85,8 @@ def test_gemm_rejects_bad_arguments_on_the_host(mx):
     assert g(64, 64, 64, None, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # null
     assert g(64, 64, 64, FAKE + 4, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 2  # misaligned
     assert g(64, 64, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 68, s) == 2      # ldy*2 % 16
+    big = 1 << 30                                       # 2^44 work units: beyond 32-bit indexing
+    assert g(big, big, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, big, s) == 3
     assert ok
 
 
@@ -126,6 +128,8 @@ def test_grouped_backward_calls_reject_bad_arguments_on_the_host(mx):
     assert wg(0, FAKE, 100, 64, 64, 256, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 1, 0) == 1      # groups
     assert wg(4, FAKE, 100, 64, 60, 256, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 1, 0) == 1      # n % 8
     assert wg(4, FAKE, 100, 64, 64, 256, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE + 4, 1, 0) == 2  # y align
+    # 1000 experts x 4096 x 4096 work units of 256x256: more than 2^31
+    assert wg(1000, FAKE, 100, 1 << 20, 1 << 20, 256, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 1, 0) == 3
 
 
 def test_fused_epilogue_rejects_bad_arguments_on_the_host(mx):
