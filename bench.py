@@ -370,12 +370,27 @@ def flush_l2(buf):
     buf.add_(1)
 
 
+def launch_floor(stream, scrub, clean) -> dict:
+    """The timing harness's own floor: the per-launch time (CUDA events
+    around one launch, behind the same flushes as the bandwidth rows) of a
+    trivial kernel, a one-block fill of 16 floats."""
+    import torch
+    tiny = torch.zeros(16, device=scrub.device)
+    t, _ = timed_launches(lambda: tiny.fill_(1.0), stream, pre=lambda: flush_l2(scrub))
+    tc, _ = timed_launches(lambda: tiny.fill_(1.0), stream,
+                           pre=lambda: (flush_l2(scrub), clean.sum()))
+    return {"flush_ms": round(t, 4), "clean_l2_ms": round(tc, 4),
+            "form": "one-block fill of 16 floats between the same CUDA events, behind the "
+                    "same flushes"}
+
+
 def bandwidth_row(fn, stream, scrub, clean, nbytes: float, hbm: float, bpe: float,
-                  clocks: RowClocks, steady=None) -> dict:
+                  clocks: RowClocks, steady=None, floor=None) -> dict:
     """A bandwidth row: one launch timed right behind an L2 write flush, and
     behind the write flush plus a read pass (clean L2); with `steady`
     (call(i), buffer sets, launches per graph), also the steady-state time
-    per launch of back-to-back launches over rotating buffers."""
+    per launch of back-to-back launches over rotating buffers; with `floor`
+    (launch_floor()), the clean-L2 rate once the harness floor is taken off."""
     t, win = timed_launches(fn, stream, pre=lambda: flush_l2(scrub))
     tc, _ = timed_launches(fn, stream, pre=lambda: (flush_l2(scrub), clean.sum()))
     gbs = nbytes / (t * 1e-3) / 1e9
@@ -383,6 +398,9 @@ def bandwidth_row(fn, stream, scrub, clean, nbytes: float, hbm: float, bpe: floa
     row = {"ms": round(t, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3),
            "bytes_per_elem": bpe,
            "clean_l2": {"ms": round(tc, 4), "GB/s": round(gbc, 1), "frac_hbm": round(gbc / hbm, 3)}}
+    if floor is not None and tc > floor["clean_l2_ms"]:
+        gbf = nbytes / ((tc - floor["clean_l2_ms"]) * 1e-3) / 1e9
+        row["clean_l2"]["frac_hbm_beyond_floor"] = round(gbf / hbm, 3)
     if steady is not None:
         call, nbuf, launches = steady
         ts, _ = timed_graph(call, nbuf, stream, launches)
@@ -490,6 +508,8 @@ def _measure_rows(mx, peaks, dev, stream, clocks: RowClocks):
     # quantize bandwidth sweep: 4096x4096 and 16384x8192.  Each launch is
     # timed alone right behind an L2 write flush (and behind a flush plus a
     # read pass), and back to back over rotating buffer sets in a CUDA graph.
+    floor = launch_floor(stream, scrub, clean)
+    out["launch_floor"] = floor
     for (r, c), seed in (((4096, 4096), 0), ((16384, 8192), 1)):
         set_bytes = r * c * 2 + r * c + mx.mx_scale_bytes(r, c)
         nbuf = max(2, -(-4 * l2_bytes // set_bytes) + 1)
@@ -517,7 +537,8 @@ def _measure_rows(mx, peaks, dev, stream, clocks: RowClocks):
                     assert st == 0
                 steady = (qi, nbuf, 4 * nbuf)
             out[f"quantize_{r}x{c}_{mode}"] = bandwidth_row(q, stream, scrub, clean,
-                                                            r * c * bpe, hbm, bpe, clocks, steady)
+                                                            r * c * bpe, hbm, bpe, clocks, steady,
+                                                            floor)
         if (r, c) == (16384, 8192):
             # the page's conservative (ceil) scale rule, rowwise E4M3
             def qceil():
