@@ -66,9 +66,9 @@ struct QuantizeParams {
                        // 128-padded token capacity, a multiple of 128)
 };
 
-// tmap_x: 2-D bf16 tensor map over x (box 128 x 128, no swizzle); tmap_r:
-// the same over the 16-bit random integers for stochastic rounding, or
-// nullptr for round-to-nearest-even.
+// tmap_x: 2-D bf16 tensor map over x (box 64 columns x 128 rows, 128-byte
+// swizzle); tmap_r: the same over the 16-bit random integers for stochastic
+// rounding, or nullptr for round-to-nearest-even.
 cudaError_t launch_quantize(const QuantizeParams& p, const CUtensorMap& tmap_x,
                             const CUtensorMap* tmap_r, int num_sms, cudaStream_t stream);
 // Grouped: rowwise (q_row) and/or columnwise (q_col, per-group padded
