@@ -277,3 +277,16 @@ def test_moe_backward_full_size_sampled(mx):
         y_ref, t_ref = O.grouped_wgrad(a, b)
         assert_gemm_close(dw[e][ncols_t][:, kcols_t], y_ref[0], t_ref[0], "fp32")
     assert (sizes == 0).sum() >= 2
+
+
+def test_grouped_backward_largest_group_count(mx):
+    """1000 experts (the library's maximum), most of them without tokens and
+    a few ragged: the data gradient (experts side by side along K) and the
+    weight gradient (grouped along K, zeros for the empty experts) read
+    every entry of the device group table."""
+    sizes = np.zeros(1000, dtype=np.int64)
+    rng = np.random.default_rng(21)
+    sizes[rng.choice(1000, 10, replace=False)] = rng.integers(1, 300, 10)
+    sizes = [int(v) for v in sizes]
+    run_dgrad(mx, sizes, 136, 128, "fp32", seed=21)
+    run_wgrad(mx, sizes, 128, 136, "fp32", seed=22)
