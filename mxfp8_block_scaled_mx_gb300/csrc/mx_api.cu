@@ -422,6 +422,9 @@ mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_
   if (row && cols % 32 != 0) return MX_ERR_INVALID_ARG;
   if (col && (ldq_col <= 0 || ldq_col % 128 != 0)) return MX_ERR_INVALID_ARG;
   if (ceil_div(cols, 128) > 65535) return MX_ERR_UNSUPPORTED;
+  // the columnwise pass numbers its 128x128 tiles in 32 bits
+  if (col && (ceil_div(total_rows, 128) + groups) * ceil_div(cols, 128) > UINT32_MAX)
+    return MX_ERR_UNSUPPORTED;
   if (!aligned16(x) || ldx % 8 != 0) return MX_ERR_MISALIGNED;
   if ((row && (!aligned16(q_row) || !aligned16(s_row))) ||
       (col && (!aligned16(q_col) || !aligned16(s_col))))

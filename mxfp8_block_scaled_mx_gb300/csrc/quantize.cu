@@ -261,16 +261,32 @@ struct GroupInfo {
 };
 
 // Tile t of the launch: dense tiles are (row tile, column tile) in
-// row-major order; grouped tiles walk the per-group padded row tiles.
-template <bool GROUPED>
+// row-major order; grouped tiles walk the per-group padded row tiles.  The
+// grouped columnwise pass divides in 32 bits (the host keeps its tile
+// count below 2^32) and finds the tile's group by walking forward from the
+// previous tile's group (`g_hint`, per caller: its tiles come in increasing
+// order) instead of a binary search: 11 % faster there, while the walk
+// measured slower on the rowwise pass, which keeps the search.
+template <bool GROUPED, bool COL>
 __device__ __forceinline__ Tile tile_of(const QuantizeParams& p, int64_t t, int64_t col_tiles,
-                                        const GroupInfo* gi) {
+                                        const GroupInfo* gi, int& g_hint) {
   Tile tl;
-  const int64_t rt = t / col_tiles;
+  int64_t rt;
+  if constexpr (GROUPED && COL)
+    rt = static_cast<uint32_t>(t) / static_cast<uint32_t>(col_tiles);
+  else
+    rt = t / col_tiles;
   tl.c0 = (t - rt * col_tiles) * kTile;
   tl.scale_rt = rt;
   if constexpr (GROUPED) {
-    const int g = find_group(gi->tiles, p.groups, static_cast<int32_t>(rt));
+    int g;
+    if constexpr (COL) {
+      g = g_hint;
+      while (g + 1 < p.groups && gi->tiles[g + 1] <= rt) ++g;
+      g_hint = g;
+    } else {
+      g = find_group(gi->tiles, p.groups, static_cast<int32_t>(rt));
+    }
     tl.x_row0 = static_cast<int64_t>(gi->off[g]) + (rt - gi->tiles[g]) * kTile;
     tl.rows_valid = ::min(static_cast<int64_t>(kTile), gi->off[g + 1] - tl.x_row0);
   } else {
@@ -659,11 +675,12 @@ __global__ void __launch_bounds__(QSmem<COL, SR>::kThreads, 1)
   if (warp == kProducerWarp) {
     if (lane == 0) {
       int64_t issued = 0;
+      int g_hint = 0;
       for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x, ++issued) {
         const uint32_t s = static_cast<uint32_t>(issued % kStages);
         const uint32_t ph = static_cast<uint32_t>((issued / kStages) & 1);
         if (!mbar_wait(&empty[s], ph ^ 1u, s_abort, p.status, p.wait_limit_ns)) break;
-        const Tile tl = tile_of<GROUPED>(p, t, col_tiles, gi);
+        const Tile tl = tile_of<GROUPED, COL>(p, t, col_tiles, gi, g_hint);
         mbar_arrive_expect_tx(&full[s], QSmem::kSlotBytes);
         uint8_t* slot = smem + QSmem::kOffRing + s * QSmem::kSlotBytes;
         // two 64-column halves (128-byte swizzle), also for the random integers
@@ -691,11 +708,12 @@ __global__ void __launch_bounds__(QSmem<COL, SR>::kThreads, 1)
     uint8_t* s_unit_row = gbuf + (COL ? kTile * kColPitch : 0);
     uint8_t* s_unit_col = s_unit_row + 512;
     int64_t i = group;  // this block's tile counter; the group takes every kGroups-th tile
+    int g_hint = 0;
     for (int64_t t = blockIdx.x + group * static_cast<int64_t>(gridDim.x); t < num_tiles;
          t += kGroups * static_cast<int64_t>(gridDim.x), i += kGroups) {
       const uint32_t s = static_cast<uint32_t>(i % kStages);
       const uint32_t ph = static_cast<uint32_t>((i / kStages) & 1);
-      const Tile tl = tile_of<GROUPED>(p, t, col_tiles, gi);
+      const Tile tl = tile_of<GROUPED, COL>(p, t, col_tiles, gi, g_hint);
       group_bar(group);  // the group's previous tile is fully written out
       if (lt < 128) {
         if (ROW) reinterpret_cast<uint32_t*>(s_unit_row)[lt] = 0u;

@@ -115,6 +115,10 @@ def test_grouped_backward_calls_reject_bad_arguments_on_the_host(mx):
     assert qx(FAKE, 0, 64, 64, 64, 0, 2, 0, 0, FAKE, None, None, FAKE, 256, FAKE, 0) == 1  # groups
     assert qx(FAKE, 0, 64, 40, 40, 0, 3, 0, 4, FAKE, FAKE, FAKE, FAKE, 256, FAKE, 0) == 1  # row cols % 32
     assert qx(FAKE, 0, 64, 64, 64, 0, 2, 0, 4, FAKE, None, None, FAKE + 8, 256, FAKE, 0) == 2  # align
+    # (2^24 + 4) x 65535 padded column tiles: beyond 32-bit tile numbers
+    big = (1 << 31) - 1
+    assert qx(FAKE, 0, big, 65535 * 128, 65535 * 128, 0, 2, 0, 4, FAKE, None, None, FAKE,
+              1 << 31, FAKE, 0) == 3
     bc = mx.mx_grouped_gemm_bcat
     # (groups, offsets, total_m, n, k, a, sa, fa, b, ldb, sb, fb, y, y_dtype, s)
     assert bc(4, FAKE, 64, 128, 96, FAKE, FAKE, 0, FAKE, 384, FAKE, 0, FAKE, 0, 0) == 1     # k % 128
