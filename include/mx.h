@@ -41,8 +41,8 @@
  *    dimension must span a multiple of 16 bytes (MX_ERR_MISALIGNED).
  *  - Sizes: rows, K and leading dimensions up to 2^31 - 1; a GEMM whose
  *    256x256 output tiles (over all groups) number 2^31 or more, and a
- *    grouped columnwise quantization whose padded 128x128 tiles number 2^32
- *    or more, return MX_ERR_UNSUPPORTED.
+ *    quantization whose (padded) 128x128 tiles number 2^32 or more, return
+ *    MX_ERR_UNSUPPORTED.
  *
  * Scale layout ("swizzled", the operand layout of the tensor-core
  * block-scaled MMA; the pages require the layout to be recorded with the

@@ -333,6 +333,9 @@ mx_status quantize_common(const void* x, mx_dtype x_dtype, int64_t rows, int64_t
   if (row && cols % 32 != 0) return MX_ERR_INVALID_ARG;
   if (col && rows % 32 != 0) return MX_ERR_INVALID_ARG;
   if (ceil_div(cols, 128) > 65535) return MX_ERR_UNSUPPORTED;
+  // the kernels number their 128x128 tiles in 32 bits
+  if (cols > 0 && ceil_div(rows, 128) > static_cast<int64_t>(UINT32_MAX) / ceil_div(cols, 128))
+    return MX_ERR_UNSUPPORTED;
   if (!aligned16(x) || ldx % 8 != 0) return MX_ERR_MISALIGNED;
   if (rbits && (!aligned16(rbits) || ldr % 8 != 0)) return MX_ERR_MISALIGNED;
   if ((row && (!aligned16(q_row) || !aligned16(s_row))) ||

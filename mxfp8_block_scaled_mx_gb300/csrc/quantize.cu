@@ -262,17 +262,19 @@ struct GroupInfo {
 
 // Tile t of the launch: dense tiles are (row tile, column tile) in
 // row-major order; grouped tiles walk the per-group padded row tiles.  The
-// grouped columnwise pass divides in 32 bits (the host keeps its tile
-// count below 2^32) and finds the tile's group by walking forward from the
-// previous tile's group (`g_hint`, per caller: its tiles come in increasing
-// order) instead of a binary search: 11 % faster there, while the walk
-// measured slower on the rowwise pass, which keeps the search.
-template <bool GROUPED, bool COL>
+// grouped columnwise pass divides in 32 bits and finds the tile's group by
+// walking forward from the previous tile's group (`g_hint`, per caller: its
+// tiles come in increasing order) instead of a binary search: 11 % faster
+// there, while the walk measured slower on the rowwise pass, which keeps
+// the search.  Dense single-orientation passes divide in 32 bits too (1-2 %
+// faster; the two-orientation pass measured slower that way).  The host
+// keeps those launches' tile counts below 2^32.
+template <bool GROUPED, bool ROW, bool COL>
 __device__ __forceinline__ Tile tile_of(const QuantizeParams& p, int64_t t, int64_t col_tiles,
                                         const GroupInfo* gi, int& g_hint) {
   Tile tl;
   int64_t rt;
-  if constexpr (GROUPED && COL)
+  if constexpr ((GROUPED && COL) || (!GROUPED && ROW != COL))
     rt = static_cast<uint32_t>(t) / static_cast<uint32_t>(col_tiles);
   else
     rt = t / col_tiles;
@@ -680,7 +682,7 @@ __global__ void __launch_bounds__(QSmem<COL, SR>::kThreads, 1)
         const uint32_t s = static_cast<uint32_t>(issued % kStages);
         const uint32_t ph = static_cast<uint32_t>((issued / kStages) & 1);
         if (!mbar_wait(&empty[s], ph ^ 1u, s_abort, p.status, p.wait_limit_ns)) break;
-        const Tile tl = tile_of<GROUPED, COL>(p, t, col_tiles, gi, g_hint);
+        const Tile tl = tile_of<GROUPED, ROW, COL>(p, t, col_tiles, gi, g_hint);
         mbar_arrive_expect_tx(&full[s], QSmem::kSlotBytes);
         uint8_t* slot = smem + QSmem::kOffRing + s * QSmem::kSlotBytes;
         // two 64-column halves (128-byte swizzle), also for the random integers
@@ -713,7 +715,7 @@ __global__ void __launch_bounds__(QSmem<COL, SR>::kThreads, 1)
          t += kGroups * static_cast<int64_t>(gridDim.x), i += kGroups) {
       const uint32_t s = static_cast<uint32_t>(i % kStages);
       const uint32_t ph = static_cast<uint32_t>((i / kStages) & 1);
-      const Tile tl = tile_of<GROUPED, COL>(p, t, col_tiles, gi, g_hint);
+      const Tile tl = tile_of<GROUPED, ROW, COL>(p, t, col_tiles, gi, g_hint);
       group_bar(group);  // the group's previous tile is fully written out
       if (lt < 128) {
         if (ROW) reinterpret_cast<uint32_t*>(s_unit_row)[lt] = 0u;

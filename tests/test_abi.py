@@ -70,6 +70,8 @@ def test_quantize_rejects_bad_arguments_on_the_host(mx):
     assert q(FAKE + 2, 0, 64, 64, 64, 0, 1, 0, FAKE, FAKE, None, None, s) == 2
     assert q(FAKE, 0, 64, 64, 68, 0, 1, 0, FAKE, FAKE, None, None, s) == 2
     assert q(FAKE, 0, 64, 64, 64, 0, 1, 0, FAKE + 8, FAKE, None, None, s) == 2
+    # 2^32 or more 128x128 tiles (tile numbers are 32-bit)
+    assert q(FAKE, 0, 1 << 40, 8192, 8192, 0, 1, 0, FAKE, FAKE, None, None, s) == 3
 
 
 def test_gemm_rejects_bad_arguments_on_the_host(mx):
