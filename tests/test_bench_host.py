@@ -106,3 +106,29 @@ def test_moe_roofline_bounds():
         assert m["per_expert_ms"] >= m["time_ms"] - 1e-9
         row = bench.with_roofline({"ms": 2 * m["time_ms"]}, m)
         assert row["roofline"]["frac"] == 0.5
+
+
+def test_gemm_row_reports_loop_and_burst_against_both_peaks():
+    fl = 2 * 16384 * 18432 * 7168
+    row = bench._gemm_row(fl, 1.30, 1.14, 3781.4, 3393.4)
+    assert row["ms"] == 1.3 and row["burst"]["ms"] == 1.14
+    assert abs(row["TFLOP/s"] - fl / 1.30e-3 / 1e12) < 0.1
+    assert abs(row["frac_fp8_peak"] - row["TFLOP/s"] / 3781.4) < 1e-3
+    assert abs(row["frac_fp8_sustained_peak"] - row["TFLOP/s"] / 3393.4) < 1e-3
+    assert abs(row["burst"]["frac_fp8_peak"] - row["burst"]["TFLOP/s"] / 3781.4) < 1e-3
+    roof = {"time_ms": 0.5, "per_expert_ms": 0.6}
+    bench.with_roofline(row, roof)
+    assert row["roofline"]["frac"] == round(0.5 / 1.30, 3)
+    assert row["burst"]["roofline_frac"] == round(0.5 / 1.14, 3)
+
+
+def test_row_clocks_record_the_sampled_median_only():
+    class Sampler:
+        def summary(self, t0, t1):
+            return {"sm_mhz": 1500.0, "samples": 4}
+    rc = bench.RowClocks()
+    row = {"TFLOP/s": 3000.0}
+    rc.mark(row, (0.0, 1.0), "TFLOP/s")
+    rc.fill(Sampler())
+    assert row["sm_mhz_median"] == 1500.0 and row["clock_samples"] == 4
+    assert "clock_normalized" not in row
