@@ -200,3 +200,63 @@ def test_packed_mxfp4_weights_full_size_sampled(mx):
     assert torch.equal(qb.codes[cols_t].cpu(), torch.from_numpy(O.pack_dense(b.codes, "e2m1")))
     y_ref, t_ref = O.gemm(a, b)
     assert_gemm_close(y[rows_t][:, cols_t], y_ref, t_ref, "bf16")
+
+
+# ---------------------------------------------------------------- narrow expert weights
+
+MOE_SIZES = [0, 1, 31, 200, 0, 128, 129, 5]
+
+
+@pytest.mark.parametrize("fb", ["e2m1", "e2m1_packed", "e2m3_packed", "e3m2"])
+def test_grouped_gemm_narrow_expert_weights(mx, fb):
+    """Mixture-of-experts forward with E4M3 tokens and MXFP4 / MXFP6 expert
+    weights, container or packed storage: every expert against the oracle's
+    block sum, and packed weights equal bit for bit to the container layout
+    of the same codes."""
+    offsets = np.concatenate([[0], np.cumsum(MOE_SIZES)]).astype(np.int32)
+    groups, total = len(MOE_SIZES), int(offsets[-1])
+    n, k = 256, 384
+    x = inputs(total, k, seed=31)
+    g = torch.Generator().manual_seed(32)
+    w = (torch.randn(groups, n, k, generator=g) * 0.05).to(torch.bfloat16)
+    d_off = torch.from_numpy(offsets).cuda()
+    qa = mx.quantize_grouped(x.cuda(), d_off, "e4m3")
+    qw = mx.quantize(w.cuda().view(groups * n, k), fb, "row")
+    qb = mx.MxTensor(qw.codes.view(groups, n, -1), qw.scales, fb)
+    y = mx.grouped_gemm(qa, d_off, qb, "fp32")
+    assert mx.device_status() == 0
+    a = O.quantize(to_f64(x), "e4m3", "row")
+    for e in range(groups):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi == lo:
+            continue
+        be = O.quantize(to_f64(w[e]), base_fmt(fb), "row")
+        y_ref, t_ref = O.gemm(O.MxBlocks(a.codes[lo:hi], a.scales[lo:hi], a.fmt), be)
+        assert_gemm_close(y[lo:hi], y_ref, t_ref, "fp32")
+    if fb.endswith("_packed"):
+        qc = mx.quantize(w.cuda().view(groups * n, k), base_fmt(fb), "row")
+        yc = mx.grouped_gemm(qa, d_off, mx.MxTensor(qc.codes.view(groups, n, k), qc.scales,
+                                                    base_fmt(fb)), "fp32")
+        assert torch.equal(y, yc)
+
+
+@pytest.mark.parametrize("fb", ["e2m1_packed", "e2m3"])
+def test_grouped_dgrad_narrow_expert_weights(mx, fb):
+    """Mixture-of-experts data gradient (experts side by side along K) with
+    E5M2 gradients and MXFP4 / MXFP6 expert weights quantized columnwise
+    from the stacked weights, against the oracle per expert."""
+    offsets = np.concatenate([[0], np.cumsum(MOE_SIZES)]).astype(np.int32)
+    groups, total = len(MOE_SIZES), int(offsets[-1])
+    n_model, n_expert = 264, 256
+    dy = inputs(total, n_expert, seed=41)
+    g = torch.Generator().manual_seed(42)
+    w = (torch.randn(groups, n_expert, n_model, generator=g) * 0.02).to(torch.bfloat16)
+    d_off = torch.from_numpy(offsets).cuda()
+    qa = mx.quantize_grouped(dy.cuda(), d_off, "e5m2")
+    qb = mx.quantize(w.cuda().view(groups * n_expert, n_model), fb, "col")
+    y = mx.grouped_gemm_bcat(qa, d_off, qb, "fp32")
+    assert mx.device_status() == 0
+    a = O.quantize(to_f64(dy), "e5m2", "row")
+    bs = [O.quantize(to_f64(w[e]), base_fmt(fb), "col") for e in range(groups)]
+    y_ref, t_ref = O.grouped_gemm(a, offsets, bs)
+    assert_gemm_close(y, y_ref, t_ref, "fp32")
