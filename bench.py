@@ -414,9 +414,11 @@ def bandwidth_row(fn, stream, scrub, clean, nbytes: float, hbm: float, bpe: floa
 
 # ---------------------------------------------------------------- per-row measurements
 
-def moe_roofline(sizes, n: int, k: int, kind: str, flops_peak: float, hbm_gbs: float) -> dict:
+def moe_roofline(sizes, n: int, k: int, kind: str, flops_peak: float, hbm_gbs: float,
+                 w_code_bytes: float = 1.0) -> dict:
     """Roofline of a mixture-of-experts GEMM.  Per expert with t tokens
-    (codes 1 byte and scales 1/32 byte per element):
+    (codes 1 byte and scales 1/32 byte per element; the expert weights'
+    codes w_code_bytes per element, 0.5 for packed MXFP4):
       forward  y[t, n] = x[t, k] w_g[n, k]^T, BF16 out
       dgrad    dx[t, k] = dy[t, n] w_g[n, k], FP32 out
       wgrad    dw_g[n, k] = dy[t, n]^T x[t, k], FP32 out (written for every
@@ -427,12 +429,13 @@ def moe_roofline(sizes, n: int, k: int, kind: str, flops_peak: float, hbm_gbs: f
     one after another (small experts bound by their weight or output bytes).
     flops_peak in TFLOP/s, hbm_gbs in GB/s."""
     sc = 1.0 + 1.0 / 32.0
+    wsc = w_code_bytes + 1.0 / 32.0
     flops_sum = bytes_sum = per_expert = 0.0
     for t in sizes:
         t = int(t)
         flops = 2.0 * t * n * k
         if kind == "forward":
-            nbytes = (t * k + n * k) * sc + t * n * 2 if t else 0.0
+            nbytes = t * k * sc + n * k * wsc + t * n * 2 if t else 0.0
         elif kind == "dgrad":
             nbytes = (t * n + n * k) * sc + t * k * 4 if t else 0.0
         elif kind == "wgrad":
@@ -629,6 +632,13 @@ def _measure_rows(mx, peaks, dev, stream, clocks: RowClocks):
                    {"group_sizes_min_max": [min(sizes), max(sizes)],
                     "empty_groups": sizes.count(0)})
     with_roofline(row, moe_roofline(sizes, n, k, "forward", fp8_peak, hbm))
+    # the same with MXFP4 expert weights in packed storage (two codes a byte)
+    qw4 = mx.quantize(wm.view(e * n, k), "e2m1_packed", "row", stream=stream)
+    qb4 = mx.MxTensor(qw4.codes.view(e, n, k // 2), qw4.scales, "e2m1_packed")
+    row = gemm_row("moe_grouped_mxfp4_packed_weights_64x(2048x7168)_65536tok_bf16",
+                   lambda: mx.grouped_gemm(qa, d_off, qb4, "bf16", out=ym, stream=stream), fl)
+    with_roofline(row, moe_roofline(sizes, n, k, "forward", fp8_peak, hbm, w_code_bytes=0.5))
+    del qw4, qb4
 
     # grouped rowwise quantize into the buffers above (the C call: no
     # allocation inside the timed launches; inputs 940 MB, larger than L2)
