@@ -366,6 +366,51 @@ def dequantize(q: MxBlocks) -> np.ndarray:
     return (vals.reshape(rows, k // BLOCK, BLOCK) * s[:, :, None]).reshape(rows, k)
 
 
+@dataclass
+class IncidentTrace:
+    amax: np.ndarray     # [rows, K/32] block amax over the finite values
+    scales: np.ndarray   # [rows, K/32] the selected E8M0 bytes
+    clip_count: int      # finite values whose exactly scaled magnitude exceeds the format max
+    zero_count: int      # finite non-zero values that encode to a zero code
+    nan_blocks: int      # blocks holding NaN or Inf (scale byte 0xFF)
+    binades: dict        # floor(log2|x|) -> count, over finite non-zero values
+
+
+def incident_trace(x: np.ndarray, fmt, axis: str = "row", rule: str = "floor") -> IncidentTrace:
+    """The numerical fields of the incident trace that "Troubleshooting
+    numerical failures" asks for, for one quantization: an input histogram
+    (counts per binade), the amax of every 32-element scale group, the
+    selected scale bytes, clip counts and zero counts.  A value is clipped
+    when its exactly scaled magnitude lies above the format's largest finite
+    value (its code is that maximum whatever the rounding), and counted as a
+    zero when it is finite and non-zero but its code is +0 or -0.  Blocks
+    holding NaN or Inf are counted apart and excluded from both."""
+    f = fmt_of(fmt)
+    q = quantize(x, f, axis, rule)
+    xx = np.asarray(x, dtype=np.float64)
+    if axis == "col":
+        xx = xx.T
+    rows, k = xx.shape
+    blocks = xx.reshape(rows, k // BLOCK, BLOCK)
+    finite = np.isfinite(blocks)
+    bad = ~np.all(finite, axis=2)
+    vals = np.where(finite, blocks, 0.0)
+    amax = np.max(np.abs(vals), axis=2)
+    e = q.scales.astype(np.int64) - 127
+    scaled = np.ldexp(vals, -np.where(bad, 0, e)[:, :, None])
+    good = ~bad[:, :, None]
+    clipped = good & (np.abs(scaled) > f.max_finite)
+    decoded = decode_table(f)[q.codes.reshape(rows, k // BLOCK, BLOCK)]
+    zeros = good & (vals != 0.0) & (decoded == 0.0)
+    nz = vals[(vals != 0.0) & finite]
+    _, ex = np.frexp(np.abs(nz))
+    binades = {}
+    for b, c in zip(*np.unique(ex - 1, return_counts=True)):
+        binades[int(b)] = int(c)
+    return IncidentTrace(amax, q.scales, int(clipped.sum()), int(zeros.sum()), int(bad.sum()),
+                         binades)
+
+
 # --------------------------------------------------------------------------
 # Swizzled scale layout (tensor-core operand layout; not defined by the pages)
 # --------------------------------------------------------------------------

@@ -22,8 +22,15 @@ def golden_dir():
 def pytest_terminal_summary(terminalreporter):
     """Observed GEMM accuracy of the parity tests that ran: the worst error
     as a fraction of the allowed bound and as a fraction of T = sum |a*b|,
-    per test file and output type."""
-    from mxcheck import ERROR_LOG
+    per test file and output type; and the incident-trace counts (clipped,
+    zeroed values, NaN/Inf blocks) read off GPU-quantized tensors."""
+    from mxcheck import ERROR_LOG, INCIDENT_LOG
+    if INCIDENT_LOG:
+        terminalreporter.write_sep("-", "incident-trace counts of GPU-quantized tensors")
+        for test, what, n, clipped, zeroed, nan_blocks in INCIDENT_LOG:
+            terminalreporter.write_line(
+                f"{what}: {n} values, {clipped} clipped, {zeroed} zeroed, "
+                f"{nan_blocks} NaN/Inf blocks")
     if not ERROR_LOG:
         return
     worst = {}

@@ -55,6 +55,34 @@ def bf16_ulp(y: np.ndarray) -> np.ndarray:
     return np.where(a > 0, 2.0 ** (e - 7), 2.0 ** -133)
 
 
+# Incident-trace counts read off GPU-quantized tensors (test id, what,
+# values, clipped, zeroed, NaN/Inf blocks); conftest prints them.
+INCIDENT_LOG: list = []
+
+
+def incident_counts(x_bf16: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, fmt: str,
+                    axis: str):
+    """Clip and zero counts of a quantization read off its codes and
+    swizzled scales (the incident trace's definitions: a finite value is
+    clipped when its value over the block scale exceeds the format max, and
+    zeroed when it is non-zero and its code decodes to zero)."""
+    f = O.fmt_of(fmt)
+    x = to_f64(x_bf16)
+    if axis == "col":
+        x = x.T
+    rows, k = x.shape
+    sc = O.unswizzle_scales(scales.cpu().numpy(), rows, k // 32)
+    blocks = x.reshape(rows, k // 32, 32)
+    bad = (sc == O.E8M0_NAN)
+    good = ~bad[:, :, None] & np.isfinite(blocks)
+    e = sc.astype(np.int64) - 127
+    scaled = np.ldexp(np.where(good, blocks, 0.0), -np.where(bad, 0, e)[:, :, None])
+    dec = O.decode_table(f)[codes.cpu().numpy().reshape(rows, k // 32, 32)]
+    clipped = int((good & (np.abs(scaled) > f.max_finite)).sum())
+    zeroed = int((good & (blocks != 0.0) & (dec == 0.0)).sum())
+    return clipped, zeroed, int(bad.sum())
+
+
 # Observed GEMM accuracy, one record per checked block of outputs:
 # (test id, output dtype, max error / allowed bound, max |y - y_ref| / T over
 # entries with T > 0, entries checked).  conftest prints a summary.

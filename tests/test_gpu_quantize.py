@@ -6,7 +6,8 @@ import numpy as np
 import pytest
 import torch
 
-from mxcheck import canonical_scales, ensure_built, oracle_quant, to_f64
+from mxcheck import (INCIDENT_LOG, canonical_scales, ensure_built, incident_counts,
+                     oracle_quant, to_f64)
 from oracle import mx_oracle as O
 
 pytestmark = pytest.mark.gpu
@@ -280,3 +281,25 @@ def test_stochastic_rounding_full_size_sampled(mx):
         rn = rand[:, c0:c0 + 128].cpu().numpy().view(np.uint16).astype(np.int64)
         q = O.quantize(to_f64(xs), "e5m2", "col", rand=rn)
         assert torch.equal(c.codes[c0:c0 + 128].cpu(), torch.from_numpy(q.codes))
+
+
+@pytest.mark.parametrize("fmt,rule", [("e4m3", "floor"), ("e4m3", "ceil"), ("e5m2", "floor")])
+def test_incident_trace_counts_of_gpu_output(mx, fmt, rule):
+    """The incident trace's clip and zero counts read off the GPU's codes and
+    scales equal the oracle's, on the forward layer's activations (2048 of
+    its rows, spikes included) and the quantize sweep's 4096x4096 tensor
+    (with +-U(100, 1e4) outliers), rowwise and columnwise."""
+    from mxfp8_block_scaled_mx_gb300 import workloads as W
+    x_fwd, _ = W.dense_forward(device="cuda")
+    cases = [("forward X[:2048]", x_fwd[:2048].contiguous()),
+             ("sweep 4096x4096", W.quantize_sweep((4096, 4096), seed=0, device="cuda"))]
+    del x_fwd
+    for name, x in cases:
+        xc = x.cpu()
+        for axis in ("row", "col"):
+            q = mx.quantize(x, fmt, axis, rule=rule)
+            assert mx.device_status() == 0
+            got = incident_counts(xc, q.codes, q.scales, fmt, axis)
+            t = O.incident_trace(to_f64(xc), fmt, axis, rule)
+            assert got == (t.clip_count, t.zero_count, t.nan_blocks)
+            INCIDENT_LOG.append((f"{name}", f"{name} {axis} {fmt} {rule}", xc.numel(), *got))

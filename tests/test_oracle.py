@@ -389,6 +389,54 @@ def test_troubleshooting_spike_moved_into_small_row(golden_dir, rule):
     assert ys.ravel().tolist() == [spike, spike]
 
 
+# Incident-trace counts for the two-row fixture and the page's troubleshooting
+# changes, derived by hand: (clip count, zero count).  Original fixture: the
+# ceil rule never clips (amax <= 448 S by construction) and keeps every small
+# value non-zero (S = 2^-8); the floor rule keeps S = 1 for the large row, so
+# its four 500s (500 > 448) are clipped.  500 moved into the small row's
+# block: under the ceil rule S = 2 and the four 0.001s (0.0005 after scaling,
+# below half the smallest subnormal 2^-9) become zeros; under the floor rule
+# S = 1 keeps them (2^-9) and the moved 500 is clipped beside the large
+# row's four.  An all-zero small row has no non-zero value to lose.
+INCIDENT_COUNTS = {
+    ("original", "ceil"): (0, 0), ("original", "floor"): (4, 0),
+    ("spike", "ceil"): (0, 4), ("spike", "floor"): (5, 0),
+    ("zero_row", "ceil"): (0, 0), ("zero_row", "floor"): (4, 0),
+}
+
+
+@pytest.mark.parametrize("variant", ["original", "spike", "zero_row"])
+@pytest.mark.parametrize("rule", ["ceil", "floor"])
+def test_incident_trace_counts_on_the_fixture(golden_dir, variant, rule):
+    g = load(golden_dir, "two_row_fixture.json")
+    x, _ = two_row_fixture(g)
+    if variant == "spike":
+        x[0, 3] = 500.0
+    elif variant == "zero_row":
+        x[0, :] = 0.0
+    t = O.incident_trace(x, "e4m3", "row", rule)
+    assert (t.clip_count, t.zero_count, t.nan_blocks) == INCIDENT_COUNTS[(variant, rule)] + (0,)
+    small_amax = {"original": 1.0, "spike": 500.0, "zero_row": 0.0}[variant]
+    assert t.amax.ravel().tolist() == [small_amax, 500.0]
+    assert np.array_equal(t.scales, O.quantize(x, "e4m3", "row", rule).scales)
+    if variant == "original":
+        # the pattern's binades, four repeats each (0.03 and 2^-6 share one, as
+        # do 0.117 and 2^-4)
+        want = {-10: 4, -6: 8, -4: 8, -2: 4, -1: 4, 0: 4}
+        want.update({b: 4 for b in range(1, 9)})
+        assert t.binades == want
+
+
+def test_incident_trace_counts_nan_blocks_apart():
+    x = np.full((2, 64), 1000.0)
+    x[0, 5] = np.nan
+    x[1, 40] = np.inf
+    t = O.incident_trace(x, "e4m3", "row", "floor")
+    # every finite 1000 outside the two NaN/Inf blocks is clipped (S = 2 under
+    # the floor rule: 1000 / 2 = 500 > 448); the NaN and Inf blocks count apart
+    assert t.nan_blocks == 2 and t.clip_count == 64 and t.zero_count == 0
+
+
 @pytest.mark.parametrize("rule", ["ceil", "floor"])
 def test_troubleshooting_selector_column(golden_dir, rule):
     """The selector column quantizes exactly (amax 1: S = 2^-8 under both
