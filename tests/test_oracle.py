@@ -934,3 +934,21 @@ def test_stochastic_quantize_uses_the_same_scales_as_rne():
         assert np.array_equal(q.scales, s.scales)
         dq, ds = O.dequantize(q), O.dequantize(s)
         assert np.all(np.abs(dq - ds) <= np.abs(dq) / 8 + 2.0 ** -9 * O.e8m0_values(q.scales).repeat(32, axis=1))
+
+
+@pytest.mark.parametrize("rule", ["floor", "ceil"])
+def test_block_amax_is_a_magnitude(rule):
+    """A block whose largest magnitude is negative: the scale follows |x|,
+    not the signed maximum (floor rule: floor(log2 500) - 8 = 0, byte 127;
+    ceil rule: ceil(log2(500 / 448)) = 1, byte 128), and -500 comes back as
+    -448 (floor: saturated at S = 1) or -512 (ceil: -250 rounds to the code
+    -256 at S = 2)."""
+    x = np.array([[-500.0, 1.0, 2.0, 3.0] + [0.5] * 28,
+                  [-1.0] * 32], dtype=np.float64)
+    q = O.quantize(x, "e4m3", "row", rule)
+    assert q.scales[0, 0] == (127 if rule == "floor" else 128)
+    # an all-negative block: amax 1 -> scale 2^-8 under both rules
+    assert q.scales[1, 0] == 119
+    xh = O.dequantize(q)
+    assert xh[0, 0] == (-448.0 if rule == "floor" else -512.0)
+    assert xh[1].tolist() == [-1.0] * 32

@@ -214,3 +214,29 @@ def test_silu_with_the_wrong_sign(monkeypatch):
     monkeypatch.setattr(O, "silu", bad)
     monkeypatch.setitem(O.ACTIVATIONS, "silu", O.silu)
     assert caught(lambda: T.test_silu_matches_torch_and_identities())
+
+
+def test_block_amax_takes_the_signed_maximum(monkeypatch):
+    """amax = max(x) instead of max(|x|): the scale of a block led by a
+    negative value is far too small."""
+    good = O.quantize_rows
+
+    def bad(x, fmt, rule="floor", rand=None):
+        x = np.asarray(x, dtype=np.float64)
+        rows, k = x.shape
+        blocks = x.reshape(rows, k // 32, 32)
+        signed_max = np.max(np.where(np.isfinite(blocks), blocks, 0.0), axis=2)
+        # rescale every block so that its |x| maximum equals the signed one,
+        # which is what a scale taken from max(x) quantizes against
+        mag = np.max(np.abs(np.where(np.isfinite(blocks), blocks, 0.0)), axis=2)
+        ratio = np.where((mag > 0) & (signed_max > 0), signed_max / np.where(mag > 0, mag, 1), 1.0)
+        q = good(x, fmt, rule, rand)
+        f = O.fmt_of(fmt)
+        e = (O.scale_exponent_floor(f, mag * ratio) if rule == "floor"
+             else O.scale_exponent_ceil(f, mag * ratio))
+        scaled = np.ldexp(np.where(np.isfinite(blocks), blocks, 0.0), -e[:, :, None])
+        codes = O.encode_sat_rne(f, scaled).reshape(rows, k).astype(np.uint8)
+        return O.MxBlocks(codes, (e + 127).astype(np.uint8), q.fmt)
+    monkeypatch.setattr(O, "quantize_rows", bad)
+    assert caught(lambda: T.test_block_amax_is_a_magnitude("floor"),
+                  lambda: T.test_block_amax_is_a_magnitude("ceil"))
