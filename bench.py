@@ -578,7 +578,17 @@ def _measure_rows(mx, peaks, dev, stream, clocks: RowClocks):
             out[f"quantize_{r}x{c}_row_sr_e5m2"] = bandwidth_row(qsr, stream, scrub, clean,
                                                                  r * c * 5.03125, hbm, 5.03125,
                                                                  clocks)
-            del rb
+            # stochastic rounding to packed MXFP4 (gradients in E2M1): bf16 and
+            # draws read, half a byte of code written per element
+            q4s_codes = torch.empty((r, c // 2), dtype=torch.uint8, device=dev)
+
+            def qsr4():
+                st = mx.mx_quantize_sr(x.data_ptr(), 0, r, c, c, rb.data_ptr(), c, 7, 1, 0,
+                                       q4s_codes.data_ptr(), sr.data_ptr(), None, None, h)
+                assert st == 0
+            out[f"quantize_{r}x{c}_row_sr_e2m1_packed"] = bandwidth_row(
+                qsr4, stream, scrub, clean, r * c * 4.53125, hbm, 4.53125, clocks)
+            del rb, q4s_codes
         del x, xs, qr, sr, qrs, srs, qc, sc
 
     # backward GEMMs (FP32 out), the fused bias+SiLU forward, MXFP4/6 operands

@@ -173,7 +173,9 @@ mx_status mx_quantize(const void* x, mx_dtype x_dtype, int64_t rows, int64_t col
  * < u the neighbouring grid values of the exactly scaled element v, |v| goes
  * to u iff r < floor(2^16 (|v| - l) / (u - l)), else to l; the result then
  * saturates like the RNE path.  Scales are those of mx_quantize (they depend
- * only on the block amax).  For a given rbits the codes are bit-exact. */
+ * only on the block amax).  Every element format and storage of mx_quantize
+ * is accepted (FP8, and the 6- and 4-bit codes in the container or packed
+ * storage).  For a given rbits the codes are bit-exact. */
 mx_status mx_quantize_sr(const void* x, mx_dtype x_dtype, int64_t rows, int64_t cols,
                          int64_t ldx, const uint16_t* rbits, int64_t ldr, mx_fmt fmt,
                          mx_axis axis, mx_scale_rule rule,

@@ -323,7 +323,6 @@ mx_status quantize_common(const void* x, mx_dtype x_dtype, int64_t rows, int64_t
   if (x_dtype != MX_BF16) return x_dtype == MX_FP32 ? MX_ERR_UNSUPPORTED : MX_ERR_INVALID_ARG;
   if (!valid_gemm_fmt(fmt) || (rule != MX_SCALE_FLOOR && rule != MX_SCALE_CEIL))
     return MX_ERR_INVALID_ARG;
-  if (rbits && !valid_fmt(fmt)) return MX_ERR_UNSUPPORTED;  // stochastic rounding: FP8 codes
   if (axis != MX_ROWWISE && axis != MX_COLWISE && axis != MX_BOTH) return MX_ERR_INVALID_ARG;
   const bool row = axis & MX_ROWWISE;
   const bool col = axis & MX_COLWISE;

@@ -179,8 +179,10 @@ __device__ __forceinline__ uint2 encode8(const uint4 v, float mul) {
 // bits below those the comparison reads.
 template <int FMT>
 __device__ __forceinline__ float sr_to_grid(float v, uint32_t r16) {
-  constexpr int kMantBits = FMT == 0 ? 3 : 2;
-  constexpr int kMinNormalExp = FMT == 0 ? -6 : -14;
+  // significand bits and smallest normal exponent: E4M3 3 / -6, E5M2 2 /
+  // -14, E2M3 3 / 0, E3M2 2 / -2, E2M1 1 / 0
+  constexpr int kMantBits = (FMT == 0 || FMT == 2) ? 3 : FMT == 4 ? 1 : 2;
+  constexpr int kMinNormalExp = FMT == 0 ? -6 : FMT == 1 ? -14 : FMT == 3 ? -2 : 0;
   constexpr int kDrop = 23 - kMantBits;  // FP32 significand bits below the format's grid
   // In the format's normal range the grid keeps the top kMantBits of the
   // FP32 significand: l is |v| with the dropped bits cleared, u = l plus one
@@ -209,11 +211,18 @@ __device__ __forceinline__ uint32_t encode_word_sr(uint32_t w, uint32_t r, float
   return cvt_pair<FMT>(sr_to_grid<FMT>(lo, r & 0xFFFFu), sr_to_grid<FMT>(hi, r >> 16));
 }
 
+// Eight bf16 with their random integers -> eight codes, laid out as encode8.
 template <int FMT>
 __device__ __forceinline__ uint2 encode8_sr(const uint4 v, const uint4 r, float mul) {
   uint2 q;
-  q.x = encode_word_sr<FMT>(v.x, r.x, mul) | (encode_word_sr<FMT>(v.y, r.y, mul) << 16);
-  q.y = encode_word_sr<FMT>(v.z, r.z, mul) | (encode_word_sr<FMT>(v.w, r.w, mul) << 16);
+  if constexpr (FMT == 4) {
+    q.x = encode_word_sr<FMT>(v.x, r.x, mul) | (encode_word_sr<FMT>(v.y, r.y, mul) << 8) |
+          (encode_word_sr<FMT>(v.z, r.z, mul) << 16) | (encode_word_sr<FMT>(v.w, r.w, mul) << 24);
+    q.y = 0u;
+  } else {
+    q.x = encode_word_sr<FMT>(v.x, r.x, mul) | (encode_word_sr<FMT>(v.y, r.y, mul) << 16);
+    q.y = encode_word_sr<FMT>(v.z, r.z, mul) | (encode_word_sr<FMT>(v.w, r.w, mul) << 16);
+  }
   return q;
 }
 
@@ -329,7 +338,6 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
                                               uint8_t* s_unit_row, uint8_t* s_unit_col,
                                               uint64_t* empty_bar, int group, int lt) {
   using F = ElemFmt<FMT>;
-  static_assert(!SR || F::kBits == 8, "stochastic rounding is built for FP8 codes");
   const uint32_t lane = lt & 31;
 
   if constexpr (ROW) {
@@ -461,13 +469,14 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
         // the random integer of column 2cp sits in the low half of the
         // random word, that of column 2cp + 1 in the high half
         const uint32_t r0 = rw[4 * i], r1 = rw[4 * i + 1], r2 = rw[4 * i + 2], r3 = rw[4 * i + 3];
+        constexpr int kPairShift = FMT == 4 ? 8 : 16;  // FP4: a code pair in 8 bits
         q_lo[i] = cvt_pair<FMT>(sr_to_grid<FMT>(s0.x, r0 & 0xFFFFu),
                                 sr_to_grid<FMT>(s1.x, r1 & 0xFFFFu)) |
                   (cvt_pair<FMT>(sr_to_grid<FMT>(s2.x, r2 & 0xFFFFu),
-                                 sr_to_grid<FMT>(s3.x, r3 & 0xFFFFu)) << 16);
+                                 sr_to_grid<FMT>(s3.x, r3 & 0xFFFFu)) << kPairShift);
         q_hi[i] = cvt_pair<FMT>(sr_to_grid<FMT>(s0.y, r0 >> 16), sr_to_grid<FMT>(s1.y, r1 >> 16)) |
                   (cvt_pair<FMT>(sr_to_grid<FMT>(s2.y, r2 >> 16), sr_to_grid<FMT>(s3.y, r3 >> 16))
-                   << 16);
+                   << kPairShift);
         if (nan_lo) q_lo[i] = F::kNanWord;
         if (nan_hi) q_hi[i] = F::kNanWord;
         continue;
@@ -765,14 +774,12 @@ cudaError_t launch_dense(const QuantizeParams& p, const CUtensorMap& tmap_x,
   const bool row = p.q_row != nullptr;
   const bool col = p.q_col != nullptr;
   const CUtensorMap& tr = tmap_r ? *tmap_r : tmap_x;
-  if constexpr (FMT <= 1) {
-    if (tmap_r) {  // stochastic rounding (FP8 codes)
-      if (row && col) return launch_one<FMT, true, true, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
-      if (row) return launch_one<FMT, true, false, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
-      return launch_one<FMT, false, true, false, true>(p, tmap_x, tr, tiles, num_sms, stream);
-    }
-  } else {
-    if (tmap_r) return cudaErrorNotSupported;
+  if (tmap_r) {  // stochastic rounding
+    if (row && col)
+      return launch_one<FMT, true, true, false, true, PACKED>(p, tmap_x, tr, tiles, num_sms, stream);
+    if (row)
+      return launch_one<FMT, true, false, false, true, PACKED>(p, tmap_x, tr, tiles, num_sms, stream);
+    return launch_one<FMT, false, true, false, true, PACKED>(p, tmap_x, tr, tiles, num_sms, stream);
   }
   if (row && col)
     return launch_one<FMT, true, true, false, false, PACKED>(p, tmap_x, tr, tiles, num_sms, stream);

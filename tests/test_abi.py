@@ -154,11 +154,14 @@ def test_stochastic_quantize_rejects_bad_arguments_on_the_host(mx):
 
 
 def test_narrow_formats_on_the_host(mx):
-    """MXFP6 / MXFP4 codes: accepted by the quantizer and the GEMM; not by
-    stochastic rounding or the grouped quantizer (FP8 only)."""
+    """MXFP6 / MXFP4 codes: accepted by the quantizer, stochastic rounding
+    and the GEMM (the host checks apply as for FP8); not by the grouped
+    quantizer (FP8 only)."""
     sr = mx.mx_quantize_sr
     for fmt in (2, 3, 4):
-        assert sr(FAKE, 0, 64, 64, 64, FAKE, 64, fmt, 1, 0, FAKE, FAKE, None, None, 0) == 3
+        assert sr(FAKE, 0, 64, 64, 64, FAKE, 64, fmt, 1, 0, FAKE, FAKE, None, None, 0) != 3
+        assert sr(FAKE, 0, 64, 64, 64, FAKE, 32, fmt, 1, 0, FAKE, FAKE, None, None, 0) == 1
+        assert sr(FAKE, 0, 64, 64, 64, FAKE + 2, 64, fmt, 1, 0, FAKE, FAKE, None, None, 0) == 2
         assert mx.mx_quantize_grouped(FAKE, 0, 64, 64, 64, fmt, 0, 4, FAKE, FAKE, FAKE, 0) == 3
     q = mx.mx_quantize
     assert q(FAKE, 0, 64, 64, 64, 8, 1, 0, FAKE, FAKE, None, None, 0) == 1           # no format 8
@@ -167,8 +170,8 @@ def test_narrow_formats_on_the_host(mx):
 
 def test_packed_formats_on_the_host(mx):
     """Packed 6- and 4-bit storage (formats 5-7): the GEMM wants K % 128 and
-    32-byte aligned packed code pointers; stochastic rounding and the
-    grouped quantizer stay FP8 only."""
+    32-byte aligned packed code pointers; stochastic rounding accepts them,
+    the grouped quantizer stays FP8 only."""
     g = mx.mx_gemm
     for fmt in (5, 6, 7):
         assert g(64, 64, 96, FAKE, FAKE, fmt, FAKE, FAKE, 0, FAKE, 0, 64, 0) == 1        # k % 128
@@ -176,7 +179,7 @@ def test_packed_formats_on_the_host(mx):
         assert g(64, 64, 128, FAKE + 16, FAKE, fmt, FAKE, FAKE, 0, FAKE, 0, 64, 0) == 2  # a % 32
         assert g(64, 64, 128, FAKE, FAKE, 0, FAKE + 16, FAKE, fmt, FAKE, 0, 64, 0) == 2  # b % 32
         assert mx.mx_quantize_sr(FAKE, 0, 64, 64, 64, FAKE, 64, fmt, 1, 0, FAKE, FAKE, None, None,
-                                 0) == 3
+                                 0) != 3
         assert mx.mx_quantize_grouped(FAKE, 0, 64, 64, 64, fmt, 0, 4, FAKE, FAKE, FAKE, 0) == 3
     assert mx.storage_bytes("e2m1_packed", 128) == 64
     assert mx.storage_bytes("e3m2_packed", 128) == 96

@@ -260,3 +260,44 @@ def test_grouped_dgrad_narrow_expert_weights(mx, fb):
     bs = [O.quantize(to_f64(w[e]), base_fmt(fb), "col") for e in range(groups)]
     y_ref, t_ref = O.grouped_gemm(a, offsets, bs)
     assert_gemm_close(y, y_ref, t_ref, "fp32")
+
+
+# ---------------------------------------------------------------- stochastic rounding
+
+@pytest.mark.parametrize("fmt", ["e2m1", "e2m3", "e3m2", "e2m1_packed", "e3m2_packed"])
+@pytest.mark.parametrize("axis", ["row", "col", "both"])
+def test_narrow_stochastic_rounding_matches_oracle(mx, fmt, axis):
+    """MXFP4 / MXFP6 codes with stochastic rounding (container or packed
+    storage): bit-exact against the oracle given the same 16-bit random
+    integers, scales equal to the round-to-nearest path's."""
+    from mxfp8_block_scaled_mx_gb300 import workloads as W
+    rows, cols = 160, 256
+    x = inputs(rows, cols, seed=51)
+    rand = W.random_bits16((rows, cols), seed=52)
+    got = mx.quantize(x.cuda(), fmt, axis, rand=rand.cuda())
+    assert mx.device_status() == 0
+    rnp = rand.numpy().view(np.uint16).astype(np.int64)
+    outs = got if axis == "both" else (got,)
+    axes = ("row", "col") if axis == "both" else (axis,)
+    pack = O.pack_dense if fmt.endswith("_packed") else O.pack_container
+    for g, ax in zip(outs, axes):
+        q = O.quantize(to_f64(x), base_fmt(fmt), ax, rand=rnp)
+        assert torch.equal(g.codes.cpu(), torch.from_numpy(pack(q.codes, base_fmt(fmt)))), ax
+        rq = O.quantize(to_f64(x), base_fmt(fmt), ax)
+        assert np.array_equal(canonical_scales(g.scales, *q.codes.shape), rq.scales), ax
+
+
+def test_mxfp4_stochastic_rounding_is_unbiased_on_the_gpu(mx):
+    """Every element 5.5 in blocks whose amax is 6 (scale 1): over 2^16 rows
+    of distinct random integers per column the GPU's E2M1 codes average to
+    5.5 exactly (three quarters of the draws go up to 6)."""
+    rows, cols = 1 << 16, 32
+    x = torch.full((rows, cols), 5.5)
+    x[:, 0] = 6.0
+    r = torch.arange(rows, dtype=torch.int32).to(torch.int16).view(rows, 1).repeat(1, cols)
+    q = mx.quantize(x.to(torch.bfloat16).cuda(), "e2m1", "row", rand=r.cuda().contiguous())
+    assert mx.device_status() == 0
+    codes = O.unpack_container(q.codes.cpu().numpy(), "e2m1")
+    vals = O.decode_table("e2m1")[codes[:, 1:]]
+    assert np.all(canonical_scales(q.scales, rows, cols) == 127)
+    assert float(vals.mean()) == 5.5

@@ -891,7 +891,7 @@ def test_stochastic_rounding_probability_from_page(golden_dir):
     assert abs(ups / (1 << 16) - 2 / 25) < 2 ** -16
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m3", "e3m2", "e2m1"])
 def test_stochastic_rounding_is_unbiased_for_dyadic_inputs(fmt):
     """E[SR(x)] = x exactly over all 2^16 draws when the fraction of a grid
     step has at most 16 bits (closed form), and grid values never move."""
@@ -919,6 +919,23 @@ def test_stochastic_rounding_saturates_and_keeps_signed_zero():
     z = O.encode_sat_sr("e4m3", np.array([-2.0 ** -30, -2.0 ** -30]), r)
     assert np.all(z == 0x80)
     assert O.encode_sat_sr("e4m3", np.array([np.nan]), np.array([0]))[0] == O.NAN_CODE
+
+
+def test_stochastic_rounding_of_mxfp4_codes():
+    """E2M1 (grid 0, 0.5, 1, 1.5, 2, 3, 4, 6): 5.5 lies a quarter step below
+    6 and goes up for 3/4 of the draws; 0.25 (half the subnormal step 0.5)
+    for half of them; 7 lies past the maximum and saturates to 6 for every
+    draw (its neighbours 6 and 8, the grid extended one step); -0.1 rounds
+    to -0 or -0.5 and keeps its sign."""
+    t = O.decode_table("e2m1")
+    r = np.arange(1 << 16)
+    up = t[O.encode_sat_sr("e2m1", np.full(1 << 16, 5.5), r)]
+    assert set(up.tolist()) == {4.0, 6.0} and int((up == 6.0).sum()) == 3 * (1 << 14)
+    half = t[O.encode_sat_sr("e2m1", np.full(1 << 16, 0.25), r)]
+    assert set(half.tolist()) == {0.0, 0.5} and int((half == 0.5).sum()) == 1 << 15
+    assert np.all(t[O.encode_sat_sr("e2m1", np.full(1 << 16, 7.0), r)] == 6.0)
+    neg = O.encode_sat_sr("e2m1", np.full(1 << 16, -0.1), r)
+    assert set(t[neg].tolist()) == {-0.0, -0.5} and np.all(neg & 0x8)
 
 
 def test_stochastic_quantize_uses_the_same_scales_as_rne():
