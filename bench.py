@@ -589,6 +589,19 @@ def _measure_rows(mx, peaks, dev, stream, clocks: RowClocks):
             out[f"quantize_{r}x{c}_row_sr_e2m1_packed"] = bandwidth_row(
                 qsr4, stream, scrub, clean, r * c * 4.53125, hbm, 4.53125, clocks)
             del rb, q4s_codes
+            # FP32 input (the same values): 4 bytes read per element
+            xf = x.float()
+            for mode, axis, bpe in (("row", 1, 5.03125), ("both", 3, 6.0625)):
+                def qf(axis=axis):
+                    st = mx.mx_quantize(xf.data_ptr(), 1, r, c, c, 0, axis, 0,
+                                        qr.data_ptr() if axis & 1 else None,
+                                        sr.data_ptr() if axis & 1 else None,
+                                        qc.data_ptr() if axis & 2 else None,
+                                        sc.data_ptr() if axis & 2 else None, h)
+                    assert st == 0
+                out[f"quantize_{r}x{c}_fp32_{mode}"] = bandwidth_row(
+                    qf, stream, scrub, clean, r * c * bpe, hbm, bpe, clocks)
+            del xf
         del x, xs, qr, sr, qrs, srs, qc, sc
 
     # backward GEMMs (FP32 out), the fused bias+SiLU forward, MXFP4/6 operands

@@ -41,8 +41,8 @@
  *    dimension must span a multiple of 16 bytes (MX_ERR_MISALIGNED).
  *  - Sizes: rows, K and leading dimensions up to 2^31 - 1; a GEMM whose
  *    256x256 output tiles (over all groups) number 2^31 or more, and a
- *    quantization whose (padded) 128x128 tiles number 2^32 or more, return
- *    MX_ERR_UNSUPPORTED.
+ *    quantization whose (padded) tiles of 128 rows x 128 bf16 or 64 FP32
+ *    columns number 2^32 or more, return MX_ERR_UNSUPPORTED.
  *
  * Scale layout ("swizzled", the operand layout of the tensor-core
  * block-scaled MMA; the pages require the layout to be recorded with the
@@ -109,7 +109,10 @@ typedef enum {
   MX_E2M3_PACKED = 5, MX_E3M2_PACKED = 6, MX_E2M1_PACKED = 7
 } mx_fmt;
 
-/* Wide element types: quantizer input and GEMM output. */
+/* Wide element types: quantizer input (bf16 or FP32, both taken exactly:
+ * every input value is representable, so the block amax, the scale and the
+ * one rounding to the element grid are those of the exact value) and GEMM
+ * output. */
 typedef enum { MX_BF16 = 0, MX_FP32 = 1 } mx_dtype;
 
 /* Which quantizations to produce from one read of the wide tensor.
@@ -145,8 +148,9 @@ size_t mx_scale_bytes(int64_t rows, int64_t k);
  * `groups` groups: (ceil(total_rows/128) + groups) * 128 * ceil(k/128) * 4. */
 size_t mx_grouped_scale_bytes(int64_t total_rows, int32_t groups, int64_t k);
 
-/* MX quantization of a bf16 matrix x[rows, cols] (row-major, leading
- * dimension ldx elements), section "Microscaling: the two-row experiment".
+/* MX quantization of a bf16 or FP32 matrix x[rows, cols] (x_dtype;
+ * row-major, leading dimension ldx elements), section "Microscaling: the
+ * two-row experiment".
  *
  *  ROWWISE (needs cols % 32 == 0): q_row[rows, cols] codes (row-major,
  *    leading dimension cols) and s_row = swizzled scales of the
@@ -159,7 +163,9 @@ size_t mx_grouped_scale_bytes(int64_t total_rows, int32_t groups, int64_t k);
  *    (q_row: rows x cols*w/8 bytes; q_col: cols x rows*w/8 bytes).
  *
  * x, q_*, s_* are device pointers; unused outputs may be NULL.
- * cols % 8 == 0, ldx % 8 == 0, ldx >= cols.  x_dtype must be MX_BF16.
+ * cols % 8 == 0, ldx >= cols, and rows of x start on 16-byte boundaries:
+ * ldx % 8 == 0 for MX_BF16, ldx % 4 == 0 for MX_FP32 (else
+ * MX_ERR_MISALIGNED); another x_dtype is MX_ERR_INVALID_ARG.
  * Codes and scales are bit-exact functions of x (no rounding-order freedom). */
 mx_status mx_quantize(const void* x, mx_dtype x_dtype, int64_t rows, int64_t cols,
                       int64_t ldx, mx_fmt fmt, mx_axis axis, mx_scale_rule rule,
@@ -192,7 +198,8 @@ mx_status mx_quantize_sr(const void* x, mx_dtype x_dtype, int64_t rows, int64_t 
  * last group are left untouched.  d_offsets: device int32[groups + 1],
  * d_offsets[0] = 0, non-decreasing, d_offsets[groups] = total_rows; invalid
  * offsets are reported through mx_device_status (MX_ERR_DEVICE_ARG) and
- * nothing is written.  1 <= groups <= 1000. */
+ * nothing is written.  1 <= groups <= 1000.  x_dtype and ldx as for
+ * mx_quantize; fmt MX_E4M3 or MX_E5M2 (other formats MX_ERR_UNSUPPORTED). */
 mx_status mx_quantize_grouped(const void* x, mx_dtype x_dtype, int64_t total_rows,
                               int64_t cols, int64_t ldx, mx_fmt fmt, mx_scale_rule rule,
                               int32_t groups, const int32_t* d_offsets,
@@ -220,8 +227,9 @@ int64_t mx_grouped_cols_capacity(int64_t total_rows, int32_t groups);
  *   always suffices); a layout that does not fit is reported through
  *   mx_device_status (MX_ERR_DEVICE_ARG) and nothing is written.  This is
  *   the operand layout of mx_grouped_gemm_wgrad.
- * cols % 8 == 0 (ROWWISE also cols % 32 == 0); d_offsets and groups as for
- * mx_quantize_grouped.  Unused outputs may be NULL. */
+ * cols % 8 == 0 (ROWWISE also cols % 32 == 0); x_dtype, ldx, d_offsets and
+ * groups as for mx_quantize and mx_quantize_grouped.  Unused outputs may be
+ * NULL. */
 mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_rows,
                                  int64_t cols, int64_t ldx, mx_fmt fmt, mx_axis axis,
                                  mx_scale_rule rule, int32_t groups, const int32_t* d_offsets,

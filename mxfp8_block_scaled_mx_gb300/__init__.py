@@ -41,7 +41,10 @@ def storage_bytes(fmt: str, elems: int) -> int:
 def storage_elems(fmt: str, nbytes: int) -> int:
     """Codes of `fmt` held by `nbytes` bytes along K."""
     return nbytes * 8 // STORAGE_BITS.get(fmt, 8)
+
+
 DTYPE = {"bf16": 0, "fp32": 1}
+_X_DTYPE = {torch.bfloat16: DTYPE["bf16"], torch.float32: DTYPE["fp32"]}  # quantizer inputs
 AXIS = {"row": 1, "col": 2, "both": 3}
 RULE = {"floor": 0, "ceil": 1}
 
@@ -286,12 +289,12 @@ class MxTensor:
 
 def quantize(x: torch.Tensor, fmt: str = "e4m3", axis: str = "row", rule: str = "floor",
              stream=None, rand: torch.Tensor | None = None):
-    """bf16 [rows, cols] -> MxTensor (axis 'row' or 'col') or a (row, col)
-    pair (axis 'both').  Column-wise codes come back as [cols, rows].  With
-    `rand` (16-bit random integers, int16 [rows, cols]) the codes use
-    stochastic rounding."""
-    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda:
-        raise ValueError("x must be a 2-D bf16 CUDA tensor")
+    """bf16 or fp32 [rows, cols] -> MxTensor (axis 'row' or 'col') or a
+    (row, col) pair (axis 'both').  Column-wise codes come back as [cols,
+    rows].  With `rand` (16-bit random integers, int16 [rows, cols]) the
+    codes use stochastic rounding."""
+    if x.dtype not in _X_DTYPE or x.dim() != 2 or not x.is_cuda:
+        raise ValueError("x must be a 2-D bf16 or fp32 CUDA tensor")
     _on_current_device(x, "x")
     if x.stride(1) != 1:
         raise ValueError("x must be row-major with unit column stride")
@@ -305,7 +308,7 @@ def quantize(x: torch.Tensor, fmt: str = "e4m3", axis: str = "row", rule: str = 
         q_col = torch.empty((cols, storage_bytes(fmt, rows)), dtype=torch.uint8, device=dev)
         s_col = torch.empty(max(mx_scale_bytes(cols, rows), 1), dtype=torch.uint8, device=dev)
     if rand is None:
-        st = mx_quantize(_ptr(x), DTYPE["bf16"], rows, cols, x.stride(0), FMT[fmt], AXIS[axis],
+        st = mx_quantize(_ptr(x), _X_DTYPE[x.dtype], rows, cols, x.stride(0), FMT[fmt], AXIS[axis],
                          RULE[rule], _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col),
                          _stream(stream))
         _check("mx_quantize", st)
@@ -315,7 +318,7 @@ def quantize(x: torch.Tensor, fmt: str = "e4m3", axis: str = "row", rule: str = 
         _on_current_device(rand, "rand")
         if rand.stride(1) != 1:
             raise ValueError("rand must have unit column stride")
-        st = mx_quantize_sr(_ptr(x), DTYPE["bf16"], rows, cols, x.stride(0), _ptr(rand),
+        st = mx_quantize_sr(_ptr(x), _X_DTYPE[x.dtype], rows, cols, x.stride(0), _ptr(rand),
                             rand.stride(0), FMT[fmt], AXIS[axis], RULE[rule], _ptr(q_row),
                             _ptr(s_row), _ptr(q_col), _ptr(s_col), _stream(stream))
         _check("mx_quantize_sr", st)
@@ -339,8 +342,8 @@ def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt: str = "e4m3",
     zero-padded), the operand layout of grouped_gemm_wgrad; ldq defaults to
     mx_grouped_cols_capacity(total, groups).  axis 'both': (row, col) from
     one read."""
-    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
-        raise ValueError("x must be a row-major 2-D bf16 CUDA tensor")
+    if x.dtype not in _X_DTYPE or x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
+        raise ValueError("x must be a row-major 2-D bf16 or fp32 CUDA tensor")
     _on_current_device(x, "x")
     groups = _require_offsets(offsets)
     rows, cols = x.shape
@@ -355,12 +358,12 @@ def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt: str = "e4m3",
         q_col = torch.zeros((cols, ldq), dtype=torch.uint8, device=x.device)
         s_col = torch.zeros(max(mx_scale_bytes(cols, ldq), 1), dtype=torch.uint8, device=x.device)
     if axis == "row":
-        st = mx_quantize_grouped(_ptr(x), DTYPE["bf16"], rows, cols, x.stride(0), FMT[fmt],
+        st = mx_quantize_grouped(_ptr(x), _X_DTYPE[x.dtype], rows, cols, x.stride(0), FMT[fmt],
                                  RULE[rule], groups, _ptr(offsets), _ptr(q_row), _ptr(s_row),
                                  _stream(stream))
         _check("mx_quantize_grouped", st)
         return MxTensor(q_row, s_row, fmt)
-    st = mx_quantize_grouped_ex(_ptr(x), DTYPE["bf16"], rows, cols, x.stride(0), FMT[fmt],
+    st = mx_quantize_grouped_ex(_ptr(x), _X_DTYPE[x.dtype], rows, cols, x.stride(0), FMT[fmt],
                                 AXIS[axis], RULE[rule], groups, _ptr(offsets), _ptr(q_row),
                                 _ptr(s_row), _ptr(q_col), ldq or 0, _ptr(s_col), _stream(stream))
     _check("mx_quantize_grouped_ex", st)

@@ -1,7 +1,7 @@
 """Run one hot-path kernel on one shape a few times (for profilers).
 
     python -m mxfp8_block_scaled_mx_gb300.cases gemm --m 4096 --n 18432 --k 7168 [--reps 3] [--fused]
-    python -m mxfp8_block_scaled_mx_gb300.cases quantize --rows 16384 --cols 8192 --axis row [--sr]
+    python -m mxfp8_block_scaled_mx_gb300.cases quantize --rows 16384 --cols 8192 --axis row [--sr] [--fp32]
     python -m mxfp8_block_scaled_mx_gb300.cases moe_quantize --tokens 65536 --experts 64 --axis col
     python -m mxfp8_block_scaled_mx_gb300.cases grouped --tokens 16384 --experts 16
     python -m mxfp8_block_scaled_mx_gb300.cases moe_dgrad --tokens 16384 --experts 16
@@ -50,6 +50,7 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--fused", action="store_true", help="gemm: FP32 bias + SiLU epilogue")
     ap.add_argument("--sr", action="store_true", help="quantize: stochastic rounding (E5M2)")
+    ap.add_argument("--fp32", action="store_true", help="quantize: FP32 input (same values)")
     a = ap.parse_args(argv)
     dev = torch.device("cuda", 0)
     if a.case == "gemm":
@@ -69,13 +70,17 @@ def main(argv=None):
     elif a.case == "quantize":
         x = W.quantize_sweep((a.rows, a.cols), seed=1, device=dev)
         bpe = 4.0625 if a.axis == "both" else 3.03125
+        if a.fp32:
+            x = x.float()
+            bpe += 2.0
         if a.sr:  # stochastic rounding to E5M2: the random draws are a second input
             rb = W.random_bits16((a.rows, a.cols), seed=11, device=dev)
             ms = _time(lambda: mx.quantize(x, "e5m2", a.axis, rand=rb), a.reps)
             bpe += 2.0
         else:
             ms = _time(lambda: mx.quantize(x, "e4m3", a.axis), a.reps)
-        print(f"quantize {a.rows}x{a.cols} {a.axis}{' sr' if a.sr else ''}: {ms:.4f} ms, "
+        print(f"quantize {a.rows}x{a.cols} {a.axis}{' sr' if a.sr else ''}"
+              f"{' fp32' if a.fp32 else ''}: {ms:.4f} ms, "
               f"{a.rows * a.cols * bpe / ms / 1e6:.1f} GB/s")
     elif a.case == "moe_quantize":
         # the routed tokens [tokens, k], per-expert groups: rowwise (forward

@@ -47,7 +47,8 @@ class PerDeviceOnce {
 };
 
 struct QuantizeParams {
-  const uint16_t* x;   // bf16 bit patterns, [rows, cols], leading dimension ldx
+  const void* x;       // bf16 or FP32 elements, [rows, cols], leading dimension ldx
+                       // (the kernels read x through its tensor map)
   int64_t rows;
   int64_t cols;
   int64_t ldx;
@@ -75,6 +76,12 @@ cudaError_t launch_quantize(const QuantizeParams& p, const CUtensorMap& tmap_x,
 // segments of 128 columns) quantization of token groups.
 cudaError_t launch_quantize_grouped(const QuantizeParams& p, const CUtensorMap& tmap_x,
                                     int num_sms, cudaStream_t stream);
+// The same for FP32 x: tmap_x is a 2-D FP32 tensor map (box 32 columns x 128
+// rows, 128-byte swizzle); tmap_r as above.
+cudaError_t launch_quantize_f32(const QuantizeParams& p, const CUtensorMap& tmap_x,
+                                const CUtensorMap* tmap_r, int num_sms, cudaStream_t stream);
+cudaError_t launch_quantize_grouped_f32(const QuantizeParams& p, const CUtensorMap& tmap_x,
+                                        int num_sms, cudaStream_t stream);
 
 // GEMM modes: dense; grouped by rows of A (each expert owns a range of A
 // rows and its own B); grouped along K (each expert owns a 128-aligned

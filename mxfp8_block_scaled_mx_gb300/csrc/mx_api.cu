@@ -148,6 +148,22 @@ mx_status encode_bf16_map(CUtensorMap* map, const void* base, int64_t cols, int6
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
+// 2-D tensor map over an FP32 [rows, cols] matrix with leading dimension
+// ldx: box 32 columns x 128 rows (128-byte rows, two boxes per 128 x 64
+// tile), 128-byte swizzle, zero fill outside the matrix.
+mx_status encode_f32_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
+                         int64_t ldx) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx * 4)};
+  cuuint32_t box[2] = {32u, 128u};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
 // 2-D tensor map over packed 6- or 4-bit codes [rows, inner elements] with
 // row stride `stride` bytes, read with the unpacking element type: each run
 // of 16 codes lands in 16 bytes of shared memory (the container layout the
@@ -320,7 +336,8 @@ mx_status quantize_common(const void* x, mx_dtype x_dtype, int64_t rows, int64_t
                           int64_t ldx, const uint16_t* rbits, int64_t ldr, mx_fmt fmt,
                           mx_axis axis, mx_scale_rule rule, uint8_t* q_row, uint8_t* s_row,
                           uint8_t* q_col, uint8_t* s_col, cudaStream_t stream) {
-  if (x_dtype != MX_BF16) return x_dtype == MX_FP32 ? MX_ERR_UNSUPPORTED : MX_ERR_INVALID_ARG;
+  if (x_dtype != MX_BF16 && x_dtype != MX_FP32) return MX_ERR_INVALID_ARG;
+  const bool f32 = x_dtype == MX_FP32;
   if (!valid_gemm_fmt(fmt) || (rule != MX_SCALE_FLOOR && rule != MX_SCALE_CEIL))
     return MX_ERR_INVALID_ARG;
   if (axis != MX_ROWWISE && axis != MX_COLWISE && axis != MX_BOTH) return MX_ERR_INVALID_ARG;
@@ -332,10 +349,12 @@ mx_status quantize_common(const void* x, mx_dtype x_dtype, int64_t rows, int64_t
   if (row && cols % 32 != 0) return MX_ERR_INVALID_ARG;
   if (col && rows % 32 != 0) return MX_ERR_INVALID_ARG;
   if (ceil_div(cols, 128) > 65535) return MX_ERR_UNSUPPORTED;
-  // the kernels number their 128x128 tiles in 32 bits
-  if (cols > 0 && ceil_div(rows, 128) > static_cast<int64_t>(UINT32_MAX) / ceil_div(cols, 128))
+  // the kernels number their tiles (128 rows x 128 bf16 or 64 FP32 columns) in 32 bits
+  const int64_t col_tiles = ceil_div(cols, f32 ? 64 : 128);
+  if (cols > 0 && ceil_div(rows, 128) > static_cast<int64_t>(UINT32_MAX) / col_tiles)
     return MX_ERR_UNSUPPORTED;
-  if (!aligned16(x) || ldx % 8 != 0) return MX_ERR_MISALIGNED;
+  // rows of x start on 16-byte boundaries
+  if (!aligned16(x) || ldx % (f32 ? 4 : 8) != 0) return MX_ERR_MISALIGNED;
   if (rbits && (!aligned16(rbits) || ldr % 8 != 0)) return MX_ERR_MISALIGNED;
   if ((row && (!aligned16(q_row) || !aligned16(s_row))) ||
       (col && (!aligned16(q_col) || !aligned16(s_col))))
@@ -344,7 +363,7 @@ mx_status quantize_common(const void* x, mx_dtype x_dtype, int64_t rows, int64_t
   mx_status s = device_state(&st);
   if (s != MX_OK) return s;
   mx::QuantizeParams p{};
-  p.x = static_cast<const uint16_t*>(x);
+  p.x = x;
   p.rows = rows;
   p.cols = cols;
   p.ldx = ldx;
@@ -361,13 +380,14 @@ mx_status quantize_common(const void* x, mx_dtype x_dtype, int64_t rows, int64_t
   if (!all_on_device(st->device, {x, rbits, p.q_row, p.s_row, p.q_col, p.s_col}))
     return MX_ERR_INVALID_ARG;
   CUtensorMap tmap, tmap_r;
-  if ((s = encode_bf16_map(&tmap, x, cols, rows, ldx)) != MX_OK) return s;
-  // the random integers are 16-bit like bf16: the same tile geometry
+  s = f32 ? encode_f32_map(&tmap, x, cols, rows, ldx) : encode_bf16_map(&tmap, x, cols, rows, ldx);
+  if (s != MX_OK) return s;
+  // the random integers are 16-bit like bf16: the bf16 box geometry
   if (rbits && (s = encode_bf16_map(&tmap_r, rbits, cols, rows, ldr)) != MX_OK) return s;
-  return mx::launch_quantize(p, tmap, rbits ? &tmap_r : nullptr, st->num_sms, stream) ==
-                 cudaSuccess
-             ? MX_OK
-             : MX_ERR_CUDA;
+  const CUtensorMap* tr = rbits ? &tmap_r : nullptr;
+  const cudaError_t err = f32 ? mx::launch_quantize_f32(p, tmap, tr, st->num_sms, stream)
+                              : mx::launch_quantize(p, tmap, tr, st->num_sms, stream);
+  return err == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
 }  // namespace
@@ -409,7 +429,8 @@ mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_
                                  mx_scale_rule rule, int32_t groups, const int32_t* d_offsets,
                                  uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, int64_t ldq_col,
                                  uint8_t* s_col, cudaStream_t stream) {
-  if (x_dtype != MX_BF16) return x_dtype == MX_FP32 ? MX_ERR_UNSUPPORTED : MX_ERR_INVALID_ARG;
+  if (x_dtype != MX_BF16 && x_dtype != MX_FP32) return MX_ERR_INVALID_ARG;
+  const bool f32 = x_dtype == MX_FP32;
   if (!valid_gemm_fmt(fmt) || (rule != MX_SCALE_FLOOR && rule != MX_SCALE_CEIL))
     return MX_ERR_INVALID_ARG;
   if (!valid_fmt(fmt)) return MX_ERR_UNSUPPORTED;  // grouped: FP8 codes
@@ -424,10 +445,11 @@ mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_
   if (row && cols % 32 != 0) return MX_ERR_INVALID_ARG;
   if (col && (ldq_col <= 0 || ldq_col % 128 != 0)) return MX_ERR_INVALID_ARG;
   if (ceil_div(cols, 128) > 65535) return MX_ERR_UNSUPPORTED;
-  // the columnwise pass numbers its 128x128 tiles in 32 bits
-  if (col && (ceil_div(total_rows, 128) + groups) * ceil_div(cols, 128) > UINT32_MAX)
+  // the columnwise pass numbers its tiles (128 rows x 128 bf16 or 64 FP32
+  // columns) in 32 bits
+  if (col && (ceil_div(total_rows, 128) + groups) * ceil_div(cols, f32 ? 64 : 128) > UINT32_MAX)
     return MX_ERR_UNSUPPORTED;
-  if (!aligned16(x) || ldx % 8 != 0) return MX_ERR_MISALIGNED;
+  if (!aligned16(x) || ldx % (f32 ? 4 : 8) != 0) return MX_ERR_MISALIGNED;
   if ((row && (!aligned16(q_row) || !aligned16(s_row))) ||
       (col && (!aligned16(q_col) || !aligned16(s_col))))
     return MX_ERR_MISALIGNED;
@@ -435,7 +457,7 @@ mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_
   mx_status status = device_state(&st);
   if (status != MX_OK) return status;
   mx::QuantizeParams p{};
-  p.x = static_cast<const uint16_t*>(x);
+  p.x = x;
   p.rows = total_rows;
   p.cols = cols;
   p.ldx = ldx;
@@ -455,10 +477,13 @@ mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_
     return MX_ERR_INVALID_ARG;
   CUtensorMap tmap;
   // an empty token set still needs a valid map (1 row) for the offsets check
-  if ((status = encode_bf16_map(&tmap, x, cols, total_rows > 0 ? total_rows : 1, ldx)) != MX_OK)
-    return status;
-  return mx::launch_quantize_grouped(p, tmap, st->num_sms, stream) == cudaSuccess ? MX_OK
-                                                                                  : MX_ERR_CUDA;
+  const int64_t map_rows = total_rows > 0 ? total_rows : 1;
+  status = f32 ? encode_f32_map(&tmap, x, cols, map_rows, ldx)
+               : encode_bf16_map(&tmap, x, cols, map_rows, ldx);
+  if (status != MX_OK) return status;
+  const cudaError_t err = f32 ? mx::launch_quantize_grouped_f32(p, tmap, st->num_sms, stream)
+                              : mx::launch_quantize_grouped(p, tmap, st->num_sms, stream);
+  return err == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
 mx_status mx_gemm(int64_t m, int64_t n, int64_t k, const uint8_t* a, const uint8_t* sa, mx_fmt fa,

@@ -1,6 +1,7 @@
 """Seeded synthetic inputs for the MXFP8 matmul workloads.
 
-This module only draws random numbers and arranges them into bf16 tensors;
+This module only draws random numbers and arranges them into bf16 (or
+fp32) tensors;
 it holds none of the quantization or GEMM arithmetic, so both the CUDA path
 and the CPU oracle can take their inputs from it.
 
@@ -8,7 +9,7 @@ Recipe (one reading, used everywhere):
 
 * A value "N(0, s)" is drawn in float32 with torch's generator for the
   device it is made on, multiplied by s, then cast to bf16 (round to nearest
-  even, torch's cast).
+  even, torch's cast); an fp32 workload skips the cast.
 * "p of entries replaced by +-U(lo, hi) spikes" means exactly round(p * numel)
   distinct positions (a prefix of a seeded random permutation), each set to a
   magnitude drawn from U(lo, hi) with a fair random sign, before the bf16 cast.
@@ -24,8 +25,10 @@ import torch
 
 
 def synth_matrix(shape, std: float, spike_frac: float = 0.0, spike_lo: float = 0.0,
-                 spike_hi: float = 0.0, seed: int = 0, device="cpu") -> torch.Tensor:
-    """bf16 tensor of N(0, std) with an exact count of +-U(lo, hi) spikes."""
+                 spike_hi: float = 0.0, seed: int = 0, device="cpu",
+                 dtype=torch.bfloat16) -> torch.Tensor:
+    """bf16 (or `dtype`) tensor of N(0, std) with an exact count of
+    +-U(lo, hi) spikes."""
     dev = torch.device(device)
     g = torch.Generator(device=dev)
     g.manual_seed(int(seed))
@@ -40,7 +43,7 @@ def synth_matrix(shape, std: float, spike_frac: float = 0.0, spike_lo: float = 0
         sign = torch.randint(0, 2, (count,), generator=g, device=dev).to(torch.float32) * 2 - 1
         x.view(-1)[idx] = mag * sign
         del idx
-    return x.to(torch.bfloat16)
+    return x.to(dtype)
 
 
 def random_bits16(shape, seed: int = 0, device="cpu") -> torch.Tensor:
@@ -70,9 +73,10 @@ def pr1_reference(device="cpu", seed: int = 0):
     return x, w
 
 
-def quantize_sweep(shape, seed: int, device="cpu"):
+def quantize_sweep(shape, seed: int, device="cpu", dtype=torch.bfloat16):
     """Quantize bandwidth input: N(0,1) with 0.1% outliers +-U(100, 1e4)."""
-    return synth_matrix(shape, 1.0, 0.001, 100.0, 1e4, seed=seed * 100 + 3, device=device)
+    return synth_matrix(shape, 1.0, 0.001, 100.0, 1e4, seed=seed * 100 + 3, device=device,
+                        dtype=dtype)
 
 
 def dense_forward(m=16384, n=18432, k=7168, seed: int = 0, device="cpu"):

@@ -59,8 +59,13 @@ def test_quantize_rejects_bad_arguments_on_the_host(mx):
     assert q(FAKE, 0, 64, 64, 64, 8, 1, 0, FAKE, FAKE, None, None, s) == 1
     assert q(FAKE, 0, 64, 64, 64, 0, 4, 0, FAKE, FAKE, None, None, s) == 1
     assert q(FAKE, 0, 64, 64, 64, 0, 1, 9, FAKE, FAKE, None, None, s) == 1
-    # fp32 input is a valid type but not implemented
-    assert q(FAKE, 1, 64, 64, 64, 0, 1, 0, FAKE, FAKE, None, None, s) == 3
+    # input types: bf16 (0) and fp32 (1) only
+    assert q(FAKE, 2, 64, 64, 64, 0, 1, 0, FAKE, FAKE, None, None, s) == 1
+    # fp32 rows must start on 16-byte boundaries: ldx % 4
+    assert q(FAKE, 1, 64, 64, 66, 0, 1, 0, FAKE, FAKE, None, None, s) == 2
+    # fp32 tiles are 64 columns wide: 3 * 2^24 row tiles x 128 column tiles
+    # are 2^32 or more (as bf16, 64 column tiles, they would fit)
+    assert q(FAKE, 1, 3 << 31, 8192, 8192, 0, 1, 0, FAKE, FAKE, None, None, s) == 3
     # null outputs
     assert q(FAKE, 0, 64, 64, 64, 0, 1, 0, None, FAKE, None, None, s) == 1
     assert q(None, 0, 64, 64, 64, 0, 1, 0, FAKE, FAKE, None, None, s) == 1
