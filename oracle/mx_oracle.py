@@ -23,7 +23,8 @@ states.  Sources (page title, section):
   S = 2^ceil(log2(amax / max)) with the exponent clamped at -127.
 * same page, "Scale ownership and the GEMM dataflow" -- with 32-element
   blocks along K the block scale product stays inside the outer sum:
-  Y_ij = sum_b S_X[i,b] * S_W[b,j] * sum_{k in b} Xq[i,k] * Wq[k,j].
+  Y_ij = sum_b S_X[i,b] * S_W[b,j] * sum_{k in b} Xq[i,k] * Wq[k,j],
+  a partial final block (K not a multiple of 32) completed with zeros.
 * same page, "Hardware support and kernel ABI contracts" -- the kernel
   contract's epilogue: an FP32 bias per output column, then SiLU, then BF16.
   SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z)).
@@ -302,10 +303,24 @@ def scale_exponent_ceil(fmt, amax: np.ndarray) -> np.ndarray:
     return np.clip(e, -127, 127)
 
 
+def pad_final_block(x: np.ndarray) -> np.ndarray:
+    """x[rows, K] completed with zero columns to a whole number of 32-element
+    blocks: the zero-padded partial final block of "Scale ownership and the
+    GEMM dataflow".  Zeros raise no block amax and add nothing to a block
+    sum.  x itself when K is a multiple of 32."""
+    rows, k = x.shape
+    kp = -(-k // BLOCK) * BLOCK
+    if kp == k:
+        return x
+    out = np.zeros((rows, kp), dtype=x.dtype)
+    out[:, :k] = x
+    return out
+
+
 @dataclass
 class MxBlocks:
     codes: np.ndarray   # uint8 [rows, K]
-    scales: np.ndarray  # uint8 [rows, K/32], E8M0 bytes, canonical order
+    scales: np.ndarray  # uint8 [rows, ceil(K/32)], E8M0 bytes, canonical order
     fmt: Fp8Format
 
 
@@ -315,14 +330,16 @@ def quantize_rows(x: np.ndarray, fmt, rule: str = "floor", rand=None) -> MxBlock
     Per 32-element block: amax = max |x|; S = 2^e from the scale rule;
     code = encode_sat_rne(x / S), or encode_sat_sr(x / S, rand) when a
     [rows, K] array of 16-bit random integers is given.  A block holding NaN
-    or Inf takes scale 0xFF and NaN codes.
+    or Inf takes scale 0xFF and NaN codes.  When K is not a multiple of 32
+    the final block is the zero-padded partial block (pad_final_block); the
+    codes of the padding are not returned.
     """
     f = fmt_of(fmt)
     x = np.asarray(x, dtype=np.float64)
     rows, k = x.shape
-    if k % BLOCK:
-        raise ValueError("K must be a multiple of 32")
-    blocks = x.reshape(rows, k // BLOCK, BLOCK)
+    x = pad_final_block(x)
+    nb = x.shape[1] // BLOCK
+    blocks = x.reshape(rows, nb, BLOCK)
     bad = ~np.all(np.isfinite(blocks), axis=2)
     amax = np.max(np.abs(np.where(np.isfinite(blocks), blocks, 0.0)), axis=2)
     if rule == "floor":
@@ -336,12 +353,12 @@ def quantize_rows(x: np.ndarray, fmt, rule: str = "floor", rand=None) -> MxBlock
     if rand is None:
         codes = encode_sat_rne(f, finite_scaled)
     else:
-        r = np.asarray(rand, dtype=np.int64).reshape(rows, k // BLOCK, BLOCK)
+        r = pad_final_block(np.asarray(rand, dtype=np.int64)).reshape(rows, nb, BLOCK)
         codes = encode_sat_sr(f, finite_scaled, r)
     codes = np.where(bad[:, :, None], np.uint8(f.nan_code), codes)
     scales = (e + 127).astype(np.uint8)
     scales[bad] = E8M0_NAN
-    return MxBlocks(codes.reshape(rows, k).astype(np.uint8), scales, f)
+    return MxBlocks(codes.reshape(rows, nb * BLOCK)[:, :k].astype(np.uint8), scales, f)
 
 
 def quantize(x: np.ndarray, fmt, axis: str, rule: str = "floor", rand=None) -> MxBlocks:
@@ -360,16 +377,17 @@ def quantize(x: np.ndarray, fmt, axis: str, rule: str = "floor", rand=None) -> M
 
 def dequantize(q: MxBlocks) -> np.ndarray:
     """x_hat = S * decode(code), NaN where the scale is NaN."""
-    vals = decode_table(q.fmt)[q.codes]
+    vals = pad_final_block(decode_table(q.fmt)[q.codes])
     s = e8m0_values(q.scales)
     rows, k = q.codes.shape
-    return (vals.reshape(rows, k // BLOCK, BLOCK) * s[:, :, None]).reshape(rows, k)
+    nb = vals.shape[1] // BLOCK
+    return (vals.reshape(rows, nb, BLOCK) * s[:, :, None]).reshape(rows, nb * BLOCK)[:, :k]
 
 
 @dataclass
 class IncidentTrace:
-    amax: np.ndarray     # [rows, K/32] block amax over the finite values
-    scales: np.ndarray   # [rows, K/32] the selected E8M0 bytes
+    amax: np.ndarray     # [rows, ceil(K/32)] block amax over the finite values
+    scales: np.ndarray   # [rows, ceil(K/32)] the selected E8M0 bytes
     clip_count: int      # finite values whose exactly scaled magnitude exceeds the format max
     zero_count: int      # finite non-zero values that encode to a zero code
     nan_blocks: int      # blocks holding NaN or Inf (scale byte 0xFF)
@@ -391,7 +409,9 @@ def incident_trace(x: np.ndarray, fmt, axis: str = "row", rule: str = "floor") -
     if axis == "col":
         xx = xx.T
     rows, k = xx.shape
-    blocks = xx.reshape(rows, k // BLOCK, BLOCK)
+    xx = pad_final_block(xx)
+    nb = xx.shape[1] // BLOCK
+    blocks = xx.reshape(rows, nb, BLOCK)
     finite = np.isfinite(blocks)
     bad = ~np.all(finite, axis=2)
     vals = np.where(finite, blocks, 0.0)
@@ -400,7 +420,7 @@ def incident_trace(x: np.ndarray, fmt, axis: str = "row", rule: str = "floor") -
     scaled = np.ldexp(vals, -np.where(bad, 0, e)[:, :, None])
     good = ~bad[:, :, None]
     clipped = good & (np.abs(scaled) > f.max_finite)
-    decoded = decode_table(f)[q.codes.reshape(rows, k // BLOCK, BLOCK)]
+    decoded = pad_final_block(decode_table(f)[q.codes]).reshape(rows, nb, BLOCK)
     zeros = good & (vals != 0.0) & (decoded == 0.0)
     nz = vals[(vals != 0.0) & finite]
     _, ex = np.frexp(np.abs(nz))
@@ -600,7 +620,9 @@ def gemm(a: MxBlocks, b: MxBlocks):
     A is [M, K] and B is [N, K] (the K-contiguous W^T), both quantized along
     K.  The inner per-block sums are a float64 matmul of decoded codes (each
     product is exact); the scale products multiply each block's partial sum
-    before the outer sum, as the definition states.  Also returns
+    before the outer sum, as the definition states.  A partial final block
+    (K not a multiple of 32) sums its K % 32 products (zero padding adds
+    nothing).  Also returns
     T[i, j] = sum_k |A_hat[i, k] B_hat[j, k]|, the magnitude the GEMM
     tolerance is relative to.
     """
@@ -608,9 +630,11 @@ def gemm(a: MxBlocks, b: MxBlocks):
     n, k2 = b.codes.shape
     if k != k2:
         raise ValueError("K mismatch")
-    nb = k // BLOCK
-    av = decode_table(a.fmt)[a.codes].reshape(m, nb, BLOCK)
-    bv = decode_table(b.fmt)[b.codes].reshape(n, nb, BLOCK)
+    av = pad_final_block(decode_table(a.fmt)[a.codes])
+    bv = pad_final_block(decode_table(b.fmt)[b.codes])
+    nb = av.shape[1] // BLOCK
+    av = av.reshape(m, nb, BLOCK)
+    bv = bv.reshape(n, nb, BLOCK)
     sa = e8m0_values(a.scales)
     sb = e8m0_values(b.scales)
     y = np.zeros((m, n), dtype=np.float64)
@@ -739,11 +763,11 @@ def exact_gemm_fraction(a: MxBlocks, b: MxBlocks):
     for i in range(m):
         for j in range(n):
             acc = Fraction(0)
-            for blk in range(k // BLOCK):
+            for blk in range(-(-k // BLOCK)):
                 sa = Fraction(2) ** (int(a.scales[i, blk]) - 127)
                 sb = Fraction(2) ** (int(b.scales[j, blk]) - 127)
                 part = sum(ta[a.codes[i, kk]] * tb[b.codes[j, kk]]
-                           for kk in range(blk * BLOCK, (blk + 1) * BLOCK))
+                           for kk in range(blk * BLOCK, min(k, (blk + 1) * BLOCK)))
                 acc += sa * sb * part
             out[i][j] = acc
     return out

@@ -479,7 +479,7 @@ def random_mx(rng, rows, k, fmt, scale_lo=110, scale_hi=140):
     t = O.decode_table(fmt)
     finite = np.array([c for c in range(256) if np.isfinite(t[c])], dtype=np.uint8)
     codes = rng.choice(finite, size=(rows, k))
-    scales = rng.integers(scale_lo, scale_hi, size=(rows, k // 32)).astype(np.uint8)
+    scales = rng.integers(scale_lo, scale_hi, size=(rows, -(-k // 32))).astype(np.uint8)
     return O.MxBlocks(codes, scales, O.FORMATS[fmt])
 
 
@@ -607,6 +607,103 @@ def test_grouped_col_partial_block_is_zero_padded():
     for c in range(64):
         _, ex = math.frexp(abs(x[32, c]))      # |x| = f * 2^ex, f in [0.5, 1)
         assert q.scales[c, 1] == (ex - 1) - 8 + 127
+
+
+# ------------------------------------------- partial final blocks (K % 32 != 0)
+
+
+def test_partial_final_block_worked_example():
+    """K = 48: a whole block of ones, then a 16-element block whose amax is 3.
+    By hand (E4M3, floor rule): block 0 has e = 0 - 8, scale byte 119, and
+    1 * 2^8 = 256 = 1.0 * 2^8 is code (8 + 7) << 3 = 0x78; block 1 has
+    e = floor(log2 3) - 8 = -7, scale byte 120, 3 * 2^7 = 384 = 1.5 * 2^8 is
+    code 0x78 | 4 = 0x7C, -0.75 * 2^7 = -96 = -1.5 * 2^6 is code
+    0x80 | (6 + 7) << 3 | 4 = 0xEC, and 0.5 * 2^7 = 64 = 2^6 is 0x68.  The
+    same values down a column give the same codes and scales."""
+    x = np.zeros((1, 48))
+    x[0, :32] = 1.0
+    x[0, 32:36] = [3.0, -0.75, 0.0, 0.5]
+    q = O.quantize(x, "e4m3", "row")
+    assert q.codes.shape == (1, 48) and q.scales.shape == (1, 2)
+    assert list(q.scales[0]) == [119, 120]
+    assert np.all(q.codes[0, :32] == 0x78)
+    assert list(q.codes[0, 32:36]) == [0x7C, 0xEC, 0x00, 0x68]
+    assert np.all(q.codes[0, 36:] == 0)
+    c = O.quantize(x.T.copy(), "e4m3", "col")
+    assert np.array_equal(c.codes, q.codes) and np.array_equal(c.scales, q.scales)
+
+
+@pytest.mark.parametrize("k", [16, 48, 80, 112])
+def test_partial_block_takes_the_floor_rule_of_its_own_values(k):
+    """The final block's scale is the floor rule applied to its K % 32 real
+    values (frexp closed form), and its codes are torch's saturating E4M3
+    cast of those values over the scale."""
+    rng = np.random.default_rng(k)
+    x = rng.standard_normal((6, k)) * np.exp2(rng.integers(-10, 10, size=(6, 1)))
+    x = torch.tensor(x).to(torch.bfloat16).double().numpy()
+    q = O.quantize(x, "e4m3", "row")
+    last = k // 32
+    assert q.scales.shape == (6, last + 1)
+    for r in range(6):
+        _, ex = math.frexp(float(np.max(np.abs(x[r, 32 * last:]))))
+        e = (ex - 1) - 8
+        assert q.scales[r, last] == e + 127
+        scaled = torch.tensor(x[r, 32 * last:] * 2.0 ** -e).clamp(-448, 448)
+        want = scaled.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(q.codes[r, 32 * last:], want)
+
+
+@pytest.mark.parametrize("k", [16, 48, 208])
+def test_ragged_k_gemm_of_lossless_integers_is_the_integer_matmul(k):
+    """Integers in [-4, 4], each block holding a 4 or a -4: every value
+    quantizes exactly (v * 2^6 is an E4M3 value), so the GEMM over K
+    elements, partial final block included, is the integer matmul."""
+    rng = np.random.default_rng(k + 1)
+    av = rng.integers(-4, 5, size=(5, k))
+    bv = rng.integers(-4, 5, size=(3, k))
+    for m in (av, bv):
+        m[:, ::32] = 4
+    a = O.quantize(av.astype(np.float64), "e4m3", "row")
+    b = O.quantize(bv.astype(np.float64), "e4m3", "row")
+    y, t = O.gemm(a, b)
+    assert np.array_equal(y, (av @ bv.T).astype(np.float64))
+    assert np.array_equal(t, (np.abs(av) @ np.abs(bv).T).astype(np.float64))
+
+
+def test_ragged_k_gemm_matches_exact_rational_sum():
+    """K = 80 (two whole blocks and a 16-element one), random codes and
+    scales: float64 oracle vs exact Fractions, and T by brute force."""
+    rng = np.random.default_rng(18)
+    a = random_mx(rng, 3, 80, "e4m3")
+    b = random_mx(rng, 2, 80, "e5m2")
+    assert a.scales.shape == (3, 3)
+    y, t = O.gemm(a, b)
+    exact = O.exact_gemm_fraction(a, b)
+    ta, tb = O.decode_table("e4m3"), O.decode_table("e5m2")
+    sa, sb = O.e8m0_values(a.scales), O.e8m0_values(b.scales)
+    for i in range(3):
+        for j in range(2):
+            assert abs(Fraction(y[i, j]) - exact[i][j]) <= Fraction(t[i, j]) * Fraction(1, 2 ** 45)
+            want = sum(abs(ta[a.codes[i, kk]] * sa[i, kk // 32] * tb[b.codes[j, kk]] * sb[j, kk // 32])
+                       for kk in range(80))
+            assert abs(t[i, j] - want) <= 1e-12 * want
+
+
+def test_ragged_k_equals_the_zero_extended_k():
+    """The page's zero-padded final block: quantizing and multiplying K = 48
+    columns gives the codes, scales and product of the same data extended
+    with 16 zero columns (the padding's codes are +0)."""
+    rng = np.random.default_rng(19)
+    x = rng.standard_normal((4, 48))
+    w = rng.standard_normal((3, 48)) * 0.1
+    xp = np.concatenate([x, np.zeros((4, 16))], axis=1)
+    wp = np.concatenate([w, np.zeros((3, 16))], axis=1)
+    for fmt in ("e4m3", "e2m1"):
+        a, ap = O.quantize(x, fmt, "row"), O.quantize(xp, fmt, "row")
+        b, bp = O.quantize(w, fmt, "row"), O.quantize(wp, fmt, "row")
+        assert np.array_equal(a.scales, ap.scales) and np.array_equal(a.codes, ap.codes[:, :48])
+        assert np.all(ap.codes[:, 48:] == 0)
+        assert np.array_equal(O.gemm(a, b)[0], O.gemm(ap, bp)[0])
 
 
 def test_stacked_weights_colwise_equal_per_expert_operands():

@@ -240,3 +240,19 @@ def test_block_amax_takes_the_signed_maximum(monkeypatch):
     monkeypatch.setattr(O, "quantize_rows", bad)
     assert caught(lambda: T.test_block_amax_is_a_magnitude("floor"),
                   lambda: T.test_block_amax_is_a_magnitude("ceil"))
+
+
+def test_partial_block_padding_placed_in_front(monkeypatch):
+    """The zeros of a partial final block put before the row's data, so that
+    every block boundary after the first shifts."""
+    def bad(x):
+        rows, k = x.shape
+        kp = -(-k // O.BLOCK) * O.BLOCK
+        if kp == k:
+            return x
+        out = np.zeros((rows, kp), dtype=x.dtype)
+        out[:, kp - k:] = x
+        return out
+    monkeypatch.setattr(O, "pad_final_block", bad)
+    assert caught(lambda: T.test_partial_final_block_worked_example(),
+                  lambda: T.test_ragged_k_gemm_of_lossless_integers_is_the_integer_matmul(48))
