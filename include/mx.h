@@ -48,12 +48,14 @@
  * block-scaled MMA; the pages require the layout to be recorded with the
  * kernel but do not define it -- section "Hardware support and kernel ABI
  * contracts"):
- *  - Scales of a [rows, K] operand (K/32 blocks per row) are stored in tiles
+ *  - Scales of a [rows, K] operand (ceil(K/32) blocks per row; a final
+ *    block of K % 32 elements is the page's zero-padded partial block) are
+ *    stored in tiles
  *    of 128 rows x 4 blocks = 512 bytes.  Tile (rt, kt) starts at byte
  *    (rt * ceil(K/128) + kt) * 512.  Inside a tile, the scale of local row r
  *    (0..127) and local block c (0..3) is at byte
  *    (r % 32) * 16 + (r / 32) * 4 + c.
- *  - Padding entries (rows >= rows, blocks >= K/32) are written as 0x00 by
+ *  - Padding entries (rows >= rows, blocks >= ceil(K/32)) are written as 0x00 by
  *    the quantizer and never influence a valid GEMM output.
  *  - A scale byte c encodes 2^(c - 127); 0xFF is NaN.
  *
@@ -139,7 +141,7 @@ typedef enum { MX_ROWWISE = 1, MX_COLWISE = 2, MX_BOTH = 3 } mx_axis;
 typedef enum { MX_SCALE_FLOOR = 0, MX_SCALE_CEIL = 1 } mx_scale_rule;
 
 /* Bytes of the swizzled scale buffer of a [rows, k] operand:
- * ceil(rows/128)*128 * ceil(k/32/4)*4.  k must be a multiple of 32
+ * ceil(rows/128)*128 * ceil(ceil(k/32)/4)*4.  k must be a multiple of 16
  * (returns 0 otherwise or for negative sizes). */
 size_t mx_scale_bytes(int64_t rows, int64_t k);
 
@@ -152,12 +154,17 @@ size_t mx_grouped_scale_bytes(int64_t total_rows, int32_t groups, int64_t k);
  * row-major, leading dimension ldx elements), section "Microscaling: the
  * two-row experiment".
  *
- *  ROWWISE (needs cols % 32 == 0): q_row[rows, cols] codes (row-major,
+ *  ROWWISE (needs cols % 16 == 0): q_row[rows, cols] codes (row-major,
  *    leading dimension cols) and s_row = swizzled scales of the
  *    [rows, cols] operand (mx_scale_bytes(rows, cols) bytes).
- *  COLWISE (needs rows % 32 == 0): q_col[cols, rows] codes -- the transpose,
+ *  COLWISE (needs rows % 16 == 0): q_col[cols, rows] codes -- the transpose,
  *    leading dimension rows -- and s_col = swizzled scales of the
  *    [cols, rows] operand (mx_scale_bytes(cols, rows) bytes).
+ *  Blocked axis not a multiple of 32: the final block holds 16 elements
+ *    and is quantized as the zero-padded partial block of section "Scale
+ *    ownership and the GEMM dataflow" (its amax and scale are those of its
+ *    16 elements; no code is written past the matrix).  Packed formats
+ *    need the blocked axis % 32 == 0.
  *  BOTH: both of the above from one read of x.
  *  Packed formats (MX_*_PACKED): a code row of n elements takes n*w/8 bytes
  *    (q_row: rows x cols*w/8 bytes; q_col: cols x rows*w/8 bytes).
@@ -227,7 +234,7 @@ int64_t mx_grouped_cols_capacity(int64_t total_rows, int32_t groups);
  *   always suffices); a layout that does not fit is reported through
  *   mx_device_status (MX_ERR_DEVICE_ARG) and nothing is written.  This is
  *   the operand layout of mx_grouped_gemm_wgrad.
- * cols % 8 == 0 (ROWWISE also cols % 32 == 0); x_dtype, ldx, d_offsets and
+ * cols % 8 == 0 (ROWWISE also cols % 16 == 0); x_dtype, ldx, d_offsets and
  * groups as for mx_quantize and mx_quantize_grouped.  Unused outputs may be
  * NULL. */
 mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_rows,
@@ -248,7 +255,9 @@ mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_
  *    k % 128 == 0, code pointer 32-byte aligned, row stride k*w/8 bytes).
  * y: device, [m, n] row-major with leading dimension ldy (elements),
  *    FP32 or BF16 (RNE from the FP32 accumulator).
- * Constraints: k % 32 == 0, k >= 32, n % 8 == 0, ldy >= n.
+ * Constraints: k % 16 == 0, k >= 16, n % 8 == 0, ldy >= n.  When k % 32 ==
+ * 16 the final block is the zero-padded partial block (codes past k read as
+ * zero; its scales are those mx_quantize writes for it).
  * Accumulation is FP32 on the tensor cores; its internal order is
  * implementation-defined (section "Accumulator type isn't the whole
  * arithmetic contract"). */
@@ -284,7 +293,7 @@ mx_status mx_gemm_bias_act(int64_t m, int64_t n, int64_t k,
  * y: [total_m, n] row-major (leading dimension n).  Rows of empty groups do
  *    not exist; rows outside [0, total_m) are never written.
  * d_offsets: device int32[groups + 1] as for mx_quantize_grouped; read on
- *    the device (no host synchronization).  n % 128 == 0, k % 32 == 0. */
+ *    the device (no host synchronization).  n % 128 == 0, k % 16 == 0. */
 mx_status mx_grouped_gemm(int32_t groups, const int32_t* d_offsets, int64_t total_m,
                           int64_t n, int64_t k,
                           const uint8_t* a, const uint8_t* sa, mx_fmt fa,

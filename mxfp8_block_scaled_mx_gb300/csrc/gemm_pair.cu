@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(PairWarps<FUSED>::kThreads, 1)
     // Grouped along K every group has its own contraction length; a group
     // without tokens has none (its output tile is written as zeros).
     const uint32_t group_units = static_cast<uint32_t>(m_units * n_tiles);
-    int32_t k_blocks = static_cast<int32_t>(p.k / 32);
+    int32_t k_blocks = static_cast<int32_t>((p.k + 31) / 32);
     uint32_t stage = 0, phase = 0, acc_phase = 0;
     bool ok = true;
     for (int64_t u = cluster_id; u < num_units && ok; u += num_clusters) {

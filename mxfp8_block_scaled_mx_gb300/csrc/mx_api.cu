@@ -229,8 +229,9 @@ mx_status gemm_common(const GemmShape& g, const uint8_t* a, const uint8_t* sa, m
   const int64_t m = g.m, n = g.n, k = g.k;
   if (!a || !sa || !b || !sb || !y) return MX_ERR_INVALID_ARG;
   if (m < 0 || n <= 0 || k < 0 || n % 8 != 0 || ldy < n) return MX_ERR_INVALID_ARG;
-  // grouped along K, k is the token total that the offsets split
-  if (g.mode != mx::kModeGroupK && (k < 32 || k % 32 != 0)) return MX_ERR_INVALID_ARG;
+  // grouped along K, k is the token total that the offsets split; else
+  // whole 16-element runs (a final partial block of 16 is zero-padded)
+  if (g.mode != mx::kModeGroupK && (k < 16 || k % 16 != 0)) return MX_ERR_INVALID_ARG;
   if (!valid_gemm_fmt(fa) || !valid_gemm_fmt(fb)) return MX_ERR_INVALID_ARG;
   if (y_dtype != MX_BF16 && y_dtype != MX_FP32) return MX_ERR_INVALID_ARG;
   if (m > INT32_MAX || g.b_rows > INT32_MAX || k > INT32_MAX || g.lda > INT32_MAX ||
@@ -319,12 +320,12 @@ GemmShape dense_shape(int64_t m, int64_t n, int64_t k) {
 extern "C" {
 
 size_t mx_scale_bytes(int64_t rows, int64_t k) {
-  if (rows < 0 || k < 0 || k % 32 != 0) return 0;
-  return static_cast<size_t>(ceil_div(rows, 128) * 128 * ceil_div(k / 32, 4) * 4);
+  if (rows < 0 || k < 0 || k % 16 != 0) return 0;
+  return static_cast<size_t>(ceil_div(rows, 128) * 128 * ceil_div(ceil_div(k, 32), 4) * 4);
 }
 
 size_t mx_grouped_scale_bytes(int64_t total_rows, int32_t groups, int64_t k) {
-  if (total_rows < 0 || groups < 0 || k < 0 || k % 32 != 0) return 0;
+  if (total_rows < 0 || groups < 0 || k < 0 || k % 16 != 0) return 0;
   return static_cast<size_t>((ceil_div(total_rows, 128) + groups) * 128 * ceil_div(k, 128) * 4);
 }
 
@@ -346,8 +347,11 @@ mx_status quantize_common(const void* x, mx_dtype x_dtype, int64_t rows, int64_t
   if (!x || (row && (!q_row || !s_row)) || (col && (!q_col || !s_col))) return MX_ERR_INVALID_ARG;
   if (rows < 0 || cols < 0 || ldx < cols || cols % 8 != 0) return MX_ERR_INVALID_ARG;
   if (rbits && ldr < cols) return MX_ERR_INVALID_ARG;
-  if (row && cols % 32 != 0) return MX_ERR_INVALID_ARG;
-  if (col && rows % 32 != 0) return MX_ERR_INVALID_ARG;
+  // the blocked axis: whole 16-element runs (16-byte code rows; a final
+  // partial block of 16 is zero-padded), whole blocks in packed storage
+  const int64_t k_unit = is_packed(fmt) ? 32 : 16;
+  if (row && cols % k_unit != 0) return MX_ERR_INVALID_ARG;
+  if (col && rows % k_unit != 0) return MX_ERR_INVALID_ARG;
   if (ceil_div(cols, 128) > 65535) return MX_ERR_UNSUPPORTED;
   // the kernels number their tiles (128 rows x 128 bf16 or 64 FP32 columns) in 32 bits
   const int64_t col_tiles = ceil_div(cols, f32 ? 64 : 128);
@@ -442,7 +446,7 @@ mx_status mx_quantize_grouped_ex(const void* x, mx_dtype x_dtype, int64_t total_
   if (groups < 1 || groups > 1000) return MX_ERR_INVALID_ARG;
   if (total_rows < 0 || total_rows > INT32_MAX || cols < 0 || ldx < cols || cols % 8 != 0)
     return MX_ERR_INVALID_ARG;
-  if (row && cols % 32 != 0) return MX_ERR_INVALID_ARG;
+  if (row && cols % 16 != 0) return MX_ERR_INVALID_ARG;
   if (col && (ldq_col <= 0 || ldq_col % 128 != 0)) return MX_ERR_INVALID_ARG;
   if (ceil_div(cols, 128) > 65535) return MX_ERR_UNSUPPORTED;
   // the columnwise pass numbers its tiles (128 rows x 128 bf16 or 64 FP32

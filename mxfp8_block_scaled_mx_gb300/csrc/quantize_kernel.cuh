@@ -410,20 +410,23 @@ __device__ __forceinline__ bool group_bar_any(int group, bool pred) {
 // One block's 32 codes (c[j]: codes 8j..8j+7, laid out as encode8 gives
 // them) into the code row at `rowp`, starting at element column gcb: FP8 32
 // bytes; FP6 / FP4 one 16-byte container per 16-element run; packed
-// storage 16 (FP4) or 24 (FP6) bytes.
+// storage 16 (FP4) or 24 (FP6) bytes.  With `half` (a partial final block
+// of 16 elements; not in packed storage) only the first run is stored.
 template <int FMT, bool PACKED>
-__device__ __forceinline__ void store_row_block(uint8_t* rowp, int64_t gcb, const uint2 (&c)[4]) {
+__device__ __forceinline__ void store_row_block(uint8_t* rowp, int64_t gcb, const uint2 (&c)[4],
+                                                bool half) {
   using F = ElemFmt<FMT>;
   if constexpr (F::kBits == 8) {
     *reinterpret_cast<uint4*>(rowp + gcb) = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
-    *reinterpret_cast<uint4*>(rowp + gcb + 16) = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
+    if (!half)
+      *reinterpret_cast<uint4*>(rowp + gcb + 16) = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
   } else if constexpr (F::kBits == 4) {
     // eight codes per 32-bit word (code i in bits [4i, 4i + 4))
     if constexpr (PACKED) {
       *reinterpret_cast<uint4*>(rowp + gcb / 2) = make_uint4(c[0].x, c[1].x, c[2].x, c[3].x);
     } else {  // two 16-element runs, each 8 bytes of codes then 8 zero bytes
       *reinterpret_cast<uint4*>(rowp + gcb) = make_uint4(c[0].x, c[1].x, 0u, 0u);
-      *reinterpret_cast<uint4*>(rowp + gcb + 16) = make_uint4(c[2].x, c[3].x, 0u, 0u);
+      if (!half) *reinterpret_cast<uint4*>(rowp + gcb + 16) = make_uint4(c[2].x, c[3].x, 0u, 0u);
     }
   } else {
     // 6-bit codes: each run of 16 is 96 packed bits (12 bytes)
@@ -442,7 +445,7 @@ __device__ __forceinline__ void store_row_block(uint8_t* rowp, int64_t gcb, cons
       d[2] = make_uint2(w4, w5);
     } else {  // each run's 12 bytes, then 4 zero bytes
       *reinterpret_cast<uint4*>(rowp + gcb) = make_uint4(w0, w1, w2, 0u);
-      *reinterpret_cast<uint4*>(rowp + gcb + 16) = make_uint4(w3, w4, w5, 0u);
+      if (!half) *reinterpret_cast<uint4*>(rowp + gcb + 16) = make_uint4(w3, w4, w5, 0u);
     }
   }
 }
@@ -511,7 +514,9 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
     const int lr = lt & 127;
     const int bq = lt >> 7;
     const int64_t gcb = tl.c0 + bq * 32;  // first column of the block
-    const bool blk_ok = gcb < p.cols;     // cols % 32 == 0: a block is whole or absent
+    // cols % 16 == 0: a block is whole, absent, or a final block of 16
+    // columns (the tensor copy filled the rest with zeros)
+    const bool blk_ok = gcb < p.cols;
     uint4 v[8];
     uint4 rv[SR ? 4 : 1];
 #pragma unroll
@@ -546,7 +551,8 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
       sbyte = static_cast<uint8_t>(e + 127);
     }
     if (blk_ok && lr < tl.rows_valid) {
-      store_row_block<FMT, PACKED>(p.q_row + (tl.x_row0 + lr) * row_bytes, gcb, c);
+      store_row_block<FMT, PACKED>(p.q_row + (tl.x_row0 + lr) * row_bytes, gcb, c,
+                                   gcb + 16 >= p.cols);
       s_unit_row[unit_offset(lr, 2 * half + bq)] = sbyte;
     }
   } else if constexpr (ROW) {
@@ -556,7 +562,9 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
     const int bq = lt & 3;
     const int lr0 = lt >> 2;
     const int64_t gcb = tl.c0 + bq * 32;  // first column of the block
-    const bool blk_ok = gcb < p.cols;     // cols % 32 == 0: a block is whole or absent
+    // cols % 16 == 0: a block is whole, absent, or a final block of 16
+    // columns (the tensor copy filled the rest with zeros)
+    const bool blk_ok = gcb < p.cols;
     uint4 v[2][4];
     uint4 rv[SR ? 2 : 1][4];
 #pragma unroll
@@ -596,7 +604,8 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
         sbyte = static_cast<uint8_t>(e + 127);
       }
       if (!blk_ok || lr >= tl.rows_valid) continue;
-      store_row_block<FMT, PACKED>(p.q_row + (tl.x_row0 + lr) * row_bytes, gcb, c);
+      store_row_block<FMT, PACKED>(p.q_row + (tl.x_row0 + lr) * row_bytes, gcb, c,
+                                   gcb + 16 >= p.cols);
       s_unit_row[unit_offset(lr, bq)] = sbyte;
     }
   }

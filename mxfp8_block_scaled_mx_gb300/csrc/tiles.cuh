@@ -32,7 +32,8 @@ struct TileInfo {
   int64_t sfa_unit;  // first 512-byte scale unit of A (-1: this block's tile is padding)
   int64_t sfb_unit;  // first scale unit of the B tile's first 128-row tile
   int64_t sfb_step;  // scale units between consecutive 128-row tiles of B
-  int32_t k_blocks;  // 32-element K blocks of the tile's contraction
+  int32_t k_blocks;  // 32-element K blocks of the tile's contraction (a partial
+                     // final block, zero-filled past K by the tensor copy, counts)
   // The same scale units as (row tile, first K tile) coordinates of the
   // [row tiles][K tiles] unit grid (3-D tensor-map copies); sfa_rt is set
   // even for a padding tile (its scales are loaded and never used).
@@ -58,7 +59,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t u, in
   ti.a_kx0 = 0;
   ti.b_kx0 = 0;
   ti.sfb_step = b_tiles_k;
-  ti.k_blocks = static_cast<int32_t>(p.k / 32);
+  ti.k_blocks = static_cast<int32_t>((p.k + 31) / 32);
   const uint32_t u32 = static_cast<uint32_t>(u);
   const uint32_t nt32 = static_cast<uint32_t>(n_tiles);
   if constexpr (MODE == kModeGroupM) {

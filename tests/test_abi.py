@@ -40,6 +40,9 @@ def test_scale_bytes(mx):
     assert mx.mx_scale_bytes(130, 160) == 256 * 8
     assert mx.mx_scale_bytes(16384, 7168) == 16384 * 224
     assert mx.mx_scale_bytes(10, 33) == 0
+    assert mx.mx_scale_bytes(10, 40) == 0                 # k % 16
+    assert mx.mx_scale_bytes(130, 48) == 256 * 4          # a partial final block of 16
+    assert mx.mx_scale_bytes(1, 16) == 128 * 4
     assert mx.mx_grouped_scale_bytes(65536, 64, 7168) == (512 + 64) * 128 * 224
     assert mx.mx_status_str(0) == "MX_OK"
     assert mx.mx_status_str(5) == "MX_ERR_TIMEOUT"
@@ -51,10 +54,13 @@ FAKE = 0x10000  # an aligned non-null address; validation rejects before any use
 def test_quantize_rejects_bad_arguments_on_the_host(mx):
     q = mx.mx_quantize
     s = 0
-    # K (cols) not a multiple of 32 for rowwise
+    # K (cols) not a multiple of 16 for rowwise
     assert q(FAKE, 0, 64, 40, 40, 0, 1, 0, FAKE, FAKE, None, None, s) == 1
-    # rows not a multiple of 32 for colwise
+    # rows not a multiple of 16 for colwise
     assert q(FAKE, 0, 40, 64, 64, 0, 2, 0, None, None, FAKE, FAKE, s) == 1
+    # packed storage: the blocked axis in whole 32-element blocks
+    assert q(FAKE, 0, 64, 48, 48, 7, 1, 0, FAKE, FAKE, None, None, s) == 1
+    assert q(FAKE, 0, 48, 64, 64, 5, 2, 0, None, None, FAKE, FAKE, s) == 1
     # bad enums
     assert q(FAKE, 0, 64, 64, 64, 8, 1, 0, FAKE, FAKE, None, None, s) == 1
     assert q(FAKE, 0, 64, 64, 64, 0, 4, 0, FAKE, FAKE, None, None, s) == 1
@@ -83,7 +89,8 @@ def test_gemm_rejects_bad_arguments_on_the_host(mx):
     g = mx.mx_gemm
     s = 0
     ok = dict(m=64, n=64, k=64)
-    assert g(64, 64, 48, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # k % 32
+    assert g(64, 64, 40, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # k % 16
+    assert g(64, 64, 48, FAKE, FAKE, 7, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # packed: k % 128
     assert g(64, 64, 0, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1       # k == 0
     assert g(64, 60, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # n % 8
     assert g(64, 64, 64, FAKE, FAKE, 7, FAKE, FAKE, 0, FAKE, 0, 64, s) == 1      # fmt
@@ -105,7 +112,7 @@ def test_grouped_calls_reject_bad_arguments_on_the_host(mx):
     assert gg(4, FAKE, 64, 136, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 0) == 1      # n % 128
     qg = mx.mx_quantize_grouped
     assert qg(FAKE, 0, 64, 64, 64, 0, 0, 0, FAKE, FAKE, FAKE, 0) == 1                  # groups
-    assert qg(FAKE, 0, 64, 48, 48, 0, 0, 4, FAKE, FAKE, FAKE, 0) == 1                  # cols % 32
+    assert qg(FAKE, 0, 64, 40, 40, 0, 0, 4, FAKE, FAKE, FAKE, 0) == 1                  # cols % 16
     assert qg(FAKE, 0, 64, 64, 64, 0, 0, 4, None, FAKE, FAKE, 0) == 1                  # offsets
 
 
@@ -120,7 +127,7 @@ def test_grouped_backward_calls_reject_bad_arguments_on_the_host(mx):
     assert qx(FAKE, 0, 64, 64, 64, 0, 2, 0, 4, FAKE, None, None, None, 256, FAKE, 0) == 1  # q_col
     assert qx(FAKE, 0, 64, 64, 64, 0, 2, 0, 4, None, None, None, FAKE, 256, FAKE, 0) == 1  # offsets
     assert qx(FAKE, 0, 64, 64, 64, 0, 2, 0, 0, FAKE, None, None, FAKE, 256, FAKE, 0) == 1  # groups
-    assert qx(FAKE, 0, 64, 40, 40, 0, 3, 0, 4, FAKE, FAKE, FAKE, FAKE, 256, FAKE, 0) == 1  # row cols % 32
+    assert qx(FAKE, 0, 64, 40, 40, 0, 3, 0, 4, FAKE, FAKE, FAKE, FAKE, 256, FAKE, 0) == 1  # row cols % 16
     assert qx(FAKE, 0, 64, 64, 64, 0, 2, 0, 4, FAKE, None, None, FAKE + 8, 256, FAKE, 0) == 2  # align
     # (2^24 + 4) x 65535 padded column tiles: beyond 32-bit tile numbers
     big = (1 << 31) - 1
@@ -147,7 +154,7 @@ def test_fused_epilogue_rejects_bad_arguments_on_the_host(mx):
     f = mx.mx_gemm_bias_act
     assert f(64, 64, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, None, 7, FAKE, 0, 64, 0) == 1      # act
     assert f(64, 64, 64, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE + 4, 1, FAKE, 0, 64, 0) == 2  # bias align
-    assert f(64, 64, 48, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 1, FAKE, 0, 64, 0) == 1      # k % 32
+    assert f(64, 64, 40, FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 1, FAKE, 0, 64, 0) == 1      # k % 16
 
 
 def test_stochastic_quantize_rejects_bad_arguments_on_the_host(mx):
@@ -170,7 +177,7 @@ def test_narrow_formats_on_the_host(mx):
         assert mx.mx_quantize_grouped(FAKE, 0, 64, 64, 64, fmt, 0, 4, FAKE, FAKE, FAKE, 0) == 3
     q = mx.mx_quantize
     assert q(FAKE, 0, 64, 64, 64, 8, 1, 0, FAKE, FAKE, None, None, 0) == 1           # no format 8
-    assert q(FAKE, 0, 64, 40, 40, 4, 1, 0, FAKE, FAKE, None, None, 0) == 1           # cols % 32
+    assert q(FAKE, 0, 64, 40, 40, 4, 1, 0, FAKE, FAKE, None, None, 0) == 1           # cols % 16
 
 
 def test_packed_formats_on_the_host(mx):
