@@ -175,3 +175,29 @@ def test_grouped_gemm_with_partial_block(mx):
     bs = [O.quantize(to_f64(w[e]), "e4m3", "row") for e in range(groups)]
     y_ref, t_ref = O.grouped_gemm(a, offsets, bs)
     assert_gemm_close(y, y_ref, t_ref, "fp32")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_grouped_quantize_both_with_partial_row_blocks(mx, dtype):
+    """Expert-grouped tokens with 208 columns (a 16-column final rowwise
+    block), both orientations from one read: rowwise codes and per-group
+    padded scales, and the per-expert columnwise operand, against the
+    oracle."""
+    sizes = [0, 1, 31, 200, 0, 128, 129, 5]
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    total, cols = int(offsets[-1]), 208
+    x = data(total, cols, seed=21, dtype=dtype)
+    d_off = torch.from_numpy(offsets).cuda()
+    ldq = mx.mx_grouped_cols_capacity(total, len(sizes))
+    row, col = mx.quantize_grouped(x.cuda(), d_off, "e4m3", axis="both", ldq=ldq)
+    assert mx.device_status() == 0
+    ref = O.quantize(to_f64(x), "e4m3", "row")
+    assert torch.equal(row.codes.cpu(), torch.from_numpy(ref.codes))
+    want = O.swizzle_scales_grouped(ref.scales, offsets)
+    assert np.array_equal(row.scales.cpu().numpy()[:want.size], want)
+    qs = O.quantize_grouped_cols(to_f64(x), offsets, "e4m3")
+    codes, scales = O.pack_grouped_cols(qs, offsets, ldq)
+    used = int(O.grouped_scale_rows(offsets)[-1])
+    assert torch.equal(col.codes[:, :used].cpu(), torch.from_numpy(codes[:, :used]))
+    got = O.unswizzle_scales(col.scales.cpu().numpy(), cols, ldq // 32)
+    assert np.array_equal(got[:, :used // 32], scales[:, :used // 32])
