@@ -216,3 +216,23 @@ def test_f32_quantize_16384x8192_sampled(mx):
         q = O.quantize(to_f64(x[:, c0:c0 + 64]), "e4m3", "col")
         assert torch.equal(c.codes[c0:c0 + 64].cpu(), torch.from_numpy(q.codes))
         assert np.array_equal(cs[c0:c0 + 64], q.scales)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "e2m3", "e3m2", "e2m1"])
+def test_f32_ceil_rule_at_the_significand_threshold(mx, fmt):
+    """Block maxima one FP32 step below, at, and one step above the
+    significand of the format's maximum (1.75, 1.875 or 1.5) across
+    binades: the ceil rule raises the exponent only strictly above it,
+    which only the 23-bit FP32 significand can show."""
+    sig = {"e4m3": 1.75, "e5m2": 1.75, "e3m2": 1.75, "e2m3": 1.875, "e2m1": 1.5}[fmt]
+    rows = []
+    for e in range(-20, 21, 4):
+        for d in (-2.0 ** -23, 0.0, 2.0 ** -23, 2.0 ** -22):
+            r = np.full(32, 0.25 * 2.0 ** e)
+            r[7] = (sig + d) * 2.0 ** e
+            r[9] = -(sig + d) * 2.0 ** e / 3
+            rows.append(r)
+    x = torch.tensor(np.array(rows), dtype=torch.float32)
+    for rule in ("ceil", "floor"):
+        q = mx.quantize(x.cuda(), fmt, "row", rule)
+        check(q, x, fmt, "row", rule)
