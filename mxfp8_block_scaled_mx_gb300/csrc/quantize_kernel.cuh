@@ -10,8 +10,8 @@
 // nearest even, subnormals kept, saturation after rounding).
 //
 // The kernel is HBM-bound, so it is built around deep prefetch: one
-// persistent block per SM, a producer thread that streams 32 KB tiles of x
-// (128 rows x 256 bytes: 128 bf16 or 64 FP32 columns) into a ring of
+// persistent block per SM, a producer thread that streams tiles of x (128
+// rows of 128 bf16 or FP32 columns, 32 or 64 KB) into a ring of
 // shared-memory slots with cp.async.bulk.tensor, and groups of eight
 // consumer warps that take tiles round-robin, straight out of shared memory
 // while the next tiles are in flight.
@@ -26,10 +26,12 @@
 //    row), the codes are transposed in shared memory and written back as
 //    128-byte rows of the [cols, rows] output, again with one 512-byte scale
 //    unit per tile.
-//  - FP32 input: the same tile bytes hold 64 columns, so each thread takes
-//    one block (rowwise) or one column block (columnwise), and a tile fills
-//    half of each 512-byte scale unit (the half is written in place, the
-//    whole unit when the tile is the matrix's last).
+//  - FP32 input: a rowwise-only pass takes 128-column tiles (64 KB slots,
+//    two blocks a thread, one after the other); with columnwise codes the
+//    tiles hold 64 columns in 32 KB, each thread takes one block (rowwise)
+//    or one column block (columnwise), and a tile fills half of each
+//    512-byte scale unit (the half is written in place, the whole unit when
+//    the tile is the matrix's last).
 #pragma once
 
 #include <cuda.h>
@@ -49,9 +51,11 @@ constexpr int kTile = 128;                    // rows of x per tile (and bf16 co
 constexpr int kGroupThreads = 256;            // one consumer group: 8 warps
 constexpr int kTileBytes = kTile * kTile * 2; // 32 KB: 128 rows of 256 bytes
 
-// Columns of x per tile: 128 bf16 or 64 FP32.
-template <bool F32>
-constexpr int kTileCols = F32 ? 64 : 128;
+// Columns of x per tile: 128 bf16 (32 KB); FP32 128 (64 KB) for a
+// rowwise-only pass and 64 (32 KB, half of each scale unit) when the
+// columnwise codes are written too.
+template <bool F32, bool COL>
+constexpr int kTileCols = (F32 && COL) ? 64 : 128;
 constexpr int kColPitch = 144;                // bytes per transposed code row in smem
 
 // Per-halfword unsigned max of two packed pairs (one SIMD instruction).
@@ -501,13 +505,65 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
                                               uint8_t* s_unit_row, uint8_t* s_unit_col,
                                               uint64_t* empty_bar, int group, int lt) {
   using F = ElemFmt<FMT>;
-  constexpr int kCols = kTileCols<F32>;
+  constexpr int kCols = kTileCols<F32, COL>;
   const uint32_t lane = lt & 31;
   const int half = static_cast<int>(tl.c0 >> 6) & 1;  // FP32: which half of the scale units
   // bytes per code row: one per element, or w / 8 in packed storage
   const int64_t row_bytes = PACKED ? p.cols * F::kBits / 8 : p.cols;
 
-  if constexpr (ROW && F32) {
+  if constexpr (ROW && F32 && kCols == 128) {
+    // 128 FP32 columns, four blocks a row: thread lt quantizes blocks
+    // lt / 128 and lt / 128 + 2 of tile row lt % 128, one after the other
+    // (a warp reads 32 consecutive rows, conflict-free under the swizzle).
+    const int lr = lt & 127;
+    // not unrolled: the second block's loads would be hoisted above the
+    // first block's work and spill with stochastic rounding
+#pragma unroll 1
+    for (int j = 0; j < 2; ++j) {
+      const int bq = (lt >> 7) + 2 * j;
+      const int64_t gcb = tl.c0 + bq * 32;
+      const bool blk_ok = gcb < p.cols;
+      uint4 v[8];
+      uint4 rv[SR ? 4 : 1];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        v[i] = *reinterpret_cast<const uint4*>(xs + tile_offset(lr, bq * 128 + i * 16));
+      if constexpr (SR) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          rv[i] = *reinterpret_cast<const uint4*>(rs + tile_offset(lr, bq * 64 + i * 16));
+      }
+      if (j == 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar);  // slot fully read by this warp
+      }
+      uint2 c[4];
+      uint8_t sbyte;
+      const uint32_t a = amax_bits32_f32(v);
+      if (a >= 0x7F800000u) {  // NaN or Inf in the block
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[i] = make_uint2(F::kNanWord, F::kNanWord);
+        sbyte = kNanScale;
+      } else {
+        const int e = scale_exponent<FMT, true>(a, p.rule);
+        const float mul = pow2_neg(e);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if constexpr (SR) {
+            c[i] = encode8_f32_sr<FMT>(v[2 * i], v[2 * i + 1], rv[SR ? i : 0], mul);
+          } else {
+            c[i] = encode8_f32<FMT>(v[2 * i], v[2 * i + 1], mul);
+          }
+        }
+        sbyte = static_cast<uint8_t>(e + 127);
+      }
+      if (blk_ok && lr < tl.rows_valid) {
+        store_row_block<FMT, PACKED>(p.q_row + (tl.x_row0 + lr) * row_bytes, gcb, c,
+                                     gcb + 16 >= p.cols);
+        s_unit_row[unit_offset(lr, bq)] = sbyte;
+      }
+    }
+  } else if constexpr (ROW && F32) {
     // Thread lt quantizes block lt / 128 (of the tile's two) of tile row
     // lt % 128; a warp reads 32 consecutive rows, conflict-free under the
     // swizzle.
@@ -718,9 +774,9 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
   }
   group_bar(group);  // scale units and transposed codes complete
 
-  // An FP32 tile writes its half of each scale unit in place, or the whole
-  // unit (the other half zero) when no tile to its right exists.
-  const bool whole_unit = !F32 || (half == 0 && tl.c0 + 64 >= p.cols);
+  // A 64-column FP32 tile writes its half of each scale unit in place, or
+  // the whole unit (the other half zero) when no tile to its right exists.
+  const bool whole_unit = kCols == 128 || (half == 0 && tl.c0 + 64 >= p.cols);
   if constexpr (ROW) {
     const int64_t tiles_k = (p.cols + 127) / 128;
     const int64_t unit = tl.scale_rt * tiles_k + tl.c0 / 128;
@@ -794,16 +850,18 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
 }
 
 // Shared memory: the tile ring, then per consumer group the transposed-code
-// buffer (columnwise modes only) and two scale units.
-template <bool COL, bool SR = false>
+// buffer (columnwise modes only) and two scale units.  WIDE: the 64 KB
+// tiles of the rowwise-only FP32 pass.
+template <bool COL, bool SR = false, bool WIDE = false>
 struct QSmem {
   // consumer groups (round-robin tiles): three for the rowwise-only ring
-  // of six slots, two otherwise
+  // of six (wide: three) slots, two otherwise
   static constexpr int kGroups = (!COL && !SR) ? 3 : 2;
   static constexpr int kThreads = kGroups * kGroupThreads + 32;  // + one producer warp
-  // a slot holds the bf16 tile, plus its 16-bit random integers with SR
-  static constexpr int kSlotBytes = SR ? 2 * kTileBytes : kTileBytes;
-  static constexpr int kStages = SR ? 2 : (COL ? 4 : 6);   // tile slots in flight
+  // a slot holds the tile of x, plus its 16-bit random integers with SR
+  static constexpr int kXBytes = WIDE ? 2 * kTileBytes : kTileBytes;
+  static constexpr int kSlotBytes = kXBytes + (SR ? kTileBytes : 0);
+  static constexpr int kStages = WIDE ? (SR ? 2 : 3) : SR ? 2 : (COL ? 4 : 6);   // tile slots in flight
   // Tile i lives in slot i % kStages and is consumed by group i % kGroups.
   // Successive users of a slot (tiles i and i + kStages) must belong to the
   // same group: a group can then never wait on a slot's next phase while
@@ -821,10 +879,10 @@ struct QSmem {
 };
 
 template <int FMT, bool ROW, bool COL, bool GROUPED, bool SR, bool PACKED, bool F32>
-__global__ void __launch_bounds__(QSmem<COL, SR>::kThreads, 1)
+__global__ void __launch_bounds__(QSmem<COL, SR, F32 && !COL>::kThreads, 1)
     quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     const __grid_constant__ CUtensorMap tmap_r, const QuantizeParams p) {
-  using QSmem = mx::QSmem<COL, SR>;
+  using QSmem = mx::QSmem<COL, SR, F32 && !COL>;
   constexpr int kStages = QSmem::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -838,10 +896,10 @@ __global__ void __launch_bounds__(QSmem<COL, SR>::kThreads, 1)
   const int lane = tid & 31;
   constexpr int kGroups = QSmem::kGroups;
   constexpr int kProducerWarp = kGroups * kGroupThreads / 32;
-  constexpr int kCols = kTileCols<F32>;
-  // bytes one tile brings in: x, plus the random integers with SR (64
-  // columns of them, 16 KB, for an FP32 tile)
-  constexpr uint32_t kTxBytes = kTileBytes + (SR ? (F32 ? kTileBytes / 2 : kTileBytes) : 0);
+  constexpr int kCols = kTileCols<F32, COL>;
+  // bytes one tile brings in: x, plus the random integers with SR (2 bytes
+  // per column of the tile)
+  constexpr uint32_t kTxBytes = QSmem::kXBytes + (SR ? kTile * kCols * 2 : 0);
 
   if (warp == kProducerWarp && lane == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -887,15 +945,17 @@ __global__ void __launch_bounds__(QSmem<COL, SR>::kThreads, 1)
         mbar_arrive_expect_tx(&full[s], kTxBytes);
         uint8_t* slot = smem + QSmem::kOffRing + s * QSmem::kSlotBytes;
         const int32_t ry = static_cast<int32_t>(tl.x_row0);
-        // two boxes of 128-byte rows (128-byte swizzle): 64 bf16 or 32 FP32
-        // columns each; the random integers likewise in 64-column boxes
-        for (int half = 0; half < 2; ++half) {
-          const int32_t cx = static_cast<int32_t>(tl.c0) + (kCols / 2) * half;
-          tma_load_2d(slot + half * (kTileBytes / 2), &tmap_x, &full[s], cx, ry);
-          if constexpr (SR) {
-            if (!F32 || half == 0)
-              tma_load_2d(slot + kTileBytes + half * (kTileBytes / 2), &tmap_r, &full[s], cx, ry);
-          }
+        // boxes of 128 rows x 128 bytes (128-byte swizzle), 16 KB apart: 64
+        // bf16 or 32 FP32 columns each; the random integers in boxes of 64
+        // columns after x
+        constexpr int kBoxCols = F32 ? 32 : 64;
+        for (int b = 0; b < kCols / kBoxCols; ++b)
+          tma_load_2d(slot + b * (kTileBytes / 2), &tmap_x, &full[s],
+                      static_cast<int32_t>(tl.c0) + kBoxCols * b, ry);
+        if constexpr (SR) {
+          for (int b = 0; b < kCols / 64; ++b)
+            tma_load_2d(slot + QSmem::kXBytes + b * (kTileBytes / 2), &tmap_r, &full[s],
+                        static_cast<int32_t>(tl.c0) + 64 * b, ry);
         }
       }
       // every issued copy lands before the block exits
@@ -929,7 +989,7 @@ __global__ void __launch_bounds__(QSmem<COL, SR>::kThreads, 1)
       // scale units zeroed; a wait that gave up anywhere stops the whole group
       if (group_bar_any(group, !got)) break;
       const uint8_t* slot = smem + QSmem::kOffRing + s * QSmem::kSlotBytes;
-      quantize_tile<FMT, ROW, COL, GROUPED, SR, PACKED, F32>(p, tl, slot, slot + kTileBytes, s_q,
+      quantize_tile<FMT, ROW, COL, GROUPED, SR, PACKED, F32>(p, tl, slot, slot + QSmem::kXBytes, s_q,
                                                             s_unit_row, s_unit_col, &empty[s],
                                                             group, lt);
     }
@@ -943,7 +1003,7 @@ template <int FMT, bool ROW, bool COL, bool GROUPED, bool SR = false, bool PACKE
 cudaError_t launch_one(const QuantizeParams& p, const CUtensorMap& tmap, const CUtensorMap& tmap_r,
                        int64_t tiles, int num_sms, cudaStream_t stream) {
   auto kern = quantize_kernel<FMT, ROW, COL, GROUPED, SR, PACKED, F32>;
-  using QSmem = mx::QSmem<COL, SR>;
+  using QSmem = mx::QSmem<COL, SR, F32 && !COL>;
   static PerDeviceOnce setup;
   const cudaError_t err = setup.run([&] {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QSmem::kBytes);
@@ -990,7 +1050,7 @@ template <bool F32>
 cudaError_t launch_quantize_dense(const QuantizeParams& p, const CUtensorMap& tmap_x,
                                   const CUtensorMap* tmap_r, int num_sms, cudaStream_t stream) {
   if (p.rows == 0 || p.cols == 0) return cudaSuccess;
-  constexpr int kCols = kTileCols<F32>;
+  constexpr int kCols = kTileCols<F32, true>;  // the narrowest tile: an upper bound
   const int64_t tiles = ((p.rows + kTile - 1) / kTile) * ((p.cols + kCols - 1) / kCols);
   switch (p.fmt) {
     case 0: return launch_dense<0, false, F32>(p, tmap_x, tmap_r, tiles, num_sms, stream);
@@ -1012,7 +1072,7 @@ cudaError_t launch_quantize_groups(const QuantizeParams& p, const CUtensorMap& t
                                    int num_sms, cudaStream_t stream) {
   if (p.cols == 0) return cudaSuccess;
   if (p.fmt > 1) return cudaErrorNotSupported;  // grouped: FP8 codes
-  constexpr int kCols = kTileCols<F32>;
+  constexpr int kCols = kTileCols<F32, true>;  // the narrowest tile: an upper bound
   // upper bound of the padded row tiles; the kernel computes the exact count
   const int64_t tiles = ((p.rows + kTile - 1) / kTile + p.groups) * ((p.cols + kCols - 1) / kCols);
   const bool row = p.q_row != nullptr;
