@@ -611,6 +611,49 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
                                    gcb + 16 >= p.cols);
       s_unit_row[unit_offset(lr, 2 * half + bq)] = sbyte;
     }
+  } else if constexpr (ROW && SR && !COL) {
+    // Rowwise-only stochastic rounding: the same blocks as below, the
+    // thread's two rows one after the other, so that only one row's values
+    // and draws (32 registers) are live at a time; loading both rows first
+    // spilled and ran 3 % slower.
+    const int bq = lt & 3;
+    const int lr0 = lt >> 2;
+    const int64_t gcb = tl.c0 + bq * 32;
+    const bool blk_ok = gcb < p.cols;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      const int lr = lr0 + 64 * h;
+      uint4 v[4], rv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int off = tile_offset(lr, bq * 64 + j * 16);
+        v[j] = *reinterpret_cast<const uint4*>(xs + off);
+        rv[j] = *reinterpret_cast<const uint4*>(rs + off);
+      }
+      if (h == 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar);  // slot fully read by this warp
+      }
+      uint2 c[4];
+      uint8_t sbyte;
+      const uint32_t a = amax_bits32(v);
+      if (a >= 0x7F80u) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) c[j] = make_uint2(F::kNanWord, F::kNanWord);
+        sbyte = kNanScale;
+      } else {
+        const int e = scale_exponent<FMT>(a, p.rule);
+        const float mul = pow2_neg(e);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) c[j] = encode8_sr<FMT>(v[j], rv[j], mul);
+        sbyte = static_cast<uint8_t>(e + 127);
+      }
+      if (blk_ok && lr < tl.rows_valid) {
+        store_row_block<FMT, PACKED>(p.q_row + (tl.x_row0 + lr) * row_bytes, gcb, c,
+                                     gcb + 16 >= p.cols);
+        s_unit_row[unit_offset(lr, bq)] = sbyte;
+      }
+    }
   } else if constexpr (ROW) {
     // Thread lt quantizes the 32-element block lt % 4 of tile rows lt / 4
     // and lt / 4 + 64: it holds the whole block, so the amax needs no
