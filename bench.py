@@ -578,6 +578,16 @@ def _measure_rows(mx, peaks, dev, stream, clocks: RowClocks):
             out[f"quantize_{r}x{c}_row_sr_e5m2"] = bandwidth_row(qsr, stream, scrub, clean,
                                                                  r * c * 5.03125, hbm, 5.03125,
                                                                  clocks)
+
+            # both orientations with stochastic rounding (gradients feeding the
+            # data and the weight gradient): 2 + 2 + 2 x (1 + 1/32) B per element
+            def qsr_both():
+                st = mx.mx_quantize_sr(x.data_ptr(), 0, r, c, c, rb.data_ptr(), c, 1, 3, 0,
+                                       qr.data_ptr(), sr.data_ptr(), qc.data_ptr(), sc.data_ptr(),
+                                       h)
+                assert st == 0
+            out[f"quantize_{r}x{c}_both_sr_e5m2"] = bandwidth_row(
+                qsr_both, stream, scrub, clean, r * c * 6.0625, hbm, 6.0625, clocks)
             # stochastic rounding to packed MXFP4 (gradients in E2M1): bf16 and
             # draws read, half a byte of code written per element
             q4s_codes = torch.empty((r, c // 2), dtype=torch.uint8, device=dev)
