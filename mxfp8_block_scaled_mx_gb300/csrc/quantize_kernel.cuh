@@ -237,19 +237,21 @@ __device__ __forceinline__ float sr_to_grid(float v, uint32_t r16) {
   // In the format's normal range the grid keeps the top kMantBits of the
   // FP32 significand: l is |v| with the dropped bits cleared, u = l plus one
   // step (a carry into the exponent gives the next binade's first value),
-  // and the top 16 of the dropped bits are floor(frac * 2^16).  Below the
-  // smallest normal m = 2^kMinNormalExp the step is the subnormal quantum,
-  // which is also the step of the binade [m, 2m): there |v| + m (rounded
-  // toward zero, which keeps the top 16 dropped bits exact) is rounded the
-  // same way and m is taken off again (exact: both are multiples of the step).
+  // and the top 16 of the dropped bits are floor(frac * 2^16).  Adding
+  // 0xFFFF - r to those 16 bits carries into the kept bits exactly when
+  // r < floor(frac * 2^16) (the bits below them are too few to carry), so
+  // u or l is the sum with the dropped bits cleared.  Below the smallest
+  // normal m = 2^kMinNormalExp the step is the subnormal quantum, which is
+  // also the step of the binade [m, 2m): there |v| + m (rounded toward
+  // zero, which keeps the top 16 dropped bits exact) is rounded the same
+  // way and m is taken off again (exact: both are multiples of the step);
+  // elsewhere the same two operations add and take off zero.
   const float m = __uint_as_float(static_cast<uint32_t>(127 + kMinNormalExp) << 23);
   const float a = fabsf(v);
-  const bool small = a < m;
-  const uint32_t bits = __float_as_uint(small ? __fadd_rz(a, m) : a);
-  const uint32_t frac16 = (bits >> (kDrop - 16)) & 0xFFFFu;
-  const uint32_t low = bits & ~((1u << kDrop) - 1u);
-  const float r = __uint_as_float(low + (r16 < frac16 ? (1u << kDrop) : 0u));
-  return copysignf(small ? __fsub_rn(r, m) : r, v);
+  const float ms = a < m ? m : 0.0f;
+  const uint32_t bits = __float_as_uint(__fadd_rz(a, ms));
+  const uint32_t t = (bits + ((r16 ^ 0xFFFFu) << (kDrop - 16))) & ~((1u << kDrop) - 1u);
+  return copysignf(__fsub_rn(__uint_as_float(t), ms), v);
 }
 
 // Two bf16 of a word with their two 16-bit random integers -> two codes.
