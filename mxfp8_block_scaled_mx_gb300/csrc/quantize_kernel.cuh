@@ -9,9 +9,11 @@
 // "Numerical hazards: subnormals, saturation, and rounding" (round to
 // nearest even, subnormals kept, saturation after rounding).
 //
-// The kernel is HBM-bound, so it is built around deep prefetch: one
-// persistent block per SM, a producer thread that streams tiles of x (128
-// rows of 128 bf16 or FP32 columns, 32 or 64 KB) into a ring of
+// The kernel is HBM-bound (stochastic rounding of both orientations from
+// one read excepted: that is bound by the integer pipe), so it is built
+// around deep prefetch: one persistent block per SM, a producer thread that
+// streams tiles of x (128 rows of 128 bf16 or FP32 columns, 32 or 64 KB;
+// 64 FP32 columns when columnwise codes are written too) into a ring of
 // shared-memory slots with cp.async.bulk.tensor, and groups of eight
 // consumer warps that take tiles round-robin, straight out of shared memory
 // while the next tiles are in flight.
