@@ -236,3 +236,30 @@ def test_f32_ceil_rule_at_the_significand_threshold(mx, fmt):
     for rule in ("ceil", "floor"):
         q = mx.quantize(x.cuda(), fmt, "row", rule)
         check(q, x, fmt, "row", rule)
+
+
+def test_f32_empty_quantize_writes_nothing(mx):
+    """rows = 0 or cols = 0 are valid for FP32 input and launch nothing,
+    also with stochastic rounding."""
+    h = int(torch.cuda.current_stream().cuda_stream)
+    sentinel = torch.full((256,), 0xAB, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(64, dtype=torch.float32, device="cuda")
+    r = torch.zeros(64, dtype=torch.int16, device="cuda")
+    s = sentinel.data_ptr()
+    assert mx.mx_quantize(x.data_ptr(), 1, 0, 32, 32, 0, 3, 0, s, s, s, s, h) == 0
+    assert mx.mx_quantize(x.data_ptr(), 1, 32, 0, 0, 0, 1, 0, s, s, None, None, h) == 0
+    assert mx.mx_quantize_sr(x.data_ptr(), 1, 0, 32, 32, r.data_ptr(), 32, 1, 3, 0, s, s, s, s,
+                             h) == 0
+    assert mx.device_status() == 0
+    assert (sentinel == 0xAB).all()
+
+
+@pytest.mark.parametrize("shape,axis", [((1, 16), "row"), ((16, 8), "col"), ((16, 16), "both")])
+def test_f32_smallest_shapes(mx, shape, axis):
+    """The smallest legal FP32 shapes: one 16-element partial block."""
+    x = special_f32(*shape, seed=shape[0] + shape[1])
+    out = mx.quantize(x.cuda(), "e4m3", axis)
+    assert mx.device_status() == 0
+    pairs = [(out[0], "row"), (out[1], "col")] if axis == "both" else [(out, axis)]
+    for q, ax in pairs:
+        check(q, x, "e4m3", ax)
