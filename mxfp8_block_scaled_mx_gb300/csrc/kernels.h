@@ -1,6 +1,7 @@
 // kernels.h -- launch interface between the C-ABI layer (mx_api.cu) and the
-// CUDA kernels (quantize.cu, gemm_pair.cu, status.cu).  Not part of the
-// public ABI.
+// CUDA kernels (quantize.cu and quantize_f32.cu, which instantiate
+// quantize_kernel.cuh; gemm_pair.cu; status.cu).  Not part of the public
+// ABI.
 #pragma once
 
 #include <cuda.h>
@@ -11,10 +12,6 @@
 
 namespace mx {
 
-// One-time set-up of a kernel per device (its dynamic shared-memory limit):
-// `fn` runs until it first succeeds on the current device.  The flags are
-// guarded by a mutex, so concurrent first calls from several host threads
-// are safe.
 // Launch attribute of every kernel of the library: programmatic stream
 // serialization (the kernels wait for their predecessor with griddepcontrol
 // before touching global memory).
@@ -25,6 +22,10 @@ inline cudaLaunchAttribute pdl_attribute() {
   return a;
 }
 
+// One-time set-up of a kernel per device (its dynamic shared-memory limit):
+// `fn` runs until it first succeeds on the current device.  The flags are
+// guarded by a mutex, so concurrent first calls from several host threads
+// are safe.
 class PerDeviceOnce {
  public:
   template <typename Fn>
@@ -94,8 +95,9 @@ struct GemmParams {
   int64_t m;           // rows of A and Y (grouped by rows: total rows; grouped
                        // along K: rows of A and of each output matrix)
   int64_t n;           // rows of each B (columns of Y)
-  int64_t k;           // contraction length, multiple of 32 (grouped along K:
-                       // unused, each group's length comes from the offsets)
+  int64_t k;           // contraction length, a multiple of 16 (a final block of
+                       // 16 is zero-filled past K; grouped along K: unused,
+                       // each group's length comes from the offsets)
   int64_t lda;         // columns of the A code matrix (K-contiguous)
   int64_t ldb;         // columns of the B code matrix
   int32_t b_concat;    // grouped by rows: 1 = B is one [n, ldb] matrix with
