@@ -225,10 +225,9 @@ __device__ __forceinline__ uint2 encode8_f32(const uint4 a, const uint4 b, float
 // neighbouring grid values, |v| goes to u iff the element's 16-bit random
 // integer r is below floor(frac * 2^16), frac = (|v| - l) / (u - l).  The
 // result is a grid value (or one step past the maximum, which the
-// saturating conversion then clamps).  v is exact (a bf16 or an FP32 times a
-// power of two; an FP32 product below 2^-126 goes to zero either way), and
-// so is every step below: the one rounded addition only drops bits below
-// those the comparison reads.
+// saturating conversion then clamps), with the sign of v.  v is exact (a
+// bf16 or an FP32 times a power of two; an FP32 product below 2^-126 goes
+// to zero either way).
 template <int FMT>
 __device__ __forceinline__ float sr_to_grid(float v, uint32_t r16) {
   // significand bits and smallest normal exponent: E4M3 3 / -6, E5M2 2 /
@@ -236,24 +235,25 @@ __device__ __forceinline__ float sr_to_grid(float v, uint32_t r16) {
   constexpr int kMantBits = (FMT == 0 || FMT == 2) ? 3 : FMT == 4 ? 1 : 2;
   constexpr int kMinNormalExp = FMT == 0 ? -6 : FMT == 1 ? -14 : FMT == 3 ? -2 : 0;
   constexpr int kDrop = 23 - kMantBits;  // FP32 significand bits below the format's grid
-  // In the format's normal range the grid keeps the top kMantBits of the
-  // FP32 significand: l is |v| with the dropped bits cleared, u = l plus one
-  // step (a carry into the exponent gives the next binade's first value),
-  // and the top 16 of the dropped bits are floor(frac * 2^16).  Adding
-  // 0xFFFF - r to those 16 bits carries into the kept bits exactly when
-  // r < floor(frac * 2^16) (the bits below them are too few to carry), so
-  // u or l is the sum with the dropped bits cleared.  Below the smallest
-  // normal m = 2^kMinNormalExp the step is the subnormal quantum, which is
-  // also the step of the binade [m, 2m): there |v| + m (rounded toward
-  // zero, which keeps the top 16 dropped bits exact) is rounded the same
-  // way and m is taken off again (exact: both are multiples of the step);
-  // elsewhere the same two operations add and take off zero.
-  const float m = __uint_as_float(static_cast<uint32_t>(127 + kMinNormalExp) << 23);
-  const float a = fabsf(v);
-  const float ms = a < m ? m : 0.0f;
-  const uint32_t bits = __float_as_uint(__fadd_rz(a, ms));
+  // v * 2^-kShift takes the format's smallest normal m = 2^kMinNormalExp
+  // to FP32's (2^-126).  Above it the FP32 pattern keeps the format's
+  // significand bits over kDrop dropped bits; below it the pattern is an
+  // FP32 subnormal, linear in the value, whose unit 2^-149 makes the
+  // format's subnormal quantum exactly 2^kDrop units: in both ranges l is
+  // the pattern with the low kDrop bits cleared and u is l plus one step (a
+  // carry into the exponent gives the next binade's first value, or m).
+  // The top 16 dropped bits are floor(frac * 2^16) (the multiply rounds
+  // toward zero, which only clears bits below them), and adding 0xFFFF - r
+  // to them carries into the kept bits exactly when r < floor(frac * 2^16)
+  // (the bits below them are too few to carry), so u or l is the sum with
+  // the dropped bits cleared.  The sign bit rides along (signed zeros
+  // included), and the scaling back by 2^kShift is exact.
+  constexpr int kShift = kMinNormalExp + 126;
+  const float down = __uint_as_float(static_cast<uint32_t>(127 - kShift) << 23);
+  const float up = __uint_as_float(static_cast<uint32_t>(127 + kShift) << 23);
+  const uint32_t bits = __float_as_uint(__fmul_rz(v, down));
   const uint32_t t = (bits + ((r16 ^ 0xFFFFu) << (kDrop - 16))) & ~((1u << kDrop) - 1u);
-  return copysignf(__fsub_rn(__uint_as_float(t), ms), v);
+  return __fmul_rn(__uint_as_float(t), up);
 }
 
 // Two bf16 of a word with their two 16-bit random integers -> two codes.
