@@ -10,7 +10,7 @@
 // nearest even, subnormals kept, saturation after rounding).
 //
 // The kernel is HBM-bound (stochastic rounding of both orientations from
-// one read excepted: that is bound by the integer pipe), so it is built
+// one read comes closest to being compute-bound), so it is built
 // around deep prefetch: one persistent block per SM, a producer thread that
 // streams tiles of x (128 rows of 128 bf16 or FP32 columns, 32 or 64 KB;
 // 64 FP32 columns when columnwise codes are written too) into a ring of
