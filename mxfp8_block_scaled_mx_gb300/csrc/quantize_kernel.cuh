@@ -220,16 +220,17 @@ __device__ __forceinline__ uint2 encode8_f32(const uint4 a, const uint4 b, float
   return make_uint2(p0 | p1 << 16, p2 | p3 << 16);
 }
 
-// Stochastic rounding of an exactly scaled value v onto the format grid
-// (section "Rounding: RNE versus stochastic rounding"): with l <= |v| < u
-// neighbouring grid values, |v| goes to u iff the element's 16-bit random
-// integer r is below floor(frac * 2^16), frac = (|v| - l) / (u - l).  The
+// Stochastic rounding of two exactly scaled values onto the format grid
+// (section "Rounding: RNE versus stochastic rounding"), r holding v.x's
+// 16-bit random integer in its low half and v.y's in its high half: with
+// l <= |v| < u neighbouring grid values, |v| goes to u iff its random
+// integer is below floor(frac * 2^16), frac = (|v| - l) / (u - l).  Each
 // result is a grid value (or one step past the maximum, which the
 // saturating conversion then clamps), with the sign of v.  v is exact (a
 // bf16 or an FP32 times a power of two; an FP32 product below 2^-126 goes
 // to zero either way).
 template <int FMT>
-__device__ __forceinline__ float sr_to_grid(float v, uint32_t r16) {
+__device__ __forceinline__ float2 sr_to_grid2(float2 v, uint32_t r) {
   // significand bits and smallest normal exponent: E4M3 3 / -6, E5M2 2 /
   // -14, E2M3 3 / 0, E3M2 2 / -2, E2M1 1 / 0
   constexpr int kMantBits = (FMT == 0 || FMT == 2) ? 3 : FMT == 4 ? 1 : 2;
@@ -247,22 +248,34 @@ __device__ __forceinline__ float sr_to_grid(float v, uint32_t r16) {
   // to them carries into the kept bits exactly when r < floor(frac * 2^16)
   // (the bits below them are too few to carry), so u or l is the sum with
   // the dropped bits cleared.  The sign bit rides along (signed zeros
-  // included), and the scaling back by 2^kShift is exact.
+  // included), and the scaling back by 2^kShift is exact.  Both multiplies
+  // work on the pair at once (FP32x2).
   constexpr int kShift = kMinNormalExp + 126;
+  constexpr uint32_t kMask = ~((1u << kDrop) - 1u);
   const float down = __uint_as_float(static_cast<uint32_t>(127 - kShift) << 23);
   const float up = __uint_as_float(static_cast<uint32_t>(127 + kShift) << 23);
-  const uint32_t bits = __float_as_uint(__fmul_rz(v, down));
-  const uint32_t t = (bits + ((r16 ^ 0xFFFFu) << (kDrop - 16))) & ~((1u << kDrop) - 1u);
-  return __fmul_rn(__uint_as_float(t), up);
+  uint64_t x, m, p;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(v.x), "f"(v.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(m) : "f"(down), "f"(down));
+  asm("mul.rz.f32x2 %0, %1, %2;" : "=l"(p) : "l"(x), "l"(m));
+  uint32_t b0, b1;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(b0), "=r"(b1) : "l"(p));
+  const uint32_t nr = ~r;  // 0xFFFF - r in each half
+  const uint32_t t0 = (b0 + ((nr & 0xFFFFu) << (kDrop - 16))) & kMask;
+  const uint32_t t1 = (b1 + ((nr >> 16) << (kDrop - 16))) & kMask;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(t0), "r"(t1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(m) : "f"(up), "f"(up));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p) : "l"(x), "l"(m));
+  float2 g;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(g.x), "=f"(g.y) : "l"(p));
+  return g;
 }
 
 // Two bf16 of a word with their two 16-bit random integers -> two codes.
 template <int FMT>
 __device__ __forceinline__ uint32_t encode_word_sr(uint32_t w, uint32_t r, float mul) {
-  // scalar multiplies: the packed form measured slower here
-  const float lo = __fmul_rn(__uint_as_float(w << 16), mul);
-  const float hi = __fmul_rn(__uint_as_float(w & 0xFFFF0000u), mul);
-  return cvt_pair<FMT>(sr_to_grid<FMT>(lo, r & 0xFFFFu), sr_to_grid<FMT>(hi, r >> 16));
+  const float2 g = sr_to_grid2<FMT>(scale_pair(w, mul, mul), r);
+  return cvt_pair<FMT>(g.x, g.y);
 }
 
 // Eight bf16 with their random integers -> eight codes, laid out as encode8.
@@ -285,9 +298,8 @@ __device__ __forceinline__ uint2 encode8_sr(const uint4 v, const uint4 r, float 
 template <int FMT>
 __device__ __forceinline__ uint32_t encode_f32_pair_sr(uint32_t lo, uint32_t hi, uint32_t r,
                                                        float mul) {
-  const float vlo = __fmul_rn(__uint_as_float(lo), mul);
-  const float vhi = __fmul_rn(__uint_as_float(hi), mul);
-  return cvt_pair<FMT>(sr_to_grid<FMT>(vlo, r & 0xFFFFu), sr_to_grid<FMT>(vhi, r >> 16));
+  const float2 g = sr_to_grid2<FMT>(scale_f32_pair(lo, hi, mul, mul), r);
+  return cvt_pair<FMT>(g.x, g.y);
 }
 
 // Eight FP32 with their random integers (r: two per word, element order)
@@ -811,14 +823,12 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
       if constexpr (SR) {
         // the random integer of column 2cp sits in the low half of the
         // random word, that of column 2cp + 1 in the high half
-        const uint32_t r0 = rw[4 * i], r1 = rw[4 * i + 1], r2 = rw[4 * i + 2], r3 = rw[4 * i + 3];
-        q_lo[i] = cvt_pair<FMT>(sr_to_grid<FMT>(s0.x, r0 & 0xFFFFu),
-                                sr_to_grid<FMT>(s1.x, r1 & 0xFFFFu)) |
-                  (cvt_pair<FMT>(sr_to_grid<FMT>(s2.x, r2 & 0xFFFFu),
-                                 sr_to_grid<FMT>(s3.x, r3 & 0xFFFFu)) << kPairShift);
-        q_hi[i] = cvt_pair<FMT>(sr_to_grid<FMT>(s0.y, r0 >> 16), sr_to_grid<FMT>(s1.y, r1 >> 16)) |
-                  (cvt_pair<FMT>(sr_to_grid<FMT>(s2.y, r2 >> 16), sr_to_grid<FMT>(s3.y, r3 >> 16))
-                   << kPairShift);
+        const float2 g0 = sr_to_grid2<FMT>(s0, rw[4 * i]);
+        const float2 g1 = sr_to_grid2<FMT>(s1, rw[4 * i + 1]);
+        const float2 g2 = sr_to_grid2<FMT>(s2, rw[4 * i + 2]);
+        const float2 g3 = sr_to_grid2<FMT>(s3, rw[4 * i + 3]);
+        q_lo[i] = cvt_pair<FMT>(g0.x, g1.x) | (cvt_pair<FMT>(g2.x, g3.x) << kPairShift);
+        q_hi[i] = cvt_pair<FMT>(g0.y, g1.y) | (cvt_pair<FMT>(g2.y, g3.y) << kPairShift);
       } else {
         q_lo[i] = cvt_pair<FMT>(s0.x, s1.x) | (cvt_pair<FMT>(s2.x, s3.x) << kPairShift);
         q_hi[i] = cvt_pair<FMT>(s0.y, s1.y) | (cvt_pair<FMT>(s2.y, s3.y) << kPairShift);
