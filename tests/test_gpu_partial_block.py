@@ -201,3 +201,17 @@ def test_grouped_quantize_both_with_partial_row_blocks(mx, dtype):
     assert torch.equal(col.codes[:, :used].cpu(), torch.from_numpy(codes[:, :used]))
     got = O.unswizzle_scales(col.scales.cpu().numpy(), cols, ldq // 32)
     assert np.array_equal(got[:, :used // 32], scales[:, :used // 32])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("fmt", ["e5m2", "e2m1", "e3m2"])
+def test_rowwise_sr_with_partial_block(mx, dtype, fmt):
+    """The rowwise-only stochastic-rounding pass (its own thread layout,
+    and 128-column tiles for FP32) on 208 columns: a 16-column final block
+    in the last tile."""
+    from mxfp8_block_scaled_mx_gb300 import workloads as W
+    x = data(130, 208, seed=17, dtype=dtype)
+    rand = W.random_bits16((130, 208), seed=18)
+    q = mx.quantize(x.cuda(), fmt, "row", rand=rand.cuda())
+    assert mx.device_status() == 0
+    check(q, x, fmt, "row", rand=rand.numpy().view(np.uint16).astype(np.int64))
