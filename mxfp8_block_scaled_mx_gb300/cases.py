@@ -1,7 +1,7 @@
 """Run one hot-path kernel on one shape a few times (for profilers).
 
     python -m mxfp8_block_scaled_mx_gb300.cases gemm --m 4096 --n 18432 --k 7168 [--reps 3] [--fused]
-    python -m mxfp8_block_scaled_mx_gb300.cases quantize --rows 16384 --cols 8192 --axis row [--sr] [--fp32]
+    python -m mxfp8_block_scaled_mx_gb300.cases quantize --rows 16384 --cols 8192 --axis row [--sr] [--fp32] [--flush write]
     python -m mxfp8_block_scaled_mx_gb300.cases moe_quantize --tokens 65536 --experts 64 --axis col
     python -m mxfp8_block_scaled_mx_gb300.cases grouped --tokens 16384 --experts 16
     python -m mxfp8_block_scaled_mx_gb300.cases moe_dgrad --tokens 16384 --experts 16
@@ -21,17 +21,44 @@ import mxfp8_block_scaled_mx_gb300 as mx
 from mxfp8_block_scaled_mx_gb300 import workloads as W
 
 
-def _time(fn, reps):
+def _time(fn, reps, pre=None):
     fn()  # warm-up launch (module load, attributes)
     torch.cuda.synchronize()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record()
+    if pre is None:
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+    # one launch at a time behind `pre` (an L2 flush), timed on its own
+    ts = []
     for _ in range(reps):
+        pre()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
         fn()
-    b.record()
+        b.record()
+        ts.append((a, b))
     torch.cuda.synchronize()
-    return a.elapsed_time(b) / reps
+    return sum(a.elapsed_time(b) for a, b in ts) / reps
+
+
+def _flush(kind, dev):
+    """The L2 state before each timed launch: `write` adds 1 to a 256 MB
+    buffer (L2 left full of dirty lines, as the bench's flush leaves it),
+    `read` does that and then sums another 256 MB buffer (L2 left full of
+    clean lines), `none` launches back to back."""
+    if kind == "none":
+        return None
+    scrub = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    if kind == "write":
+        return lambda: scrub.add_(1)
+    clean = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    return lambda: (scrub.add_(1), clean.sum())
 
 
 def main(argv=None):
@@ -51,6 +78,8 @@ def main(argv=None):
     ap.add_argument("--fused", action="store_true", help="gemm: FP32 bias + SiLU epilogue")
     ap.add_argument("--sr", action="store_true", help="quantize: stochastic rounding (E5M2)")
     ap.add_argument("--fp32", action="store_true", help="quantize: FP32 input (same values)")
+    ap.add_argument("--flush", default="none", choices=["none", "write", "read"],
+                    help="quantize: L2 state before each launch (see _flush)")
     a = ap.parse_args(argv)
     dev = torch.device("cuda", 0)
     if a.case == "gemm":
@@ -75,10 +104,11 @@ def main(argv=None):
             bpe += 2.0
         if a.sr:  # stochastic rounding to E5M2: the random draws are a second input
             rb = W.random_bits16((a.rows, a.cols), seed=11, device=dev)
-            ms = _time(lambda: mx.quantize(x, "e5m2", a.axis, rand=rb), a.reps)
+            ms = _time(lambda: mx.quantize(x, "e5m2", a.axis, rand=rb), a.reps,
+                       _flush(a.flush, dev))
             bpe += 2.0
         else:
-            ms = _time(lambda: mx.quantize(x, "e4m3", a.axis), a.reps)
+            ms = _time(lambda: mx.quantize(x, "e4m3", a.axis), a.reps, _flush(a.flush, dev))
         print(f"quantize {a.rows}x{a.cols} {a.axis}{' sr' if a.sr else ''}"
               f"{' fp32' if a.fp32 else ''}: {ms:.4f} ms, "
               f"{a.rows * a.cols * bpe / ms / 1e6:.1f} GB/s")
