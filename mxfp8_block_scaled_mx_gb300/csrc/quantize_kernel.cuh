@@ -972,17 +972,22 @@ __global__ void __launch_bounds__(QSmem<COL, SR, F32 && !COL>::kThreads, 1)
   // bytes one tile brings in: x, plus the random integers with SR (2 bytes
   // per column of the tile)
   constexpr uint32_t kTxBytes = QSmem::kXBytes + (SR ? kTile * kCols * 2 : 0);
-  // Copies in flight per block.  The dense passes keep fewer than their
-  // ring holds (landed tiles still fill the whole ring): three of six bf16
-  // rowwise tiles, three of four with columns, two of three FP32 rowwise
-  // tiles.  Measured on 16384x8192 back to back: bf16 rowwise 66.4 us
-  // against 73.6 with all six in flight (two 66.1, four 69.5, five 71.6),
-  // columnwise 67.6-68.0 against 69.5-69.9, FP32 rowwise 103.8-104.3
-  // against 106.4; and 4096x4096 bf16 rowwise with a clean L2 13.3 against
-  // 14.6 us.  The grouped passes keep the whole ring in flight (grouped
-  // rowwise 207 us that way, 219 with three), as do the two-slot
+  // Copies in flight per block, fewer than the ring holds (landed tiles
+  // still fill the whole ring): three of six in the dense bf16 rowwise
+  // pass, three of four in every pass with columns, two of three in the
+  // dense FP32 rowwise pass.  Measured back to back: bf16 rowwise
+  // 16384x8192 66.4 us against 73.6 with all six in flight (two 66.1, four
+  // 69.5, five 71.6), columnwise 67.6-68.0 against 69.5-69.9, FP32 rowwise
+  // 103.8-104.3 against 106.4, grouped columnwise 65536x7168 (64 experts)
+  // 221 against 225 us (two: 236); 4096x4096 bf16 rowwise with a clean L2
+  // 13.3 against 14.6 us.  The grouped rowwise passes keep the whole ring
+  // in flight (bf16: 207 us that way, 219 with three), as do the two-slot
   // stochastic-rounding rings.
-  constexpr int kWindow = (GROUPED || kStages <= 2) ? kStages : kStages == 3 ? 2 : 3;
+  constexpr int kWindow = kStages <= 2 ? kStages
+                          : kStages == 4 ? 3
+                          : GROUPED      ? kStages
+                          : kStages == 3 ? 2
+                                         : 3;
 
   if (warp == kProducerWarp && lane == 0) {
     for (int s = 0; s < kStages; ++s) {
