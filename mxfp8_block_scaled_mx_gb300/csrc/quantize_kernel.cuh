@@ -926,14 +926,15 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams& p, const Til
 // tiles of the rowwise-only FP32 pass.
 template <bool COL, bool SR = false, bool WIDE = false>
 struct QSmem {
-  // consumer groups (round-robin tiles): three for the rowwise-only ring
-  // of six (wide: three) slots, two otherwise
-  static constexpr int kGroups = (!COL && !SR) ? 3 : 2;
+  // consumer groups (round-robin tiles): three for the rowwise-only rings
+  // (bf16: six slots, or three of 64 KB with the random integers; FP32:
+  // three 64 KB slots), two otherwise
+  static constexpr int kGroups = (!COL && (!SR || !WIDE)) ? 3 : 2;
   static constexpr int kThreads = kGroups * kGroupThreads + 32;  // + one producer warp
   // a slot holds the tile of x, plus its 16-bit random integers with SR
   static constexpr int kXBytes = WIDE ? 2 * kTileBytes : kTileBytes;
   static constexpr int kSlotBytes = kXBytes + (SR ? kTileBytes : 0);
-  static constexpr int kStages = WIDE ? (SR ? 2 : 3) : SR ? 2 : (COL ? 4 : 6);   // tile slots
+  static constexpr int kStages = WIDE ? (SR ? 2 : 3) : SR ? (COL ? 2 : 3) : (COL ? 4 : 6);
   // Tile i lives in slot i % kStages and is consumed by group i % kGroups.
   // Successive users of a slot (tiles i and i + kStages) must belong to the
   // same group: a group can then never wait on a slot's next phase while
@@ -975,14 +976,18 @@ __global__ void __launch_bounds__(QSmem<COL, SR, F32 && !COL>::kThreads, 1)
   // Copies in flight per block, fewer than the ring holds (landed tiles
   // still fill the whole ring): three of six in the dense bf16 rowwise
   // pass, three of four in every pass with columns, two of three in the
-  // dense FP32 rowwise pass.  Measured back to back: bf16 rowwise
+  // dense FP32 and stochastic-rounding rowwise passes.  Measured back to
+  // back: bf16 rowwise
   // 16384x8192 66.4 us against 73.6 with all six in flight (two 66.1, four
   // 69.5, five 71.6), columnwise 67.6-68.0 against 69.5-69.9, FP32 rowwise
   // 103.8-104.3 against 106.4, grouped columnwise 65536x7168 (64 experts)
   // 221 against 225 us (two: 236); 4096x4096 bf16 rowwise with a clean L2
   // 13.3 against 14.6 us.  The grouped rowwise passes keep the whole ring
   // in flight (bf16: 207 us that way, 219 with three), as do the two-slot
-  // stochastic-rounding rings.
+  // rings of stochastic rounding with columns.  The bf16 stochastic-rounding
+  // rowwise pass (three 64 KB slots, two copies in flight, three groups)
+  // measured 104.3-105.2 us against 108.5-108.8 with two slots and two
+  // groups (E5M2, 16384x8192), its whole ring in flight 106.4.
   constexpr int kWindow = kStages <= 2 ? kStages
                           : kStages == 4 ? 3
                           : GROUPED      ? kStages
